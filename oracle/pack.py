@@ -104,7 +104,7 @@ def pack_ref(seqs, seq_weights=None) -> dict:
             starts.append(i)
     n_nodes = len(starts)
     node_start = np.array(starts, dtype=np.int32)
-    node_end = np.array(starts[1:] + [T], dtype=np.int32) - 1
+    node_end = (np.array(starts[1:] + [T], dtype=np.int32) - 1) if starts else np.zeros(0, np.int32)
     node_of_token = np.empty(T, dtype=np.int32)
     for c in range(n_nodes):
         node_of_token[node_start[c]:node_end[c] + 1] = c
