@@ -41,7 +41,7 @@ def _scale(d: int, scale) -> float:
 def _path_softmax(qp, kp, scale):
     """Causal attention probabilities along one path. qp,kp: [L,H,d] -> P [H,L,L], lse [H,L]."""
     L = qp.shape[0]
-    s = np.einsum("ihd,jhd->hij", qp, kp) * scale
+    s = np.matmul(qp.transpose(1, 0, 2), kp.transpose(1, 2, 0)) * scale     # [H, L, L]
     causal = np.triu(np.ones((L, L), dtype=bool), k=1)
     s[:, causal] = -np.inf
     m = s.max(axis=-1, keepdims=True)
@@ -71,7 +71,7 @@ def attn_ref_fwd(q, k, v, paths, scale=None, head_chunk: int = 8):
         for h0 in range(0, Hq, head_chunk):
             hs = np.arange(h0, min(Hq, h0 + head_chunk))
             p, l_ = _path_softmax(q[path][:, hs], k[path][:, kv[hs]], sc)
-            op = np.einsum("hij,jhd->ihd", p, v[path][:, kv[hs]])
+            op = np.matmul(p, v[path][:, kv[hs]].transpose(1, 0, 2)).transpose(1, 0, 2)
             old = done[path]
             if old.any():
                 ref_o = o[path[old]][:, hs]
@@ -107,12 +107,13 @@ def attn_ref_bwd(q, k, v, dout, paths, scale=None, head_chunk: int = 8):
             qp, kp, vp = q[path][:, hs], k[path][:, kv[hs]], v[path][:, kv[hs]]
             p, _ = _path_softmax(qp, kp, sc)
             dop = dout[path][:, hs] * assigned[:, None, None]
-            dvp = np.einsum("hij,ihd->jhd", p, dop)
-            dpp = np.einsum("ihd,jhd->hij", dop, vp)
+            qh, kh, vh, doh = (x.transpose(1, 0, 2) for x in (qp, kp, vp, dop))   # [H, L, d]
+            dvp = np.matmul(p.transpose(0, 2, 1), doh).transpose(1, 0, 2)          # P^T dO
+            dpp = np.matmul(doh, vh.transpose(0, 2, 1))                            # dO V^T
             delta = (p * dpp).sum(axis=-1, keepdims=True)
             ds = p * (dpp - delta)
-            dqp = np.einsum("hij,jhd->ihd", ds, kp) * sc
-            dkp = np.einsum("hij,ihd->jhd", ds, qp) * sc
+            dqp = np.matmul(ds, kh).transpose(1, 0, 2) * sc                        # dS K
+            dkp = np.matmul(ds.transpose(0, 2, 1), qh).transpose(1, 0, 2) * sc     # dS^T Q
             dq[path[:, None], hs[None, :]] += dqp
             for hi, h in enumerate(hs):
                 np.add.at(dk, (path, kv[h]), dkp[:, hi])
