@@ -1,0 +1,258 @@
+/*
+ * tree_attn.h -- C ABI of the tree-packed training hot path (GB300 / sm_103a).
+ *
+ * Tree packing stores every token of a set of sequences that share prefixes
+ * once, in depth-first (preorder) order, so that one forward/backward pass
+ * computes each shared prefix a single time:
+ *   - Tree Training: Accelerating Agentic LLMs Training via Shared Prefix Reuse
+ *     (arXiv 2511.00413), cited below as [TT];
+ *   - Trie packing, agillm.io visualisation, cited as [TP];
+ *   - Claw-R1 documentation "Prefix Tree Merge", cited as [PTM].
+ *
+ * Conventions shared by every call
+ *   - Row i of a packed tree is the token at preorder index i; its preorder
+ *     index IS i, so no separate preorder array exists.
+ *   - The ancestor mask is never stored densely. Key j is visible to query i
+ *     iff  j <= i <= subtree_end[j]  (subtree_end[j] = last row of j's
+ *     subtree). This per-key interval form equals [TT] §3.2 "Attention Mask"
+ *     (j <= i and both on one root-to-leaf path) and [TT] Appendix A.1
+ *     (whole ancestor chunks, causal inside a token's own chunk).
+ *   - Tensors are dense, row-major, contiguous, with no padding:
+ *       Q, dQ, O, dO [T, Hq, d];  K, V, dK, dV [T, Hkv, d];  LSE [Hq, T] fp32;
+ *       hidden, d_hidden [T, K_h];  W_LM, dW [K_h, V].
+ *     Query head h reads KV head h / (Hq / Hkv) (contiguous GQA groups).
+ *   - dtype is TREE_DTYPE_BF16 (bf16 storage, fp32 accumulation on tensor
+ *     cores) or TREE_DTYPE_F32 (fp32 storage and arithmetic).
+ *   - Pointers named "device" are CUDA device addresses owned by the caller;
+ *     the library never allocates, frees or keeps device memory. Scratch space
+ *     is the caller's `workspace` (device, at least the size returned by the
+ *     matching *_workspace_size query, 256-byte aligned).
+ *   - Every device call is asynchronous on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream) and returns after enqueueing its kernels.
+ *   - Every call returns a tree_status. Argument errors are found on the host
+ *     before anything is enqueued and leave outputs untouched. Device-side
+ *     range checks never trap: they set a device error word that
+ *     tree_check_device_status() reads. tree_last_error() describes the most
+ *     recent failure on the calling host thread. No C++ exception crosses
+ *     this interface.
+ */
+#ifndef TREE_ATTN_H_
+#define TREE_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared here so the header needs no CUDA headers. */
+typedef struct CUstream_st* tree_stream_t;
+
+typedef enum {
+  TREE_OK = 0,
+  TREE_ERR_INVALID_ARG = 1,   /* null pointer, negative size, bad flag */
+  TREE_ERR_SHAPE = 2,         /* unsupported or inconsistent sizes */
+  TREE_ERR_DTYPE = 3,         /* dtype not one of TREE_DTYPE_* */
+  TREE_ERR_ALIGNMENT = 4,     /* pointer not 16-byte (workspace: 256-byte) aligned */
+  TREE_ERR_CUDA = 5,          /* a CUDA runtime/driver call failed */
+  TREE_ERR_TIMEOUT = 6,       /* a bounded device-side wait gave up */
+  TREE_ERR_DEVICE_CHECK = 7,  /* a device-side range check failed */
+  TREE_ERR_WORKSPACE = 8      /* workspace smaller than the size query says */
+} tree_status;
+
+typedef enum { TREE_DTYPE_F32 = 0, TREE_DTYPE_BF16 = 1 } tree_dtype;
+
+/* ------------------------------------------------------------------------ */
+/* Host packing                                                              */
+/* ------------------------------------------------------------------------ */
+/*
+ * Packing follows [TP] "Step 1 - Store each node once" (a token is shared
+ * only when its whole preceding context is identical; position = depth),
+ * [TT] §3.1 eq. 8 (DFS serialisation), [TT] §3.2 eq. 9 (positions) and
+ * [PTM] "1. build and compress" (insert into a trie, compress single-child
+ * chains into nodes, number nodes in preorder).
+ *
+ * Readings fixed by this interface:
+ *   - children and roots are ordered by first insertion (both worked examples);
+ *   - several distinct first tokens give a forest; positions restart at 0;
+ *   - a node (chunk) ends at a fork, at a leaf, and where an input sequence
+ *     ends ([PTM]'s node list);
+ *   - occurrences are the original next-token predictions ([TP] "Share
+ *     logits, preserve every prediction"): for each input sequence k in input
+ *     order and t = 0 .. len_k - 2, (row of token t, token t+1, weight w_k);
+ *     duplicated sequences keep their own occurrences; no EOS is added.
+ *
+ * Two phases so that the caller owns every output array:
+ *   tree_pack_plan() builds the trie and reports sizes; the caller allocates;
+ *   tree_pack_emit() fills the arrays; tree_plan_free() releases the plan.
+ */
+typedef struct tree_plan tree_plan;
+
+typedef struct {
+  int64_t T;          /* packed rows (unique prefixes) */
+  int64_t n_nodes;    /* compressed nodes (chunks) */
+  int64_t n_occ;      /* next-token occurrences = sum_k max(len_k - 1, 0) */
+  int64_t n_roots;    /* trees in the forest */
+  int64_t n_tokens;   /* total input tokens = seq_offsets[n_seqs] */
+} tree_pack_sizes;
+
+/* Host arrays, caller-allocated; any pointer may be NULL to skip that output. */
+typedef struct {
+  int32_t* packed_ids;      /* [T]   token id of row i */
+  int32_t* position_ids;    /* [T]   depth of row i (eq. 9) */
+  int32_t* subtree_end;     /* [T]   last row of row i's subtree (>= i) */
+  int32_t* path_count;      /* [T]   input sequences whose path holds row i */
+  int32_t* parent_row;      /* [T]   parent row, -1 for a root */
+  int32_t* node_of_token;   /* [T]   node (chunk) holding row i */
+  int32_t* node_start;      /* [n_nodes] first row of the node */
+  int32_t* node_end;        /* [n_nodes] last row of the node (inclusive) */
+  int32_t* node_parent;     /* [n_nodes] parent node, -1 for a root node */
+  int32_t* token_rows;      /* [n_tokens] packed row of every input token (unpacking map) */
+  int32_t* occ_source_rows; /* [n_occ] row whose logits make the prediction */
+  int32_t* occ_targets;     /* [n_occ] predicted token id */
+  int32_t* occ_seq;         /* [n_occ] input sequence of the occurrence */
+  float*   occ_weights;     /* [n_occ] weight of that sequence (1.0 if none given) */
+  int32_t* occ_row_ptr;     /* [T+1] CSR: occurrences of row r are
+                                occ_perm[occ_row_ptr[r] .. occ_row_ptr[r+1]) */
+  int32_t* occ_perm;        /* [n_occ] occurrence ids stably sorted by source row */
+} tree_pack_out;
+
+/* tokens: host [n_tokens] int32; seq_offsets: host [n_seqs+1] int64, nondecreasing,
+ * seq_offsets[0] == 0. Writes a new plan to *plan (free with tree_plan_free) and
+ * its sizes to *sizes. Errors: TREE_ERR_INVALID_ARG (null pointers, bad offsets),
+ * TREE_ERR_SHAPE (more than 2^31 - 1 rows or occurrences). */
+int tree_pack_plan(const int32_t* tokens, const int64_t* seq_offsets, int64_t n_seqs,
+                   tree_plan** plan, tree_pack_sizes* sizes);
+
+/* seq_weights: host [n_seqs] or NULL (all 1.0). Fills the non-NULL arrays of *out. */
+int tree_pack_emit(const tree_plan* plan, const float* seq_weights, const tree_pack_out* out);
+
+void tree_plan_free(tree_plan* plan);
+
+/* Host check that subtree_end (host [T]) is a preorder forest: i <= end[i] < T and
+ * the intervals [i, end[i]] nest. TREE_OK or TREE_ERR_INVALID_ARG. */
+int tree_validate_subtree_end(const int32_t* subtree_end, int64_t T);
+
+/* ------------------------------------------------------------------------ */
+/* RoPE on depth positions                                                   */
+/* ------------------------------------------------------------------------ */
+/*
+ * [TT] §3.2 "Position Embedding" (eq. 9) and [TP] Step 1: every row is rotated
+ * by its depth position, so packed rows see the rotation of their own
+ * per-path sequence. Variant (the pages name RoPE only): rotate-half pairs
+ * (x[k], x[k + d/2]) turned by angle pos * theta_base^(-2k/d), k < d/2; the
+ * angle is formed in fp32 and sin/cos are CUDA's accurate sincosf.
+ * inverse = 1 applies the transposed rotation (the backward of the forward
+ * rotation, used on dQ/dK).
+ *
+ * q: device [T, Hq, d], k: device [T, Hkv, d], rotated in place (either may be
+ * NULL); position_ids: device [T] int32, >= 0. d even, 2 <= d <= 256.
+ */
+int tree_rope(void* q, void* k, const int32_t* position_ids, int64_t T, int Hq, int Hkv,
+              int d, float theta_base, int dtype, int inverse, tree_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Tree attention                                                            */
+/* ------------------------------------------------------------------------ */
+/*
+ * Forward ([TP] "Step 2 - Allow only ancestors and self", "Step 3";
+ * [TT] §3.2 "Attention Mask", eq. 6 forward equivalence):
+ *   O_i   = sum_{j : j <= i <= subtree_end[j]} softmax_j(q_i . k_j * scale) v_j
+ *   LSE_i = ln sum_{same j} exp(q_i . k_j * scale)          (per query head)
+ * scale = softmax_scale if > 0, else 1/sqrt(d). No dropout, no softcap.
+ *
+ * Backward ([TP] "Same chain rule, shared computation graph", Step 3: a key
+ * collects the gradients of every descendant query that sees it):
+ *   dV_j = sum_i P_ij dO_i,  dS_ij = P_ij (dO_i . v_j - Delta_i),
+ *   Delta_i = dO_i . O_i,  dQ_i = scale sum_j dS_ij k_j,  dK_j = scale sum_i dS_ij q_i,
+ * with dK/dV of a KV head summed over its query heads.
+ *
+ * Sizes: 1 <= T < 2^31, Hq % Hkv == 0, d in {64, 128}. q, k, v, o, dout, dq, dk,
+ * dv: device, 16-byte aligned, dtype elements; lse: device fp32 [Hq, T];
+ * subtree_end: device int32 [T]. Rows with an out-of-range subtree_end
+ * (end < i or end >= T) set TREE_ERR_DEVICE_CHECK in the device error word;
+ * outputs are then unspecified (never out-of-bounds accesses). Nesting is not
+ * checked on the device (see tree_validate_subtree_end).
+ * deterministic: 0 lets dQ accumulate with fp32 atomics (order may vary run to
+ * run); 1 computes dQ without atomics (bitwise reproducible, more FLOPs).
+ */
+size_t tree_attn_workspace_size(int64_t T, int Hq, int Hkv, int d, int dtype);
+
+int tree_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                  const int32_t* subtree_end, int64_t T, int Hq, int Hkv, int d, int dtype,
+                  float softmax_scale, void* workspace, size_t workspace_bytes,
+                  tree_stream_t stream);
+
+int tree_attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                  const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                  const int32_t* subtree_end, int64_t T, int Hq, int Hkv, int d, int dtype,
+                  float softmax_scale, int deterministic, void* workspace,
+                  size_t workspace_bytes, tree_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Shared-logit log-probs                                                    */
+/* ------------------------------------------------------------------------ */
+/*
+ * Forward ([TP] "Share logits, preserve every prediction" and "The
+ * training-loop change is small"): z_r = hidden_r W_LM (never stored),
+ *   lse[r]  = ln sum_v exp(z_rv)                  for every row r in [0, T)
+ *   logp[o] = z_{r_o, y_o} - lse[r_o]             for every occurrence o
+ * with r_o = source row, y_o = occ_targets[o]. Occurrences are reached through
+ * the row CSR (occ_row_ptr [T+1], occ_perm [n_occ]) from tree_pack_emit.
+ *
+ * Backward ([TP] "Same chain rule, shared computation graph", Step 1;
+ * [TT] §3.2 "Loss Weights"): with g_o = grad_logp[o] = dL/dlogp_o
+ * (= -w_o for the weighted loss L = -sum_o w_o logp_o),
+ *   G_z[r]   = sum_{o at r} g_o (e_{y_o} - softmax(z_r))   (targets at a shared row add)
+ *   d_hidden = G_z W_LM^T,   d_w = hidden^T G_z            (both overwritten)
+ * z is recomputed from hidden, W_LM and lse.
+ *
+ * hidden, d_hidden: device [T, K_h]; w_lm, d_w: device [K_h, V]; dtype elements,
+ * 16-byte aligned; K_h % 64 == 0 and V % 8 == 0. lse: device fp32 [T];
+ * logp, grad_logp: device fp32 [n_occ]; index arrays device int32.
+ * Out-of-range targets or CSR entries set TREE_ERR_DEVICE_CHECK and are skipped.
+ */
+size_t tree_logprob_workspace_size(int64_t T, int64_t K_h, int64_t V, int dtype);
+
+int tree_logprob_fwd(const void* hidden, const void* w_lm, const int32_t* occ_row_ptr,
+                     const int32_t* occ_perm, const int32_t* occ_targets, int64_t T,
+                     int64_t K_h, int64_t V, int64_t n_occ, float* lse, float* logp,
+                     int dtype, void* workspace, size_t workspace_bytes,
+                     tree_stream_t stream);
+
+int tree_logprob_bwd(const void* hidden, const void* w_lm, const float* lse,
+                     const int32_t* occ_row_ptr, const int32_t* occ_perm,
+                     const int32_t* occ_targets, const float* grad_logp, int64_t T,
+                     int64_t K_h, int64_t V, int64_t n_occ, void* d_hidden, void* d_w,
+                     int dtype, void* workspace, size_t workspace_bytes,
+                     tree_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Status                                                                    */
+/* ------------------------------------------------------------------------ */
+/* Synchronises `stream`, reads and clears the device error word of the current
+ * device: TREE_OK, TREE_ERR_DEVICE_CHECK or TREE_ERR_TIMEOUT (a bounded
+ * pipeline wait gave up; the kernel then returned early and its outputs are
+ * unspecified), or TREE_ERR_CUDA if a CUDA error is pending. */
+int tree_check_device_status(tree_stream_t stream);
+
+/* Message of the last failure on this host thread ("" if none). Valid until the
+ * next call into the library from the same thread. */
+const char* tree_last_error(void);
+
+/* Which kernel family a call with these arguments runs: 0 = SIMT fp32 kernels,
+ * 1 = tcgen05/TMA tensor-core kernels. op: 0 attention forward, 1 attention
+ * backward, 2 log-prob forward, 3 log-prob backward. */
+int tree_kernel_path(int op, int dtype, int d);
+
+/* Kernel launches this library has enqueued in this process (all devices, all
+ * threads), for launch accounting by benchmarks. */
+uint64_t tree_launch_count(void);
+
+const char* tree_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TREE_ATTN_H_ */

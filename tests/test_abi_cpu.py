@@ -1,0 +1,103 @@
+"""CPU tests of the native library: it loads, exports every declared symbol,
+packs bit-exactly like the oracle and rejects bad arguments on the host."""
+import ctypes as C
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from conftest import ROOT
+
+
+@pytest.fixture(scope="module")
+def tma():
+    import __graft_entry__
+    __graft_entry__.build()
+    import tree_masked_attention_gb300 as m
+    return m
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "tree_attn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(tree_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(tma):
+    names = _declared()
+    assert "tree_attn_fwd" in names and "tree_logprob_bwd" in names
+    L = tma.lib()
+    for n in names:
+        assert hasattr(L, n), n
+    from tree_masked_attention_gb300._lib import SIGNATURES
+    assert sorted(SIGNATURES) == names
+
+
+KEYS = ("packed_ids", "position_ids", "subtree_end", "path_count", "parent_row", "node_of_token",
+        "node_start", "node_end", "node_parent", "occ_source_rows", "occ_targets", "occ_seq",
+        "occ_weights", "occ_row_ptr", "occ_perm")
+
+
+def _same(a, b):
+    for k in KEYS:
+        assert np.array_equal(a[k], b[k]), k
+    assert [x.tolist() for x in a["paths"]] == [x.tolist() for x in b["paths"]]
+    for k in ("T", "n_nodes", "n_occ", "n_roots"):
+        assert a[k] == b[k], k
+
+
+@pytest.mark.parametrize("seed", range(60))
+def test_pack_bit_exact_random(tma, seed):
+    rng = np.random.default_rng(1000 + seed)
+    seqs = synth.random_sequences(rng, int(rng.integers(0, 9)), 12, vocab=int(rng.integers(1, 5)))
+    w = rng.random(len(seqs)).astype(np.float32)
+    _same(tma.tree_pack(seqs, w), oracle.pack_ref(seqs, w))
+
+
+@pytest.mark.parametrize("gen", ["tiny_tree", "agentic_short", "agentic_long", "galton_watson", "lm_head_tree"])
+def test_pack_bit_exact_workloads(tma, gen):
+    t = getattr(synth, gen)()
+    _same(tma.tree_pack(t.seqs), oracle.pack_ref(t.seqs))
+
+
+def test_pack_pages_examples(tma):
+    from conftest import golden
+    g = golden("trie_packing_example.json")
+    p = tma.tree_pack(g["sequences"])
+    assert p["position_ids"].tolist() == g["position_ids"]
+    assert p["occ_source_rows"].tolist() == g["source_rows"]
+    g3 = golden("prefix_tree_merge_example.json")
+    p3 = tma.tree_pack(g3["sequences"])
+    assert [[int(a), int(b)] for a, b in zip(p3["node_start"], p3["node_end"])] == [n["pos"] for n in g3["nodes"]]
+
+
+def test_pack_edge_cases(tma):
+    p = tma.tree_pack([])
+    assert p["T"] == 0 and p["n_occ"] == 0
+    p = tma.tree_pack([[], [7]])
+    assert p["T"] == 1 and p["occ_row_ptr"].tolist() == [0, 0]
+
+
+def test_validate_subtree_end(tma):
+    tma.tree_validate_subtree_end([6, 6, 4, 3, 4, 6, 6])
+    with pytest.raises(tma.TreeError):
+        tma.tree_validate_subtree_end([1, 2, 2])       # row 1's subtree leaves row 0's
+    with pytest.raises(tma.TreeError):
+        tma.tree_validate_subtree_end([0, 0])          # end < i
+
+
+def test_host_argument_errors(tma):
+    L = tma.lib()
+    # bad shapes / dtypes are refused before any CUDA call
+    assert L.tree_attn_fwd(None, None, None, None, None, None, 16, 4, 3, 64, 1, 0.0, None, 0, None) == 2
+    assert L.tree_attn_fwd(None, None, None, None, None, None, 16, 4, 2, 96, 1, 0.0, None, 0, None) == 2
+    assert L.tree_attn_fwd(None, None, None, None, None, None, 16, 4, 2, 64, 7, 0.0, None, 0, None) == 3
+    assert L.tree_attn_fwd(None, None, None, None, None, None, 16, 4, 2, 64, 1, 0.0, None, 0, None) == 1
+    assert b"null" in L.tree_last_error()
+    assert L.tree_logprob_fwd(None, None, None, None, None, 8, 60, 512, 4, None, None, 1, None, 0, None) == 2
+    assert L.tree_rope(None, None, None, 4, 1, 1, 7, 10000.0, 1, 0, None) == 2
+    assert L.tree_attn_workspace_size(4096, 32, 8, 128, 1) > 0
+    assert L.tree_logprob_workspace_size(64, 64, 512, 0) > 0

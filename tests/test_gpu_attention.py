@@ -1,0 +1,136 @@
+"""GPU parity of tree attention (forward and backward) against the oracle."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from gpu_common import BF16_TOL, F32_TOL, assert_close, dev, host, need_cuda, tma, torch
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(m, pk, q, k, v, do, dtype, deterministic=False):
+    td = torch.bfloat16 if dtype == "bf16" else torch.float32
+    tq, tk, tv, tdo = (dev(x, td) for x in (q, k, v, do))
+    end = dev(pk["subtree_end"])
+    o, lse = m.tree_attn_fwd(tq, tk, tv, end)
+    dq, dk, dv = m.tree_attn_bwd(tq, tk, tv, o, tdo, lse, end, deterministic=deterministic)
+    m.tree_check_device_status()
+    return o, lse, dq, dk, dv
+
+
+def _full_check(seqs, Hq, Hkv, d, dtype, seed=0, deterministic=False):
+    need_cuda()
+    m = tma()
+    pk = m.tree_pack(seqs)
+    T = pk["T"]
+    bf = dtype == "bf16"
+    q = synth.normal(10 * seed + 1, (T, Hq, d), bf16=bf)
+    k = synth.normal(10 * seed + 2, (T, Hkv, d), bf16=bf)
+    v = synth.normal(10 * seed + 3, (T, Hkv, d), bf16=bf)
+    do = synth.normal(10 * seed + 4, (T, Hq, d), bf16=bf)
+    o, lse, dq, dk, dv = _run(m, pk, q, k, v, do, dtype, deterministic)
+    ref = oracle.pack_ref(seqs)
+    ro, rlse = oracle.attn_ref_fwd(q, k, v, ref["paths"])
+    rdq, rdk, rdv = oracle.attn_ref_bwd(q, k, v, do, ref["paths"])
+    tol = BF16_TOL if bf else F32_TOL
+    assert_close("O", o, ro, tol)
+    assert_close("LSE", lse, rlse, F32_TOL)
+    assert_close("dQ", dq, rdq, tol)
+    assert_close("dK", dk, rdk, tol)
+    assert_close("dV", dv, rdv, tol)
+    return m, pk, (q, k, v, do), (o, lse, dq, dk, dv)
+
+
+def test_tiny_tree_fp32():
+    t = synth.tiny_tree()
+    _full_check(t.seqs, 1, 1, 64, "f32")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_random_trees(d, dtype, seed):
+    """Galton-Watson trees of a few hundred rows: several 128-row tiles and a ragged tail."""
+    t = synth.galton_watson(seed=seed, budget=[333, 517, 700][seed], seg=(5, 90), vocab=1000)
+    _full_check(t.seqs, 4, 2, d, dtype, seed=seed)
+
+
+def test_short_prompt_agentic_full_size():
+    """The short-prompt agentic tree at full size (T = 2304, 32/8 heads, d = 128, bf16)."""
+    t = synth.agentic_short()
+    _full_check(t.seqs, 32, 8, 128, "bf16")
+
+
+@pytest.mark.parametrize("case", ["chain", "forest_of_singletons", "single_token", "two_roots"])
+def test_degenerate_trees(case):
+    rng = np.random.default_rng(5)
+    if case == "chain":
+        seqs = [rng.integers(0, 100, size=1000)]
+    elif case == "forest_of_singletons":
+        seqs = [[i] for i in range(300)]
+    elif case == "single_token":
+        seqs = [[42]]
+    else:
+        seqs = [rng.integers(0, 100, size=200), [1000] + list(rng.integers(0, 100, size=150))]
+    _full_check(seqs, 2, 1, 128, "bf16")
+
+
+def test_deterministic_flag_repeats_bitwise():
+    need_cuda()
+    t = synth.galton_watson(seed=4, budget=600, seg=(5, 90), vocab=1000)
+    m = tma()
+    pk = m.tree_pack(t.seqs)
+    q, k, v, do = synth.attention_config("agentic_short", pk["T"], seed=3)
+    r1 = _run(m, pk, q, k, v, do, "bf16", deterministic=True)
+    r2 = _run(m, pk, q, k, v, do, "bf16", deterministic=True)
+    for a, b in zip(r1, r2):
+        assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("name", ["agentic_long", "galton_watson"])
+def test_full_size_sampled(name):
+    """T = 16k workloads: sampled rows against the oracle row by row, plus the
+    identities sum_j dV_j = sum_i dO_i (per KV group) and sum_j dK_j = 0."""
+    need_cuda()
+    m = tma()
+    t = synth.CONFIGS[name]["tree"]()
+    pk = m.tree_pack(t.seqs)
+    T = pk["T"]
+    q, k, v, do = synth.attention_config(name, T)
+    o, lse, dq, dk, dv = _run(m, pk, q, k, v, do, "bf16")
+    ref = oracle.pack_ref(t.seqs)
+    rng = np.random.default_rng(11)
+    rows = np.unique(np.concatenate([[0, 1, T - 1], rng.integers(0, T, size=24)]))
+    ro, rlse = oracle.attn_ref_rows(q, k, v, ref["paths"], rows)
+    assert_close("O rows", host(o)[rows], ro, BF16_TOL)
+    assert_close("LSE rows", host(lse)[:, rows], rlse, F32_TOL)
+    assert_close("dQ rows", host(dq)[rows], oracle.attn_ref_dq_rows(q, k, v, do, ref["paths"], rows), BF16_TOL)
+    # keys with small subtrees (cheap to sum over every descendant query)
+    size = pk["subtree_end"] - np.arange(T) + 1
+    small = np.nonzero(size <= 300)[0]
+    keys = np.unique(np.concatenate([[T - 1], rng.choice(small, size=12, replace=False)]))
+    rdk, rdv = oracle.attn_ref_dkdv_rows(q, k, v, do, ref["paths"], keys)
+    assert_close("dK rows", host(dk)[keys], rdk, BF16_TOL)
+    assert_close("dV rows", host(dv)[keys], rdv, BF16_TOL)
+    g = q.shape[1] // k.shape[1]
+    sum_do = do.astype(np.float64).reshape(T, k.shape[1], g, -1).sum(axis=(0, 2))
+    assert_close("sum dV", host(dv).sum(0), sum_do, 0.5)
+    assert_close("sum dK", host(dk).sum(0), np.zeros_like(sum_do), 0.5)
+
+
+def test_bad_subtree_end_sets_device_flag():
+    """An out-of-range subtree_end is reported through the device error word;
+    the kernels never index memory with it, so nothing faults."""
+    need_cuda()
+    m = tma()
+    T = 200
+    end = np.arange(T, dtype=np.int32)
+    end[17] = T + 5
+    q = torch.zeros((T, 2, 64), dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros((T, 1, 64), dtype=torch.bfloat16, device="cuda")
+    m.tree_attn_fwd(q, k, k, dev(end))
+    with pytest.raises(m.TreeError) as ei:
+        m.tree_check_device_status()
+    assert ei.value.status == 7
+    m.tree_check_device_status()   # cleared

@@ -1,0 +1,125 @@
+"""GPU parity of depth-position RoPE and the shared-logit log-prob path."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from gpu_common import BF16_TOL, F32_TOL, assert_close, dev, host, need_cuda, tma, torch
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("name,d,dtype", [("tiny_fp32", 64, "f32"), ("agentic_short", 128, "bf16"),
+                                          ("galton_watson", 128, "bf16")])
+def test_rope(name, d, dtype):
+    need_cuda()
+    m = tma()
+    t = synth.CONFIGS[name]["tree"]()
+    pk = m.tree_pack(t.seqs)
+    ref = oracle.pack_ref(t.seqs)
+    T = pk["T"]
+    c = synth.CONFIGS[name]
+    q, k, _, _ = synth.attention_config(name, T)
+    td = torch.bfloat16 if dtype == "bf16" else torch.float32
+    tq, tk = dev(q, td), dev(k, td)
+    pos = dev(pk["position_ids"])
+    m.tree_rope(tq, tk, pos)
+    tol = BF16_TOL if dtype == "bf16" else F32_TOL
+    assert_close("rope q", tq, oracle.rope_ref(q, ref["paths"]), tol)
+    assert_close("rope k", tk, oracle.rope_ref(k, ref["paths"]), tol)
+    m.tree_rope(tq, tk, pos, inverse=True)
+    assert_close("rope^-1 q", tq, q, 2 * tol)
+    m.tree_check_device_status()
+
+
+def _lm_case(T, K, V, n_occ_rows, bf16, seed, src=None):
+    rng = np.random.default_rng(seed)
+    if src is None:
+        src = np.sort(rng.integers(0, n_occ_rows, size=3 * n_occ_rows)).astype(np.int32)
+    h, w, tg, wt = synth.lm_head_config(T, K, V, len(src), bf16=bf16, seed=seed)
+    order = np.argsort(src, kind="stable").astype(np.int32)
+    row_ptr = np.zeros(T + 1, np.int32)
+    row_ptr[1:] = np.cumsum(np.bincount(src, minlength=T))
+    return h, w, src, tg, wt, row_ptr, order
+
+
+def _run_lm(m, h, w, tg, wt, row_ptr, perm, bf16):
+    td = torch.bfloat16 if bf16 else torch.float32
+    th, tw = dev(h, td), dev(w, td)
+    lse, logp = m.tree_logprob_fwd(th, tw, dev(row_ptr), dev(perm), dev(tg))
+    g = (-wt).astype(np.float32)
+    dh, dw = m.tree_logprob_bwd(th, tw, lse, dev(row_ptr), dev(perm), dev(tg), dev(g))
+    m.tree_check_device_status()
+    return lse, logp, dh, dw, g
+
+
+def test_logprob_tiny_fp32():
+    need_cuda()
+    m = tma()
+    t = synth.tiny_tree()
+    pk = m.tree_pack(t.seqs)
+    h, w, _, _ = synth.lm_head_config(pk["T"], 64, 512, pk["n_occ"], bf16=False)
+    wt = np.ones(pk["n_occ"], np.float32)
+    lse, logp, dh, dw, g = _run_lm(m, h, w, pk["occ_targets"], wt, pk["occ_row_ptr"], pk["occ_perm"], False)
+    rl, rlse = oracle.logprob_ref_fwd(h, w, pk["occ_source_rows"], pk["occ_targets"])
+    used = np.unique(pk["occ_source_rows"])
+    assert_close("logp", logp, rl, F32_TOL)
+    assert_close("lse", host(lse)[used], rlse[used], F32_TOL)
+    rdh, rdw = oracle.logprob_ref_bwd(h, w, pk["occ_source_rows"], pk["occ_targets"], g)
+    assert_close("dH", dh, rdh, F32_TOL)
+    assert_close("dW", dw, rdw, F32_TOL)
+
+
+@pytest.mark.parametrize("T,K,V,bf16", [(200, 128, 1000, True), (333, 256, 4104, True), (130, 64, 520, False)])
+def test_logprob_random(T, K, V, bf16):
+    """Ragged row/vocabulary tails, rows without occurrences, repeated targets."""
+    need_cuda()
+    m = tma()
+    h, w, src, tg, wt, row_ptr, perm = _lm_case(T, K, V, T - 7, bf16, seed=T)
+    tg[::5] = tg[0]      # repeated targets across rows
+    tg[1] = tg[2]        # and within a row
+    lse, logp, dh, dw, g = _run_lm(m, h, w, tg, wt, row_ptr, perm, bf16)
+    rl, rlse = oracle.logprob_ref_fwd(h, w, src, tg)
+    used = np.unique(src)
+    assert_close("logp", logp, rl, F32_TOL)
+    assert_close("lse", host(lse)[used], rlse[used], F32_TOL)
+    rdh, rdw = oracle.logprob_ref_bwd(h, w, src, tg, g)
+    tol = BF16_TOL if bf16 else F32_TOL
+    assert_close("dH", dh, rdh, tol)
+    assert_close("dW", dw, rdw, tol)
+
+
+def test_logprob_full_vocab_rows():
+    """Full hidden and vocabulary sizes (4096 x 128256) on 256 rows: every output."""
+    need_cuda()
+    m = tma()
+    T, K, V = 256, 4096, 128256
+    h, w, src, tg, wt, row_ptr, perm = _lm_case(T, K, V, T, True, seed=7)
+    lse, logp, dh, dw, g = _run_lm(m, h, w, tg, wt, row_ptr, perm, True)
+    rl, rlse = oracle.logprob_ref_fwd(h, w, src, tg)
+    assert_close("logp", logp, rl, F32_TOL)
+    rdh, rdw = oracle.logprob_ref_bwd(h, w, src, tg, g)
+    assert_close("dH", dh, rdh, BF16_TOL)
+    assert_close("dW", dw, rdw, BF16_TOL)
+
+
+def test_logprob_full_size_sampled():
+    """The 8192-row tree at full size: sampled rows, and sum_v dW[k, v] = 0."""
+    need_cuda()
+    m = tma()
+    t = synth.lm_head_tree()
+    pk = m.tree_pack(t.seqs)
+    T, K, V = pk["T"], 4096, 128256
+    h, w, tg, wt = synth.lm_head_config(T, K, V, pk["n_occ"], bf16=True)
+    lse, logp, dh, dw, g = _run_lm(m, h, w, tg, wt, pk["occ_row_ptr"], pk["occ_perm"], True)
+    src = pk["occ_source_rows"]
+    rng = np.random.default_rng(3)
+    rows = rng.choice(np.unique(src), size=48, replace=False)
+    sel = np.nonzero(np.isin(src, rows))[0]
+    rl, rlse = oracle.logprob_ref_fwd(h, w, src[sel], tg[sel])
+    assert_close("logp sampled", host(logp)[sel], rl, F32_TOL)
+    assert_close("lse sampled", host(lse)[rows], rlse[rows], F32_TOL)
+    gz = oracle.logprob_ref_gz(h, w, src, tg, g, rows)
+    assert_close("dH sampled", host(dh)[rows], gz @ w.astype(np.float64).T, BF16_TOL)
+    colsum = dw.float().sum(dim=1).double().cpu().numpy()
+    assert np.abs(colsum).max() < 0.5, np.abs(colsum).max()

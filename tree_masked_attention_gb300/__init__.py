@@ -1,0 +1,248 @@
+"""Tree-packed training hot path on GB300 (sm_103a): Python binding of libtreeattn.so.
+
+Thin argument marshalling over the C ABI in include/tree_attn.h. Every step of
+the path runs in the library's CUDA kernels (or, for tree_pack, its C++ host
+code); PyTorch provides device memory and the current stream only. There is no
+CPU fallback: calls raise when the library is missing or a tensor is not on a
+CUDA device.
+
+Functions (same names as the C ABI):
+  tree_pack(seqs, seq_weights=None)                 -> dict of numpy arrays
+  tree_rope(q, k, position_ids, theta_base, inverse) -> rotates q, k in place
+  tree_attn_fwd(q, k, v, subtree_end, ...)          -> (o, lse)
+  tree_attn_bwd(q, k, v, o, dout, lse, subtree_end, ...) -> (dq, dk, dv)
+  tree_logprob_fwd(hidden, w_lm, occ_row_ptr, occ_perm, occ_targets, ...) -> (lse, logp)
+  tree_logprob_bwd(hidden, w_lm, lse, occ_row_ptr, occ_perm, occ_targets, grad_logp, ...)
+                                                    -> (d_hidden, d_w)
+"""
+from __future__ import annotations
+
+import ctypes as C
+
+import numpy as np
+
+from ._lib import PackOut, PackSizes, TreeError, check, lib
+
+__all__ = [
+    "tree_pack", "tree_validate_subtree_end", "tree_rope", "tree_attn_workspace_size",
+    "tree_attn_fwd", "tree_attn_bwd", "tree_logprob_workspace_size", "tree_logprob_fwd",
+    "tree_logprob_bwd", "tree_check_device_status", "tree_kernel_path", "tree_launch_count", "TreeError", "lib",
+    "DTYPE_F32", "DTYPE_BF16",
+]
+
+DTYPE_F32 = 0
+DTYPE_BF16 = 1
+
+_PACK_T = ("packed_ids", "position_ids", "subtree_end", "path_count", "parent_row", "node_of_token")
+_PACK_NODE = ("node_start", "node_end", "node_parent")
+_PACK_OCC = ("occ_source_rows", "occ_targets", "occ_seq", "occ_perm")
+
+
+def _ptr(a: np.ndarray, ctype):
+    return a.ctypes.data_as(C.POINTER(ctype))
+
+
+def tree_pack(seqs, seq_weights=None) -> dict:
+    """Pack host token sequences (iterables of ints) into a preorder trie.
+
+    Returns numpy arrays named as in tree_pack_out (include/tree_attn.h), plus
+    T, n_nodes, n_occ, n_roots and ``paths`` (packed rows of every sequence).
+    """
+    L = lib()
+    seqs = [np.asarray(s, dtype=np.int32).reshape(-1) for s in seqs]
+    offs = np.zeros(len(seqs) + 1, dtype=np.int64)
+    offs[1:] = np.cumsum([len(s) for s in seqs])
+    toks = np.ascontiguousarray(np.concatenate(seqs) if seqs else np.zeros(0, np.int32), dtype=np.int32)
+    plan = C.c_void_p()
+    sizes = PackSizes()
+    check(L.tree_pack_plan(_ptr(toks, C.c_int32), _ptr(offs, C.c_int64), len(seqs), C.byref(plan),
+                           C.byref(sizes)), "tree_pack_plan")
+    try:
+        T, nn, no = sizes.T, sizes.n_nodes, sizes.n_occ
+        res = {n: np.empty(T, np.int32) for n in _PACK_T}
+        res.update({n: np.empty(nn, np.int32) for n in _PACK_NODE})
+        res.update({n: np.empty(no, np.int32) for n in _PACK_OCC})
+        res["occ_weights"] = np.empty(no, np.float32)
+        res["occ_row_ptr"] = np.empty(T + 1, np.int32)
+        res["token_rows"] = np.empty(sizes.n_tokens, np.int32)
+        out = PackOut()
+        for name, _ in PackOut._fields_:
+            setattr(out, name, _ptr(res[name], C.c_float if name == "occ_weights" else C.c_int32))
+        w = None
+        if seq_weights is not None:
+            w = np.ascontiguousarray(seq_weights, dtype=np.float32)
+            if w.shape != (len(seqs),):
+                raise ValueError("seq_weights must have one entry per sequence")
+        check(L.tree_pack_emit(plan, _ptr(w, C.c_float) if w is not None else None, C.byref(out)),
+              "tree_pack_emit")
+    finally:
+        L.tree_plan_free(plan)
+    res.update(T=T, n_nodes=nn, n_occ=no, n_roots=sizes.n_roots)
+    res["paths"] = [res["token_rows"][offs[k]:offs[k + 1]] for k in range(len(seqs))]
+    return res
+
+
+def tree_validate_subtree_end(subtree_end) -> None:
+    a = np.ascontiguousarray(subtree_end, dtype=np.int32)
+    check(lib().tree_validate_subtree_end(_ptr(a, C.c_int32), a.size), "tree_validate_subtree_end")
+
+
+# ---------------------------------------------------------------- device calls
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return DTYPE_BF16
+    if t.dtype == torch.float32:
+        return DTYPE_F32
+    raise TypeError(f"unsupported dtype {t.dtype}: bfloat16 or float32")
+
+
+def _dev(t, name, dtype=None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (no CPU path exists)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return C.c_void_p(t.data_ptr())
+
+
+def _stream(t):
+    torch = _torch()
+    return C.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _workspace(nbytes, device, workspace):
+    torch = _torch()
+    if workspace is not None:
+        if workspace.numel() * workspace.element_size() < nbytes:
+            raise ValueError(f"workspace too small: {nbytes} bytes needed")
+        return workspace
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def tree_rope(q, k, position_ids, theta_base: float = 10000.0, inverse: bool = False) -> None:
+    """Rotate q [T,Hq,d] and k [T,Hkv,d] in place by depth positions (int32 [T])."""
+    torch = _torch()
+    ref = q if q is not None else k
+    T, d = ref.shape[0], ref.shape[2]
+    Hq = q.shape[1] if q is not None else 0
+    Hkv = k.shape[1] if k is not None else 0
+    check(lib().tree_rope(_dev(q, "q", ref.dtype), _dev(k, "k", ref.dtype),
+                          _dev(position_ids, "position_ids", torch.int32), T, Hq, Hkv, d,
+                          float(theta_base), _dtype_code(ref), int(bool(inverse)), _stream(ref)),
+          "tree_rope")
+
+
+def tree_attn_workspace_size(T, Hq, Hkv, d, dtype_code) -> int:
+    return int(lib().tree_attn_workspace_size(T, Hq, Hkv, d, dtype_code))
+
+
+def tree_attn_fwd(q, k, v, subtree_end, softmax_scale: float = 0.0, workspace=None, out=None, lse=None):
+    """Tree attention forward; returns (o [T,Hq,d], lse [Hq,T] fp32)."""
+    torch = _torch()
+    T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    dt = _dtype_code(q)
+    o = torch.empty_like(q) if out is None else out
+    lse = torch.empty((Hq, T), dtype=torch.float32, device=q.device) if lse is None else lse
+    nbytes = tree_attn_workspace_size(T, Hq, Hkv, d, dt)
+    ws = _workspace(nbytes, q.device, workspace)
+    check(lib().tree_attn_fwd(_dev(q, "q"), _dev(k, "k", q.dtype), _dev(v, "v", q.dtype),
+                              _dev(o, "o", q.dtype), _dev(lse, "lse", torch.float32),
+                              _dev(subtree_end, "subtree_end", torch.int32), T, Hq, Hkv, d, dt,
+                              float(softmax_scale), C.c_void_p(ws.data_ptr()),
+                              ws.numel() * ws.element_size(), _stream(q)), "tree_attn_fwd")
+    return o, lse
+
+
+def tree_attn_bwd(q, k, v, o, dout, lse, subtree_end, softmax_scale: float = 0.0,
+                  deterministic: bool = False, workspace=None, grads=None):
+    """Tree attention backward; returns (dq, dk, dv) in the input dtype."""
+    torch = _torch()
+    T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    dt = _dtype_code(q)
+    if grads is None:
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    else:
+        dq, dk, dv = grads
+    nbytes = tree_attn_workspace_size(T, Hq, Hkv, d, dt)
+    ws = _workspace(nbytes, q.device, workspace)
+    check(lib().tree_attn_bwd(_dev(q, "q"), _dev(k, "k", q.dtype), _dev(v, "v", q.dtype),
+                              _dev(o, "o", q.dtype), _dev(dout, "dout", q.dtype),
+                              _dev(lse, "lse", torch.float32), _dev(dq, "dq", q.dtype),
+                              _dev(dk, "dk", q.dtype), _dev(dv, "dv", q.dtype),
+                              _dev(subtree_end, "subtree_end", torch.int32), T, Hq, Hkv, d, dt,
+                              float(softmax_scale), int(bool(deterministic)),
+                              C.c_void_p(ws.data_ptr()), ws.numel() * ws.element_size(), _stream(q)),
+          "tree_attn_bwd")
+    return dq, dk, dv
+
+
+def tree_logprob_workspace_size(T, K_h, V, dtype_code) -> int:
+    return int(lib().tree_logprob_workspace_size(T, K_h, V, dtype_code))
+
+
+def tree_logprob_fwd(hidden, w_lm, occ_row_ptr, occ_perm, occ_targets, workspace=None, lse=None, logp=None):
+    """Shared-logit log-probs; returns (lse [T] fp32, logp [n_occ] fp32)."""
+    torch = _torch()
+    T, K = hidden.shape
+    V = w_lm.shape[1]
+    n_occ = occ_targets.shape[0]
+    dt = _dtype_code(hidden)
+    lse = torch.empty(T, dtype=torch.float32, device=hidden.device) if lse is None else lse
+    logp = torch.empty(n_occ, dtype=torch.float32, device=hidden.device) if logp is None else logp
+    ws = _workspace(tree_logprob_workspace_size(T, K, V, dt), hidden.device, workspace)
+    i32 = torch.int32
+    check(lib().tree_logprob_fwd(_dev(hidden, "hidden"), _dev(w_lm, "w_lm", hidden.dtype),
+                                 _dev(occ_row_ptr, "occ_row_ptr", i32), _dev(occ_perm, "occ_perm", i32),
+                                 _dev(occ_targets, "occ_targets", i32), T, K, V, n_occ,
+                                 _dev(lse, "lse", torch.float32), _dev(logp, "logp", torch.float32), dt,
+                                 C.c_void_p(ws.data_ptr()), ws.numel() * ws.element_size(),
+                                 _stream(hidden)), "tree_logprob_fwd")
+    return lse, logp
+
+
+def tree_logprob_bwd(hidden, w_lm, lse, occ_row_ptr, occ_perm, occ_targets, grad_logp, workspace=None,
+                     grads=None):
+    """Backward of the shared-logit log-probs; returns (d_hidden, d_w) in the input dtype."""
+    torch = _torch()
+    T, K = hidden.shape
+    V = w_lm.shape[1]
+    n_occ = occ_targets.shape[0]
+    dt = _dtype_code(hidden)
+    dh, dw = (torch.empty_like(hidden), torch.empty_like(w_lm)) if grads is None else grads
+    ws = _workspace(tree_logprob_workspace_size(T, K, V, dt), hidden.device, workspace)
+    i32 = torch.int32
+    check(lib().tree_logprob_bwd(_dev(hidden, "hidden"), _dev(w_lm, "w_lm", hidden.dtype),
+                                 _dev(lse, "lse", torch.float32), _dev(occ_row_ptr, "occ_row_ptr", i32),
+                                 _dev(occ_perm, "occ_perm", i32), _dev(occ_targets, "occ_targets", i32),
+                                 _dev(grad_logp, "grad_logp", torch.float32), T, K, V, n_occ,
+                                 _dev(dh, "d_hidden", hidden.dtype), _dev(dw, "d_w", hidden.dtype), dt,
+                                 C.c_void_p(ws.data_ptr()), ws.numel() * ws.element_size(),
+                                 _stream(hidden)), "tree_logprob_bwd")
+    return dh, dw
+
+
+def tree_check_device_status(stream=None) -> None:
+    """Synchronise and raise TreeError if a kernel flagged a range error or a timeout."""
+    torch = _torch()
+    s = torch.cuda.current_stream().cuda_stream if stream is None else stream
+    check(lib().tree_check_device_status(C.c_void_p(s)), "tree_check_device_status")
+
+
+def tree_launch_count() -> int:
+    """Kernel launches the library has enqueued in this process."""
+    return int(lib().tree_launch_count())
+
+
+def tree_kernel_path(op: int, dtype_code: int, d: int) -> int:
+    return int(lib().tree_kernel_path(op, dtype_code, d))

@@ -1,0 +1,77 @@
+// Internal interface between the C ABI and the attention kernels.
+#pragma once
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace tree {
+
+// Scratch carved out of the caller's workspace (every region 256-byte aligned).
+struct AttnWs {
+  int32_t* kmax32;   // [ceil(T/32)]  per 32-key tile: max subtree_end
+  int32_t* kmin32;   // [ceil(T/32)]  per 32-key tile: min subtree_end
+  int32_t* kmax128;  // [ceil(T/128)] per 128-key tile: max subtree_end
+  int32_t* kmin128;  // [ceil(T/128)] per 128-key tile: min subtree_end
+  float* delta;      // [Hq, T]       dO . O per query row and head
+  float* dq_acc;     // [T, Hq, d]    fp32 dQ accumulator (tensor-core backward)
+};
+
+struct AttnArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;             // forward output / backward input
+  float* lse;          // forward output / backward input, [Hq, T]
+  const void* dout;
+  void* dq;
+  void* dk;
+  void* dv;
+  const int32_t* end;  // subtree_end [T]
+  int64_t T;
+  int Hq, Hkv, d, dtype;
+  float scale;
+  int deterministic;
+  AttnWs ws;
+};
+
+// Bytes of workspace, and the carve-up of `base` when it is non-null.
+size_t attn_ws_layout(int64_t T, int Hq, int Hkv, int d, int dtype, void* base, AttnWs* ws);
+
+int tile_meta_launch(const int32_t* end, int64_t n, int tile, int32_t* kmax, int32_t* kmin,
+                     cudaStream_t st);
+int attn_fwd_simt(const AttnArgs& a, cudaStream_t st);
+int attn_bwd_simt(const AttnArgs& a, cudaStream_t st);
+
+int rope_launch(void* q, void* k, const int32_t* pos, int64_t T, int Hq, int Hkv, int d,
+                float theta_base, int dtype, int inverse, cudaStream_t st);
+
+// ---- log-prob path ----
+struct LogprobWs {
+  float* part_max;   // [n_vtiles, T] per vocabulary tile: row max of the logits
+  float* part_sum;   // [n_vtiles, T] per vocabulary tile: sum exp(z - max)
+  float* crow;       // [T]           sum of grad_logp over the row's occurrences
+  void* gz;          // [T, V]        G_z (fp32 on the SIMT path)
+};
+
+struct LogprobArgs {
+  const void* h;
+  const void* w;
+  const int32_t* row_ptr;
+  const int32_t* perm;
+  const int32_t* targets;
+  const float* grad;   // grad_logp (backward)
+  float* lse;
+  float* logp;
+  void* dh;
+  void* dw;
+  int64_t T, K, V, n_occ;
+  int dtype;
+  LogprobWs ws;
+};
+
+size_t logprob_ws_layout(int64_t T, int64_t K, int64_t V, int dtype, void* base, LogprobWs* ws);
+int logprob_fwd_simt(const LogprobArgs& a, cudaStream_t st);
+int logprob_bwd_simt(const LogprobArgs& a, cudaStream_t st);
+
+}  // namespace tree
