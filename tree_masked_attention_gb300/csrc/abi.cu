@@ -37,6 +37,7 @@ size_t attn_ws_layout(int64_t T, int Hq, int Hkv, int d, int dtype, void* base, 
   w.kmin32 = c.take<int32_t>(t32);
   w.kmax128 = c.take<int32_t>(t128);
   w.kmin128 = c.take<int32_t>(t128);
+  w.end_pad = c.take<int32_t>(t128 * 128);
   w.delta = c.take<float>(static_cast<size_t>(Hq) * T);
   w.dq_acc = c.take<float>(static_cast<size_t>(T) * Hq * d);
   if (ws) *ws = w;
@@ -116,6 +117,7 @@ extern "C" int tree_attn_fwd(const void* q, const void* k, const void* v, void* 
   a.T = T; a.Hq = Hq; a.Hkv = Hkv; a.d = d; a.dtype = dtype;
   a.scale = softmax_scale > 0.f ? softmax_scale : static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
   attn_ws_layout(T, Hq, Hkv, d, dtype, workspace, &a.ws);
+  if (attn_fwd_tc_supported(dtype, d, Hq, Hkv)) return attn_fwd_tc(a, reinterpret_cast<cudaStream_t>(stream));
   return attn_fwd_simt(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -204,8 +206,6 @@ extern "C" int tree_logprob_bwd(const void* hidden, const void* w_lm, const floa
 }
 
 extern "C" int tree_kernel_path(int op, int dtype, int d) {
-  (void)op;
-  (void)dtype;
-  (void)d;
+  if (op == 0) return attn_fwd_tc_supported(dtype, d, 2, 1) ? 1 : 0;
   return 0;
 }

@@ -13,6 +13,7 @@ struct AttnWs {
   int32_t* kmin32;   // [ceil(T/32)]  per 32-key tile: min subtree_end
   int32_t* kmax128;  // [ceil(T/128)] per 128-key tile: max subtree_end
   int32_t* kmin128;  // [ceil(T/128)] per 128-key tile: min subtree_end
+  int32_t* end_pad;  // [ceil(T/128)*128] subtree_end, -1 past T
   float* delta;      // [Hq, T]       dO . O per query row and head
   float* dq_acc;     // [T, Hq, d]    fp32 dQ accumulator (tensor-core backward)
 };
@@ -42,6 +43,11 @@ int tile_meta_launch(const int32_t* end, int64_t n, int tile, int32_t* kmax, int
                      cudaStream_t st);
 int attn_fwd_simt(const AttnArgs& a, cudaStream_t st);
 int attn_bwd_simt(const AttnArgs& a, cudaStream_t st);
+
+// tcgen05 / TMA kernels (bf16, d = 128, even GQA group)
+bool attn_fwd_tc_supported(int dtype, int d, int Hq, int Hkv);
+int tile_meta128_launch(const AttnArgs& a, cudaStream_t st);
+int attn_fwd_tc(const AttnArgs& a, cudaStream_t st);
 
 int rope_launch(void* q, void* k, const int32_t* pos, int64_t T, int Hq, int Hkv, int d,
                 float theta_base, int dtype, int inverse, cudaStream_t st);
