@@ -35,7 +35,7 @@ using namespace sm100;
 namespace tcfwd {
 
 constexpr int BM = 128, BN = 128, D = 128;
-constexpr int kThreads = 384;
+constexpr int kThreads = 320;  // 8 softmax warps, TMA warp, MMA warp
 constexpr int kWarpProducer = 8, kWarpMma = 9;
 constexpr uint32_t kSub = 128 * 128;   // 128 rows x 128 B (64 bf16): one swizzle-128 sub-tile
 constexpr uint32_t kTile = 2 * kSub;   // 128 rows x 128 bf16
@@ -202,7 +202,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       mbar_wait(&S.mma_done, 0, p.err);
     }
     __syncwarp();
-  } else {
+  } else if (warp < 8) {
     // ------------------------------------------------------------ softmax warps
     const int h = warp >> 2, q4 = warp & 3;
     const int r = q4 * 32 + lane, i = i0 + r;
