@@ -184,6 +184,26 @@ int tree_attn_fwd(const void* q, const void* k, const void* v, void* o, float* l
                   float softmax_scale, void* workspace, size_t workspace_bytes,
                   tree_stream_t stream);
 
+/*
+ * tree_attn_fwd_noalloc -- the same forward as tree_attn_fwd, for callers that
+ * cannot allocate device memory for a workspace (a framework whose pool already
+ * owns the device memory it may use, a serving loop that forbids cudaMalloc after
+ * start-up, a plugin interface with no workspace slot). The pages have no
+ * counterpart to this call; it only changes where the scratch lives.
+ *
+ * Its scratch is a fixed ~276 KB array in device memory inside the library, held
+ * on every GPU that loads the library until the process exits. T may not exceed
+ * 65536 rows (TREE_ERR_SHAPE otherwise); the other arguments and the results are
+ * those of tree_attn_fwd. All calls share the array: calls whose kernels overlap
+ * on the GPU (e.g. on two streams) race, so keep them ordered on one stream. Each
+ * call rewrites every scratch entry it reads. The first call on a device looks up
+ * the array's device address, so make it before any stream capture. No call
+ * allocates or frees device memory.
+ */
+int tree_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                          const int32_t* subtree_end, int64_t T, int Hq, int Hkv, int d,
+                          int dtype, float softmax_scale, tree_stream_t stream);
+
 int tree_attn_bwd(const void* q, const void* k, const void* v, const void* o,
                   const void* dout, const float* lse, void* dq, void* dk, void* dv,
                   const int32_t* subtree_end, int64_t T, int Hq, int Hkv, int d, int dtype,
