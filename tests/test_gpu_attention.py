@@ -56,6 +56,19 @@ def test_random_trees(d, dtype, seed):
     _full_check(t.seqs, 4, 2, d, dtype, seed=seed)
 
 
+@pytest.mark.parametrize("Hq,Hkv", [(3, 1), (8, 8), (8, 2), (6, 3)])
+def test_group_sizes(Hq, Hkv):
+    """Odd and even GQA groups, MHA: the tensor-core kernels and their fallbacks."""
+    t = synth.galton_watson(seed=9, budget=600, seg=(5, 90), vocab=1000)
+    _full_check(t.seqs, Hq, Hkv, 128, "bf16", seed=9)
+
+
+def test_deterministic_matches_default():
+    """Both backward modes agree with the oracle (and so with each other)."""
+    t = synth.galton_watson(seed=8, budget=640, seg=(5, 90), vocab=1000)
+    _full_check(t.seqs, 4, 2, 128, "bf16", seed=8, deterministic=True)
+
+
 def test_short_prompt_agentic_full_size():
     """The short-prompt agentic tree at full size (T = 2304, 32/8 heads, d = 128, bf16)."""
     t = synth.agentic_short()

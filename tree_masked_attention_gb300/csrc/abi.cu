@@ -40,6 +40,9 @@ size_t attn_ws_layout(int64_t T, int Hq, int Hkv, int d, int dtype, void* base, 
   w.end_pad = c.take<int32_t>(t128 * 128);
   w.delta = c.take<float>(static_cast<size_t>(Hq) * T);
   w.dq_acc = c.take<float>(static_cast<size_t>(T) * Hq * d);
+  const size_t t_pad = static_cast<size_t>((T + 63) / 64 * 64);
+  w.lse2_pad = c.take<float>(static_cast<size_t>(Hq) * t_pad);
+  w.delta_pad = c.take<float>(static_cast<size_t>(Hq) * t_pad);
   if (ws) *ws = w;
   return round_up(c.off, 256);
 }
@@ -144,6 +147,7 @@ extern "C" int tree_attn_bwd(const void* q, const void* k, const void* v, const 
   a.T = T; a.Hq = Hq; a.Hkv = Hkv; a.d = d; a.dtype = dtype; a.deterministic = deterministic;
   a.scale = softmax_scale > 0.f ? softmax_scale : static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
   attn_ws_layout(T, Hq, Hkv, d, dtype, workspace, &a.ws);
+  if (attn_bwd_tc_supported(dtype, d, deterministic)) return attn_bwd_tc(a, reinterpret_cast<cudaStream_t>(stream));
   return attn_bwd_simt(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -207,5 +211,6 @@ extern "C" int tree_logprob_bwd(const void* hidden, const void* w_lm, const floa
 
 extern "C" int tree_kernel_path(int op, int dtype, int d) {
   if (op == 0) return attn_fwd_tc_supported(dtype, d, 2, 1) ? 1 : 0;
+  if (op == 1) return attn_bwd_tc_supported(dtype, d, 0) ? 1 : 0;
   return 0;
 }

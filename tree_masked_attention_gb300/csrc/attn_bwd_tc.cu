@@ -1,0 +1,430 @@
+// Tree attention backward on tcgen05 tensor cores (bf16 in, fp32 accumulate, d = 128).
+//
+// Trie packing, "Same chain rule, shared computation graph", Step 3: a key collects
+// the gradients of every descendant query that sees it. With key j visible to query
+// i iff j <= i <= subtree_end[j], the queries of a 128-key tile are exactly the
+// contiguous rows [first key, max subtree_end of the tile] (every row in between lies
+// in some key's subtree), so the CTA of one key tile and one KV head walks that range
+// in 64-row query tiles, for every query head of the GQA group, and keeps dK and dV
+// in TMEM for the whole walk.
+//
+// Per step (key tile K/V resident; query tile Q_i, dO_i, LSE_i, Delta_i from a TMA ring):
+//   S^T  = K Q_i^T          (M=128 keys, N=64 queries)      -> TMEM
+//   dP^T = V dO_i^T         (M=128, N=64)                   -> TMEM
+//   P^T  = exp2(S^T scale log2e - LSE_i log2e) on visible pairs, 0 elsewhere
+//   dS^T = P^T (dP^T - Delta_i)                              (compute warps, one key row each)
+//   dV  += P^T dO_i         (A = P^T bf16 from TMEM, B = dO_i MN-major)
+//   dK  += dS^T Q_i         (A = dS^T bf16 in shared memory, B = Q_i MN-major)
+//   dQ_i^T = K^T dS^T       (M=128 dims, N=64 queries; A = K MN-major, B = dS^T MN-major)
+//   dQ_i += scale dQ_i^T    (fp32 reductions into the workspace accumulator, coalesced
+//                            along the head dimension; a final kernel converts to bf16)
+// Two compute warpgroups own alternate steps (TMEM: S/P and dP/dQ per stream, 2 x 128
+// columns, plus dV and dK, 128 each), so the tensor core works on one stream while the
+// other stream's warps run the softmax backward or drain dQ.
+//   warps 0-3, 4-7  compute streams 0 and 1; at the end warps 0-3 write dK, 4-7 dV
+//   warp 8          TMA producer;  warp 9  MMA issuer (and TMEM owner)
+#include <cmath>
+
+#include "attn_internal.h"
+#include "common.h"
+#include "device_common.cuh"
+#include "sm100.cuh"
+#include "tmap.h"
+
+namespace tree {
+using namespace sm100;
+
+namespace tcbwd {
+
+constexpr int BN = 128, BQ = 64, D = 128, NST = 3;
+constexpr int kThreads = 320;
+constexpr int kWarpProducer = 8, kWarpMma = 9;
+constexpr uint32_t kKSub = 128 * 128;          // 128 key rows x 128 B
+constexpr uint32_t kKTile = 2 * kKSub;         // K or V: 128 x 128 bf16
+constexpr uint32_t kQSub = BQ * 128;           // 64 query rows x 128 B
+constexpr uint32_t kQTile = 2 * kQSub;         // Q_i or dO_i: 64 x 128 bf16
+constexpr uint32_t kDsTile = BN * 128;         // dS^T: 128 key rows x 64 bf16
+
+struct Smem {
+  uint8_t k[kKTile];
+  uint8_t v[kKTile];
+  uint8_t q[NST][kQTile];
+  uint8_t dout[NST][kQTile];
+  uint8_t ds[2][kDsTile];
+  float lse2[NST][BQ];
+  float delta[NST][BQ];
+  uint64_t kv_full, qdo_full[NST], qdo_empty[NST], s_full[2], ds_ready[2], dq_full[2], drain_done[2], mma_done;
+  uint32_t tmem_base;
+};
+constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
+
+struct Params {
+  int T, T_pad, Hq, Hkv, n_kt;
+  float scale_log2, scale;
+  const int32_t* kmax;
+  const int32_t* endp;
+  const float* lse2;    // [Hq, T_pad] LSE * log2(e), +inf past T
+  const float* delta;   // [Hq, T_pad] dO . O, 0 past T
+  float* dq_acc;        // [T, Hq, d] fp32, zeroed by the preprocess kernel
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int* err;
+};
+
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+__device__ __forceinline__ void red_add(float* p, float v) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                   const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO, Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  if (p.err && (*reinterpret_cast<volatile int*>(p.err) & (1 << TREE_ERR_TIMEOUT))) return;
+  Smem& S = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int kt = blockIdx.x, kvh = blockIdx.y;
+  const int j0 = kt * BN;
+  const int G = p.Hq / p.Hkv;
+  const int last_row = min(p.kmax[kt], p.T - 1);
+  const int qt_lo = j0 / BQ;
+  const int nq = last_row >= j0 ? last_row / BQ - qt_lo + 1 : 0;
+  const int N = G * nq;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&S.kv_full, 1);
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(&S.qdo_full[s], 1);
+      mbar_init(&S.qdo_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&S.s_full[s], 1);
+      mbar_init(&S.ds_ready[s], 4);
+      mbar_init(&S.dq_full[s], 1);
+      mbar_init(&S.drain_done[s], 4);
+    }
+    mbar_init(&S.mma_done, 1);
+    fence_mbarrier_init();
+  }
+  if (warp == kWarpMma) tmem_alloc(&S.tmem_base, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = S.tmem_base;
+  constexpr uint32_t kColDV = 256, kColDK = 384;
+
+  if (warp == kWarpProducer) {
+    if (lane == 0 && N > 0) {
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmDO);
+      mbar_arrive_expect_tx(&S.kv_full, 2 * kKTile);
+      tma_load_3d(S.k, &tmK, &S.kv_full, 0, kvh, j0);
+      tma_load_3d(S.k + kKSub, &tmK, &S.kv_full, 64, kvh, j0);
+      tma_load_3d(S.v, &tmV, &S.kv_full, 0, kvh, j0);
+      tma_load_3d(S.v + kKSub, &tmV, &S.kv_full, 64, kvh, j0);
+      int n = 0;
+      for (; n < N; ++n) {
+        const int st = n % NST;
+        if (n >= NST && !mbar_wait(&S.qdo_empty[st], ((n / NST) - 1) & 1, p.err)) break;
+        const int h = kvh * G + n / nq;
+        const int i0 = (qt_lo + n % nq) * BQ;
+        mbar_arrive_expect_tx(&S.qdo_full[st], 2 * kQTile + 2 * BQ * 4);
+        tma_load_3d(S.q[st], &tmQ, &S.qdo_full[st], 0, h, i0);
+        tma_load_3d(S.q[st] + kQSub, &tmQ, &S.qdo_full[st], 64, h, i0);
+        tma_load_3d(S.dout[st], &tmDO, &S.qdo_full[st], 0, h, i0);
+        tma_load_3d(S.dout[st] + kQSub, &tmDO, &S.qdo_full[st], 64, h, i0);
+        bulk_load(S.lse2[st], p.lse2 + static_cast<int64_t>(h) * p.T_pad + i0, BQ * 4, &S.qdo_full[st]);
+        bulk_load(S.delta[st], p.delta + static_cast<int64_t>(h) * p.T_pad + i0, BQ * 4, &S.qdo_full[st]);
+      }
+      // no copy left in flight
+      mbar_wait(&S.kv_full, 0, p.err);
+      for (int m = (n > NST ? n - NST : 0); m < n; ++m) mbar_wait(&S.qdo_full[m % NST], (m / NST) & 1, p.err);
+    }
+  } else if (warp == kWarpMma) {
+    if (lane == 0 && N > 0) {
+      constexpr uint32_t id_s = idesc_bf16(BN, BQ, 0, 0);     // S^T, dP^T
+      constexpr uint32_t id_kv = idesc_bf16(BN, D, 0, 1);     // dV, dK (B MN-major)
+      constexpr uint32_t id_dq = idesc_bf16(D, BQ, 1, 1);     // dQ^T (A and B MN-major)
+      const uint32_t kb = smem_u32(S.k), vb = smem_u32(S.v);
+      auto issue_sdp = [&](int n) -> bool {
+        const int st = n % NST, s = n & 1;
+        if (!mbar_wait(&S.qdo_full[st], (n / NST) & 1, p.err)) return false;
+        tc_fence_after();
+        const uint32_t qb = smem_u32(S.q[st]), ob = smem_u32(S.dout[st]);
+        const uint32_t tS = tmem + s * 128, tD = tmem + s * 128 + 64;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t ka = (kk >> 2) * kKSub + (kk & 3) * 32, qa = (kk >> 2) * kQSub + (kk & 3) * 32;
+          mma_ss(tS, desc_sw128(kb + ka, 16, 1024), desc_sw128(qb + qa, 16, 1024), id_s, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t ka = (kk >> 2) * kKSub + (kk & 3) * 32, qa = (kk >> 2) * kQSub + (kk & 3) * 32;
+          mma_ss(tD, desc_sw128(vb + ka, 16, 1024), desc_sw128(ob + qa, 16, 1024), id_s, kk > 0);
+        }
+        mma_commit(&S.s_full[s]);
+        return true;
+      };
+      bool ok = mbar_wait(&S.kv_full, 0, p.err);
+      if (ok) ok = issue_sdp(0);
+      if (ok && N > 1) ok = issue_sdp(1);
+      for (int n = 0; ok && n < N; ++n) {
+        const int s = n & 1, st = n % NST;
+        if (!(ok = mbar_wait(&S.ds_ready[s], (n >> 1) & 1, p.err))) break;
+        tc_fence_after();
+        const uint32_t qb = smem_u32(S.q[st]), ob = smem_u32(S.dout[st]), db = smem_u32(S.ds[s]);
+        const uint32_t tS = tmem + s * 128, tD = tmem + s * 128 + 64;
+#pragma unroll
+        for (int kk = 0; kk < BQ / 16; ++kk)  // dV += P^T dO
+          mma_ts(tmem + kColDV, tS + kk * 8, desc_sw128(ob + kk * 2048, kQSub, 1024), id_kv,
+                 (n > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < BQ / 16; ++kk)  // dK += dS^T Q
+          mma_ss(tmem + kColDK, desc_sw128(db + kk * 32, 16, 1024), desc_sw128(qb + kk * 2048, kQSub, 1024),
+                 id_kv, (n > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&S.qdo_empty[st]);
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)  // dQ^T = K^T dS^T
+          mma_ss(tD, desc_sw128(kb + kk * 2048, kKSub, 1024), desc_sw128(db + kk * 2048, kQSub, 1024), id_dq,
+                 kk > 0);
+        mma_commit(&S.dq_full[s]);
+        if (n + 2 < N) {
+          if (!(ok = mbar_wait(&S.drain_done[s], (n >> 1) & 1, p.err))) break;
+          tc_fence_after();
+          ok = issue_sdp(n + 2);
+        }
+      }
+      mma_commit(&S.mma_done);
+      mbar_wait(&S.mma_done, 0, p.err);
+    }
+    __syncwarp();
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ compute warps
+    const int s = warp >> 2, q4 = warp & 3;
+    const int r = q4 * 32 + lane;                 // key row (S^T, dP^T, dK, dV) or head dim (dQ^T)
+    const int j = j0 + r;
+    const int ej = p.endp[j];                     // -1 past T
+    const uint32_t lanes = static_cast<uint32_t>(q4 * 32) << 16;
+    const uint32_t tS = tmem + lanes + s * 128, tD = tmem + lanes + s * 128 + 64;
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    for (int n = s; n < N; n += 2) {
+      const int st = n % NST;
+      const int h = kvh * G + n / nq;
+      const int i0 = (qt_lo + n % nq) * BQ;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&S.s_full[s], (n >> 1) & 1, p.err) &&
+                                             mbar_wait(&S.qdo_full[st], (n / NST) & 1, p.err))))
+        break;
+      tc_fence_after();
+      uint8_t* dsrow = S.ds[s] + r * 128;
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
+        uint32_t sv[32], dp[32], pk[16], dk[16];
+        tmem_ld32(tS + c * 32, sv);
+        tmem_ld32(tD + c * 32, dp);
+        tmem_ld_wait();
+#pragma unroll
+        for (int t = 0; t < 32; t += 2) {
+          float pr[2], dsv[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int col = c * 32 + t + u;
+            const int i = i0 + col;
+            const bool vis = (j <= i) && (i <= ej);
+            const float pp = vis ? exp2f(__uint_as_float(sv[t + u]) * sl2 - S.lse2[st][col]) : 0.f;
+            pr[u] = pp;
+            dsv[u] = pp * (__uint_as_float(dp[t + u]) - S.delta[st][col]);
+          }
+          pk[t / 2] = pack_bf16(pr[0], pr[1]);
+          dk[t / 2] = pack_bf16(dsv[0], dsv[1]);
+        }
+        tmem_st16(tS + c * 16, pk);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int chunk = (c * 4 + u) ^ (r & 7);
+          *reinterpret_cast<uint4*>(dsrow + chunk * 16) = make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.ds_ready[s]);
+      // drain dQ^T of this step: TMEM lane = head dimension r, column = query
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&S.dq_full[s], (n >> 1) & 1, p.err)))) break;
+      tc_fence_after();
+      float* base = p.dq_acc + static_cast<int64_t>(h) * D + r;
+      const int64_t row_stride = static_cast<int64_t>(p.Hq) * D;
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tD + c * 32, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int t = 0; t < 32; ++t) {
+          const int i = i0 + c * 32 + t;
+          if (i < p.T) red_add(base + i * row_stride, __uint_as_float(v[t]) * p.scale);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.drain_done[s]);
+    }
+    // epilogue: warps 0-3 write dK (scaled), warps 4-7 write dV, one key row per thread
+    ok = __all_sync(0xffffffffu, ok && (N == 0 || mbar_wait(&S.mma_done, 0, p.err)));
+    tc_fence_after();
+    {
+      __nv_bfloat16* out = (s == 0 ? p.dk : p.dv) + (static_cast<int64_t>(j) * p.Hkv + kvh) * D;
+      const float mul = s == 0 ? p.scale : 1.f;
+      const uint32_t tacc = tmem + lanes + (s == 0 ? kColDK : kColDV);
+      const bool have = ok && N > 0;  // warp-uniform: every lane takes part in the TMEM loads
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32], pk[16];
+        if (have) {
+          tmem_ld32(tacc + c * 32, v);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int t = 0; t < 32; ++t) v[t] = 0u;
+        }
+#pragma unroll
+        for (int t = 0; t < 32; t += 2)
+          pk[t / 2] = pack_bf16(__uint_as_float(v[t]) * mul, __uint_as_float(v[t + 1]) * mul);
+        if (j < p.T) {
+          uint4* o4 = reinterpret_cast<uint4*>(out + c * 32);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) o4[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace tcbwd
+
+// Delta = dO . O and LSE * log2(e) per (row, head), padded to T_pad with (0, +inf);
+// zeroes the fp32 dQ accumulator. One warp per (row, head), 4 dims per lane.
+__global__ void attn_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
+                                    const float* __restrict__ lse, int64_t T, int64_t T_pad, int Hq,
+                                    float* __restrict__ lse2, float* __restrict__ delta, float* __restrict__ dq_acc) {
+  const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
+  const int lane = threadIdx.x % 32;
+  if (w >= T_pad * Hq) return;
+  const int64_t i = w / Hq;
+  const int h = static_cast<int>(w % Hq);
+  float dl = 0.f, l2 = INFINITY;
+  if (i < T) {
+    const int64_t off = w * 128 + lane * 4;
+    const uint2 a = *reinterpret_cast<const uint2*>(o + off);
+    const uint2 b = *reinterpret_cast<const uint2*>(dout + off);
+    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+    const float2 a0 = __bfloat1622float2(a2[0]), a1 = __bfloat1622float2(a2[1]);
+    const float2 b0 = __bfloat1622float2(b2[0]), b1 = __bfloat1622float2(b2[1]);
+    dl = a0.x * b0.x + a0.y * b0.y + a1.x * b1.x + a1.y * b1.y;
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) dl += __shfl_xor_sync(0xffffffffu, dl, s);
+    l2 = lse[static_cast<int64_t>(h) * T + i] * 1.4426950408889634f;
+    *reinterpret_cast<float4*>(dq_acc + off) = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  if (lane == 0) {
+    lse2[static_cast<int64_t>(h) * T_pad + i] = l2;
+    delta[static_cast<int64_t>(h) * T_pad + i] = dl;
+  }
+}
+
+// dQ (bf16) from the fp32 accumulator, 4 elements per thread.
+__global__ void attn_dq_convert_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq, int64_t n4) {
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= n4) return;
+  const float4 v = reinterpret_cast<const float4*>(acc)[t];
+  uint2 u;
+  u.x = sm100::pack_bf16(v.x, v.y);
+  u.y = sm100::pack_bf16(v.z, v.w);
+  reinterpret_cast<uint2*>(dq)[t] = u;
+}
+
+static int rows_map(CUtensorMap* m, const void* base, int64_t T, int H, uint32_t rows) {
+  const uint64_t dims[3] = {128, static_cast<uint64_t>(H), static_cast<uint64_t>(T)};
+  const uint64_t strides[2] = {128 * 2, static_cast<uint64_t>(H) * 128 * 2};
+  const uint32_t box[3] = {64, 1, rows};
+  return make_tmap(m, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, dims, strides, box, true);
+}
+
+bool attn_bwd_tc_supported(int dtype, int d, int deterministic) {
+  return dtype == TREE_DTYPE_BF16 && d == 128 && deterministic == 0;
+}
+
+int attn_bwd_tc(const AttnArgs& a, cudaStream_t st) {
+  using namespace tcbwd;
+  int rc = tile_meta128_launch(a, st);
+  if (rc) return rc;
+  const int64_t T_pad = (a.T + BQ - 1) / BQ * BQ;
+  {
+    const int64_t warps = T_pad * a.Hq;
+    attn_bwd_pre_kernel<<<static_cast<unsigned>((warps * 32 + 255) / 256), 256, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout), a.lse, a.T, T_pad,
+        a.Hq, a.ws.lse2_pad, a.ws.delta_pad, a.ws.dq_acc);
+    TREE_LAUNCH_CHECK("attn_bwd_pre_kernel");
+  }
+  CUtensorMap mk, mv, mq, mdo;
+  if ((rc = rows_map(&mk, a.k, a.T, a.Hkv, 128)) || (rc = rows_map(&mv, a.v, a.T, a.Hkv, 128)) ||
+      (rc = rows_map(&mq, a.q, a.T, a.Hq, BQ)) || (rc = rows_map(&mdo, a.dout, a.T, a.Hq, BQ)))
+    return rc;
+  static bool attr_set = false;
+  if (!attr_set) {
+    TREE_CUDA_TRY(cudaFuncSetAttribute(attn_bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kSmemBytes)));
+    attr_set = true;
+  }
+  Params p{};
+  p.T = static_cast<int>(a.T);
+  p.T_pad = static_cast<int>(T_pad);
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  p.n_kt = static_cast<int>((a.T + BN - 1) / BN);
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.scale = a.scale;
+  p.kmax = a.ws.kmax128;
+  p.endp = a.ws.end_pad;
+  p.lse2 = a.ws.lse2_pad;
+  p.delta = a.ws.delta_pad;
+  p.dq_acc = a.ws.dq_acc;
+  p.dk = static_cast<__nv_bfloat16*>(a.dk);
+  p.dv = static_cast<__nv_bfloat16*>(a.dv);
+  p.err = device_error_word();
+  dim3 grid(p.n_kt, a.Hkv);
+  attn_bwd_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(mk, mv, mq, mdo, p);
+  TREE_LAUNCH_CHECK("attn_bwd_tc_kernel");
+  const int64_t n4 = a.T * a.Hq * a.d / 4;
+  attn_dq_convert_kernel<<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, st>>>(
+      a.ws.dq_acc, static_cast<__nv_bfloat16*>(a.dq), n4);
+  TREE_LAUNCH_CHECK("attn_dq_convert_kernel");
+  return TREE_OK;
+}
+
+}  // namespace tree

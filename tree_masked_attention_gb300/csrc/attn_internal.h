@@ -16,6 +16,8 @@ struct AttnWs {
   int32_t* end_pad;  // [ceil(T/128)*128] subtree_end, -1 past T
   float* delta;      // [Hq, T]       dO . O per query row and head
   float* dq_acc;     // [T, Hq, d]    fp32 dQ accumulator (tensor-core backward)
+  float* lse2_pad;   // [Hq, T_pad]   LSE * log2(e), +inf past T (T_pad = T rounded up to 64)
+  float* delta_pad;  // [Hq, T_pad]   dO . O, 0 past T
 };
 
 struct AttnArgs {
@@ -48,6 +50,8 @@ int attn_bwd_simt(const AttnArgs& a, cudaStream_t st);
 bool attn_fwd_tc_supported(int dtype, int d, int Hq, int Hkv);
 int tile_meta128_launch(const AttnArgs& a, cudaStream_t st);
 int attn_fwd_tc(const AttnArgs& a, cudaStream_t st);
+bool attn_bwd_tc_supported(int dtype, int d, int deterministic);
+int attn_bwd_tc(const AttnArgs& a, cudaStream_t st);
 
 int rope_launch(void* q, void* k, const int32_t* pos, int64_t T, int Hq, int Hkv, int d,
                 float theta_base, int dtype, int inverse, cudaStream_t st);
