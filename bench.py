@@ -48,8 +48,8 @@ BAD_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
 def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="agentic_short",
                     choices=["agentic_short", "agentic_long", "galton_watson", "tiny_fp32"])
@@ -100,53 +100,67 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+    """nvidia-smi clocks and throttle reasons, sampled every 20 ms from before the warm-up
+    until after the timed region; each line is stamped with the host time it arrived, so
+    the samples inside the timed window can be picked out (the nearest ones when the
+    window is shorter than the sampling period)."""
     FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
               "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
               "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.rows = []
+        self.thread = None
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", "--query-gpu=" + ",".join(self.FIELDS),
-                 "--format=csv,noheader,nounits", "-lms", "200"],
-                stdout=self.out, stderr=subprocess.DEVNULL)
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True, bufsize=1)
         except OSError:
             self.proc = None
+            return self
+
+        def reader():
+            for line in self.proc.stdout:
+                self.rows.append((time.perf_counter(), line.strip().split(", ")))
+        self.thread = threading.Thread(target=reader, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
         return self
 
-    def stop(self):
+    def stop(self, t0: float, t1: float):
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "samples": 0, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        self.out.flush()
-        self.out.seek(0)
-        rows = [ln.strip().split(", ") for ln in self.out.read().splitlines() if ln.strip()]
-        os.unlink(self.out.name)
+        if self.thread:
+            self.thread.join(timeout=2)
+        good = [(t, r) for t, r in self.rows if len(r) >= len(self.FIELDS)]
+        inside = [x for x in good if t0 <= x[0] <= t1 + 0.02]
+        chosen = inside
+        if not chosen and good:
+            chosen = sorted(good, key=lambda x: min(abs(x[0] - t0), abs(x[0] - t1)))[:2]
         sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
-            if len(r) < len(self.FIELDS):
-                continue
+        for _, r in chosen:
             try:
                 sm.append(float(r[1]))
                 mx.append(float(r[2]))
             except ValueError:
                 continue
-            for n, v in zip(names, r[5:9]):
+            for n, v in zip(self.NAMES, r[5:9]):
                 if v.strip().lower() == "active":
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "samples": len(sm), "reasons": sorted(reasons)}
+                "samples": len(sm), "samples_in_window": len(inside), "reasons": sorted(reasons)}
 
 
 def source_sha(*names) -> str:
@@ -244,6 +258,7 @@ def run_ours(args):
         tma.tree_rope(dq, dk, pos, inverse=True)
         if ev: ev[4].record(stream)
 
+    clocks = ClockSampler(local).start()
     for _ in range(max(args.warmup, 0)):
         flush.zero_()
         step()
@@ -252,7 +267,6 @@ def run_ours(args):
 
     K = args.steps
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
-    clocks = ClockSampler(local).start()
     barrier(world)
     torch.cuda.synchronize()
     n0 = tma.tree_launch_count()
@@ -262,9 +276,10 @@ def run_ours(args):
         step(evs[s])
     torch.cuda.synchronize()
     barrier(world)
-    wall = time.perf_counter() - w0
+    w1 = time.perf_counter()
+    wall = w1 - w0
     launches = tma.tree_launch_count() - n0
-    clk = clocks.stop()
+    clk = clocks.stop(w0, w1)
     tma.tree_check_device_status()
     op_ms = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(4)] for e in evs])  # [K, 4]
     step_ms = op_ms.sum(axis=1)
@@ -355,10 +370,10 @@ def run_ours(args):
 
 
 def kernel_sources(tma, key):
-    fam = tma.tree_kernel_path(0 if key == "attn_fwd" else 1, 1, 128)
-    if fam == 1:
-        return ["attn_tc.cu"]
-    return ["attn_simt.cu"]
+    """Source files of the kernel that a roofline entry describes."""
+    if key == "attn_fwd":
+        return ["attn_tc.cu"] if tma.tree_kernel_path(0, 1, 128) == 1 else ["attn_simt.cu"]
+    return ["attn_bwd_tc.cu"] if tma.tree_kernel_path(1, 1, 128) == 1 else ["attn_simt.cu"]
 
 
 def run_lm_head(args, dev, peaks, peak_src):

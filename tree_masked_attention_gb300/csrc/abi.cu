@@ -28,7 +28,6 @@ bool dtype_ok(int dtype) { return dtype == TREE_DTYPE_F32 || dtype == TREE_DTYPE
 }  // namespace
 
 size_t attn_ws_layout(int64_t T, int Hq, int Hkv, int d, int dtype, void* base, AttnWs* ws) {
-  (void)Hkv;
   (void)dtype;
   Carver c{static_cast<char*>(base)};
   AttnWs w{};
@@ -43,6 +42,11 @@ size_t attn_ws_layout(int64_t T, int Hq, int Hkv, int d, int dtype, void* base, 
   const size_t t_pad = static_cast<size_t>((T + 63) / 64 * 64);
   w.lse2_pad = c.take<float>(static_cast<size_t>(Hq) * t_pad);
   w.delta_pad = c.take<float>(static_cast<size_t>(Hq) * t_pad);
+  w.dk_acc = c.take<float>(static_cast<size_t>(T) * Hkv * d);
+  w.dv_acc = c.take<float>(static_cast<size_t>(T) * Hkv * d);
+  w.units = c.take<int32_t>(static_cast<size_t>(attn_bwd_max_units(T, Hkv)) * 4);
+  w.n_units = c.take<int32_t>(1);
+  w.counter = c.take<int32_t>(1);
   if (ws) *ws = w;
   return round_up(c.off, 256);
 }

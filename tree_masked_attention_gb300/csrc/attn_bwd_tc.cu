@@ -23,6 +23,7 @@
 // other stream's warps run the softmax backward or drain dQ.
 //   warps 0-3, 4-7  compute streams 0 and 1; at the end warps 0-3 write dK, 4-7 dV
 //   warp 8          TMA producer;  warp 9  MMA issuer (and TMEM owner)
+#include <algorithm>
 #include <cmath>
 
 #include "attn_internal.h"
@@ -59,15 +60,18 @@ struct Smem {
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
 
 struct Params {
-  int T, T_pad, Hq, Hkv, n_kt;
+  int T, T_pad, Hq, Hkv;
   float scale_log2, scale;
   const int32_t* kmax;
   const int32_t* endp;
   const float* lse2;    // [Hq, T_pad] LSE * log2(e), +inf past T
   const float* delta;   // [Hq, T_pad] dO . O, 0 past T
   float* dq_acc;        // [T, Hq, d] fp32, zeroed by the preprocess kernel
-  __nv_bfloat16* dk;
-  __nv_bfloat16* dv;
+  float* dk_acc;        // [T, Hkv, d] fp32 (scaled), zeroed by the preprocess kernel
+  float* dv_acc;        // [T, Hkv, d] fp32, zeroed by the preprocess kernel
+  const int4* units;    // work units {key tile, KV head, first step, end step}
+  const int* n_units;
+  int* counter;         // next unit to hand out
   int* err;
 };
 
@@ -91,20 +95,31 @@ __device__ __forceinline__ void red_add(float* p, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
 
+__device__ __forceinline__ void red_add4(float* p, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
+// Query tiles of 64 rows seen by key tile kt: [qt_lo, qt_lo + nq).
+__device__ __forceinline__ int key_tile_queries(const Params& p, int kt, int* qt_lo) {
+  const int j0 = kt * BN;
+  const int last_row = min(p.kmax[kt], p.T - 1);
+  *qt_lo = j0 / BQ;
+  return last_row >= j0 ? last_row / BQ - *qt_lo + 1 : 0;
+}
+
+// Persistent: each CTA takes work units {key tile, KV head, steps [b, e)} from a counter.
+// Step t of a key tile is query head kvh*G + t / nq and query tile qt_lo + t % nq.
+// Barrier phases run on over the CTA's whole life: g counts its steps, uit its units.
 __global__ void __launch_bounds__(kThreads, 1)
 attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO, Params p) {
   extern __shared__ uint8_t smem_raw[];
+  __shared__ int s_unit, s_abort;
   if (p.err && (*reinterpret_cast<volatile int*>(p.err) & (1 << TREE_ERR_TIMEOUT))) return;
   Smem& S = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int kt = blockIdx.x, kvh = blockIdx.y;
-  const int j0 = kt * BN;
   const int G = p.Hq / p.Hkv;
-  const int last_row = min(p.kmax[kt], p.T - 1);
-  const int qt_lo = j0 / BQ;
-  const int nq = last_row >= j0 ? last_row / BQ - qt_lo + 1 : 0;
-  const int N = G * nq;
 
   if (threadIdx.x == 0) {
     mbar_init(&S.kv_full, 1);
@@ -120,6 +135,7 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
     }
     mbar_init(&S.mma_done, 1);
     fence_mbarrier_init();
+    s_abort = 0;
   }
   if (warp == kWarpMma) tmem_alloc(&S.tmem_base, 512);
   tc_fence_before();
@@ -127,194 +143,223 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
   tc_fence_after();
   const uint32_t tmem = S.tmem_base;
   constexpr uint32_t kColDV = 256, kColDK = 384;
+  const int n_units = *p.n_units;
+  int g0 = 0, uit = 0;  // steps and units this CTA has run
 
-  if (warp == kWarpProducer) {
-    if (lane == 0 && N > 0) {
-      prefetch_tmap(&tmK);
-      prefetch_tmap(&tmV);
-      prefetch_tmap(&tmQ);
-      prefetch_tmap(&tmDO);
-      mbar_arrive_expect_tx(&S.kv_full, 2 * kKTile);
-      tma_load_3d(S.k, &tmK, &S.kv_full, 0, kvh, j0);
-      tma_load_3d(S.k + kKSub, &tmK, &S.kv_full, 64, kvh, j0);
-      tma_load_3d(S.v, &tmV, &S.kv_full, 0, kvh, j0);
-      tma_load_3d(S.v + kKSub, &tmV, &S.kv_full, 64, kvh, j0);
-      int n = 0;
-      for (; n < N; ++n) {
-        const int st = n % NST;
-        if (n >= NST && !mbar_wait(&S.qdo_empty[st], ((n / NST) - 1) & 1, p.err)) break;
-        const int h = kvh * G + n / nq;
-        const int i0 = (qt_lo + n % nq) * BQ;
-        mbar_arrive_expect_tx(&S.qdo_full[st], 2 * kQTile + 2 * BQ * 4);
-        tma_load_3d(S.q[st], &tmQ, &S.qdo_full[st], 0, h, i0);
-        tma_load_3d(S.q[st] + kQSub, &tmQ, &S.qdo_full[st], 64, h, i0);
-        tma_load_3d(S.dout[st], &tmDO, &S.qdo_full[st], 0, h, i0);
-        tma_load_3d(S.dout[st] + kQSub, &tmDO, &S.qdo_full[st], 64, h, i0);
-        bulk_load(S.lse2[st], p.lse2 + static_cast<int64_t>(h) * p.T_pad + i0, BQ * 4, &S.qdo_full[st]);
-        bulk_load(S.delta[st], p.delta + static_cast<int64_t>(h) * p.T_pad + i0, BQ * 4, &S.qdo_full[st]);
-      }
-      // no copy left in flight
-      mbar_wait(&S.kv_full, 0, p.err);
-      for (int m = (n > NST ? n - NST : 0); m < n; ++m) mbar_wait(&S.qdo_full[m % NST], (m / NST) & 1, p.err);
+  while (true) {
+    if (threadIdx.x == 0) s_unit = atomicAdd(p.counter, 1);
+    __syncthreads();
+    const int u = s_unit;
+    if (u >= n_units || s_abort) break;
+    const int4 U = p.units[u];
+    const int kt = U.x, kvh = U.y, b = U.z, L = U.w - U.z;
+    int qt_lo = 0;
+    const bool unit_ok = kt >= 0 && kt * BN < p.T && kvh >= 0 && kvh < p.Hkv && b >= 0 && L > 0;
+    const int nq = unit_ok ? key_tile_queries(p, kt, &qt_lo) : 0;
+    if (!unit_ok || U.w > G * nq) {  // a malformed unit: report it and run nothing
+      if (threadIdx.x == 0) raise_error(p.err, TREE_ERR_DEVICE_CHECK);
+      __syncthreads();
+      continue;
     }
-  } else if (warp == kWarpMma) {
-    if (lane == 0 && N > 0) {
-      constexpr uint32_t id_s = idesc_bf16(BN, BQ, 0, 0);     // S^T, dP^T
-      constexpr uint32_t id_kv = idesc_bf16(BN, D, 0, 1);     // dV, dK (B MN-major)
-      constexpr uint32_t id_dq = idesc_bf16(D, BQ, 1, 1);     // dQ^T (A and B MN-major)
-      const uint32_t kb = smem_u32(S.k), vb = smem_u32(S.v);
-      auto issue_sdp = [&](int n) -> bool {
-        const int st = n % NST, s = n & 1;
-        if (!mbar_wait(&S.qdo_full[st], (n / NST) & 1, p.err)) return false;
-        tc_fence_after();
-        const uint32_t qb = smem_u32(S.q[st]), ob = smem_u32(S.dout[st]);
-        const uint32_t tS = tmem + s * 128, tD = tmem + s * 128 + 64;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t ka = (kk >> 2) * kKSub + (kk & 3) * 32, qa = (kk >> 2) * kQSub + (kk & 3) * 32;
-          mma_ss(tS, desc_sw128(kb + ka, 16, 1024), desc_sw128(qb + qa, 16, 1024), id_s, kk > 0);
+    const int j0 = kt * BN;
+
+    if (warp == kWarpProducer) {
+      if (lane == 0) {
+        if (uit == 0) {
+          prefetch_tmap(&tmK);
+          prefetch_tmap(&tmV);
+          prefetch_tmap(&tmQ);
+          prefetch_tmap(&tmDO);
         }
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t ka = (kk >> 2) * kKSub + (kk & 3) * 32, qa = (kk >> 2) * kQSub + (kk & 3) * 32;
-          mma_ss(tD, desc_sw128(vb + ka, 16, 1024), desc_sw128(ob + qa, 16, 1024), id_s, kk > 0);
-        }
-        mma_commit(&S.s_full[s]);
-        return true;
-      };
-      bool ok = mbar_wait(&S.kv_full, 0, p.err);
-      if (ok) ok = issue_sdp(0);
-      if (ok && N > 1) ok = issue_sdp(1);
-      for (int n = 0; ok && n < N; ++n) {
-        const int s = n & 1, st = n % NST;
-        if (!(ok = mbar_wait(&S.ds_ready[s], (n >> 1) & 1, p.err))) break;
-        tc_fence_after();
-        const uint32_t qb = smem_u32(S.q[st]), ob = smem_u32(S.dout[st]), db = smem_u32(S.ds[s]);
-        const uint32_t tS = tmem + s * 128, tD = tmem + s * 128 + 64;
-#pragma unroll
-        for (int kk = 0; kk < BQ / 16; ++kk)  // dV += P^T dO
-          mma_ts(tmem + kColDV, tS + kk * 8, desc_sw128(ob + kk * 2048, kQSub, 1024), id_kv,
-                 (n > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < BQ / 16; ++kk)  // dK += dS^T Q
-          mma_ss(tmem + kColDK, desc_sw128(db + kk * 32, 16, 1024), desc_sw128(qb + kk * 2048, kQSub, 1024),
-                 id_kv, (n > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&S.qdo_empty[st]);
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)  // dQ^T = K^T dS^T
-          mma_ss(tD, desc_sw128(kb + kk * 2048, kKSub, 1024), desc_sw128(db + kk * 2048, kQSub, 1024), id_dq,
-                 kk > 0);
-        mma_commit(&S.dq_full[s]);
-        if (n + 2 < N) {
-          if (!(ok = mbar_wait(&S.drain_done[s], (n >> 1) & 1, p.err))) break;
-          tc_fence_after();
-          ok = issue_sdp(n + 2);
-        }
-      }
-      mma_commit(&S.mma_done);
-      mbar_wait(&S.mma_done, 0, p.err);
-    }
-    __syncwarp();
-  } else if (warp < 8) {
-    // ------------------------------------------------------------ compute warps
-    const int s = warp >> 2, q4 = warp & 3;
-    const int r = q4 * 32 + lane;                 // key row (S^T, dP^T, dK, dV) or head dim (dQ^T)
-    const int j = j0 + r;
-    const int ej = p.endp[j];                     // -1 past T
-    const uint32_t lanes = static_cast<uint32_t>(q4 * 32) << 16;
-    const uint32_t tS = tmem + lanes + s * 128, tD = tmem + lanes + s * 128 + 64;
-    const float sl2 = p.scale_log2;
-    bool ok = true;
-    for (int n = s; n < N; n += 2) {
-      const int st = n % NST;
-      const int h = kvh * G + n / nq;
-      const int i0 = (qt_lo + n % nq) * BQ;
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&S.s_full[s], (n >> 1) & 1, p.err) &&
-                                             mbar_wait(&S.qdo_full[st], (n / NST) & 1, p.err))))
-        break;
-      tc_fence_after();
-      uint8_t* dsrow = S.ds[s] + r * 128;
-#pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
-        uint32_t sv[32], dp[32], pk[16], dk[16];
-        tmem_ld32(tS + c * 32, sv);
-        tmem_ld32(tD + c * 32, dp);
-        tmem_ld_wait();
-#pragma unroll
-        for (int t = 0; t < 32; t += 2) {
-          float pr[2], dsv[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int col = c * 32 + t + u;
-            const int i = i0 + col;
-            const bool vis = (j <= i) && (i <= ej);
-            const float pp = vis ? exp2f(__uint_as_float(sv[t + u]) * sl2 - S.lse2[st][col]) : 0.f;
-            pr[u] = pp;
-            dsv[u] = pp * (__uint_as_float(dp[t + u]) - S.delta[st][col]);
+        mbar_arrive_expect_tx(&S.kv_full, 2 * kKTile);
+        tma_load_3d(S.k, &tmK, &S.kv_full, 0, kvh, j0);
+        tma_load_3d(S.k + kKSub, &tmK, &S.kv_full, 64, kvh, j0);
+        tma_load_3d(S.v, &tmV, &S.kv_full, 0, kvh, j0);
+        tma_load_3d(S.v + kKSub, &tmV, &S.kv_full, 64, kvh, j0);
+        for (int l = 0; l < L; ++l) {
+          const int g = g0 + l, st = g % NST, t = b + l;
+          if (g >= NST && !mbar_wait(&S.qdo_empty[st], ((g / NST) - 1) & 1, p.err)) {
+            s_abort = 1;
+            break;
           }
-          pk[t / 2] = pack_bf16(pr[0], pr[1]);
-          dk[t / 2] = pack_bf16(dsv[0], dsv[1]);
-        }
-        tmem_st16(tS + c * 16, pk);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int chunk = (c * 4 + u) ^ (r & 7);
-          *reinterpret_cast<uint4*>(dsrow + chunk * 16) = make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
+          const int h = kvh * G + t / nq;
+          const int i0 = (qt_lo + t % nq) * BQ;
+          mbar_arrive_expect_tx(&S.qdo_full[st], 2 * kQTile + 2 * BQ * 4);
+          tma_load_3d(S.q[st], &tmQ, &S.qdo_full[st], 0, h, i0);
+          tma_load_3d(S.q[st] + kQSub, &tmQ, &S.qdo_full[st], 64, h, i0);
+          tma_load_3d(S.dout[st], &tmDO, &S.qdo_full[st], 0, h, i0);
+          tma_load_3d(S.dout[st] + kQSub, &tmDO, &S.qdo_full[st], 64, h, i0);
+          bulk_load(S.lse2[st], p.lse2 + static_cast<int64_t>(h) * p.T_pad + i0, BQ * 4, &S.qdo_full[st]);
+          bulk_load(S.delta[st], p.delta + static_cast<int64_t>(h) * p.T_pad + i0, BQ * 4, &S.qdo_full[st]);
         }
       }
-      tmem_st_wait();
-      tc_fence_before();
-      fence_proxy_async_smem();
+    } else if (warp == kWarpMma) {
+      if (lane == 0) {
+        constexpr uint32_t id_s = idesc_bf16(BN, BQ, 0, 0);  // S^T, dP^T
+        constexpr uint32_t id_kv = idesc_bf16(BN, D, 0, 1);  // dV, dK (B MN-major)
+        constexpr uint32_t id_dq = idesc_bf16(D, BQ, 1, 1);  // dQ^T (A and B MN-major)
+        const uint32_t kb = smem_u32(S.k), vb = smem_u32(S.v);
+        auto issue_sdp = [&](int g) -> bool {
+          const int st = g % NST, s = g & 1;
+          if (!mbar_wait(&S.qdo_full[st], (g / NST) & 1, p.err)) return false;
+          tc_fence_after();
+          const uint32_t qb = smem_u32(S.q[st]), ob = smem_u32(S.dout[st]);
+          const uint32_t tS = tmem + s * 128, tD = tmem + s * 128 + 64;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t ka = (kk >> 2) * kKSub + (kk & 3) * 32, qa = (kk >> 2) * kQSub + (kk & 3) * 32;
+            mma_ss(tS, desc_sw128(kb + ka, 16, 1024), desc_sw128(qb + qa, 16, 1024), id_s, kk > 0);
+          }
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t ka = (kk >> 2) * kKSub + (kk & 3) * 32, qa = (kk >> 2) * kQSub + (kk & 3) * 32;
+            mma_ss(tD, desc_sw128(vb + ka, 16, 1024), desc_sw128(ob + qa, 16, 1024), id_s, kk > 0);
+          }
+          mma_commit(&S.s_full[s]);
+          return true;
+        };
+        bool ok = mbar_wait(&S.kv_full, uit & 1, p.err) && issue_sdp(g0);
+        for (int l = 0; ok && l < L; ++l) {
+          const int g = g0 + l, s = g & 1, st = g % NST;
+          if (l + 1 < L) {
+            // next step's S/dP go to the other stream, whose dQ^T of step g-1 must be drained
+            if (l >= 1 && !(ok = mbar_wait(&S.drain_done[s ^ 1], ((g - 1) >> 1) & 1, p.err))) break;
+            tc_fence_after();
+            if (!(ok = issue_sdp(g + 1))) break;
+          }
+          if (!(ok = mbar_wait(&S.ds_ready[s], (g >> 1) & 1, p.err))) break;
+          tc_fence_after();
+          const uint32_t qb = smem_u32(S.q[st]), ob = smem_u32(S.dout[st]), db = smem_u32(S.ds[s]);
+          const uint32_t tS = tmem + s * 128, tD = tmem + s * 128 + 64;
+#pragma unroll
+          for (int kk = 0; kk < BQ / 16; ++kk)  // dV += P^T dO
+            mma_ts(tmem + kColDV, tS + kk * 8, desc_sw128(ob + kk * 2048, kQSub, 1024), id_kv,
+                   (l > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+          for (int kk = 0; kk < BQ / 16; ++kk)  // dK += dS^T Q
+            mma_ss(tmem + kColDK, desc_sw128(db + kk * 32, 16, 1024), desc_sw128(qb + kk * 2048, kQSub, 1024),
+                   id_kv, (l > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&S.qdo_empty[st]);
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)  // dQ^T = K^T dS^T
+            mma_ss(tD, desc_sw128(kb + kk * 2048, kKSub, 1024), desc_sw128(db + kk * 2048, kQSub, 1024), id_dq,
+                   kk > 0);
+          mma_commit(&S.dq_full[s]);
+        }
+        if (!ok) s_abort = 1;
+        mma_commit(&S.mma_done);
+      }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&S.ds_ready[s]);
-      // drain dQ^T of this step: TMEM lane = head dimension r, column = query
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&S.dq_full[s], (n >> 1) & 1, p.err)))) break;
-      tc_fence_after();
-      float* base = p.dq_acc + static_cast<int64_t>(h) * D + r;
-      const int64_t row_stride = static_cast<int64_t>(p.Hq) * D;
+    } else if (warp < 8) {
+      // ---------------------------------------------------------- compute warps
+      const int s = warp >> 2, q4 = warp & 3;
+      const int r = q4 * 32 + lane;  // key row (S^T, dP^T, dK, dV) or head dim (dQ^T)
+      const int j = j0 + r;
+      const int ej = p.endp[j];      // -1 past T
+      const uint32_t lanes = static_cast<uint32_t>(q4 * 32) << 16;
+      const uint32_t tS = tmem + lanes + s * 128, tD = tmem + lanes + s * 128 + 64;
+      const float sl2 = p.scale_log2;
+      bool ok = true;
+      for (int l = ((g0 & 1) == s) ? 0 : 1; l < L; l += 2) {
+        const int g = g0 + l, st = g % NST, t = b + l;
+        const int h = kvh * G + t / nq;
+        const int i0 = (qt_lo + t % nq) * BQ;
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&S.s_full[s], (g >> 1) & 1, p.err) &&
+                                               mbar_wait(&S.qdo_full[st], (g / NST) & 1, p.err))))
+          break;
+        tc_fence_after();
+        uint8_t* dsrow = S.ds[s] + r * 128;
 #pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tD + c * 32, v);
+        for (int c = 0; c < 2; ++c) {
+          uint32_t sv[32], dp[32], pk[16], dk[16];
+          tmem_ld32(tS + c * 32, sv);
+          tmem_ld32(tD + c * 32, dp);
+          tmem_ld_wait();
+#pragma unroll
+          for (int t2 = 0; t2 < 32; t2 += 2) {
+            float pr[2], dsv[2];
+#pragma unroll
+            for (int w = 0; w < 2; ++w) {
+              const int col = c * 32 + t2 + w;
+              const int i = i0 + col;
+              const bool vis = (j <= i) && (i <= ej);
+              const float pp = vis ? exp2f(__uint_as_float(sv[t2 + w]) * sl2 - S.lse2[st][col]) : 0.f;
+              pr[w] = pp;
+              dsv[w] = pp * (__uint_as_float(dp[t2 + w]) - S.delta[st][col]);
+            }
+            pk[t2 / 2] = pack_bf16(pr[0], pr[1]);
+            dk[t2 / 2] = pack_bf16(dsv[0], dsv[1]);
+          }
+          tmem_st16(tS + c * 16, pk);
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            const int chunk = (c * 4 + w) ^ (r & 7);
+            *reinterpret_cast<uint4*>(dsrow + chunk * 16) = make_uint4(dk[4 * w], dk[4 * w + 1], dk[4 * w + 2], dk[4 * w + 3]);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.ds_ready[s]);
+        // dQ^T of this step: TMEM lane = head dimension r, column = query. Free the
+        // columns as soon as they are in registers, then reduce into the accumulator.
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&S.dq_full[s], (g >> 1) & 1, p.err)))) break;
+        tc_fence_after();
+        uint32_t v0[32], v1[32];
+        tmem_ld32(tD, v0);
+        tmem_ld32(tD + 32, v1);
         tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.drain_done[s]);
+        float* base = p.dq_acc + static_cast<int64_t>(h) * D + r;
+        const int64_t row_stride = static_cast<int64_t>(p.Hq) * D;
+        const int n_rows = min(BQ, p.T - i0);
 #pragma unroll
-        for (int t = 0; t < 32; ++t) {
-          const int i = i0 + c * 32 + t;
-          if (i < p.T) red_add(base + i * row_stride, __uint_as_float(v[t]) * p.scale);
-        }
+        for (int t2 = 0; t2 < 32; ++t2)
+          if (t2 < n_rows) red_add(base + (i0 + t2) * row_stride, __uint_as_float(v0[t2]) * p.scale);
+#pragma unroll
+        for (int t2 = 0; t2 < 32; ++t2)
+          if (32 + t2 < n_rows) red_add(base + (i0 + 32 + t2) * row_stride, __uint_as_float(v1[t2]) * p.scale);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.drain_done[s]);
-    }
-    // epilogue: warps 0-3 write dK (scaled), warps 4-7 write dV, one key row per thread
-    ok = __all_sync(0xffffffffu, ok && (N == 0 || mbar_wait(&S.mma_done, 0, p.err)));
-    tc_fence_after();
-    {
-      __nv_bfloat16* out = (s == 0 ? p.dk : p.dv) + (static_cast<int64_t>(j) * p.Hkv + kvh) * D;
-      const float mul = s == 0 ? p.scale : 1.f;
-      const uint32_t tacc = tmem + lanes + (s == 0 ? kColDK : kColDV);
-      const bool have = ok && N > 0;  // warp-uniform: every lane takes part in the TMEM loads
+      // unit epilogue: warps 0-3 add scale * dK, warps 4-7 add dV (one key row per thread)
+      ok = __all_sync(0xffffffffu, ok && mbar_wait(&S.mma_done, uit & 1, p.err));
+      tc_fence_after();
+      if (ok) {
+        float* acc = (s == 0 ? p.dk_acc : p.dv_acc) + (static_cast<int64_t>(j) * p.Hkv + kvh) * D;
+        const float mul = s == 0 ? p.scale : 1.f;
+        const uint32_t tacc = tmem + lanes + (s == 0 ? kColDK : kColDV);
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32], pk[16];
-        if (have) {
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
           tmem_ld32(tacc + c * 32, v);
           tmem_ld_wait();
-        } else {
+          if (j < p.T) {
 #pragma unroll
-          for (int t = 0; t < 32; ++t) v[t] = 0u;
+            for (int w = 0; w < 8; ++w)
+              red_add4(acc + c * 32 + 4 * w, __uint_as_float(v[4 * w]) * mul, __uint_as_float(v[4 * w + 1]) * mul,
+                       __uint_as_float(v[4 * w + 2]) * mul, __uint_as_float(v[4 * w + 3]) * mul);
+          }
         }
-#pragma unroll
-        for (int t = 0; t < 32; t += 2)
-          pk[t / 2] = pack_bf16(__uint_as_float(v[t]) * mul, __uint_as_float(v[t + 1]) * mul);
-        if (j < p.T) {
-          uint4* o4 = reinterpret_cast<uint4*>(out + c * 32);
-#pragma unroll
-          for (int u = 0; u < 4; ++u) o4[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-        }
+      } else {
+        s_abort = 1;
       }
     }
+    g0 += L;
+    ++uit;
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  }
+  // On an early exit, leave no TMA copy or MMA in flight.
+  if (s_abort && threadIdx.x == kWarpProducer * 32) {
+    mbar_wait(&S.kv_full, (uit - 1) & 1, p.err);
+    for (int g = (g0 > NST ? g0 - NST : 0); g < g0; ++g) mbar_wait(&S.qdo_full[g % NST], (g / NST) & 1, p.err);
+  }
+  if (s_abort && threadIdx.x == kWarpMma * 32) {
+    mma_commit(&S.mma_done);
+    mbar_wait(&S.mma_done, uit & 1, p.err);
   }
   tc_fence_before();
   __syncthreads();
@@ -324,13 +369,79 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
   }
 }
 
+// Builds the work units: every key tile's steps (G query heads x its query tiles) cut
+// into chunks of at most `chunk` steps, for every KV head; the chunk size grows with the
+// total work so that there are at most about 4096 + Hkv * n_kt units. One block.
+__global__ void attn_bwd_plan_kernel(const int32_t* __restrict__ kmax, int n_kt, int T, int G, int Hkv,
+                                     int max_units, int4* __restrict__ units, int* __restrict__ n_units,
+                                     int* __restrict__ counter) {
+  __shared__ long long s_total;
+  __shared__ int s_carry;
+  __shared__ int warp_sums[32];
+  if (threadIdx.x == 0) {
+    s_total = 0;
+    s_carry = 0;
+    *counter = 0;
+  }
+  __syncthreads();
+  auto steps_of = [&](int kt) -> int {
+    const int j0 = kt * BN;
+    const int last_row = min(kmax[kt], T - 1);
+    const int lo = j0 / BQ;
+    return last_row >= j0 ? G * (last_row / BQ - lo + 1) : 0;
+  };
+  long long local = 0;
+  for (int kt = threadIdx.x; kt < n_kt; kt += blockDim.x) local += steps_of(kt);
+  atomicAdd(reinterpret_cast<unsigned long long*>(&s_total), static_cast<unsigned long long>(local));
+  __syncthreads();
+  const long long per_head_total = s_total;
+  const int chunk = static_cast<int>(max(32LL, (per_head_total * Hkv + 4095) / 4096));
+  // exclusive scan of chunk counts over key tiles, blockDim.x tiles at a time
+  const int lane = threadIdx.x % 32, wid = threadIdx.x / 32, nw = blockDim.x / 32;
+  for (int base = 0; base < n_kt; base += blockDim.x) {
+    const int kt = base + threadIdx.x;
+    const int st = kt < n_kt ? steps_of(kt) : 0;
+    const int c = (st + chunk - 1) / chunk;
+    int x = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sums[wid] = x;
+    __syncthreads();
+    if (wid == 0) {
+      int w = lane < nw ? warp_sums[lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
+      }
+      if (lane < nw) warp_sums[lane] = w;
+    }
+    __syncthreads();
+    const int incl = x + (wid > 0 ? warp_sums[wid - 1] : 0) + s_carry;
+    const int first = incl - c;
+    for (int q = 0; q < c; ++q)
+      for (int kvh = 0; kvh < Hkv; ++kvh) {
+        const int idx = (first + q) * Hkv + kvh;
+        if (idx < max_units) units[idx] = make_int4(kt, kvh, q * chunk, min((q + 1) * chunk, st));
+      }
+    __syncthreads();
+    if (threadIdx.x == blockDim.x - 1) s_carry = incl;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *n_units = min(s_carry * Hkv, max_units);
+}
+
 }  // namespace tcbwd
 
 // Delta = dO . O and LSE * log2(e) per (row, head), padded to T_pad with (0, +inf);
-// zeroes the fp32 dQ accumulator. One warp per (row, head), 4 dims per lane.
+// zeroes the fp32 dQ, dK and dV accumulators. One warp per (row, head), 4 dims per lane.
 __global__ void attn_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
-                                    const float* __restrict__ lse, int64_t T, int64_t T_pad, int Hq,
-                                    float* __restrict__ lse2, float* __restrict__ delta, float* __restrict__ dq_acc) {
+                                    const float* __restrict__ lse, int64_t T, int64_t T_pad, int Hq, int Hkv,
+                                    float* __restrict__ lse2, float* __restrict__ delta, float* __restrict__ dq_acc,
+                                    float* __restrict__ dk_acc, float* __restrict__ dv_acc) {
   const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
   const int lane = threadIdx.x % 32;
   if (w >= T_pad * Hq) return;
@@ -349,7 +460,13 @@ __global__ void attn_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o, const _
 #pragma unroll
     for (int s = 16; s > 0; s >>= 1) dl += __shfl_xor_sync(0xffffffffu, dl, s);
     l2 = lse[static_cast<int64_t>(h) * T + i] * 1.4426950408889634f;
-    *reinterpret_cast<float4*>(dq_acc + off) = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    *reinterpret_cast<float4*>(dq_acc + off) = z;
+    if (h < Hkv) {
+      const int64_t kv = (i * Hkv + h) * 128 + lane * 4;
+      *reinterpret_cast<float4*>(dk_acc + kv) = z;
+      *reinterpret_cast<float4*>(dv_acc + kv) = z;
+    }
   }
   if (lane == 0) {
     lse2[static_cast<int64_t>(h) * T_pad + i] = l2;
@@ -357,15 +474,15 @@ __global__ void attn_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o, const _
   }
 }
 
-// dQ (bf16) from the fp32 accumulator, 4 elements per thread.
-__global__ void attn_dq_convert_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq, int64_t n4) {
+// bf16 from an fp32 accumulator, 4 elements per thread.
+__global__ void attn_f32_to_bf16_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ out, int64_t n4) {
   const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (t >= n4) return;
   const float4 v = reinterpret_cast<const float4*>(acc)[t];
   uint2 u;
   u.x = sm100::pack_bf16(v.x, v.y);
   u.y = sm100::pack_bf16(v.z, v.w);
-  reinterpret_cast<uint2*>(dq)[t] = u;
+  reinterpret_cast<uint2*>(out)[t] = u;
 }
 
 static int rows_map(CUtensorMap* m, const void* base, int64_t T, int H, uint32_t rows) {
@@ -379,16 +496,34 @@ bool attn_bwd_tc_supported(int dtype, int d, int deterministic) {
   return dtype == TREE_DTYPE_BF16 && d == 128 && deterministic == 0;
 }
 
+int64_t attn_bwd_max_units(int64_t T, int Hkv) { return 4096 + static_cast<int64_t>(Hkv) * ((T + 127) / 128) + 64; }
+
+static int sm_count(int* n) {
+  static int cached[128] = {0};
+  int dev = 0;
+  TREE_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 128) return fail(TREE_ERR_CUDA, "device ordinal %d out of range", dev);
+  if (!cached[dev]) TREE_CUDA_TRY(cudaDeviceGetAttribute(&cached[dev], cudaDevAttrMultiProcessorCount, dev));
+  *n = cached[dev];
+  return TREE_OK;
+}
+
 int attn_bwd_tc(const AttnArgs& a, cudaStream_t st) {
   using namespace tcbwd;
   int rc = tile_meta128_launch(a, st);
   if (rc) return rc;
   const int64_t T_pad = (a.T + BQ - 1) / BQ * BQ;
+  const int n_kt = static_cast<int>((a.T + BN - 1) / BN);
+  const int max_units = static_cast<int>(attn_bwd_max_units(a.T, a.Hkv));
+  attn_bwd_plan_kernel<<<1, 1024, 0, st>>>(a.ws.kmax128, n_kt, static_cast<int>(a.T), a.Hq / a.Hkv, a.Hkv,
+                                           max_units, reinterpret_cast<int4*>(a.ws.units), a.ws.n_units,
+                                           a.ws.counter);
+  TREE_LAUNCH_CHECK("attn_bwd_plan_kernel");
   {
     const int64_t warps = T_pad * a.Hq;
     attn_bwd_pre_kernel<<<static_cast<unsigned>((warps * 32 + 255) / 256), 256, 0, st>>>(
         static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout), a.lse, a.T, T_pad,
-        a.Hq, a.ws.lse2_pad, a.ws.delta_pad, a.ws.dq_acc);
+        a.Hq, a.Hkv, a.ws.lse2_pad, a.ws.delta_pad, a.ws.dq_acc, a.ws.dk_acc, a.ws.dv_acc);
     TREE_LAUNCH_CHECK("attn_bwd_pre_kernel");
   }
   CUtensorMap mk, mv, mq, mdo;
@@ -401,12 +536,13 @@ int attn_bwd_tc(const AttnArgs& a, cudaStream_t st) {
                                        static_cast<int>(kSmemBytes)));
     attr_set = true;
   }
+  int n_sm = 0;
+  if ((rc = sm_count(&n_sm))) return rc;
   Params p{};
   p.T = static_cast<int>(a.T);
   p.T_pad = static_cast<int>(T_pad);
   p.Hq = a.Hq;
   p.Hkv = a.Hkv;
-  p.n_kt = static_cast<int>((a.T + BN - 1) / BN);
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.scale = a.scale;
   p.kmax = a.ws.kmax128;
@@ -414,17 +550,25 @@ int attn_bwd_tc(const AttnArgs& a, cudaStream_t st) {
   p.lse2 = a.ws.lse2_pad;
   p.delta = a.ws.delta_pad;
   p.dq_acc = a.ws.dq_acc;
-  p.dk = static_cast<__nv_bfloat16*>(a.dk);
-  p.dv = static_cast<__nv_bfloat16*>(a.dv);
+  p.dk_acc = a.ws.dk_acc;
+  p.dv_acc = a.ws.dv_acc;
+  p.units = reinterpret_cast<const int4*>(a.ws.units);
+  p.n_units = a.ws.n_units;
+  p.counter = a.ws.counter;
   p.err = device_error_word();
-  dim3 grid(p.n_kt, a.Hkv);
+  const int grid = static_cast<int>(std::min<int64_t>(n_sm, max_units));
   attn_bwd_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(mk, mv, mq, mdo, p);
   TREE_LAUNCH_CHECK("attn_bwd_tc_kernel");
-  const int64_t n4 = a.T * a.Hq * a.d / 4;
-  attn_dq_convert_kernel<<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, st>>>(
-      a.ws.dq_acc, static_cast<__nv_bfloat16*>(a.dq), n4);
-  TREE_LAUNCH_CHECK("attn_dq_convert_kernel");
-  return TREE_OK;
+  auto convert = [&](const float* src, void* dst, int64_t n) -> int {
+    const int64_t n4 = n / 4;
+    attn_f32_to_bf16_kernel<<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, st>>>(
+        src, static_cast<__nv_bfloat16*>(dst), n4);
+    TREE_LAUNCH_CHECK("attn_f32_to_bf16_kernel");
+    return TREE_OK;
+  };
+  if ((rc = convert(a.ws.dq_acc, a.dq, a.T * a.Hq * a.d))) return rc;
+  if ((rc = convert(a.ws.dk_acc, a.dk, a.T * a.Hkv * a.d))) return rc;
+  return convert(a.ws.dv_acc, a.dv, a.T * a.Hkv * a.d);
 }
 
 }  // namespace tree

@@ -18,6 +18,11 @@ struct AttnWs {
   float* dq_acc;     // [T, Hq, d]    fp32 dQ accumulator (tensor-core backward)
   float* lse2_pad;   // [Hq, T_pad]   LSE * log2(e), +inf past T (T_pad = T rounded up to 64)
   float* delta_pad;  // [Hq, T_pad]   dO . O, 0 past T
+  float* dk_acc;     // [T, Hkv, d]   fp32 dK accumulator (tensor-core backward)
+  float* dv_acc;     // [T, Hkv, d]   fp32 dV accumulator
+  int32_t* units;    // [max_units * 4] backward work units {key tile, KV head, first step, end step}
+  int32_t* n_units;  // [1]
+  int32_t* counter;  // [1] next unit to hand out
 };
 
 struct AttnArgs {
@@ -51,6 +56,7 @@ bool attn_fwd_tc_supported(int dtype, int d, int Hq, int Hkv);
 int tile_meta128_launch(const AttnArgs& a, cudaStream_t st);
 int attn_fwd_tc(const AttnArgs& a, cudaStream_t st);
 bool attn_bwd_tc_supported(int dtype, int d, int deterministic);
+int64_t attn_bwd_max_units(int64_t T, int Hkv);
 int attn_bwd_tc(const AttnArgs& a, cudaStream_t st);
 
 int rope_launch(void* q, void* k, const int32_t* pos, int64_t T, int Hq, int Hkv, int d,
