@@ -188,6 +188,7 @@ extern "C" int tree_logprob_fwd(const void* hidden, const void* w_lm, const int3
   a.h = hidden; a.w = w_lm; a.row_ptr = occ_row_ptr; a.perm = occ_perm; a.targets = occ_targets;
   a.lse = lse; a.logp = logp; a.T = T; a.K = K_h; a.V = V; a.n_occ = n_occ; a.dtype = dtype;
   logprob_ws_layout(T, K_h, V, dtype, workspace, &a.ws);
+  if (logprob_tc_supported(dtype)) return logprob_fwd_tc(a, reinterpret_cast<cudaStream_t>(stream));
   return logprob_fwd_simt(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -210,11 +211,13 @@ extern "C" int tree_logprob_bwd(const void* hidden, const void* w_lm, const floa
   a.grad = grad_logp; a.lse = const_cast<float*>(lse); a.dh = d_hidden; a.dw = d_w;
   a.T = T; a.K = K_h; a.V = V; a.n_occ = n_occ; a.dtype = dtype;
   logprob_ws_layout(T, K_h, V, dtype, workspace, &a.ws);
+  if (logprob_tc_supported(dtype)) return logprob_bwd_tc(a, reinterpret_cast<cudaStream_t>(stream));
   return logprob_bwd_simt(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" int tree_kernel_path(int op, int dtype, int d) {
   if (op == 0) return attn_fwd_tc_supported(dtype, d, 2, 1) ? 1 : 0;
   if (op == 1) return attn_bwd_tc_supported(dtype, d, 0) ? 1 : 0;
+  if (op == 2 || op == 3) return logprob_tc_supported(dtype) ? 1 : 0;
   return 0;
 }

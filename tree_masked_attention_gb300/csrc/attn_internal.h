@@ -89,5 +89,8 @@ struct LogprobArgs {
 size_t logprob_ws_layout(int64_t T, int64_t K, int64_t V, int dtype, void* base, LogprobWs* ws);
 int logprob_fwd_simt(const LogprobArgs& a, cudaStream_t st);
 int logprob_bwd_simt(const LogprobArgs& a, cudaStream_t st);
+bool logprob_tc_supported(int dtype);
+int logprob_fwd_tc(const LogprobArgs& a, cudaStream_t st);
+int logprob_bwd_tc(const LogprobArgs& a, cudaStream_t st);
 
 }  // namespace tree

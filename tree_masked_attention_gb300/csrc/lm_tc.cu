@@ -1,0 +1,493 @@
+// Shared-logit log-probs on tcgen05 tensor cores (bf16 in, fp32 accumulate).
+//
+// Trie packing (agillm.io), "Share logits, preserve every prediction": z_r = h_r W_LM
+// for every packed row; each original prediction (occurrence) reads the log-softmax of
+// its source row at its target; "The training-loop change is small": gathering the
+// target log-probs avoids materialising the logits. "Same chain rule, shared
+// computation graph", Step 1: G_z = p - e_y per occurrence, summed at shared rows. With
+// g_o = dL/dlogp_o and c_r = sum of g_o over row r's occurrences:
+//   G_z[r, v] = -c_r softmax(z_r)_v + sum_{o at r, y_o = v} g_o,
+//   dH = G_z W^T,   dW = H^T G_z.
+//
+// One persistent GEMM kernel (output tiles 128 x 256, K blocks of 64, four-stage TMA
+// ring, two TMEM accumulators so the epilogue of one tile overlaps the MMAs of the next)
+// runs four products:
+//   z (forward)   A = H (K-major), B = W (MN-major); epilogue: per-row max and sum of exp
+//                 of the tile (online over 32-column chunks) and the target logits of the
+//                 row's occurrences that fall in the tile (logits never reach memory);
+//   z (backward)  same operands; epilogue writes G_z (bf16) to the workspace;
+//   dH            A = G_z (K-major), B = W (K-major: rows of W are the N index);
+//   dW            A = H^T (MN-major view of H), B = G_z (MN-major).
+// Warps: 0 TMA, 1 MMA (and TMEM owner), 2-5 epilogue (one accumulator row per thread).
+#include <algorithm>
+#include <cmath>
+
+#include "attn_internal.h"
+#include "common.h"
+#include "device_common.cuh"
+#include "sm100.cuh"
+#include "tmap.h"
+
+namespace tree {
+using namespace sm100;
+
+namespace lmtc {
+
+constexpr int BM = 128, BN = 256, BK = 64, NST = 4;
+constexpr int kThreads = 192;
+constexpr uint32_t kABytes = BM * BK * 2;  // 16 KB
+constexpr uint32_t kBBytes = BN * BK * 2;  // 32 KB
+
+enum Epi { EPI_LSE = 0, EPI_GZ = 1, EPI_STORE = 2 };
+
+struct Smem {
+  uint8_t a[NST][kABytes];
+  uint8_t b[NST][kBBytes];
+  uint64_t full[NST], empty[NST], acc_full[2], acc_empty[2];
+  uint32_t tmem_base;
+};
+constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
+
+struct Params {
+  int M, N, K;
+  int a_mn, b_mn;        // operand majorness (1 = MN-major)
+  int raster_m_fast;     // tile t -> (t % n_mb, t / n_mb) when 1, else (t / n_nb, t % n_nb)
+  int epi;
+  // EPI_LSE / EPI_GZ
+  const int32_t* row_ptr;
+  const int32_t* perm;
+  const int32_t* targets;
+  int n_occ;
+  float* part_max;       // [n_nb, M]
+  float* part_sum;
+  float* logp;           // EPI_LSE: target logits
+  const float* lse;      // EPI_GZ
+  const float* crow;
+  const float* grad;
+  __nv_bfloat16* out;    // EPI_GZ: G_z [M, N]; EPI_STORE: C [M, N]
+  int* err;
+};
+
+__device__ __forceinline__ uint32_t tmem_ld1(uint32_t taddr) {
+  uint32_t v;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(v) : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+  return v;
+}
+
+// Loads the A and B blocks of k-block kb of tile (mb, nb) into stage buffers.
+__device__ __forceinline__ void load_stage(const Params& p, const CUtensorMap* ta, const CUtensorMap* tb,
+                                           uint8_t* a, uint8_t* b, uint64_t* bar, int mb, int nb, int kb) {
+  const int k0 = kb * BK;
+  if (!p.a_mn) {
+    tma_load_2d(a, ta, bar, k0, mb * BM);                       // box {64 K, 128 M}
+  } else {
+    tma_load_2d(a, ta, bar, mb * BM, k0);                       // box {64 M, 64 K}, twice
+    tma_load_2d(a + kABytes / 2, ta, bar, mb * BM + 64, k0);
+  }
+  if (!p.b_mn) {
+    tma_load_2d(b, tb, bar, k0, nb * BN);                       // box {64 K, 256 N}
+  } else {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) tma_load_2d(b + q * (kBBytes / 4), tb, bar, nb * BN + 64 * q, k0);
+  }
+}
+
+__device__ __forceinline__ void tile_coords(const Params& p, int t, int n_mb, int n_nb, int* mb, int* nb) {
+  if (p.raster_m_fast) {
+    *mb = t % n_mb;
+    *nb = t / n_mb;
+  } else {
+    *mb = t / n_nb;
+    *nb = t % n_nb;
+  }
+}
+
+// Occurrence range of row m, or an empty range (and the error flag) when the CSR is bad.
+__device__ __forceinline__ void row_occ(const Params& p, int m, int* b, int* e) {
+  *b = p.row_ptr[m];
+  *e = p.row_ptr[m + 1];
+  if (*b < 0 || *e < *b || *e > p.n_occ) {
+    raise_error(p.err, TREE_ERR_DEVICE_CHECK);
+    *b = *e = 0;
+  }
+}
+
+// Next occurrence (cursor k in [k, e)) of the row whose target lies in [n0, n0 + BN):
+// returns the column within the tile, or -1. Sets *o to the occurrence id.
+__device__ __forceinline__ int next_in_tile(const Params& p, int* k, int e, int n0, int* o) {
+  while (*k < e) {
+    const int oo = p.perm[*k];
+    if (oo < 0 || oo >= p.n_occ) {
+      raise_error(p.err, TREE_ERR_DEVICE_CHECK);
+      ++*k;
+      continue;
+    }
+    const int y = p.targets[oo];
+    if (y < 0 || y >= p.N) {
+      raise_error(p.err, TREE_ERR_DEVICE_CHECK);
+      ++*k;
+      continue;
+    }
+    if (y >= n0 && y < n0 + BN) {
+      *o = oo;
+      return y - n0;
+    }
+    ++*k;
+  }
+  return -1;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+lm_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  if (p.err && (*reinterpret_cast<volatile int*>(p.err) & (1 << TREE_ERR_TIMEOUT))) return;
+  Smem& S = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int n_mb = (p.M + BM - 1) / BM, n_nb = (p.N + BN - 1) / BN, n_kb = (p.K + BK - 1) / BK;
+  const int n_tiles = n_mb * n_nb;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(&S.full[s], 1);
+      mbar_init(&S.empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&S.acc_full[s], 1);
+      mbar_init(&S.acc_empty[s], 4);
+    }
+    fence_mbarrier_init();
+  }
+  if (warp == 1) tmem_alloc(&S.tmem_base, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = S.tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      prefetch_tmap(&tmA);
+      prefetch_tmap(&tmB);
+      int it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
+        int mb, nb;
+        tile_coords(p, t, n_mb, n_nb, &mb, &nb);
+        for (int kb = 0; kb < n_kb; ++kb, ++it) {
+          const int st = it % NST;
+          if (it >= NST && !(ok = mbar_wait(&S.empty[st], ((it / NST) - 1) & 1, p.err))) break;
+          mbar_arrive_expect_tx(&S.full[st], kABytes + kBBytes);
+          load_stage(p, &tmA, &tmB, S.a[st], S.b[st], &S.full[st], mb, nb, kb);
+        }
+      }
+      // no copy left in flight
+      for (int j = (it > NST ? it - NST : 0); j < it; ++j) mbar_wait(&S.full[j % NST], (j / NST) & 1, p.err);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(BM, BN, p.a_mn, p.b_mn);
+      int it = 0, ai = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x, ++ai) {
+        const int buf = ai & 1;
+        if (ai >= 2 && !(ok = mbar_wait(&S.acc_empty[buf], ((ai >> 1) - 1) & 1, p.err))) break;
+        tc_fence_after();
+        const uint32_t d = tmem + buf * BN;
+        for (int kb = 0; kb < n_kb; ++kb, ++it) {
+          const int st = it % NST;
+          if (!(ok = mbar_wait(&S.full[st], (it / NST) & 1, p.err))) break;
+          tc_fence_after();
+          const uint32_t ab = smem_u32(S.a[st]), bb = smem_u32(S.b[st]);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = p.a_mn ? desc_sw128(ab + kk * 2048, kABytes / 2, 1024) : desc_sw128(ab + kk * 32, 16, 1024);
+            const uint64_t bd = p.b_mn ? desc_sw128(bb + kk * 2048, kBBytes / 4, 1024) : desc_sw128(bb + kk * 32, 16, 1024);
+            mma_ss(d, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(&S.empty[st]);
+        }
+        if (ok) mma_commit(&S.acc_full[buf]);
+      }
+      // wait for the last MMAs before TMEM is freed
+      if (ai > 0) mbar_wait(&S.acc_full[(ai - 1) & 1], ((ai - 1) >> 1) & 1, p.err);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue warps 2-5
+    const int q4 = warp & 3;
+    const int r = q4 * 32 + lane;
+    const uint32_t lanes = static_cast<uint32_t>(q4 * 32) << 16;
+    int ai = 0;
+    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++ai) {
+      int mb, nb;
+      tile_coords(p, t, n_mb, n_nb, &mb, &nb);
+      const int buf = ai & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&S.acc_full[buf], (ai >> 1) & 1, p.err))) break;
+      tc_fence_after();
+      const uint32_t acc = tmem + lanes + buf * BN;
+      const int m = mb * BM + r, n0 = nb * BN;
+      const bool row_ok = m < p.M;
+      const int ncols = min(BN, p.N - n0);
+      if (p.epi == EPI_STORE) {
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32], pk[16];
+          tmem_ld32(acc + c * 32, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int u = 0; u < 16; ++u) pk[u] = pack_bf16(__uint_as_float(v[2 * u]), __uint_as_float(v[2 * u + 1]));
+          if (row_ok && c * 32 < ncols) {
+            __nv_bfloat16* dst = p.out + static_cast<int64_t>(m) * p.N + n0 + c * 32;
+            if (c * 32 + 32 <= ncols && (p.N % 8) == 0) {
+#pragma unroll
+              for (int u = 0; u < 4; ++u)
+                reinterpret_cast<uint4*>(dst)[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+            } else {
+              for (int u = 0; u < 32 && c * 32 + u < ncols; ++u)
+                dst[u] = __float2bfloat16_rn(__uint_as_float(v[u]));
+            }
+          }
+        }
+      } else if (p.epi == EPI_LSE) {
+        float mx = -INFINITY, sm = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(acc + c * 32, v);
+          tmem_ld_wait();
+          const int valid = min(32, ncols - c * 32);  // same for the whole warp
+          if (valid <= 0) continue;
+          float cm = -INFINITY;
+#pragma unroll
+          for (int u = 0; u < 32; ++u)
+            if (u < valid) cm = fmaxf(cm, __uint_as_float(v[u]));
+          const float nm = fmaxf(mx, cm);
+          float cs = 0.f;
+#pragma unroll
+          for (int u = 0; u < 32; ++u)
+            if (u < valid) cs += exp2f((__uint_as_float(v[u]) - nm) * 1.4426950408889634f);
+          sm = sm * exp2f((mx - nm) * 1.4426950408889634f) + cs;
+          mx = nm;
+        }
+        if (row_ok) {
+          p.part_max[static_cast<int64_t>(nb) * p.M + m] = mx;
+          p.part_sum[static_cast<int64_t>(nb) * p.M + m] = sm;
+        }
+        // target logits of this row's occurrences in this tile (one TMEM column per round)
+        int k = 0, e = 0, o = -1;
+        if (row_ok) row_occ(p, m, &k, &e);
+        int col = row_ok ? next_in_tile(p, &k, e, n0, &o) : -1;
+        while (true) {
+          const unsigned want = __ballot_sync(0xffffffffu, col >= 0);
+          if (!want) break;
+          const int c = __shfl_sync(0xffffffffu, col, __ffs(want) - 1);
+          const float z = __uint_as_float(tmem_ld1(acc + c));
+          if (col == c) {
+            p.logp[o] = z;
+            ++k;
+            col = next_in_tile(p, &k, e, n0, &o);
+          }
+        }
+      } else {  // EPI_GZ
+        const float l = row_ok ? p.lse[m] : 0.f, cr = row_ok ? p.crow[m] : 0.f;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32], pk[16];
+          tmem_ld32(acc + c * 32, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            const float g0 = -cr * exp2f((__uint_as_float(v[2 * u]) - l) * 1.4426950408889634f);
+            const float g1 = -cr * exp2f((__uint_as_float(v[2 * u + 1]) - l) * 1.4426950408889634f);
+            pk[u] = pack_bf16(g0, g1);
+          }
+          if (row_ok && c * 32 < ncols) {
+            __nv_bfloat16* dst = p.out + static_cast<int64_t>(m) * p.N + n0 + c * 32;
+            if (c * 32 + 32 <= ncols && (p.N % 8) == 0) {
+#pragma unroll
+              for (int u = 0; u < 4; ++u)
+                reinterpret_cast<uint4*>(dst)[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+            } else {
+              for (int u = 0; u < 32 && c * 32 + u < ncols; ++u) {
+                const __nv_bfloat162 h2 = *reinterpret_cast<const __nv_bfloat162*>(&pk[u / 2]);
+                dst[u] = (u & 1) ? h2.y : h2.x;
+              }
+            }
+          }
+        }
+        // target entries: -c p_y + sum of g over the row's occurrences with target y
+        int k = 0, e = 0, o = -1;
+        if (row_ok) row_occ(p, m, &k, &e);
+        const int kb0 = k;
+        int col = row_ok ? next_in_tile(p, &k, e, n0, &o) : -1;
+        while (true) {
+          const unsigned want = __ballot_sync(0xffffffffu, col >= 0);
+          if (!want) break;
+          const int c = __shfl_sync(0xffffffffu, col, __ffs(want) - 1);
+          const float z = __uint_as_float(tmem_ld1(acc + c));
+          if (col == c) {
+            float gsum = 0.f;
+            for (int kk = kb0; kk < e; ++kk) {
+              const int oo = p.perm[kk];
+              if (oo >= 0 && oo < p.n_occ && p.targets[oo] == n0 + c) gsum += p.grad[oo];
+            }
+            const float val = -cr * exp2f((z - l) * 1.4426950408889634f) + gsum;
+            p.out[static_cast<int64_t>(m) * p.N + n0 + c] = __float2bfloat16_rn(val);
+            // skip the row's further occurrences of the same target (already summed)
+            do {
+              ++k;
+              col = next_in_tile(p, &k, e, n0, &o);
+            } while (col == c);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.acc_empty[buf]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace lmtc
+
+bool logprob_tc_supported(int dtype) { return dtype == TREE_DTYPE_BF16; }
+
+static int map2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                 uint32_t box_rows) {
+  const uint64_t dims[2] = {inner, rows};
+  const uint64_t strides[1] = {inner * 2};
+  const uint32_t box[2] = {box_inner, box_rows};
+  return make_tmap(m, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dims, strides, box, true);
+}
+
+static int n_sms(int* n) {
+  static int cached[128] = {0};
+  int dev = 0;
+  TREE_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 128) return fail(TREE_ERR_CUDA, "device ordinal %d out of range", dev);
+  if (!cached[dev]) TREE_CUDA_TRY(cudaDeviceGetAttribute(&cached[dev], cudaDevAttrMultiProcessorCount, dev));
+  *n = cached[dev];
+  return TREE_OK;
+}
+
+static int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const lmtc::Params& p, cudaStream_t st,
+                       const char* name) {
+  using namespace lmtc;
+  static bool attr_set = false;
+  if (!attr_set) {
+    TREE_CUDA_TRY(cudaFuncSetAttribute(lm_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kSmemBytes)));
+    attr_set = true;
+  }
+  int sms = 0;
+  int rc = n_sms(&sms);
+  if (rc) return rc;
+  const int64_t tiles = static_cast<int64_t>((p.M + BM - 1) / BM) * ((p.N + BN - 1) / BN);
+  const int grid = static_cast<int>(std::min<int64_t>(sms, tiles));
+  lm_gemm_kernel<<<grid, kThreads, kSmemBytes, st>>>(ta, tb, p);
+  TREE_LAUNCH_CHECK(name);
+  return TREE_OK;
+}
+
+// Defined in logprob_simt.cu.
+int lse_combine_launch(const float* part_max, const float* part_sum, int n_tiles, int64_t T, const int32_t* row_ptr,
+                       const int32_t* perm, int64_t n_occ, float* lse, float* logp, cudaStream_t st);
+int row_grad_sum_launch(const int32_t* row_ptr, const int32_t* perm, const float* grad, int64_t T, int64_t n_occ,
+                        float* crow, cudaStream_t st);
+
+int logprob_fwd_tc(const LogprobArgs& a, cudaStream_t st) {
+  using namespace lmtc;
+  CUtensorMap ta, tb;
+  int rc;
+  if ((rc = map2d(&ta, a.h, a.K, a.T, 64, BM)) || (rc = map2d(&tb, a.w, a.V, a.K, 64, 64))) return rc;
+  Params p{};
+  p.M = static_cast<int>(a.T);
+  p.N = static_cast<int>(a.V);
+  p.K = static_cast<int>(a.K);
+  p.a_mn = 0;
+  p.b_mn = 1;
+  p.raster_m_fast = 1;
+  p.epi = EPI_LSE;
+  p.row_ptr = a.row_ptr;
+  p.perm = a.perm;
+  p.targets = a.targets;
+  p.n_occ = static_cast<int>(a.n_occ);
+  p.part_max = a.ws.part_max;
+  p.part_sum = a.ws.part_sum;
+  p.logp = a.logp;
+  p.err = device_error_word();
+  if ((rc = launch_gemm(ta, tb, p, st, "lm_gemm_kernel<lse>"))) return rc;
+  const int n_nb = static_cast<int>((a.V + BN - 1) / BN);
+  return lse_combine_launch(a.ws.part_max, a.ws.part_sum, n_nb, a.T, a.row_ptr, a.perm, a.n_occ, a.lse, a.logp, st);
+}
+
+int logprob_bwd_tc(const LogprobArgs& a, cudaStream_t st) {
+  using namespace lmtc;
+  int rc = row_grad_sum_launch(a.row_ptr, a.perm, a.grad, a.T, a.n_occ, a.ws.crow, st);
+  if (rc) return rc;
+  __nv_bfloat16* gz = static_cast<__nv_bfloat16*>(a.ws.gz);
+  // 1) G_z = recomputed softmax terms and target terms, bf16 [T, V]
+  {
+    CUtensorMap ta, tb;
+    if ((rc = map2d(&ta, a.h, a.K, a.T, 64, BM)) || (rc = map2d(&tb, a.w, a.V, a.K, 64, 64))) return rc;
+    Params p{};
+    p.M = static_cast<int>(a.T);
+    p.N = static_cast<int>(a.V);
+    p.K = static_cast<int>(a.K);
+    p.a_mn = 0;
+    p.b_mn = 1;
+    p.raster_m_fast = 1;
+    p.epi = EPI_GZ;
+    p.row_ptr = a.row_ptr;
+    p.perm = a.perm;
+    p.targets = a.targets;
+    p.n_occ = static_cast<int>(a.n_occ);
+    p.lse = a.lse;
+    p.crow = a.ws.crow;
+    p.grad = a.grad;
+    p.out = gz;
+    p.err = device_error_word();
+    if ((rc = launch_gemm(ta, tb, p, st, "lm_gemm_kernel<gz>"))) return rc;
+  }
+  // 2) dH [T, K_h] = G_z W^T: A = G_z (K-major over V), B = W rows (K-major over V)
+  {
+    CUtensorMap ta, tb;
+    if ((rc = map2d(&ta, gz, a.V, a.T, 64, BM)) || (rc = map2d(&tb, a.w, a.V, a.K, 64, BN))) return rc;
+    Params p{};
+    p.M = static_cast<int>(a.T);
+    p.N = static_cast<int>(a.K);
+    p.K = static_cast<int>(a.V);
+    p.a_mn = 0;
+    p.b_mn = 0;
+    p.raster_m_fast = 1;
+    p.epi = EPI_STORE;
+    p.out = static_cast<__nv_bfloat16*>(a.dh);
+    p.err = device_error_word();
+    if ((rc = launch_gemm(ta, tb, p, st, "lm_gemm_kernel<dh>"))) return rc;
+  }
+  // 3) dW [K_h, V] = H^T G_z: A = H viewed MN-major, B = G_z MN-major
+  {
+    CUtensorMap ta, tb;
+    if ((rc = map2d(&ta, a.h, a.K, a.T, 64, 64)) || (rc = map2d(&tb, gz, a.V, a.T, 64, 64))) return rc;
+    Params p{};
+    p.M = static_cast<int>(a.K);
+    p.N = static_cast<int>(a.V);
+    p.K = static_cast<int>(a.T);
+    p.a_mn = 1;
+    p.b_mn = 1;
+    p.raster_m_fast = 1;
+    p.epi = EPI_STORE;
+    p.out = static_cast<__nv_bfloat16*>(a.dw);
+    p.err = device_error_word();
+    if ((rc = launch_gemm(ta, tb, p, st, "lm_gemm_kernel<dw>"))) return rc;
+  }
+  return TREE_OK;
+}
+
+}  // namespace tree

@@ -251,6 +251,21 @@ static int bwd_impl(const LogprobArgs& a, cudaStream_t st) {
   return TREE_OK;
 }
 
+int lse_combine_launch(const float* part_max, const float* part_sum, int n_tiles, int64_t T, const int32_t* row_ptr,
+                       const int32_t* perm, int64_t n_occ, float* lse, float* logp, cudaStream_t st) {
+  lse_combine_kernel<<<static_cast<unsigned>((T + 255) / 256), 256, 0, st>>>(part_max, part_sum, n_tiles, T, row_ptr,
+                                                                           perm, n_occ, lse, logp);
+  TREE_LAUNCH_CHECK("lse_combine_kernel");
+  return TREE_OK;
+}
+
+int row_grad_sum_launch(const int32_t* row_ptr, const int32_t* perm, const float* grad, int64_t T, int64_t n_occ,
+                        float* crow, cudaStream_t st) {
+  row_grad_sum_kernel<<<static_cast<unsigned>((T + 255) / 256), 256, 0, st>>>(row_ptr, perm, grad, T, n_occ, crow);
+  TREE_LAUNCH_CHECK("row_grad_sum_kernel");
+  return TREE_OK;
+}
+
 int logprob_fwd_simt(const LogprobArgs& a, cudaStream_t st) {
   return a.dtype == TREE_DTYPE_BF16 ? fwd_impl<__nv_bfloat16>(a, st) : fwd_impl<float>(a, st);
 }
