@@ -393,7 +393,7 @@ def run_lm_head(args, dev, peaks, peak_src):
     gl = torch.from_numpy(-(1.0 - rng.random(n_occ)).astype(np.float32)).to(dev)
     rp = torch.from_numpy(pk["occ_row_ptr"]).to(dev)
     pm = torch.from_numpy(pk["occ_perm"]).to(dev)
-    ws = torch.empty(tma.tree_logprob_workspace_size(T, K, V, 1), dtype=torch.uint8, device=dev)
+    ws = torch.empty(tma.tree_logprob_workspace_size(T, K, V, n_occ, 1), dtype=torch.uint8, device=dev)
     lse = torch.empty(T, dtype=torch.float32, device=dev)
     logp = torch.empty(n_occ, dtype=torch.float32, device=dev)
     dh, dw = torch.empty_like(h), torch.empty_like(w)

@@ -233,7 +233,7 @@ int tree_attn_bwd(const void* q, const void* k, const void* v, const void* o,
  * logp, grad_logp: device fp32 [n_occ]; index arrays device int32.
  * Out-of-range targets or CSR entries set TREE_ERR_DEVICE_CHECK and are skipped.
  */
-size_t tree_logprob_workspace_size(int64_t T, int64_t K_h, int64_t V, int dtype);
+size_t tree_logprob_workspace_size(int64_t T, int64_t K_h, int64_t V, int64_t n_occ, int dtype);
 
 int tree_logprob_fwd(const void* hidden, const void* w_lm, const int32_t* occ_row_ptr,
                      const int32_t* occ_perm, const int32_t* occ_targets, int64_t T,

@@ -100,4 +100,4 @@ def test_host_argument_errors(tma):
     assert L.tree_logprob_fwd(None, None, None, None, None, 8, 60, 512, 4, None, None, 1, None, 0, None) == 2
     assert L.tree_rope(None, None, None, 4, 1, 1, 7, 10000.0, 1, 0, None) == 2
     assert L.tree_attn_workspace_size(4096, 32, 8, 128, 1) > 0
-    assert L.tree_logprob_workspace_size(64, 64, 512, 0) > 0
+    assert L.tree_logprob_workspace_size(64, 64, 512, 100, 0) > 0

@@ -187,8 +187,8 @@ def tree_attn_bwd(q, k, v, o, dout, lse, subtree_end, softmax_scale: float = 0.0
     return dq, dk, dv
 
 
-def tree_logprob_workspace_size(T, K_h, V, dtype_code) -> int:
-    return int(lib().tree_logprob_workspace_size(T, K_h, V, dtype_code))
+def tree_logprob_workspace_size(T, K_h, V, n_occ, dtype_code) -> int:
+    return int(lib().tree_logprob_workspace_size(T, K_h, V, n_occ, dtype_code))
 
 
 def tree_logprob_fwd(hidden, w_lm, occ_row_ptr, occ_perm, occ_targets, workspace=None, lse=None, logp=None):
@@ -200,7 +200,7 @@ def tree_logprob_fwd(hidden, w_lm, occ_row_ptr, occ_perm, occ_targets, workspace
     dt = _dtype_code(hidden)
     lse = torch.empty(T, dtype=torch.float32, device=hidden.device) if lse is None else lse
     logp = torch.empty(n_occ, dtype=torch.float32, device=hidden.device) if logp is None else logp
-    ws = _workspace(tree_logprob_workspace_size(T, K, V, dt), hidden.device, workspace)
+    ws = _workspace(tree_logprob_workspace_size(T, K, V, n_occ, dt), hidden.device, workspace)
     i32 = torch.int32
     check(lib().tree_logprob_fwd(_dev(hidden, "hidden"), _dev(w_lm, "w_lm", hidden.dtype),
                                  _dev(occ_row_ptr, "occ_row_ptr", i32), _dev(occ_perm, "occ_perm", i32),
@@ -220,7 +220,7 @@ def tree_logprob_bwd(hidden, w_lm, lse, occ_row_ptr, occ_perm, occ_targets, grad
     n_occ = occ_targets.shape[0]
     dt = _dtype_code(hidden)
     dh, dw = (torch.empty_like(hidden), torch.empty_like(w_lm)) if grads is None else grads
-    ws = _workspace(tree_logprob_workspace_size(T, K, V, dt), hidden.device, workspace)
+    ws = _workspace(tree_logprob_workspace_size(T, K, V, n_occ, dt), hidden.device, workspace)
     i32 = torch.int32
     check(lib().tree_logprob_bwd(_dev(hidden, "hidden"), _dev(w_lm, "w_lm", hidden.dtype),
                                  _dev(lse, "lse", torch.float32), _dev(occ_row_ptr, "occ_row_ptr", i32),

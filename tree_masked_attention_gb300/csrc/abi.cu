@@ -51,7 +51,7 @@ size_t attn_ws_layout(int64_t T, int Hq, int Hkv, int d, int dtype, void* base, 
   return round_up(c.off, 256);
 }
 
-size_t logprob_ws_layout(int64_t T, int64_t K, int64_t V, int dtype, void* base, LogprobWs* ws) {
+size_t logprob_ws_layout(int64_t T, int64_t K, int64_t V, int64_t n_occ, int dtype, void* base, LogprobWs* ws) {
   (void)K;
   (void)dtype;
   Carver c{static_cast<char*>(base)};
@@ -61,6 +61,9 @@ size_t logprob_ws_layout(int64_t T, int64_t K, int64_t V, int dtype, void* base,
   w.part_sum = c.take<float>(n_vt * T);
   w.crow = c.take<float>(static_cast<size_t>(T));
   w.gz = c.take<float>(static_cast<size_t>(T) * V);
+  w.occ_delta = c.take<float>(static_cast<size_t>(n_occ) + 1);
+  w.blk_ptr = c.take<int32_t>(static_cast<size_t>((V + 255) / 256) + 1);
+  w.blk_ent = c.take<int32_t>(2 * static_cast<size_t>(n_occ) + 2);
   if (ws) *ws = w;
   return round_up(c.off, 256);
 }
@@ -169,9 +172,9 @@ static int check_lm(const void* h, const void* w, const int32_t* row_ptr, const 
   return TREE_OK;
 }
 
-extern "C" size_t tree_logprob_workspace_size(int64_t T, int64_t K_h, int64_t V, int dtype) {
-  if (T < 1 || K_h < 1 || V < 1) return 0;
-  return logprob_ws_layout(T, K_h, V, dtype, nullptr, nullptr);
+extern "C" size_t tree_logprob_workspace_size(int64_t T, int64_t K_h, int64_t V, int64_t n_occ, int dtype) {
+  if (T < 1 || K_h < 1 || V < 1 || n_occ < 0) return 0;
+  return logprob_ws_layout(T, K_h, V, n_occ, dtype, nullptr, nullptr);
 }
 
 extern "C" int tree_logprob_fwd(const void* hidden, const void* w_lm, const int32_t* occ_row_ptr,
@@ -182,12 +185,12 @@ extern "C" int tree_logprob_fwd(const void* hidden, const void* w_lm, const int3
   int rc = check_lm(hidden, w_lm, occ_row_ptr, occ_perm, occ_targets, T, K_h, V, n_occ, dtype);
   if (rc) return rc;
   if (!lse || (n_occ > 0 && !logp)) return fail(TREE_ERR_INVALID_ARG, "tree_logprob_fwd: null output");
-  const size_t need = logprob_ws_layout(T, K_h, V, dtype, nullptr, nullptr);
+  const size_t need = logprob_ws_layout(T, K_h, V, n_occ, dtype, nullptr, nullptr);
   if ((rc = check_ws(workspace, workspace_bytes, need))) return rc;
   LogprobArgs a{};
   a.h = hidden; a.w = w_lm; a.row_ptr = occ_row_ptr; a.perm = occ_perm; a.targets = occ_targets;
   a.lse = lse; a.logp = logp; a.T = T; a.K = K_h; a.V = V; a.n_occ = n_occ; a.dtype = dtype;
-  logprob_ws_layout(T, K_h, V, dtype, workspace, &a.ws);
+  logprob_ws_layout(T, K_h, V, n_occ, dtype, workspace, &a.ws);
   if (logprob_tc_supported(dtype)) return logprob_fwd_tc(a, reinterpret_cast<cudaStream_t>(stream));
   return logprob_fwd_simt(a, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -204,13 +207,13 @@ extern "C" int tree_logprob_bwd(const void* hidden, const void* w_lm, const floa
     return fail(TREE_ERR_INVALID_ARG, "tree_logprob_bwd: null pointer");
   if (!aligned16(d_hidden) || !aligned16(d_w))
     return fail(TREE_ERR_ALIGNMENT, "tree_logprob_bwd: d_hidden / d_w not 16-byte aligned");
-  const size_t need = logprob_ws_layout(T, K_h, V, dtype, nullptr, nullptr);
+  const size_t need = logprob_ws_layout(T, K_h, V, n_occ, dtype, nullptr, nullptr);
   if ((rc = check_ws(workspace, workspace_bytes, need))) return rc;
   LogprobArgs a{};
   a.h = hidden; a.w = w_lm; a.row_ptr = occ_row_ptr; a.perm = occ_perm; a.targets = occ_targets;
   a.grad = grad_logp; a.lse = const_cast<float*>(lse); a.dh = d_hidden; a.dw = d_w;
   a.T = T; a.K = K_h; a.V = V; a.n_occ = n_occ; a.dtype = dtype;
-  logprob_ws_layout(T, K_h, V, dtype, workspace, &a.ws);
+  logprob_ws_layout(T, K_h, V, n_occ, dtype, workspace, &a.ws);
   if (logprob_tc_supported(dtype)) return logprob_bwd_tc(a, reinterpret_cast<cudaStream_t>(stream));
   return logprob_bwd_simt(a, reinterpret_cast<cudaStream_t>(stream));
 }

@@ -67,7 +67,10 @@ struct LogprobWs {
   float* part_max;   // [n_vtiles, T] per vocabulary tile: row max of the logits
   float* part_sum;   // [n_vtiles, T] per vocabulary tile: sum exp(z - max)
   float* crow;       // [T]           sum of grad_logp over the row's occurrences
-  void* gz;          // [T, V]        G_z (fp32 on the SIMT path)
+  void* gz;          // [T, V]        G_z (fp32 on the SIMT path, bf16 on the tensor-core path)
+  float* occ_delta;  // [n_occ]       exact minus bf16-stored G_z at each occurrence's target cell
+  int32_t* blk_ptr;  // [ceil(V/256)+1] occurrences grouped by 256-column target block
+  int32_t* blk_ent;  // [2 * n_occ]   {source row, occurrence} per group entry
 };
 
 struct LogprobArgs {
@@ -86,7 +89,7 @@ struct LogprobArgs {
   LogprobWs ws;
 };
 
-size_t logprob_ws_layout(int64_t T, int64_t K, int64_t V, int dtype, void* base, LogprobWs* ws);
+size_t logprob_ws_layout(int64_t T, int64_t K, int64_t V, int64_t n_occ, int dtype, void* base, LogprobWs* ws);
 int logprob_fwd_simt(const LogprobArgs& a, cudaStream_t st);
 int logprob_bwd_simt(const LogprobArgs& a, cudaStream_t st);
 bool logprob_tc_supported(int dtype);

@@ -38,7 +38,7 @@ constexpr int kThreads = 192;
 constexpr uint32_t kABytes = BM * BK * 2;  // 16 KB
 constexpr uint32_t kBBytes = BN * BK * 2;  // 32 KB
 
-enum Epi { EPI_LSE = 0, EPI_GZ = 1, EPI_STORE = 2 };
+enum Epi { EPI_LSE = 0, EPI_GZ = 1, EPI_STORE = 2, EPI_DW = 3 };
 
 struct Smem {
   uint8_t a[NST][kABytes];
@@ -64,7 +64,11 @@ struct Params {
   const float* lse;      // EPI_GZ
   const float* crow;
   const float* grad;
-  __nv_bfloat16* out;    // EPI_GZ: G_z [M, N]; EPI_STORE: C [M, N]
+  __nv_bfloat16* out;    // EPI_GZ: G_z [M, N]; EPI_STORE / EPI_DW: C [M, N]
+  float* occ_delta;      // EPI_GZ writes, EPI_DW reads: exact - stored G_z at target cells
+  const int32_t* blk_ptr;  // EPI_DW: occurrences grouped by 256-column target block
+  const int32_t* blk_ent;  //         {source row, occurrence}
+  const __nv_bfloat16* h;  // EPI_DW: hidden [rows, M]
   int* err;
 };
 
@@ -228,12 +232,26 @@ lm_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const int m = mb * BM + r, n0 = nb * BN;
       const bool row_ok = m < p.M;
       const int ncols = min(BN, p.N - n0);
-      if (p.epi == EPI_STORE) {
+      if (p.epi == EPI_STORE || p.epi == EPI_DW) {
+        const int lb = p.epi == EPI_DW ? p.blk_ptr[nb] : 0, le = p.epi == EPI_DW ? p.blk_ptr[nb + 1] : 0;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t v[32], pk[16];
           tmem_ld32(acc + c * 32, v);
           tmem_ld_wait();
+          // dW only: add back, in fp32, what storing G_z in bf16 dropped at target cells:
+          // dW[m, y] += H[r, m] * (exact - stored) for every occurrence cell (r, y).
+          for (int q = lb; q < le; ++q) {
+            const int oo = p.blk_ent[2 * q + 1];
+            const int idx = p.targets[oo] - n0 - c * 32;
+            if (idx < 0 || idx >= 32) continue;
+            const float dlt = p.occ_delta[oo];
+            if (dlt == 0.f || !row_ok) continue;
+            const float x = dlt * __bfloat162float(p.h[static_cast<int64_t>(p.blk_ent[2 * q]) * p.M + m]);
+#pragma unroll
+            for (int u = 0; u < 32; ++u)
+              if (u == idx) v[u] = __float_as_uint(__uint_as_float(v[u]) + x);
+          }
 #pragma unroll
           for (int u = 0; u < 16; ++u) pk[u] = pack_bf16(__uint_as_float(v[2 * u]), __uint_as_float(v[2 * u + 1]));
           if (row_ok && c * 32 < ncols) {
@@ -327,12 +345,18 @@ lm_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           const float z = __uint_as_float(tmem_ld1(acc + c));
           if (col == c) {
             float gsum = 0.f;
+            bool first = true;  // the cell's first occurrence (in CSR order) carries its residual
             for (int kk = kb0; kk < e; ++kk) {
               const int oo = p.perm[kk];
-              if (oo >= 0 && oo < p.n_occ && p.targets[oo] == n0 + c) gsum += p.grad[oo];
+              if (oo >= 0 && oo < p.n_occ && p.targets[oo] == n0 + c) {
+                gsum += p.grad[oo];
+                if (kk < k) first = false;
+              }
             }
             const float val = -cr * exp2f((z - l) * 1.4426950408889634f) + gsum;
-            p.out[static_cast<int64_t>(m) * p.N + n0 + c] = __float2bfloat16_rn(val);
+            const __nv_bfloat16 stored = __float2bfloat16_rn(val);
+            p.out[static_cast<int64_t>(m) * p.N + n0 + c] = stored;
+            if (first) p.occ_delta[o] = val - __bfloat162float(stored);
             // skip the row's further occurrences of the same target (already summed)
             do {
               ++k;
@@ -351,6 +375,52 @@ lm_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
+  }
+}
+
+// Occurrences grouped by 256-column target block, in CSR order within a block (so the
+// grouping, and every sum taken over it, is the same on every run). One warp per block:
+// pass 0 counts into blk_ptr[b + 1], pass 1 writes {source row, occurrence} entries.
+__global__ void lm_block_lists_kernel(const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ perm,
+                                      const int32_t* __restrict__ targets, int T, int n_occ, int V, int n_blk,
+                                      int32_t* __restrict__ blk_ptr, int32_t* __restrict__ blk_ent, int pass) {
+  const int w = (blockIdx.x * blockDim.x + threadIdx.x) / 32, lane = threadIdx.x % 32;
+  if (w >= n_blk) return;
+  int cursor = pass ? blk_ptr[w] : 0;
+  for (int k0 = 0; k0 < n_occ; k0 += 32) {
+    const int k = k0 + lane;
+    int o = -1;
+    bool match = false;
+    if (k < n_occ) {
+      o = perm[k];
+      if (o >= 0 && o < n_occ) {
+        const int y = targets[o];
+        match = y >= 0 && y < V && y / BN == w;
+      }
+    }
+    const unsigned bal = __ballot_sync(0xffffffffu, match);
+    if (pass && match) {
+      int lo = 0, hi = T - 1;  // last row r with row_ptr[r] <= k
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) / 2;
+        if (row_ptr[mid] <= k) lo = mid; else hi = mid - 1;
+      }
+      const int pos = cursor + __popc(bal & ((1u << lane) - 1u));
+      blk_ent[2 * pos] = lo;
+      blk_ent[2 * pos + 1] = o;
+    }
+    cursor += __popc(bal);
+  }
+  if (!pass && lane == 0) blk_ptr[w + 1] = cursor;
+}
+
+// Prefix sum of the block counts (one block) and zeroed residuals.
+__global__ void lm_block_scan_kernel(int32_t* __restrict__ blk_ptr, int n_blk, float* __restrict__ occ_delta,
+                                     int n_occ) {
+  for (int i = threadIdx.x; i < n_occ; i += blockDim.x) occ_delta[i] = 0.f;
+  if (threadIdx.x == 0) {
+    blk_ptr[0] = 0;
+    for (int b = 1; b <= n_blk; ++b) blk_ptr[b] += blk_ptr[b - 1];
   }
 }
 
@@ -431,6 +501,20 @@ int logprob_bwd_tc(const LogprobArgs& a, cudaStream_t st) {
   using namespace lmtc;
   int rc = row_grad_sum_launch(a.row_ptr, a.perm, a.grad, a.T, a.n_occ, a.ws.crow, st);
   if (rc) return rc;
+  const int n_blk = static_cast<int>((a.V + BN - 1) / BN);
+  {
+    const unsigned grid = static_cast<unsigned>((n_blk * 32 + 255) / 256);
+    lm_block_lists_kernel<<<grid, 256, 0, st>>>(a.row_ptr, a.perm, a.targets, static_cast<int>(a.T),
+                                                static_cast<int>(a.n_occ), static_cast<int>(a.V), n_blk, a.ws.blk_ptr,
+                                                a.ws.blk_ent, 0);
+    TREE_LAUNCH_CHECK("lm_block_lists_kernel<count>");
+    lm_block_scan_kernel<<<1, 1024, 0, st>>>(a.ws.blk_ptr, n_blk, a.ws.occ_delta, static_cast<int>(a.n_occ));
+    TREE_LAUNCH_CHECK("lm_block_scan_kernel");
+    lm_block_lists_kernel<<<grid, 256, 0, st>>>(a.row_ptr, a.perm, a.targets, static_cast<int>(a.T),
+                                                static_cast<int>(a.n_occ), static_cast<int>(a.V), n_blk, a.ws.blk_ptr,
+                                                a.ws.blk_ent, 1);
+    TREE_LAUNCH_CHECK("lm_block_lists_kernel<fill>");
+  }
   __nv_bfloat16* gz = static_cast<__nv_bfloat16*>(a.ws.gz);
   // 1) G_z = recomputed softmax terms and target terms, bf16 [T, V]
   {
@@ -452,6 +536,7 @@ int logprob_bwd_tc(const LogprobArgs& a, cudaStream_t st) {
     p.crow = a.ws.crow;
     p.grad = a.grad;
     p.out = gz;
+    p.occ_delta = a.ws.occ_delta;
     p.err = device_error_word();
     if ((rc = launch_gemm(ta, tb, p, st, "lm_gemm_kernel<gz>"))) return rc;
   }
@@ -482,8 +567,13 @@ int logprob_bwd_tc(const LogprobArgs& a, cudaStream_t st) {
     p.a_mn = 1;
     p.b_mn = 1;
     p.raster_m_fast = 1;
-    p.epi = EPI_STORE;
+    p.epi = EPI_DW;
     p.out = static_cast<__nv_bfloat16*>(a.dw);
+    p.targets = a.targets;
+    p.occ_delta = a.ws.occ_delta;
+    p.blk_ptr = a.ws.blk_ptr;
+    p.blk_ent = a.ws.blk_ent;
+    p.h = static_cast<const __nv_bfloat16*>(a.h);
     p.err = device_error_word();
     if ((rc = launch_gemm(ta, tb, p, st, "lm_gemm_kernel<dw>"))) return rc;
   }
