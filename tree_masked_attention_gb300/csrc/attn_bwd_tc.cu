@@ -52,12 +52,15 @@ struct Smem {
   uint8_t q[NST][kQTile];
   uint8_t dout[NST][kQTile];
   uint8_t ds[2][kDsTile];
+  float dq_stage[BQ * D];   // scale * dQ of one step, row-major [64 queries][128 dims], for the TMA reduce
   float lse2[NST][BQ];
   float delta[NST][BQ];
-  uint64_t kv_full, qdo_full[NST], qdo_empty[NST], s_full[2], ds_ready[2], dq_full[2], drain_done[2], mma_done;
+  uint64_t kv_full, qdo_full[NST], qdo_empty[NST], s_full[2], ds_ready[2], dq_full[2], drain_done[2], mma_done,
+      stage_free, stage_full;
   uint32_t tmem_base;
 };
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
+static_assert(kSmemBytes + 64 <= 232448, "backward shared memory exceeds the 227 KB per-block limit");
 
 struct Params {
   int T, T_pad, Hq, Hkv;
@@ -111,9 +114,16 @@ __device__ __forceinline__ int key_tile_queries(const Params& p, int kt, int* qt
 // Persistent: each CTA takes work units {key tile, KV head, steps [b, e)} from a counter.
 // Step t of a key tile is query head kvh*G + t / nq and query tile qt_lo + t % nq.
 // Barrier phases run on over the CTA's whole life: g counts its steps, uit its units.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                   const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO, Params p) {
+                   const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
+                   const __grid_constant__ CUtensorMap tmDQ, Params p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_unit, s_abort;
   if (p.err && (*reinterpret_cast<volatile int*>(p.err) & (1 << TREE_ERR_TIMEOUT))) return;
@@ -134,6 +144,8 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
       mbar_init(&S.drain_done[s], 4);
     }
     mbar_init(&S.mma_done, 1);
+    mbar_init(&S.stage_free, 1);
+    mbar_init(&S.stage_full, 4);
     fence_mbarrier_init();
     s_abort = 0;
   }
@@ -269,26 +281,39 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
           break;
         tc_fence_after();
         uint8_t* dsrow = S.ds[s] + r * 128;
+        // every query of the tile sees this key (no per-element test needed)?
+        const bool all_vis = __all_sync(0xffffffffu, j <= i0 && ej >= i0 + BQ - 1);
+        const float4* l4 = reinterpret_cast<const float4*>(S.lse2[st]);
+        const float4* d4 = reinterpret_cast<const float4*>(S.delta[st]);
 #pragma unroll 1
         for (int c = 0; c < 2; ++c) {
           uint32_t sv[32], dp[32], pk[16], dk[16];
           tmem_ld32(tS + c * 32, sv);
           tmem_ld32(tD + c * 32, dp);
           tmem_ld_wait();
+          if (!all_vis) {
 #pragma unroll
-          for (int t2 = 0; t2 < 32; t2 += 2) {
-            float pr[2], dsv[2];
-#pragma unroll
-            for (int w = 0; w < 2; ++w) {
-              const int col = c * 32 + t2 + w;
-              const int i = i0 + col;
-              const bool vis = (j <= i) && (i <= ej);
-              const float pp = vis ? exp2f(__uint_as_float(sv[t2 + w]) * sl2 - S.lse2[st][col]) : 0.f;
-              pr[w] = pp;
-              dsv[w] = pp * (__uint_as_float(dp[t2 + w]) - S.delta[st][col]);
+            for (int t2 = 0; t2 < 32; ++t2) {
+              const int i = i0 + c * 32 + t2;
+              if (!((j <= i) && (i <= ej))) sv[t2] = 0xff800000u;  // -inf: p = 0
             }
-            pk[t2 / 2] = pack_bf16(pr[0], pr[1]);
-            dk[t2 / 2] = pack_bf16(dsv[0], dsv[1]);
+          }
+#pragma unroll
+          for (int t4 = 0; t4 < 8; ++t4) {
+            const float4 L = l4[c * 8 + t4], Dl = d4[c * 8 + t4];
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const int t2 = t4 * 4 + h2 * 2;
+              const float2 lv = h2 ? make_float2(L.z, L.w) : make_float2(L.x, L.y);
+              const float2 dv = h2 ? make_float2(Dl.z, Dl.w) : make_float2(Dl.x, Dl.y);
+              const float2 x = __ffma2_rn(make_float2(__uint_as_float(sv[t2]), __uint_as_float(sv[t2 + 1])),
+                                          make_float2(sl2, sl2), make_float2(-lv.x, -lv.y));
+              const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+              const float2 dd = __fmul2_rn(pp, __fadd2_rn(make_float2(__uint_as_float(dp[t2]), __uint_as_float(dp[t2 + 1])),
+                                                          make_float2(-dv.x, -dv.y)));
+              pk[t2 / 2] = pack_bf16(pp.x, pp.y);
+              dk[t2 / 2] = pack_bf16(dd.x, dd.y);
+            }
           }
           tmem_st16(tS + c * 16, pk);
 #pragma unroll
@@ -303,7 +328,8 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.ds_ready[s]);
         // dQ^T of this step: TMEM lane = head dimension r, column = query. Free the
-        // columns as soon as they are in registers, then reduce into the accumulator.
+        // columns once they are in registers, write scale * dQ row-major into the staging
+        // buffer, and add the 64 x 128 tile into the fp32 accumulator with one TMA reduce.
         if (!(ok = __all_sync(0xffffffffu, mbar_wait(&S.dq_full[s], (g >> 1) & 1, p.err)))) break;
         tc_fence_after();
         uint32_t v0[32], v1[32];
@@ -313,15 +339,24 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.drain_done[s]);
-        float* base = p.dq_acc + static_cast<int64_t>(h) * D + r;
-        const int64_t row_stride = static_cast<int64_t>(p.Hq) * D;
-        const int n_rows = min(BQ, p.T - i0);
+        // the staging buffer serves the steps in order: wait for step g-1's reduce to read it
+        if (g > 0 && !(ok = __all_sync(0xffffffffu, mbar_wait(&S.stage_free, (g - 1) & 1, p.err)))) break;
 #pragma unroll
-        for (int t2 = 0; t2 < 32; ++t2)
-          if (t2 < n_rows) red_add(base + (i0 + t2) * row_stride, __uint_as_float(v0[t2]) * p.scale);
-#pragma unroll
-        for (int t2 = 0; t2 < 32; ++t2)
-          if (32 + t2 < n_rows) red_add(base + (i0 + 32 + t2) * row_stride, __uint_as_float(v1[t2]) * p.scale);
+        for (int t2 = 0; t2 < 32; ++t2) {
+          S.dq_stage[t2 * D + r] = __uint_as_float(v0[t2]) * p.scale;
+          S.dq_stage[(32 + t2) * D + r] = __uint_as_float(v1[t2]) * p.scale;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.stage_full);
+        if (q4 == 0 && lane == 0) {  // one thread issues the reduce once all four warps wrote
+          if (mbar_wait(&S.stage_full, g & 1, p.err)) {
+            tma_reduce_add_3d(&tmDQ, S.dq_stage, 0, h, i0);
+            bulk_commit();
+            bulk_wait_read0();
+          }
+          mbar_arrive(&S.stage_free);
+        }
       }
       // unit epilogue: warps 0-3 add scale * dK, warps 4-7 add dV (one key row per thread)
       ok = __all_sync(0xffffffffu, ok && mbar_wait(&S.mma_done, uit & 1, p.err));
@@ -526,10 +561,17 @@ int attn_bwd_tc(const AttnArgs& a, cudaStream_t st) {
         a.Hq, a.Hkv, a.ws.lse2_pad, a.ws.delta_pad, a.ws.dq_acc, a.ws.dk_acc, a.ws.dv_acc);
     TREE_LAUNCH_CHECK("attn_bwd_pre_kernel");
   }
-  CUtensorMap mk, mv, mq, mdo;
+  CUtensorMap mk, mv, mq, mdo, mdq;
   if ((rc = rows_map(&mk, a.k, a.T, a.Hkv, 128)) || (rc = rows_map(&mv, a.v, a.T, a.Hkv, 128)) ||
       (rc = rows_map(&mq, a.q, a.T, a.Hq, BQ)) || (rc = rows_map(&mdo, a.dout, a.T, a.Hq, BQ)))
     return rc;
+  {
+    // fp32 dQ accumulator [T, Hq, 128] as {d, head, row}, box {128, 1, 64}, no swizzle
+    const uint64_t dims[3] = {128, static_cast<uint64_t>(a.Hq), static_cast<uint64_t>(a.T)};
+    const uint64_t strides[2] = {128 * 4, static_cast<uint64_t>(a.Hq) * 128 * 4};
+    const uint32_t box[3] = {128, 1, BQ};
+    if ((rc = make_tmap(&mdq, a.ws.dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, dims, strides, box, false))) return rc;
+  }
   static bool attr_set = false;
   if (!attr_set) {
     TREE_CUDA_TRY(cudaFuncSetAttribute(attn_bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -557,7 +599,7 @@ int attn_bwd_tc(const AttnArgs& a, cudaStream_t st) {
   p.counter = a.ws.counter;
   p.err = device_error_word();
   const int grid = static_cast<int>(std::min<int64_t>(n_sm, max_units));
-  attn_bwd_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(mk, mv, mq, mdo, p);
+  attn_bwd_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(mk, mv, mq, mdo, mdq, p);
   TREE_LAUNCH_CHECK("attn_bwd_tc_kernel");
   auto convert = [&](const float* src, void* dst, int64_t n) -> int {
     const int64_t n4 = n / 4;

@@ -69,6 +69,13 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       : "memory");
 }
 
+// 2^x on the SFU (ex2.approx.ftz: ~2 ulp, flushes subnormal results to zero).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Masked, scaled scores of 32 keys (j0 .. j0+31) for query row i.
 __device__ __forceinline__ void scores32(const uint32_t (&raw)[32], float (&s)[32], float sl2, bool partial,
                                          const int32_t* __restrict__ endp, int j0, int i) {
@@ -91,7 +98,7 @@ __device__ __forceinline__ void scores32(const uint32_t (&raw)[32], float (&s)[3
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __maxnreg__(200)
 attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -212,33 +219,45 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     float m_run = -INFINITY, l = 0.f;
     int n = 0;
     bool ok = true;
+    const float rescale_raw = kRescaleLog2 / sl2;  // the 2^8 threshold in raw score units
     for (int kt = 0; kt <= qt; ++kt) {
       if (p.kmax[kt] < i0) continue;
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(&S.s_full[h], n & 1, p.err)))) break;
       tc_fence_after();
       const int j0 = kt * BN;
       const bool partial = !(j0 + BN - 1 <= i0 && p.kmin[kt] >= i0 + BM - 1);
-      float mt = -INFINITY;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t raw[32];
-        float s[32];
-        tmem_ld32(tS + c * 32, raw);
-        tmem_ld_wait();
-        scores32(raw, s, sl2, partial, p.endp, j0 + 32 * c, i);
+      // one pass over the row's 128 scores: all four TMEM loads in flight, one wait
+      uint32_t sr[128];
 #pragma unroll
-        for (int t = 0; t < 32; ++t) mt = fmaxf(mt, s[t]);
+      for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
+      tmem_ld_wait();
+      if (partial) {
+        const int4* e4 = reinterpret_cast<const int4*>(p.endp + j0);
+#pragma unroll
+        for (int g = 0; g < 32; ++g) {
+          const int4 e = __ldg(e4 + g);
+          const int ev[4] = {e.x, e.y, e.z, e.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int t = 4 * g + u;
+            if (!((j0 + t <= i) && (i <= ev[u]))) sr[t] = 0xff800000u;  // -inf
+          }
+        }
       }
+      float mt = -INFINITY;
+#pragma unroll
+      for (int t = 0; t < 128; ++t) mt = fmaxf(mt, __uint_as_float(sr[t]));
+      // lazy rescaling (raw score units): move the running max only when it grows by > 2^8
       float new_m = m_run;
       bool need = false;
-      if (mt > m_run + kRescaleLog2) {
+      if (mt > m_run + rescale_raw) {
         new_m = mt;
         need = m_run != -INFINITY;
       }
       if (__any_sync(0xffffffffu, need)) {
         if (!(ok = __all_sync(0xffffffffu, mbar_wait(&S.o_done[h], (n - 1) & 1, p.err)))) break;
         tc_fence_after();
-        const float corr = need ? exp2f(m_run - new_m) : 1.f;
+        const float corr = need ? ex2_approx((m_run - new_m) * sl2) : 1.f;
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t o[32];
@@ -250,24 +269,22 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         }
         tmem_st_wait();
       }
-      if (need) l *= exp2f(m_run - new_m);
+      if (need) l *= ex2_approx((m_run - new_m) * sl2);
       m_run = new_m;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t raw[32], pk[16];
-        float s[32];
-        tmem_ld32(tS + c * 32, raw);
-        tmem_ld_wait();
-        scores32(raw, s, sl2, partial, p.endp, j0 + 32 * c, i);
+      // p = 2^(s * scale * log2(e) - m2): one packed FFMA and one ex2 per score
+      const float m2 = m_run == -INFINITY ? 0.f : m_run * sl2;
+      const float2 scl = make_float2(sl2, sl2), off = make_float2(-m2, -m2);
+      float2 lsum = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int t = 0; t < 32; t += 2) {
-          const float p0 = s[t] == -INFINITY ? 0.f : exp2f(s[t] - m_run);
-          const float p1 = s[t + 1] == -INFINITY ? 0.f : exp2f(s[t + 1] - m_run);
-          l += p0 + p1;
-          pk[t / 2] = pack_bf16(p0, p1);
-        }
-        tmem_st16(tS + c * 16, pk);
+      for (int t = 0; t < 64; ++t) {
+        const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[2 * t]), __uint_as_float(sr[2 * t + 1])), scl, off);
+        const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+        lsum = __fadd2_rn(lsum, pp);
+        sr[t] = pack_bf16(pp.x, pp.y);  // P packed over the front half (already consumed)
       }
+      l += lsum.x + lsum.y;
+      tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
