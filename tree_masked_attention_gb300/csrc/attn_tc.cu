@@ -98,7 +98,7 @@ __device__ __forceinline__ void scores32(const uint32_t (&raw)[32], float (&s)[3
   }
 }
 
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -222,27 +222,34 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     const float rescale_raw = kRescaleLog2 / sl2;  // the 2^8 threshold in raw score units
     for (int kt = 0; kt <= qt; ++kt) {
       if (p.kmax[kt] < i0) continue;
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&S.s_full[h], n & 1, p.err)))) break;
-      tc_fence_after();
       const int j0 = kt * BN;
       const bool partial = !(j0 + BN - 1 <= i0 && p.kmin[kt] >= i0 + BM - 1);
+      // visibility bits of this row's 128 keys, formed while the MMA of S runs
+      uint32_t vis[4] = {~0u, ~0u, ~0u, ~0u};
+      if (partial) {
+        const int4* e4 = reinterpret_cast<const int4*>(p.endp + j0);
+#pragma unroll 4
+        for (int g = 0; g < 32; ++g) {
+          const int4 e = __ldg(e4 + g);
+          const int t = 4 * g;
+          const uint32_t bits = static_cast<uint32_t>((j0 + t <= i) && (i <= e.x)) |
+                                (static_cast<uint32_t>((j0 + t + 1 <= i) && (i <= e.y)) << 1) |
+                                (static_cast<uint32_t>((j0 + t + 2 <= i) && (i <= e.z)) << 2) |
+                                (static_cast<uint32_t>((j0 + t + 3 <= i) && (i <= e.w)) << 3);
+          vis[g >> 3] &= ~(0xFu << (t & 31)) | (bits << (t & 31));
+        }
+      }
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&S.s_full[h], n & 1, p.err)))) break;
+      tc_fence_after();
       // one pass over the row's 128 scores: all four TMEM loads in flight, one wait
       uint32_t sr[128];
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
       tmem_ld_wait();
       if (partial) {
-        const int4* e4 = reinterpret_cast<const int4*>(p.endp + j0);
 #pragma unroll
-        for (int g = 0; g < 32; ++g) {
-          const int4 e = __ldg(e4 + g);
-          const int ev[4] = {e.x, e.y, e.z, e.w};
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int t = 4 * g + u;
-            if (!((j0 + t <= i) && (i <= ev[u]))) sr[t] = 0xff800000u;  // -inf
-          }
-        }
+        for (int t = 0; t < 128; ++t)
+          if (!((vis[t >> 5] >> (t & 31)) & 1u)) sr[t] = 0xff800000u;  // -inf
       }
       float mt = -INFINITY;
 #pragma unroll
@@ -254,22 +261,8 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         new_m = mt;
         need = m_run != -INFINITY;
       }
-      if (__any_sync(0xffffffffu, need)) {
-        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&S.o_done[h], (n - 1) & 1, p.err)))) break;
-        tc_fence_after();
-        const float corr = need ? ex2_approx((m_run - new_m) * sl2) : 1.f;
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tO + c * 32, o);
-          tmem_ld_wait();
-#pragma unroll
-          for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * corr);
-          tmem_st32(tO + c * 32, o);
-        }
-        tmem_st_wait();
-      }
-      if (need) l *= ex2_approx((m_run - new_m) * sl2);
+      const float corr = need ? ex2_approx((m_run - new_m) * sl2) : 1.f;
+      if (need) l *= corr;
       m_run = new_m;
       // p = 2^(s * scale * log2(e) - m2): one packed FFMA and one ex2 per score
       const float m2 = m_run == -INFINITY ? 0.f : m_run * sl2;
@@ -285,6 +278,20 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       l += lsum.x + lsum.y;
       tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
       tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      // rescale O (after PV of the previous tile completed) before PV of this tile is issued
+      if (__any_sync(0xffffffffu, need)) {
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&S.o_done[h], (n - 1) & 1, p.err)))) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + c * 32, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * corr);
+          tmem_st32(tO + c * 32, o);
+        }
+      }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
