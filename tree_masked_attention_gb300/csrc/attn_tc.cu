@@ -323,7 +323,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
           *reinterpret_cast<uint4*>(row + chunk * 16) = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
         }
       }
-      if (i < p.T) p.lse[static_cast<int64_t>(h0 + h) * p.T + i] = (m_run + log2f(l)) * 0.6931471805599453f;
+      if (i < p.T) p.lse[static_cast<int64_t>(h0 + h) * p.T + i] = (m_run * sl2 + log2f(l)) * 0.6931471805599453f;
     }
     fence_proxy_async_smem();
     asm volatile("bar.sync %0, 128;" ::"r"(1 + h) : "memory");
