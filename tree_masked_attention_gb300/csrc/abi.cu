@@ -47,6 +47,7 @@ size_t attn_ws_layout(int64_t T, int Hq, int Hkv, int d, int dtype, void* base, 
   w.units = c.take<int32_t>(static_cast<size_t>(attn_bwd_max_units(T, Hkv)) * 4);
   w.n_units = c.take<int32_t>(1);
   w.counter = c.take<int32_t>(1);
+  w.bucket = c.take<int32_t>(static_cast<size_t>((T + 63) / 64) + 1);
   if (ws) *ws = w;
   return round_up(c.off, 256);
 }

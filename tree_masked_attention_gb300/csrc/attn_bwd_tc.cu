@@ -112,7 +112,8 @@ __device__ __forceinline__ int key_tile_queries(const Params& p, int kt, int* qt
 }
 
 // Persistent: each CTA takes work units {key tile, KV head, steps [b, e)} from a counter.
-// Step t of a key tile is query head kvh*G + t / nq and query tile qt_lo + t % nq.
+// Step t of a key tile is query tile qt_lo + t / G and query head kvh*G + t % G (query
+// position outermost, so a unit covers whole query tiles for every head of the group).
 // Barrier phases run on over the CTA's whole life: g counts its steps, uit its units.
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
@@ -194,8 +195,8 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
             s_abort = 1;
             break;
           }
-          const int h = kvh * G + t / nq;
-          const int i0 = (qt_lo + t % nq) * BQ;
+          const int h = kvh * G + t % G;
+          const int i0 = (qt_lo + t / G) * BQ;
           mbar_arrive_expect_tx(&S.qdo_full[st], 2 * kQTile + 2 * BQ * 4);
           tma_load_3d(S.q[st], &tmQ, &S.qdo_full[st], 0, h, i0);
           tma_load_3d(S.q[st] + kQSub, &tmQ, &S.qdo_full[st], 64, h, i0);
@@ -274,8 +275,8 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
       bool ok = true;
       for (int l = ((g0 & 1) == s) ? 0 : 1; l < L; l += 2) {
         const int g = g0 + l, st = g % NST, t = b + l;
-        const int h = kvh * G + t / nq;
-        const int i0 = (qt_lo + t % nq) * BQ;
+        const int h = kvh * G + t % G;
+        const int i0 = (qt_lo + t / G) * BQ;
         if (!(ok = __all_sync(0xffffffffu, mbar_wait(&S.s_full[s], (g >> 1) & 1, p.err) &&
                                                mbar_wait(&S.qdo_full[st], (g / NST) & 1, p.err))))
           break;
@@ -404,72 +405,73 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
   }
 }
 
-// Builds the work units: every key tile's steps (G query heads x its query tiles) cut
-// into chunks of at most `chunk` steps, for every KV head; the chunk size grows with the
-// total work so that there are at most about 4096 + Hkv * n_kt units. One block.
+// Builds the work units. Every key tile's steps (its 64-row query tiles x the G query
+// heads of the group) are cut into chunks of chunk_q whole query tiles, chunk_q growing
+// with the total work so that there are at most about 4096 + Hkv * n_kt units; the units
+// of all key tiles are then ordered by the first query tile they cover (a counting sort),
+// so the CTAs running at the same time work on nearby query rows and share the Q / dO
+// tiles and the dQ accumulator lines in L2. One block; `bucket` holds n_q64 + 1 ints.
 __global__ void attn_bwd_plan_kernel(const int32_t* __restrict__ kmax, int n_kt, int T, int G, int Hkv,
                                      int max_units, int4* __restrict__ units, int* __restrict__ n_units,
-                                     int* __restrict__ counter) {
+                                     int* __restrict__ counter, int* __restrict__ bucket) {
   __shared__ long long s_total;
-  __shared__ int s_carry;
-  __shared__ int warp_sums[32];
+  __shared__ int s_units;
+  const int n_q64 = (T + BQ - 1) / BQ;
   if (threadIdx.x == 0) {
     s_total = 0;
-    s_carry = 0;
+    s_units = 0;
     *counter = 0;
   }
+  for (int b = threadIdx.x; b <= n_q64; b += blockDim.x) bucket[b] = 0;
   __syncthreads();
-  auto steps_of = [&](int kt) -> int {
+  auto tiles_of = [&](int kt, int* lo) -> int {
     const int j0 = kt * BN;
     const int last_row = min(kmax[kt], T - 1);
-    const int lo = j0 / BQ;
-    return last_row >= j0 ? G * (last_row / BQ - lo + 1) : 0;
+    *lo = j0 / BQ;
+    return last_row >= j0 ? last_row / BQ - *lo + 1 : 0;
   };
   long long local = 0;
-  for (int kt = threadIdx.x; kt < n_kt; kt += blockDim.x) local += steps_of(kt);
+  for (int kt = threadIdx.x; kt < n_kt; kt += blockDim.x) {
+    int lo;
+    local += tiles_of(kt, &lo);
+  }
   atomicAdd(reinterpret_cast<unsigned long long*>(&s_total), static_cast<unsigned long long>(local));
   __syncthreads();
-  const long long per_head_total = s_total;
-  const int chunk = static_cast<int>(max(32LL, (per_head_total * Hkv + 4095) / 4096));
-  // exclusive scan of chunk counts over key tiles, blockDim.x tiles at a time
-  const int lane = threadIdx.x % 32, wid = threadIdx.x / 32, nw = blockDim.x / 32;
-  for (int base = 0; base < n_kt; base += blockDim.x) {
-    const int kt = base + threadIdx.x;
-    const int st = kt < n_kt ? steps_of(kt) : 0;
-    const int c = (st + chunk - 1) / chunk;
-    int x = c;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
-    }
-    if (lane == 31) warp_sums[wid] = x;
-    __syncthreads();
-    if (wid == 0) {
-      int w = lane < nw ? warp_sums[lane] : 0;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, w, o);
-        if (lane >= o) w += y;
-      }
-      if (lane < nw) warp_sums[lane] = w;
-    }
-    __syncthreads();
-    const int incl = x + (wid > 0 ? warp_sums[wid - 1] : 0) + s_carry;
-    const int first = incl - c;
-    for (int q = 0; q < c; ++q)
-      for (int kvh = 0; kvh < Hkv; ++kvh) {
-        const int idx = (first + q) * Hkv + kvh;
-        if (idx < max_units) units[idx] = make_int4(kt, kvh, q * chunk, min((q + 1) * chunk, st));
-      }
-    __syncthreads();
-    if (threadIdx.x == blockDim.x - 1) s_carry = incl;
-    __syncthreads();
+  const long long steps_all = s_total * G * Hkv;
+  const int chunk_steps = static_cast<int>(max(32LL, (steps_all + 4095) / 4096));
+  const int chunk_q = (chunk_steps + G - 1) / G;
+  // count units per first query tile
+  for (int kt = threadIdx.x; kt < n_kt; kt += blockDim.x) {
+    int lo;
+    const int nq = tiles_of(kt, &lo);
+    for (int c = 0; c * chunk_q < nq; ++c) atomicAdd(&bucket[lo + c * chunk_q], 1);
   }
-  if (threadIdx.x == 0) *n_units = min(s_carry * Hkv, max_units);
+  __syncthreads();
+  if (threadIdx.x == 0) {  // exclusive scan, in units of (key tile, chunk) pairs
+    int run = 0;
+    for (int b = 0; b < n_q64; ++b) {
+      const int x = bucket[b];
+      bucket[b] = run;
+      run += x;
+    }
+    bucket[n_q64] = run;
+    s_units = run;
+  }
+  __syncthreads();
+  for (int kt = threadIdx.x; kt < n_kt; kt += blockDim.x) {
+    int lo;
+    const int nq = tiles_of(kt, &lo);
+    for (int c = 0; c * chunk_q < nq; ++c) {
+      const int pos = atomicAdd(&bucket[lo + c * chunk_q], 1);
+      const int b0 = c * chunk_q * G, b1 = min((c + 1) * chunk_q, nq) * G;
+      for (int kvh = 0; kvh < Hkv; ++kvh) {
+        const int idx = pos * Hkv + kvh;
+        if (idx < max_units) units[idx] = make_int4(kt, kvh, b0, b1);
+      }
+    }
+  }
+  if (threadIdx.x == 0) *n_units = min(s_units * Hkv, max_units);
 }
-
-}  // namespace tcbwd
 
 // Delta = dO . O and LSE * log2(e) per (row, head), padded to T_pad with (0, +inf);
 // zeroes the fp32 dQ, dK and dV accumulators. One warp per (row, head), 4 dims per lane.
@@ -552,7 +554,7 @@ int attn_bwd_tc(const AttnArgs& a, cudaStream_t st) {
   const int max_units = static_cast<int>(attn_bwd_max_units(a.T, a.Hkv));
   attn_bwd_plan_kernel<<<1, 1024, 0, st>>>(a.ws.kmax128, n_kt, static_cast<int>(a.T), a.Hq / a.Hkv, a.Hkv,
                                            max_units, reinterpret_cast<int4*>(a.ws.units), a.ws.n_units,
-                                           a.ws.counter);
+                                           a.ws.counter, a.ws.bucket);
   TREE_LAUNCH_CHECK("attn_bwd_plan_kernel");
   {
     const int64_t warps = T_pad * a.Hq;

@@ -23,6 +23,7 @@ struct AttnWs {
   int32_t* units;    // [max_units * 4] backward work units {key tile, KV head, first step, end step}
   int32_t* n_units;  // [1]
   int32_t* counter;  // [1] next unit to hand out
+  int32_t* bucket;   // [ceil(T/64) + 1] planner: units per first query tile
 };
 
 struct AttnArgs {

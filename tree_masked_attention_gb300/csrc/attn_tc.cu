@@ -76,6 +76,23 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// Bit t set iff key jb + t is visible to query i (jb <= i <= subtree_end[jb + t]).
+__device__ __forceinline__ uint32_t visible32(const int32_t* __restrict__ endp, int jb, int i) {
+  const int4* e4 = reinterpret_cast<const int4*>(endp + jb);
+  uint32_t bits = 0;
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    const int4 e = __ldg(e4 + g);
+    const int t = 4 * g;
+    bits |= (static_cast<uint32_t>((jb + t <= i) && (i <= e.x)) |
+             (static_cast<uint32_t>((jb + t + 1 <= i) && (i <= e.y)) << 1) |
+             (static_cast<uint32_t>((jb + t + 2 <= i) && (i <= e.z)) << 2) |
+             (static_cast<uint32_t>((jb + t + 3 <= i) && (i <= e.w)) << 3))
+            << t;
+  }
+  return bits;
+}
+
 // Masked, scaled scores of 32 keys (j0 .. j0+31) for query row i.
 __device__ __forceinline__ void scores32(const uint32_t (&raw)[32], float (&s)[32], float sl2, bool partial,
                                          const int32_t* __restrict__ endp, int j0, int i) {
@@ -227,33 +244,26 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       // visibility bits of this row's 128 keys, formed while the MMA of S runs
       uint32_t vis[4] = {~0u, ~0u, ~0u, ~0u};
       if (partial) {
-        const int4* e4 = reinterpret_cast<const int4*>(p.endp + j0);
-#pragma unroll 4
-        for (int g = 0; g < 32; ++g) {
-          const int4 e = __ldg(e4 + g);
-          const int t = 4 * g;
-          const uint32_t bits = static_cast<uint32_t>((j0 + t <= i) && (i <= e.x)) |
-                                (static_cast<uint32_t>((j0 + t + 1 <= i) && (i <= e.y)) << 1) |
-                                (static_cast<uint32_t>((j0 + t + 2 <= i) && (i <= e.z)) << 2) |
-                                (static_cast<uint32_t>((j0 + t + 3 <= i) && (i <= e.w)) << 3);
-          vis[g >> 3] &= ~(0xFu << (t & 31)) | (bits << (t & 31));
-        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) vis[c] = visible32(p.endp, j0 + 32 * c, i);
       }
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(&S.s_full[h], n & 1, p.err)))) break;
       tc_fence_after();
-      // one pass over the row's 128 scores: all four TMEM loads in flight, one wait
-      uint32_t sr[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
-      tmem_ld_wait();
-      if (partial) {
-#pragma unroll
-        for (int t = 0; t < 128; ++t)
-          if (!((vis[t >> 5] >> (t & 31)) & 1u)) sr[t] = 0xff800000u;  // -inf
-      }
+      // pass 1: row max over the 128 scores, 64 columns per TMEM wait
       float mt = -INFINITY;
 #pragma unroll
-      for (int t = 0; t < 128; ++t) mt = fmaxf(mt, __uint_as_float(sr[t]));
+      for (int c = 0; c < 4; c += 2) {
+        uint32_t a[32], b[32];
+        tmem_ld32(tS + c * 32, a);
+        tmem_ld32(tS + c * 32 + 32, b);
+        tmem_ld_wait();
+#pragma unroll
+        for (int t = 0; t < 32; ++t) {
+          const bool va = !partial || ((vis[c] >> t) & 1u), vb = !partial || ((vis[c + 1] >> t) & 1u);
+          mt = fmaxf(mt, va ? __uint_as_float(a[t]) : -INFINITY);
+          mt = fmaxf(mt, vb ? __uint_as_float(b[t]) : -INFINITY);
+        }
+      }
       // lazy rescaling (raw score units): move the running max only when it grows by > 2^8
       float new_m = m_run;
       bool need = false;
@@ -264,20 +274,33 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       const float corr = need ? ex2_approx((m_run - new_m) * sl2) : 1.f;
       if (need) l *= corr;
       m_run = new_m;
-      // p = 2^(s * scale * log2(e) - m2): one packed FFMA and one ex2 per score
+      // pass 2: p = 2^(s * scale * log2(e) - m2), one packed FFMA and one ex2 per score;
+      // P (bf16 pairs) of columns [32c, 32c+32) goes to TMEM columns [16c, 16c+16), which
+      // only overlap scores already read.
       const float m2 = m_run == -INFINITY ? 0.f : m_run * sl2;
       const float2 scl = make_float2(sl2, sl2), off = make_float2(-m2, -m2);
       float2 lsum = make_float2(0.f, 0.f);
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t a[32], pk[16];
+        tmem_ld32(tS + c * 32, a);
+        tmem_ld_wait();
+        if (partial) {
+          const uint32_t vm = c == 0 ? vis[0] : c == 1 ? vis[1] : c == 2 ? vis[2] : vis[3];
 #pragma unroll
-      for (int t = 0; t < 64; ++t) {
-        const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[2 * t]), __uint_as_float(sr[2 * t + 1])), scl, off);
-        const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-        lsum = __fadd2_rn(lsum, pp);
-        sr[t] = pack_bf16(pp.x, pp.y);  // P packed over the front half (already consumed)
+          for (int t = 0; t < 32; ++t)
+            if (!((vm >> t) & 1u)) a[t] = 0xff800000u;  // -inf: p = 0
+        }
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          const float2 x = __ffma2_rn(make_float2(__uint_as_float(a[2 * t]), __uint_as_float(a[2 * t + 1])), scl, off);
+          const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+          lsum = __fadd2_rn(lsum, pp);
+          pk[t] = pack_bf16(pp.x, pp.y);
+        }
+        tmem_st16(tS + c * 16, pk);
       }
       l += lsum.x + lsum.y;
-      tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
       // rescale O (after PV of the previous tile completed) before PV of this tile is issued
       if (__any_sync(0xffffffffu, need)) {
         if (!(ok = __all_sync(0xffffffffu, mbar_wait(&S.o_done[h], (n - 1) & 1, p.err)))) break;
