@@ -473,6 +473,8 @@ __global__ void attn_bwd_plan_kernel(const int32_t* __restrict__ kmax, int n_kt,
   if (threadIdx.x == 0) *n_units = min(s_units * Hkv, max_units);
 }
 
+}  // namespace tcbwd
+
 // Delta = dO . O and LSE * log2(e) per (row, head), padded to T_pad with (0, +inf);
 // zeroes the fp32 dQ, dK and dV accumulators. One warp per (row, head), 4 dims per lane.
 __global__ void attn_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
