@@ -407,7 +407,7 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
 
 // Builds the work units. Every key tile's steps (its 64-row query tiles x the G query
 // heads of the group) are cut into chunks of chunk_q whole query tiles, chunk_q growing
-// with the total work so that there are at most about 4096 + Hkv * n_kt units; the units
+// with the total work so that there are at most about 1216 + Hkv * n_kt units; the units
 // of all key tiles are then ordered by the first query tile they cover (a counting sort),
 // so the CTAs running at the same time work on nearby query rows and share the Q / dO
 // tiles and the dQ accumulator lines in L2. One block; `bucket` holds n_q64 + 1 ints.
@@ -438,7 +438,7 @@ __global__ void attn_bwd_plan_kernel(const int32_t* __restrict__ kmax, int n_kt,
   atomicAdd(reinterpret_cast<unsigned long long*>(&s_total), static_cast<unsigned long long>(local));
   __syncthreads();
   const long long steps_all = s_total * G * Hkv;
-  const int chunk_steps = static_cast<int>(max(32LL, (steps_all + 4095) / 4096));
+  const int chunk_steps = static_cast<int>(max(32LL, (steps_all + 1215) / 1216));  // ~8 units per SM
   const int chunk_q = (chunk_steps + G - 1) / G;
   // count units per first query tile
   for (int kt = threadIdx.x; kt < n_kt; kt += blockDim.x) {

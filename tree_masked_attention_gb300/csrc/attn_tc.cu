@@ -249,21 +249,23 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       }
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(&S.s_full[h], n & 1, p.err)))) break;
       tc_fence_after();
-      // pass 1: row max over the 128 scores, 64 columns per TMEM wait
-      float mt = -INFINITY;
+      // one pass over the row's 128 scores: all four TMEM loads in flight, one wait
+      uint32_t sr[128];
 #pragma unroll
-      for (int c = 0; c < 4; c += 2) {
-        uint32_t a[32], b[32];
-        tmem_ld32(tS + c * 32, a);
-        tmem_ld32(tS + c * 32 + 32, b);
-        tmem_ld_wait();
+      for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
+      tmem_ld_wait();
+      if (partial) {
 #pragma unroll
-        for (int t = 0; t < 32; ++t) {
-          const bool va = !partial || ((vis[c] >> t) & 1u), vb = !partial || ((vis[c + 1] >> t) & 1u);
-          mt = fmaxf(mt, va ? __uint_as_float(a[t]) : -INFINITY);
-          mt = fmaxf(mt, vb ? __uint_as_float(b[t]) : -INFINITY);
-        }
+        for (int t = 0; t < 128; ++t)
+          if (!((vis[t >> 5] >> (t & 31)) & 1u)) sr[t] = 0xff800000u;  // -inf: p = 0
       }
+      // row max with eight independent chains (short dependency chains, not one of 128)
+      float m8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) m8[u] = __uint_as_float(sr[u]);
+#pragma unroll
+      for (int t = 8; t < 128; ++t) m8[t & 7] = fmaxf(m8[t & 7], __uint_as_float(sr[t]));
+      const float mt = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
       // lazy rescaling (raw score units): move the running max only when it grows by > 2^8
       float new_m = m_run;
       bool need = false;
@@ -274,33 +276,21 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       const float corr = need ? ex2_approx((m_run - new_m) * sl2) : 1.f;
       if (need) l *= corr;
       m_run = new_m;
-      // pass 2: p = 2^(s * scale * log2(e) - m2), one packed FFMA and one ex2 per score;
-      // P (bf16 pairs) of columns [32c, 32c+32) goes to TMEM columns [16c, 16c+16), which
-      // only overlap scores already read.
+      // p = 2^(s * scale * log2(e) - m2): one packed FFMA and one ex2 per score
       const float m2 = m_run == -INFINITY ? 0.f : m_run * sl2;
       const float2 scl = make_float2(sl2, sl2), off = make_float2(-m2, -m2);
-      float2 lsum = make_float2(0.f, 0.f);
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t a[32], pk[16];
-        tmem_ld32(tS + c * 32, a);
-        tmem_ld_wait();
-        if (partial) {
-          const uint32_t vm = c == 0 ? vis[0] : c == 1 ? vis[1] : c == 2 ? vis[2] : vis[3];
+      float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-          for (int t = 0; t < 32; ++t)
-            if (!((vm >> t) & 1u)) a[t] = 0xff800000u;  // -inf: p = 0
-        }
-#pragma unroll
-        for (int t = 0; t < 16; ++t) {
-          const float2 x = __ffma2_rn(make_float2(__uint_as_float(a[2 * t]), __uint_as_float(a[2 * t + 1])), scl, off);
-          const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-          lsum = __fadd2_rn(lsum, pp);
-          pk[t] = pack_bf16(pp.x, pp.y);
-        }
-        tmem_st16(tS + c * 16, pk);
+      for (int t = 0; t < 64; ++t) {
+        const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[2 * t]), __uint_as_float(sr[2 * t + 1])), scl, off);
+        const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+        ls[t & 3] = __fadd2_rn(ls[t & 3], pp);
+        sr[t] = pack_bf16(pp.x, pp.y);  // P packed over the front half (already consumed)
       }
+      const float2 lsum = __fadd2_rn(__fadd2_rn(ls[0], ls[1]), __fadd2_rn(ls[2], ls[3]));
       l += lsum.x + lsum.y;
+      tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
       // rescale O (after PV of the previous tile completed) before PV of this tile is issued
       if (__any_sync(0xffffffffu, need)) {
         if (!(ok = __all_sync(0xffffffffu, mbar_wait(&S.o_done[h], (n - 1) & 1, p.err)))) break;
