@@ -438,7 +438,8 @@ __global__ void attn_bwd_plan_kernel(const int32_t* __restrict__ kmax, int n_kt,
   atomicAdd(reinterpret_cast<unsigned long long*>(&s_total), static_cast<unsigned long long>(local));
   __syncthreads();
   const long long steps_all = s_total * G * Hkv;
-  const int chunk_steps = static_cast<int>(max(32LL, (steps_all + 1215) / 1216));  // ~8 units per SM
+  // ~8 units per SM on large trees; on small ones the 16-step floor keeps units short
+  const int chunk_steps = static_cast<int>(max(16LL, (steps_all + 1215) / 1216));
   const int chunk_q = (chunk_steps + G - 1) / G;
   // count units per first query tile
   for (int kt = threadIdx.x; kt < n_kt; kt += blockDim.x) {
@@ -513,15 +514,27 @@ __global__ void attn_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o, const _
   }
 }
 
-// bf16 from an fp32 accumulator, 4 elements per thread.
-__global__ void attn_f32_to_bf16_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ out, int64_t n4) {
-  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (t >= n4) return;
-  const float4 v = reinterpret_cast<const float4*>(acc)[t];
+// dQ, dK and dV (bf16) from their fp32 accumulators in one launch, 4 elements per thread.
+__global__ void attn_grads_to_bf16_kernel(const float* __restrict__ aq, __nv_bfloat16* __restrict__ oq, int64_t nq4,
+                                          const float* __restrict__ ak, __nv_bfloat16* __restrict__ ok, int64_t nk4,
+                                          const float* __restrict__ av, __nv_bfloat16* __restrict__ ov) {
+  int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const float* a;
+  __nv_bfloat16* o;
+  if (t < nq4) {
+    a = aq; o = oq;
+  } else if ((t -= nq4) < nk4) {
+    a = ak; o = ok;
+  } else if ((t -= nk4) < nk4) {
+    a = av; o = ov;
+  } else {
+    return;
+  }
+  const float4 v = reinterpret_cast<const float4*>(a)[t];
   uint2 u;
   u.x = sm100::pack_bf16(v.x, v.y);
   u.y = sm100::pack_bf16(v.z, v.w);
-  reinterpret_cast<uint2*>(out)[t] = u;
+  reinterpret_cast<uint2*>(o)[t] = u;
 }
 
 static int rows_map(CUtensorMap* m, const void* base, int64_t T, int H, uint32_t rows) {
@@ -605,16 +618,12 @@ int attn_bwd_tc(const AttnArgs& a, cudaStream_t st) {
   const int grid = static_cast<int>(std::min<int64_t>(n_sm, max_units));
   attn_bwd_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(mk, mv, mq, mdo, mdq, p);
   TREE_LAUNCH_CHECK("attn_bwd_tc_kernel");
-  auto convert = [&](const float* src, void* dst, int64_t n) -> int {
-    const int64_t n4 = n / 4;
-    attn_f32_to_bf16_kernel<<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, st>>>(
-        src, static_cast<__nv_bfloat16*>(dst), n4);
-    TREE_LAUNCH_CHECK("attn_f32_to_bf16_kernel");
-    return TREE_OK;
-  };
-  if ((rc = convert(a.ws.dq_acc, a.dq, a.T * a.Hq * a.d))) return rc;
-  if ((rc = convert(a.ws.dk_acc, a.dk, a.T * a.Hkv * a.d))) return rc;
-  return convert(a.ws.dv_acc, a.dv, a.T * a.Hkv * a.d);
+  const int64_t nq4 = a.T * a.Hq * a.d / 4, nk4 = a.T * a.Hkv * a.d / 4;
+  attn_grads_to_bf16_kernel<<<static_cast<unsigned>((nq4 + 2 * nk4 + 255) / 256), 256, 0, st>>>(
+      a.ws.dq_acc, static_cast<__nv_bfloat16*>(a.dq), nq4, a.ws.dk_acc, static_cast<__nv_bfloat16*>(a.dk), nk4,
+      a.ws.dv_acc, static_cast<__nv_bfloat16*>(a.dv));
+  TREE_LAUNCH_CHECK("attn_grads_to_bf16_kernel");
+  return TREE_OK;
 }
 
 }  // namespace tree

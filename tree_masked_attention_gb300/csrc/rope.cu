@@ -5,11 +5,12 @@
 // depth, the position it has in its own per-path sequence. Rotate-half pairing
 // (x[k], x[k + d/2]) with angle pos * base^(-2k/d).
 //
-// Memory-bound: every element of Q and K is read and written once. One thread
-// owns one row and 8 consecutive frequencies; it forms their 8 (cos, sin) pairs
-// once and applies them to that row in every head of Q and K, so sincosf runs
-// T * d/2 times instead of T * (Hq + Hkv) * d/2 times. Consecutive threads cover
-// consecutive 16-byte pieces of a row, so each warp access is fully coalesced.
+// Memory-bound: every element of Q and K is read and written once. One thread owns
+// one row, 8 consecutive frequencies and 4 heads (of Q, then K): it forms the 8
+// (cos, sin) pairs once and applies them to those 4 heads, so sincosf runs a quarter
+// as often as per element while the grid still has T * (d/16) * (Hq+Hkv)/4 threads
+// to keep every SM's memory pipe busy. Consecutive threads cover consecutive
+// 16-byte pieces of a head's row, so warp accesses are fully used 128-byte lines.
 #include <cmath>
 
 #include "common.h"
@@ -21,40 +22,42 @@ template <typename T>
 __global__ void rope_kernel(T* __restrict__ q, T* __restrict__ k, const int32_t* __restrict__ pos,
                             int64_t n_rows, int Hq, int Hkv, int d, float neg2_log2base_over_d,
                             float sign, int* err) {
+  constexpr int kHeadsPerThread = 4;
   const int groups = d / 16;  // groups of 8 frequencies per row
+  const int n_heads = Hq + Hkv, chunks = (n_heads + kHeadsPerThread - 1) / kHeadsPerThread;
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int64_t row = tid / groups;
   const int g = static_cast<int>(tid % groups);
+  const int64_t rest = tid / groups;
+  const int chunk = static_cast<int>(rest % chunks);
+  const int64_t row = rest / chunks;
   if (row >= n_rows) return;
-  const int p = pos[row];
-  if (p < 0) { raise_error(err, TREE_ERR_DEVICE_CHECK); return; }
+  const int p0 = pos[row];
+  if (p0 < 0) { raise_error(err, TREE_ERR_DEVICE_CHECK); return; }
   float c[8], s[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int kf = g * 8 + i;
     const float inv_freq = exp2f(static_cast<float>(kf) * neg2_log2base_over_d);
-    sincosf(static_cast<float>(p) * inv_freq, &s[i], &c[i]);
+    sincosf(static_cast<float>(p0) * inv_freq, &s[i], &c[i]);
     s[i] *= sign;
   }
   const int half = d / 2;
-  auto apply = [&](T* base, int H) {
-    if (!base) return;
-    T* r = base + row * static_cast<int64_t>(H) * d + g * 8;
-    for (int h = 0; h < H; ++h, r += d) {
-      float x1[8], x2[8], y1[8], y2[8];
-      load8(r, x1);
-      load8(r + half, x2);
+  for (int hh = chunk * kHeadsPerThread; hh < min(n_heads, (chunk + 1) * kHeadsPerThread); ++hh) {
+    T* base = hh < Hq ? q : k;
+    if (!base) continue;
+    const int H = hh < Hq ? Hq : Hkv, h = hh < Hq ? hh : hh - Hq;
+    T* r = base + (row * static_cast<int64_t>(H) + h) * d + g * 8;
+    float x1[8], x2[8], y1[8], y2[8];
+    load8(r, x1);
+    load8(r + half, x2);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        y1[i] = x1[i] * c[i] - x2[i] * s[i];
-        y2[i] = x2[i] * c[i] + x1[i] * s[i];
-      }
-      store8(r, y1);
-      store8(r + half, y2);
+    for (int i = 0; i < 8; ++i) {
+      y1[i] = x1[i] * c[i] - x2[i] * s[i];
+      y2[i] = x2[i] * c[i] + x1[i] * s[i];
     }
-  };
-  apply(q, Hq);
-  apply(k, Hkv);
+    store8(r, y1);
+    store8(r + half, y2);
+  }
 }
 
 // Scalar path for head sizes that are not a multiple of 16.
@@ -87,7 +90,7 @@ static int launch_rope(void* q, void* k, const int32_t* pos, int64_t n_rows, int
   const float sign = inverse ? -1.f : 1.f;
   int* err = device_error_word();
   if (d % 16 == 0) {
-    const int64_t threads = n_rows * (d / 16);
+    const int64_t threads = n_rows * (d / 16) * ((Hq + Hkv + 3) / 4);
     const int bs = 256;
     const int64_t grid = (threads + bs - 1) / bs;
     rope_kernel<T><<<static_cast<unsigned>(grid), bs, 0, st>>>(static_cast<T*>(q), static_cast<T*>(k), pos,
