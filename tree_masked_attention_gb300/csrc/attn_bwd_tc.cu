@@ -52,11 +52,14 @@ struct Smem {
   uint8_t q[NST][kQTile];
   uint8_t dout[NST][kQTile];
   uint8_t ds[2][kDsTile];
-  float dq_stage[BQ * D];   // scale * dQ of one step, row-major [64 queries][128 dims], for the TMA reduce
+  // scale * dQ of a step for the TMA reduce, row-major [32 queries][128 dims] per half: a
+  // stream stages queries 0-31 in its dS buffer (free once dK and dQ^T of the step are done)
+  // and queries 32-63 in its own half buffer, so the two streams never wait for each other
+  float dq_half[2][(BQ / 2) * D];
   float lse2[NST][BQ];
   float delta[NST][BQ];
   uint64_t kv_full, qdo_full[NST], qdo_empty[NST], s_full[2], ds_ready[2], dq_full[2], drain_done[2], mma_done,
-      stage_free, stage_full;
+      stage_free[2], stage_full[2];
   uint32_t tmem_base;
 };
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
@@ -145,8 +148,10 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
       mbar_init(&S.drain_done[s], 4);
     }
     mbar_init(&S.mma_done, 1);
-    mbar_init(&S.stage_free, 1);
-    mbar_init(&S.stage_full, 4);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&S.stage_free[s], 1);
+      mbar_init(&S.stage_full[s], 4);
+    }
     fence_mbarrier_init();
     s_abort = 0;
   }
@@ -280,6 +285,15 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         if (!(ok = __all_sync(0xffffffffu, mbar_wait(&S.s_full[s], (g >> 1) & 1, p.err) &&
                                                mbar_wait(&S.qdo_full[st], (g / NST) & 1, p.err))))
           break;
+        // dS[s] doubled as dQ staging in this stream's previous step: its reduce must have
+        // read it. The issuing thread waits for the read and releases the buffer.
+        if (g >= 2) {
+          if (q4 == 0 && lane == 0) {
+            bulk_wait_read0();
+            mbar_arrive(&S.stage_free[s]);
+          }
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait(&S.stage_free[s], ((g >> 1) - 1) & 1, p.err)))) break;
+        }
         tc_fence_after();
         uint8_t* dsrow = S.ds[s] + r * 128;
         // every query of the tile sees this key (no per-element test needed)?
@@ -340,23 +354,22 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.drain_done[s]);
-        // the staging buffer serves the steps in order: wait for step g-1's reduce to read it
-        if (g > 0 && !(ok = __all_sync(0xffffffffu, mbar_wait(&S.stage_free, (g - 1) & 1, p.err)))) break;
+        float* lo_half = reinterpret_cast<float*>(S.ds[s]);
+        float* hi_half = S.dq_half[s];
 #pragma unroll
         for (int t2 = 0; t2 < 32; ++t2) {
-          S.dq_stage[t2 * D + r] = __uint_as_float(v0[t2]) * p.scale;
-          S.dq_stage[(32 + t2) * D + r] = __uint_as_float(v1[t2]) * p.scale;
+          lo_half[t2 * D + r] = __uint_as_float(v0[t2]) * p.scale;
+          hi_half[t2 * D + r] = __uint_as_float(v1[t2]) * p.scale;
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&S.stage_full);
-        if (q4 == 0 && lane == 0) {  // one thread issues the reduce once all four warps wrote
-          if (mbar_wait(&S.stage_full, g & 1, p.err)) {
-            tma_reduce_add_3d(&tmDQ, S.dq_stage, 0, h, i0);
-            bulk_commit();
-            bulk_wait_read0();
+        if (lane == 0) mbar_arrive(&S.stage_full[s]);
+        if (q4 == 0 && lane == 0) {  // one thread issues the reduces once all four warps wrote
+          if (mbar_wait(&S.stage_full[s], (g >> 1) & 1, p.err)) {
+            tma_reduce_add_3d(&tmDQ, lo_half, 0, h, i0);
+            if (i0 + BQ / 2 < p.T) tma_reduce_add_3d(&tmDQ, hi_half, 0, h, i0 + BQ / 2);
+            bulk_commit();  // the read is waited for at this stream's next step (or at exit)
           }
-          mbar_arrive(&S.stage_free);
         }
       }
       // unit epilogue: warps 0-3 add scale * dK, warps 4-7 add dV (one key row per thread)
@@ -388,6 +401,8 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
     __syncthreads();
     tc_fence_after();
   }
+  // The dQ reduces issued last must have read their staging before the CTA exits.
+  if (warp < 8 && (warp & 3) == 0 && lane == 0) bulk_wait_read0();
   // On an early exit, leave no TMA copy or MMA in flight.
   if (s_abort && threadIdx.x == kWarpProducer * 32) {
     mbar_wait(&S.kv_full, (uit - 1) & 1, p.err);
@@ -586,7 +601,7 @@ int attn_bwd_tc(const AttnArgs& a, cudaStream_t st) {
     // fp32 dQ accumulator [T, Hq, 128] as {d, head, row}, box {128, 1, 64}, no swizzle
     const uint64_t dims[3] = {128, static_cast<uint64_t>(a.Hq), static_cast<uint64_t>(a.T)};
     const uint64_t strides[2] = {128 * 4, static_cast<uint64_t>(a.Hq) * 128 * 4};
-    const uint32_t box[3] = {128, 1, BQ};
+    const uint32_t box[3] = {128, 1, BQ / 2};
     if ((rc = make_tmap(&mdq, a.ws.dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, dims, strides, box, false))) return rc;
   }
   static bool attr_set = false;
