@@ -38,8 +38,11 @@ using namespace sm100;
 namespace tcbwd {
 
 constexpr int BN = 128, BQ = 64, D = 128, NST = 3;
-constexpr int kThreads = 320;
-constexpr int kWarpProducer = 8, kWarpMma = 9;
+constexpr int kThreads = 352;
+// warp 8: TMA; warp 9: issues S^T and dP^T (and owns TMEM); warp 10: issues dV, dK, dQ^T.
+// A tcgen05.mma issue occupies its issuing thread about as long as an N<=128 MMA runs, so
+// two issuers (disjoint accumulators) are needed to keep the tensor core busy.
+constexpr int kWarpProducer = 8, kWarpMma = 9, kWarpMma2 = 10;
 constexpr uint32_t kKSub = 128 * 128;          // 128 key rows x 128 B
 constexpr uint32_t kKTile = 2 * kKSub;         // K or V: 128 x 128 bf16
 constexpr uint32_t kQSub = BQ * 128;           // 64 query rows x 128 B
@@ -59,6 +62,7 @@ struct Smem {
   float lse2[NST][BQ];
   float delta[NST][BQ];
   uint64_t kv_full, qdo_full[NST], qdo_empty[NST], s_full[2], ds_ready[2], dq_full[2], drain_done[2], mma_done,
+      sdp_done,
       stage_free[2], stage_full[2];
   uint32_t tmem_base;
 };
@@ -148,6 +152,7 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
       mbar_init(&S.drain_done[s], 4);
     }
     mbar_init(&S.mma_done, 1);
+    mbar_init(&S.sdp_done, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&S.stage_free[s], 1);
       mbar_init(&S.stage_full[s], 4);
@@ -212,10 +217,9 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         }
       }
     } else if (warp == kWarpMma) {
+      // ---- issuer 1: S^T = K Q^T and dP^T = V dO^T of each step, one step ahead
       if (lane == 0) {
-        constexpr uint32_t id_s = idesc_bf16(BN, BQ, 0, 0);  // S^T, dP^T
-        constexpr uint32_t id_kv = idesc_bf16(BN, D, 0, 1);  // dV, dK (B MN-major)
-        constexpr uint32_t id_dq = idesc_bf16(D, BQ, 1, 1);  // dQ^T (A and B MN-major)
+        constexpr uint32_t id_s = idesc_bf16(BN, BQ, 0, 0);
         const uint32_t kb = smem_u32(S.k), vb = smem_u32(S.v);
         auto issue_sdp = [&](int g) -> bool {
           const int st = g % NST, s = g & 1;
@@ -237,14 +241,26 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
           return true;
         };
         bool ok = mbar_wait(&S.kv_full, uit & 1, p.err) && issue_sdp(g0);
+        for (int l = 0; ok && l + 1 < L; ++l) {
+          const int g = g0 + l;
+          // step g+1 reuses the buffers of step g-1: its dQ^T must have been drained
+          // (which also means issuer 2's dV of step g-1 has read P^T)
+          if (l >= 1 && !(ok = mbar_wait(&S.drain_done[(g - 1) & 1], ((g - 1) >> 1) & 1, p.err))) break;
+          tc_fence_after();
+          ok = issue_sdp(g + 1);
+        }
+        if (!ok) s_abort = 1;
+      }
+      __syncwarp();
+    } else if (warp == kWarpMma2) {
+      // ---- issuer 2: dV += P^T dO, dK += dS^T Q, dQ^T = K^T dS^T once the step's dS^T is ready
+      if (lane == 0) {
+        constexpr uint32_t id_kv = idesc_bf16(BN, D, 0, 1);  // dV, dK (B MN-major)
+        constexpr uint32_t id_dq = idesc_bf16(D, BQ, 1, 1);  // dQ^T (A and B MN-major)
+        const uint32_t kb = smem_u32(S.k);
+        bool ok = mbar_wait(&S.kv_full, uit & 1, p.err);  // K is read by dQ^T
         for (int l = 0; ok && l < L; ++l) {
           const int g = g0 + l, s = g & 1, st = g % NST;
-          if (l + 1 < L) {
-            // next step's S/dP go to the other stream, whose dQ^T of step g-1 must be drained
-            if (l >= 1 && !(ok = mbar_wait(&S.drain_done[s ^ 1], ((g - 1) >> 1) & 1, p.err))) break;
-            tc_fence_after();
-            if (!(ok = issue_sdp(g + 1))) break;
-          }
           if (!(ok = mbar_wait(&S.ds_ready[s], (g >> 1) & 1, p.err))) break;
           tc_fence_after();
           const uint32_t qb = smem_u32(S.q[st]), ob = smem_u32(S.dout[st]), db = smem_u32(S.ds[s]);
@@ -409,6 +425,10 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
     for (int g = (g0 > NST ? g0 - NST : 0); g < g0; ++g) mbar_wait(&S.qdo_full[g % NST], (g / NST) & 1, p.err);
   }
   if (s_abort && threadIdx.x == kWarpMma * 32) {
+    mma_commit(&S.sdp_done);
+    mbar_wait(&S.sdp_done, 0, p.err);
+  }
+  if (s_abort && threadIdx.x == kWarpMma2 * 32) {
     mma_commit(&S.mma_done);
     mbar_wait(&S.mma_done, uit & 1, p.err);
   }
