@@ -22,7 +22,7 @@
 // columns, plus dV and dK, 128 each), so the tensor core works on one stream while the
 // other stream's warps run the softmax backward or drain dQ.
 //   warps 0-3, 4-7  compute streams 0 and 1; at the end warps 0-3 write dK, 4-7 dV
-//   warp 8          TMA producer;  warp 9  MMA issuer (and TMEM owner)
+//   warp 8          TMA producer;  warps 9-11  MMA issuers (warp 9 owns TMEM)
 #include <algorithm>
 #include <cmath>
 
@@ -38,11 +38,14 @@ using namespace sm100;
 namespace tcbwd {
 
 constexpr int BN = 128, BQ = 64, D = 128, NST = 3;
-constexpr int kThreads = 352;
-// warp 8: TMA; warp 9: issues S^T and dP^T (and owns TMEM); warp 10: issues dV, dK, dQ^T.
-// A tcgen05.mma issue occupies its issuing thread about as long as an N<=128 MMA runs, so
-// two issuers (disjoint accumulators) are needed to keep the tensor core busy.
-constexpr int kWarpProducer = 8, kWarpMma = 9, kWarpMma2 = 10;
+constexpr int kThreads = 384;
+// warp 8: TMA. Three MMA-issuing warps (a tcgen05.mma issue occupies its thread about as
+// long as an N<=128 MMA runs, so one issuer cannot keep the tensor core busy):
+//   warp 9  (owns TMEM)  S^T and dP^T of a unit's first two steps, then dP^T of step g+2
+//                        once step g's dQ^T has been drained from the shared columns;
+//   warp 10              dV and dK of step g, then S^T of step g+2 (same stream, in order);
+//   warp 11              dQ^T of step g.
+constexpr int kWarpProducer = 8, kWarpMma = 9, kWarpMma2 = 10, kWarpMma3 = 11;
 constexpr uint32_t kKSub = 128 * 128;          // 128 key rows x 128 B
 constexpr uint32_t kKTile = 2 * kKSub;         // K or V: 128 x 128 bf16
 constexpr uint32_t kQSub = BQ * 128;           // 64 query rows x 128 B
@@ -62,8 +65,7 @@ struct Smem {
   float lse2[NST][BQ];
   float delta[NST][BQ];
   uint64_t kv_full, qdo_full[NST], qdo_empty[NST], s_full[2], ds_ready[2], dq_full[2], drain_done[2], mma_done,
-      sdp_done,
-      stage_free[2], stage_full[2];
+      sdp_done, dk_done[2], dq_done_all, stage_free[2], stage_full[2];
   uint32_t tmem_base;
 };
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
@@ -146,13 +148,15 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
       mbar_init(&S.qdo_empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&S.s_full[s], 1);
+      mbar_init(&S.s_full[s], 2);  // S^T and dP^T of a step come from two issuers
+      mbar_init(&S.dk_done[s], 1);
       mbar_init(&S.ds_ready[s], 4);
       mbar_init(&S.dq_full[s], 1);
       mbar_init(&S.drain_done[s], 4);
     }
     mbar_init(&S.mma_done, 1);
     mbar_init(&S.sdp_done, 1);
+    mbar_init(&S.dq_done_all, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&S.stage_free[s], 1);
       mbar_init(&S.stage_full[s], 4);
@@ -216,72 +220,72 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
           bulk_load(S.delta[st], p.delta + static_cast<int64_t>(h) * p.T_pad + i0, BQ * 4, &S.qdo_full[st]);
         }
       }
-    } else if (warp == kWarpMma) {
-      // ---- issuer 1: S^T = K Q^T and dP^T = V dO^T of each step, one step ahead
+    } else if (warp >= kWarpMma && warp <= kWarpMma3) {
       if (lane == 0) {
-        constexpr uint32_t id_s = idesc_bf16(BN, BQ, 0, 0);
+        constexpr uint32_t id_s = idesc_bf16(BN, BQ, 0, 0);  // S^T, dP^T
+        constexpr uint32_t id_kv = idesc_bf16(BN, D, 0, 1);  // dV, dK (B MN-major)
+        constexpr uint32_t id_dq = idesc_bf16(D, BQ, 1, 1);  // dQ^T (A and B MN-major)
         const uint32_t kb = smem_u32(S.k), vb = smem_u32(S.v);
-        auto issue_sdp = [&](int g) -> bool {
+        // one of S^T = K Q^T (kv = K) or dP^T = V dO^T (kv = V) of step g into its stream's columns
+        auto issue_one = [&](int g, bool is_s) -> bool {
           const int st = g % NST, s = g & 1;
           if (!mbar_wait(&S.qdo_full[st], (g / NST) & 1, p.err)) return false;
           tc_fence_after();
-          const uint32_t qb = smem_u32(S.q[st]), ob = smem_u32(S.dout[st]);
-          const uint32_t tS = tmem + s * 128, tD = tmem + s * 128 + 64;
+          const uint32_t xb = smem_u32(is_s ? S.q[st] : S.dout[st]), ab = is_s ? kb : vb;
+          const uint32_t d = tmem + s * 128 + (is_s ? 0 : 64);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t ka = (kk >> 2) * kKSub + (kk & 3) * 32, qa = (kk >> 2) * kQSub + (kk & 3) * 32;
-            mma_ss(tS, desc_sw128(kb + ka, 16, 1024), desc_sw128(qb + qa, 16, 1024), id_s, kk > 0);
-          }
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t ka = (kk >> 2) * kKSub + (kk & 3) * 32, qa = (kk >> 2) * kQSub + (kk & 3) * 32;
-            mma_ss(tD, desc_sw128(vb + ka, 16, 1024), desc_sw128(ob + qa, 16, 1024), id_s, kk > 0);
+            mma_ss(d, desc_sw128(ab + ka, 16, 1024), desc_sw128(xb + qa, 16, 1024), id_s, kk > 0);
           }
           mma_commit(&S.s_full[s]);
           return true;
         };
-        bool ok = mbar_wait(&S.kv_full, uit & 1, p.err) && issue_sdp(g0);
-        for (int l = 0; ok && l + 1 < L; ++l) {
-          const int g = g0 + l;
-          // step g+1 reuses the buffers of step g-1: its dQ^T must have been drained
-          // (which also means issuer 2's dV of step g-1 has read P^T)
-          if (l >= 1 && !(ok = mbar_wait(&S.drain_done[(g - 1) & 1], ((g - 1) >> 1) & 1, p.err))) break;
-          tc_fence_after();
-          ok = issue_sdp(g + 1);
+        bool ok = mbar_wait(&S.kv_full, uit & 1, p.err);
+        if (warp == kWarpMma) {
+          for (int l = 0; ok && l < min(2, L); ++l) ok = issue_one(g0 + l, true) && issue_one(g0 + l, false);
+          for (int l = 0; ok && l + 2 < L; ++l) {
+            const int g = g0 + l;
+            // dP^T of step g+2 overwrites the columns that held step g's dQ^T
+            if (!(ok = mbar_wait(&S.drain_done[g & 1], (g >> 1) & 1, p.err))) break;
+            tc_fence_after();
+            ok = issue_one(g + 2, false);
+          }
+        } else if (warp == kWarpMma2) {
+          for (int l = 0; ok && l < L; ++l) {
+            const int g = g0 + l, s = g & 1, st = g % NST;
+            if (!(ok = mbar_wait(&S.ds_ready[s], (g >> 1) & 1, p.err))) break;
+            tc_fence_after();
+            const uint32_t qb = smem_u32(S.q[st]), ob = smem_u32(S.dout[st]), db = smem_u32(S.ds[s]);
+            const uint32_t tS = tmem + s * 128;
+#pragma unroll
+            for (int kk = 0; kk < BQ / 16; ++kk)  // dV += P^T dO
+              mma_ts(tmem + kColDV, tS + kk * 8, desc_sw128(ob + kk * 2048, kQSub, 1024), id_kv,
+                     (l > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+            for (int kk = 0; kk < BQ / 16; ++kk)  // dK += dS^T Q
+              mma_ss(tmem + kColDK, desc_sw128(db + kk * 32, 16, 1024), desc_sw128(qb + kk * 2048, kQSub, 1024),
+                     id_kv, (l > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(&S.qdo_empty[st]);
+            mma_commit(&S.dk_done[s]);
+            // S^T of step g+2 reuses the columns whose P^T the dV above reads (same issuer: ordered)
+            if (l + 2 < L && !(ok = issue_one(g + 2, true))) break;
+          }
+          mma_commit(&S.mma_done);
+        } else {
+          for (int l = 0; ok && l < L; ++l) {
+            const int g = g0 + l, s = g & 1;
+            if (!(ok = mbar_wait(&S.ds_ready[s], (g >> 1) & 1, p.err))) break;
+            tc_fence_after();
+            const uint32_t db = smem_u32(S.ds[s]), tD = tmem + s * 128 + 64;
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk)  // dQ^T = K^T dS^T
+              mma_ss(tD, desc_sw128(kb + kk * 2048, kKSub, 1024), desc_sw128(db + kk * 2048, kQSub, 1024), id_dq,
+                     kk > 0);
+            mma_commit(&S.dq_full[s]);
+          }
         }
         if (!ok) s_abort = 1;
-      }
-      __syncwarp();
-    } else if (warp == kWarpMma2) {
-      // ---- issuer 2: dV += P^T dO, dK += dS^T Q, dQ^T = K^T dS^T once the step's dS^T is ready
-      if (lane == 0) {
-        constexpr uint32_t id_kv = idesc_bf16(BN, D, 0, 1);  // dV, dK (B MN-major)
-        constexpr uint32_t id_dq = idesc_bf16(D, BQ, 1, 1);  // dQ^T (A and B MN-major)
-        const uint32_t kb = smem_u32(S.k);
-        bool ok = mbar_wait(&S.kv_full, uit & 1, p.err);  // K is read by dQ^T
-        for (int l = 0; ok && l < L; ++l) {
-          const int g = g0 + l, s = g & 1, st = g % NST;
-          if (!(ok = mbar_wait(&S.ds_ready[s], (g >> 1) & 1, p.err))) break;
-          tc_fence_after();
-          const uint32_t qb = smem_u32(S.q[st]), ob = smem_u32(S.dout[st]), db = smem_u32(S.ds[s]);
-          const uint32_t tS = tmem + s * 128, tD = tmem + s * 128 + 64;
-#pragma unroll
-          for (int kk = 0; kk < BQ / 16; ++kk)  // dV += P^T dO
-            mma_ts(tmem + kColDV, tS + kk * 8, desc_sw128(ob + kk * 2048, kQSub, 1024), id_kv,
-                   (l > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-          for (int kk = 0; kk < BQ / 16; ++kk)  // dK += dS^T Q
-            mma_ss(tmem + kColDK, desc_sw128(db + kk * 32, 16, 1024), desc_sw128(qb + kk * 2048, kQSub, 1024),
-                   id_kv, (l > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&S.qdo_empty[st]);
-#pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)  // dQ^T = K^T dS^T
-            mma_ss(tD, desc_sw128(kb + kk * 2048, kKSub, 1024), desc_sw128(db + kk * 2048, kQSub, 1024), id_dq,
-                   kk > 0);
-          mma_commit(&S.dq_full[s]);
-        }
-        if (!ok) s_abort = 1;
-        mma_commit(&S.mma_done);
       }
       __syncwarp();
     } else if (warp < 8) {
@@ -316,42 +320,42 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         const bool all_vis = __all_sync(0xffffffffu, j <= i0 && ej >= i0 + BQ - 1);
         const float4* l4 = reinterpret_cast<const float4*>(S.lse2[st]);
         const float4* d4 = reinterpret_cast<const float4*>(S.delta[st]);
-#pragma unroll 1
-        for (int c = 0; c < 2; ++c) {
-          uint32_t sv[32], dp[32], pk[16], dk[16];
-          tmem_ld32(tS + c * 32, sv);
-          tmem_ld32(tD + c * 32, dp);
-          tmem_ld_wait();
-          if (!all_vis) {
+        // all 64 columns of S^T and dP^T in flight at once, one TMEM wait
+        uint32_t sv[64], dp[64], pk[32], dk[32];
+        tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+        tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+        tmem_ld32(tD, *reinterpret_cast<uint32_t(*)[32]>(&dp[0]));
+        tmem_ld32(tD + 32, *reinterpret_cast<uint32_t(*)[32]>(&dp[32]));
+        tmem_ld_wait();
+        if (!all_vis) {
 #pragma unroll
-            for (int t2 = 0; t2 < 32; ++t2) {
-              const int i = i0 + c * 32 + t2;
-              if (!((j <= i) && (i <= ej))) sv[t2] = 0xff800000u;  // -inf: p = 0
-            }
+          for (int t2 = 0; t2 < 64; ++t2) {
+            const int i = i0 + t2;
+            if (!((j <= i) && (i <= ej))) sv[t2] = 0xff800000u;  // -inf: p = 0
           }
+        }
 #pragma unroll
-          for (int t4 = 0; t4 < 8; ++t4) {
-            const float4 L = l4[c * 8 + t4], Dl = d4[c * 8 + t4];
+        for (int t4 = 0; t4 < 16; ++t4) {
+          const float4 L = l4[t4], Dl = d4[t4];
 #pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-              const int t2 = t4 * 4 + h2 * 2;
-              const float2 lv = h2 ? make_float2(L.z, L.w) : make_float2(L.x, L.y);
-              const float2 dv = h2 ? make_float2(Dl.z, Dl.w) : make_float2(Dl.x, Dl.y);
-              const float2 x = __ffma2_rn(make_float2(__uint_as_float(sv[t2]), __uint_as_float(sv[t2 + 1])),
-                                          make_float2(sl2, sl2), make_float2(-lv.x, -lv.y));
-              const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-              const float2 dd = __fmul2_rn(pp, __fadd2_rn(make_float2(__uint_as_float(dp[t2]), __uint_as_float(dp[t2 + 1])),
-                                                          make_float2(-dv.x, -dv.y)));
-              pk[t2 / 2] = pack_bf16(pp.x, pp.y);
-              dk[t2 / 2] = pack_bf16(dd.x, dd.y);
-            }
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const int t2 = t4 * 4 + h2 * 2;
+            const float2 lv = h2 ? make_float2(L.z, L.w) : make_float2(L.x, L.y);
+            const float2 dv = h2 ? make_float2(Dl.z, Dl.w) : make_float2(Dl.x, Dl.y);
+            const float2 x = __ffma2_rn(make_float2(__uint_as_float(sv[t2]), __uint_as_float(sv[t2 + 1])),
+                                        make_float2(sl2, sl2), make_float2(-lv.x, -lv.y));
+            const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+            const float2 dd = __fmul2_rn(pp, __fadd2_rn(make_float2(__uint_as_float(dp[t2]), __uint_as_float(dp[t2 + 1])),
+                                                        make_float2(-dv.x, -dv.y)));
+            pk[t2 / 2] = pack_bf16(pp.x, pp.y);
+            dk[t2 / 2] = pack_bf16(dd.x, dd.y);
           }
-          tmem_st16(tS + c * 16, pk);
+        }
+        tmem_st32(tS, pk);
 #pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            const int chunk = (c * 4 + w) ^ (r & 7);
-            *reinterpret_cast<uint4*>(dsrow + chunk * 16) = make_uint4(dk[4 * w], dk[4 * w + 1], dk[4 * w + 2], dk[4 * w + 3]);
-          }
+        for (int w = 0; w < 8; ++w) {
+          const int chunk = w ^ (r & 7);
+          *reinterpret_cast<uint4*>(dsrow + chunk * 16) = make_uint4(dk[4 * w], dk[4 * w + 1], dk[4 * w + 2], dk[4 * w + 3]);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -370,6 +374,8 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.drain_done[s]);
+        // dS[s] becomes staging: dK of this step (another issuer) must have read it
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&S.dk_done[s], (g >> 1) & 1, p.err)))) break;
         float* lo_half = reinterpret_cast<float*>(S.ds[s]);
         float* hi_half = S.dq_half[s];
 #pragma unroll
@@ -427,6 +433,10 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
   if (s_abort && threadIdx.x == kWarpMma * 32) {
     mma_commit(&S.sdp_done);
     mbar_wait(&S.sdp_done, 0, p.err);
+  }
+  if (s_abort && threadIdx.x == kWarpMma3 * 32) {
+    mma_commit(&S.dq_done_all);
+    mbar_wait(&S.dq_done_all, 0, p.err);
   }
   if (s_abort && threadIdx.x == kWarpMma2 * 32) {
     mma_commit(&S.mma_done);

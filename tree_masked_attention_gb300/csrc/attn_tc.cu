@@ -35,8 +35,8 @@ using namespace sm100;
 namespace tcfwd {
 
 constexpr int BM = 128, BN = 128, D = 128;
-constexpr int kThreads = 352;  // 8 softmax warps, TMA warp, two MMA warps (one per head)
-constexpr int kWarpProducer = 8, kWarpMma = 9;  // MMA warps 9 (head A) and 10 (head B)
+constexpr int kThreads = 320;  // 8 softmax warps, TMA warp, MMA warp
+constexpr int kWarpProducer = 8, kWarpMma = 9;
 constexpr uint32_t kSub = 128 * 128;   // 128 rows x 128 B (64 bf16): one swizzle-128 sub-tile
 constexpr uint32_t kTile = 2 * kSub;   // 128 rows x 128 bf16
 constexpr float kRescaleLog2 = 8.0f;   // rescale O only when the row max grows by > 2^8
@@ -45,7 +45,7 @@ struct Smem {
   uint8_t q[2][kTile];
   uint8_t k[2][kTile];
   uint8_t v[2][kTile];
-  uint64_t q_full, k_full[2], v_full[2], kv_empty[2], s_full[2], p_full[2], o_done[2], mma_done[2];
+  uint64_t q_full, k_full[2], v_full[2], kv_empty[2], s_full[2], p_full[2], o_done[2], mma_done;
   uint32_t tmem_base;
 };
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
@@ -134,13 +134,12 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     for (int s = 0; s < 2; ++s) {
       mbar_init(&S.k_full[s], 1);
       mbar_init(&S.v_full[s], 1);
-      mbar_init(&S.kv_empty[s], 2);  // released by both heads' PV
+      mbar_init(&S.kv_empty[s], 1);
       mbar_init(&S.s_full[s], 1);
       mbar_init(&S.p_full[s], 4);
       mbar_init(&S.o_done[s], 1);
     }
-    mbar_init(&S.mma_done[0], 1);
-    mbar_init(&S.mma_done[1], 1);
+    mbar_init(&S.mma_done, 1);
     fence_mbarrier_init();
   }
   if (warp == kWarpMma) tmem_alloc(&S.tmem_base, 512);
@@ -176,15 +175,11 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         mbar_wait(&S.v_full[m & 1], (m >> 1) & 1, p.err);
       }
     }
-  } else if (warp == kWarpMma || warp == kWarpMma + 1) {
-    // One issuing thread per head: a tcgen05.mma issue costs the issuing thread about as
-    // long as an N=128 MMA takes to run, so two issuers keep the tensor core fed. The
-    // heads' accumulators are disjoint; the K/V stage is released when both PVs are done.
-    const int h = warp - kWarpMma;
+  } else if (warp == kWarpMma) {
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16(BM, BN, 0, 0);
       constexpr uint32_t idesc_pv = idesc_bf16(BM, D, 0, 1);
-      auto issue_s = [&](int s) {
+      auto issue_s = [&](int h, int s) {
         const uint32_t qa = smem_u32(S.q[h]), kb = smem_u32(S.k[s]);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -194,7 +189,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         }
         mma_commit(&S.s_full[h]);
       };
-      auto issue_pv = [&](int s, int n) {
+      auto issue_pv = [&](int h, int s, int n) {
         const uint32_t vb = smem_u32(S.v[s]);
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
@@ -207,22 +202,28 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       bool ok = N > 0 && mbar_wait(&S.q_full, 0, p.err) && mbar_wait(&S.k_full[0], 0, p.err);
       if (ok) {
         tc_fence_after();
-        issue_s(0);
+        issue_s(0, 0);
+        issue_s(1, 0);
       }
       for (int n = 0; ok && n < N; ++n) {
         const int s = n & 1;
-        if (!(ok = mbar_wait(&S.p_full[h], n & 1, p.err) && mbar_wait(&S.v_full[s], (n >> 1) & 1, p.err))) break;
+        if (!(ok = mbar_wait(&S.p_full[0], n & 1, p.err) && mbar_wait(&S.v_full[s], (n >> 1) & 1, p.err))) break;
         tc_fence_after();
-        issue_pv(s, n);
-        mma_commit(&S.kv_empty[s]);
-        if (n + 1 < N) {
+        issue_pv(0, s, n);
+        const bool more = n + 1 < N;
+        if (more) {
           if (!(ok = mbar_wait(&S.k_full[s ^ 1], ((n + 1) >> 1) & 1, p.err))) break;
           tc_fence_after();
-          issue_s(s ^ 1);
+          issue_s(0, s ^ 1);
         }
+        if (!(ok = mbar_wait(&S.p_full[1], n & 1, p.err))) break;
+        tc_fence_after();
+        issue_pv(1, s, n);
+        mma_commit(&S.kv_empty[s]);
+        if (more) issue_s(1, s ^ 1);
       }
-      mma_commit(&S.mma_done[h]);
-      mbar_wait(&S.mma_done[h], 0, p.err);
+      mma_commit(&S.mma_done);
+      mbar_wait(&S.mma_done, 0, p.err);
     }
     __syncwarp();
   } else if (warp < 8) {
