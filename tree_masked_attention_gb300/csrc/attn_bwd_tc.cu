@@ -20,9 +20,15 @@
 //                            along the head dimension; a final kernel converts to bf16)
 // Two compute warpgroups own alternate steps (TMEM: S/P and dP/dQ per stream, 2 x 128
 // columns, plus dV and dK, 128 each), so the tensor core works on one stream while the
-// other stream's warps run the softmax backward or drain dQ.
-//   warps 0-3, 4-7  compute streams 0 and 1; at the end warps 0-3 write dK, 4-7 dV
-//   warp 8          TMA producer;  warps 9-11  MMA issuers (warp 9 owns TMEM)
+// other stream's warps run the softmax backward. A third warpgroup drains dQ^T out of
+// TMEM and into the fp32 accumulator, so the compute warps never wait for those
+// reductions. Roles:
+//   warps 0-3, 4-7   compute streams 0 and 1; at the end of a unit 0-3 add dK, 4-7 dV
+//   warp 8           TMA producer, and issues dK
+//   warps 9, 10, 11  issue S^T/dP^T, dV (+ the next S^T), dQ^T (warp 9 owns TMEM)
+//   warps 12-15      dQ^T drain, staging and TMA reduce
+// A tcgen05.mma issue occupies its thread for about as long as an N<=128 MMA runs, so
+// four issuing threads share a step's 32 MMAs.
 #include <algorithm>
 #include <cmath>
 
@@ -38,14 +44,12 @@ using namespace sm100;
 namespace tcbwd {
 
 constexpr int BN = 128, BQ = 64, D = 128, NST = 3;
-constexpr int kThreads = 384;
-// warp 8: TMA. Three MMA-issuing warps (a tcgen05.mma issue occupies its thread about as
-// long as an N<=128 MMA runs, so one issuer cannot keep the tensor core busy):
-//   warp 9  (owns TMEM)  S^T and dP^T of a unit's first two steps, then dP^T of step g+2
-//                        once step g's dQ^T has been drained from the shared columns;
-//   warp 10              dV and dK of step g, then S^T of step g+2 (same stream, in order);
-//   warp 11              dQ^T of step g.
-constexpr int kWarpProducer = 8, kWarpMma = 9, kWarpMma2 = 10, kWarpMma3 = 11;
+constexpr int kThreads = 512;
+constexpr int kWarpProducer = 8, kWarpMma = 9, kWarpMma2 = 10, kWarpMma3 = 11, kWarpDq = 12;
+// Registers per thread after the warpgroups re-allocate: the launch gives 512 x 128; the
+// compute warpgroups take 168 each, the issuers 56, the dQ drain 120 (sum 4 x 128).
+constexpr int kRegLaunch = 128, kRegCompute = 168, kRegIssue = 56, kRegDq = 120;
+static_assert(2 * kRegCompute + kRegIssue + kRegDq == 4 * kRegLaunch, "register split exceeds the launch");
 constexpr uint32_t kKSub = 128 * 128;          // 128 key rows x 128 B
 constexpr uint32_t kKTile = 2 * kKSub;         // K or V: 128 x 128 bf16
 constexpr uint32_t kQSub = BQ * 128;           // 64 query rows x 128 B
@@ -58,14 +62,13 @@ struct Smem {
   uint8_t q[NST][kQTile];
   uint8_t dout[NST][kQTile];
   uint8_t ds[2][kDsTile];
-  // scale * dQ of a step for the TMA reduce, row-major [32 queries][128 dims] per half: a
-  // stream stages queries 0-31 in its dS buffer (free once dK and dQ^T of the step are done)
-  // and queries 32-63 in its own half buffer, so the two streams never wait for each other
-  float dq_half[2][(BQ / 2) * D];
+  // scale * dQ of half a query tile, row-major [32 queries][128 dims], for the TMA reduce;
+  // the two halves alternate so that one is written while the other is being read
+  float dq_stage[2][(BQ / 2) * D];
   float lse2[NST][BQ];
   float delta[NST][BQ];
-  uint64_t kv_full, qdo_full[NST], qdo_empty[NST], s_full[2], ds_ready[2], dq_full[2], drain_done[2], mma_done,
-      sdp_done, dk_done[2], dq_done_all, stage_free[2], stage_full[2];
+  uint64_t kv_full, qdo_full[NST], qdo_empty[NST], s_full[2], ds_ready[2], dq_full[2], drain_done[2], dk_done[2],
+      mma_done, fin[4];
   uint32_t tmem_base;
 };
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
@@ -130,6 +133,33 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+struct Unit {
+  int kt, kvh, b, L, qt_lo;
+};
+
+// Takes the next work unit (thread `fetcher` draws it; every thread of the CTA calls this).
+// Returns 0 to run it, 1 for a malformed unit (reported; the caller skips it after a CTA
+// barrier), 2 when there is no more work or the CTA is aborting.
+__device__ __forceinline__ int fetch_unit(const Params& p, int G, int* s_unit, int* s_abort, bool fetcher, Unit& U) {
+  if (fetcher) *s_unit = atomicAdd(p.counter, 1);
+  __syncthreads();
+  const int u = *reinterpret_cast<volatile int*>(s_unit);
+  if (u >= *p.n_units || *reinterpret_cast<volatile int*>(s_abort)) return 2;
+  const int4 W = p.units[u];
+  U.kt = W.x;
+  U.kvh = W.y;
+  U.b = W.z;
+  U.L = W.w - W.z;
+  U.qt_lo = 0;
+  const bool unit_ok = U.kt >= 0 && U.kt * BN < p.T && U.kvh >= 0 && U.kvh < p.Hkv && U.b >= 0 && U.L > 0;
+  const int nq = unit_ok ? key_tile_queries(p, U.kt, &U.qt_lo) : 0;
+  if (!unit_ok || W.w > G * nq) {
+    if (fetcher) raise_error(p.err, TREE_ERR_DEVICE_CHECK);
+    return 1;
+  }
+  return 0;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
@@ -145,22 +175,17 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
     mbar_init(&S.kv_full, 1);
     for (int s = 0; s < NST; ++s) {
       mbar_init(&S.qdo_full[s], 1);
-      mbar_init(&S.qdo_empty[s], 1);
+      mbar_init(&S.qdo_empty[s], 2);  // dV (warp 10) and dK (warp 8) of the step read Q_i / dO_i
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&S.s_full[s], 2);  // S^T and dP^T of a step come from two issuers
-      mbar_init(&S.dk_done[s], 1);
+      mbar_init(&S.s_full[s], 2);  // S^T and dP^T of a step may come from two issuers
       mbar_init(&S.ds_ready[s], 4);
       mbar_init(&S.dq_full[s], 1);
       mbar_init(&S.drain_done[s], 4);
+      mbar_init(&S.dk_done[s], 1);
     }
-    mbar_init(&S.mma_done, 1);
-    mbar_init(&S.sdp_done, 1);
-    mbar_init(&S.dq_done_all, 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&S.stage_free[s], 1);
-      mbar_init(&S.stage_full[s], 4);
-    }
+    mbar_init(&S.mma_done, 2);  // dV accumulation (warp 10) and dK accumulation (warp 8)
+    for (int w = 0; w < 4; ++w) mbar_init(&S.fin[w], 1);
     fence_mbarrier_init();
     s_abort = 0;
   }
@@ -170,128 +195,27 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
   tc_fence_after();
   const uint32_t tmem = S.tmem_base;
   constexpr uint32_t kColDV = 256, kColDK = 384;
-  const int n_units = *p.n_units;
-  int g0 = 0, uit = 0;  // steps and units this CTA has run
+  int g0 = 0, uit = 0;  // steps and units this CTA has run (every role counts them)
+  int g_loaded = 0;     // producer: steps whose Q_i / dO_i loads were issued
+  int last_stage = -1;  // dQ drain leader: staging half of the most recent reduce
 
-  while (true) {
-    if (threadIdx.x == 0) s_unit = atomicAdd(p.counter, 1);
-    __syncthreads();
-    const int u = s_unit;
-    if (u >= n_units || s_abort) break;
-    const int4 U = p.units[u];
-    const int kt = U.x, kvh = U.y, b = U.z, L = U.w - U.z;
-    int qt_lo = 0;
-    const bool unit_ok = kt >= 0 && kt * BN < p.T && kvh >= 0 && kvh < p.Hkv && b >= 0 && L > 0;
-    const int nq = unit_ok ? key_tile_queries(p, kt, &qt_lo) : 0;
-    if (!unit_ok || U.w > G * nq) {  // a malformed unit: report it and run nothing
-      if (threadIdx.x == 0) raise_error(p.err, TREE_ERR_DEVICE_CHECK);
-      __syncthreads();
-      continue;
-    }
-    const int j0 = kt * BN;
-
-    if (warp == kWarpProducer) {
-      if (lane == 0) {
-        if (uit == 0) {
-          prefetch_tmap(&tmK);
-          prefetch_tmap(&tmV);
-          prefetch_tmap(&tmQ);
-          prefetch_tmap(&tmDO);
-        }
-        mbar_arrive_expect_tx(&S.kv_full, 2 * kKTile);
-        tma_load_3d(S.k, &tmK, &S.kv_full, 0, kvh, j0);
-        tma_load_3d(S.k + kKSub, &tmK, &S.kv_full, 64, kvh, j0);
-        tma_load_3d(S.v, &tmV, &S.kv_full, 0, kvh, j0);
-        tma_load_3d(S.v + kKSub, &tmV, &S.kv_full, 64, kvh, j0);
-        for (int l = 0; l < L; ++l) {
-          const int g = g0 + l, st = g % NST, t = b + l;
-          if (g >= NST && !mbar_wait(&S.qdo_empty[st], ((g / NST) - 1) & 1, p.err)) {
-            s_abort = 1;
-            break;
-          }
-          const int h = kvh * G + t % G;
-          const int i0 = (qt_lo + t / G) * BQ;
-          mbar_arrive_expect_tx(&S.qdo_full[st], 2 * kQTile + 2 * BQ * 4);
-          tma_load_3d(S.q[st], &tmQ, &S.qdo_full[st], 0, h, i0);
-          tma_load_3d(S.q[st] + kQSub, &tmQ, &S.qdo_full[st], 64, h, i0);
-          tma_load_3d(S.dout[st], &tmDO, &S.qdo_full[st], 0, h, i0);
-          tma_load_3d(S.dout[st] + kQSub, &tmDO, &S.qdo_full[st], 64, h, i0);
-          bulk_load(S.lse2[st], p.lse2 + static_cast<int64_t>(h) * p.T_pad + i0, BQ * 4, &S.qdo_full[st]);
-          bulk_load(S.delta[st], p.delta + static_cast<int64_t>(h) * p.T_pad + i0, BQ * 4, &S.qdo_full[st]);
-        }
+  // Each role runs its own copy of the unit loop (so that each is compiled under its own
+  // register limit); all of them meet at the same two CTA barriers per unit.
+  if (warp < 8) {
+    regs_inc<kRegCompute>();
+    while (true) {
+      Unit U;
+      const int fu = fetch_unit(p, G, &s_unit, &s_abort, threadIdx.x == 0, U);
+      if (fu == 2) break;
+      if (fu == 1) {
+        __syncthreads();
+        continue;
       }
-    } else if (warp >= kWarpMma && warp <= kWarpMma3) {
-      if (lane == 0) {
-        constexpr uint32_t id_s = idesc_bf16(BN, BQ, 0, 0);  // S^T, dP^T
-        constexpr uint32_t id_kv = idesc_bf16(BN, D, 0, 1);  // dV, dK (B MN-major)
-        constexpr uint32_t id_dq = idesc_bf16(D, BQ, 1, 1);  // dQ^T (A and B MN-major)
-        const uint32_t kb = smem_u32(S.k), vb = smem_u32(S.v);
-        // one of S^T = K Q^T (kv = K) or dP^T = V dO^T (kv = V) of step g into its stream's columns
-        auto issue_one = [&](int g, bool is_s) -> bool {
-          const int st = g % NST, s = g & 1;
-          if (!mbar_wait(&S.qdo_full[st], (g / NST) & 1, p.err)) return false;
-          tc_fence_after();
-          const uint32_t xb = smem_u32(is_s ? S.q[st] : S.dout[st]), ab = is_s ? kb : vb;
-          const uint32_t d = tmem + s * 128 + (is_s ? 0 : 64);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t ka = (kk >> 2) * kKSub + (kk & 3) * 32, qa = (kk >> 2) * kQSub + (kk & 3) * 32;
-            mma_ss(d, desc_sw128(ab + ka, 16, 1024), desc_sw128(xb + qa, 16, 1024), id_s, kk > 0);
-          }
-          mma_commit(&S.s_full[s]);
-          return true;
-        };
-        bool ok = mbar_wait(&S.kv_full, uit & 1, p.err);
-        if (warp == kWarpMma) {
-          for (int l = 0; ok && l < min(2, L); ++l) ok = issue_one(g0 + l, true) && issue_one(g0 + l, false);
-          for (int l = 0; ok && l + 2 < L; ++l) {
-            const int g = g0 + l;
-            // dP^T of step g+2 overwrites the columns that held step g's dQ^T
-            if (!(ok = mbar_wait(&S.drain_done[g & 1], (g >> 1) & 1, p.err))) break;
-            tc_fence_after();
-            ok = issue_one(g + 2, false);
-          }
-        } else if (warp == kWarpMma2) {
-          for (int l = 0; ok && l < L; ++l) {
-            const int g = g0 + l, s = g & 1, st = g % NST;
-            if (!(ok = mbar_wait(&S.ds_ready[s], (g >> 1) & 1, p.err))) break;
-            tc_fence_after();
-            const uint32_t qb = smem_u32(S.q[st]), ob = smem_u32(S.dout[st]), db = smem_u32(S.ds[s]);
-            const uint32_t tS = tmem + s * 128;
-#pragma unroll
-            for (int kk = 0; kk < BQ / 16; ++kk)  // dV += P^T dO
-              mma_ts(tmem + kColDV, tS + kk * 8, desc_sw128(ob + kk * 2048, kQSub, 1024), id_kv,
-                     (l > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-            for (int kk = 0; kk < BQ / 16; ++kk)  // dK += dS^T Q
-              mma_ss(tmem + kColDK, desc_sw128(db + kk * 32, 16, 1024), desc_sw128(qb + kk * 2048, kQSub, 1024),
-                     id_kv, (l > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(&S.qdo_empty[st]);
-            mma_commit(&S.dk_done[s]);
-            // S^T of step g+2 reuses the columns whose P^T the dV above reads (same issuer: ordered)
-            if (l + 2 < L && !(ok = issue_one(g + 2, true))) break;
-          }
-          mma_commit(&S.mma_done);
-        } else {
-          for (int l = 0; ok && l < L; ++l) {
-            const int g = g0 + l, s = g & 1;
-            if (!(ok = mbar_wait(&S.ds_ready[s], (g >> 1) & 1, p.err))) break;
-            tc_fence_after();
-            const uint32_t db = smem_u32(S.ds[s]), tD = tmem + s * 128 + 64;
-#pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk)  // dQ^T = K^T dS^T
-              mma_ss(tD, desc_sw128(kb + kk * 2048, kKSub, 1024), desc_sw128(db + kk * 2048, kQSub, 1024), id_dq,
-                     kk > 0);
-            mma_commit(&S.dq_full[s]);
-          }
-        }
-        if (!ok) s_abort = 1;
-      }
-      __syncwarp();
-    } else if (warp < 8) {
+      const int kt = U.kt, kvh = U.kvh, b = U.b, L = U.L, qt_lo = U.qt_lo, j0 = kt * BN;
+      (void)kt; (void)j0;
       // ---------------------------------------------------------- compute warps
       const int s = warp >> 2, q4 = warp & 3;
-      const int r = q4 * 32 + lane;  // key row (S^T, dP^T, dK, dV) or head dim (dQ^T)
+      const int r = q4 * 32 + lane;  // key row of S^T, dP^T, dK, dV
       const int j = j0 + r;
       const int ej = p.endp[j];      // -1 past T
       const uint32_t lanes = static_cast<uint32_t>(q4 * 32) << 16;
@@ -300,20 +224,10 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
       bool ok = true;
       for (int l = ((g0 & 1) == s) ? 0 : 1; l < L; l += 2) {
         const int g = g0 + l, st = g % NST, t = b + l;
-        const int h = kvh * G + t % G;
         const int i0 = (qt_lo + t / G) * BQ;
         if (!(ok = __all_sync(0xffffffffu, mbar_wait(&S.s_full[s], (g >> 1) & 1, p.err) &&
                                                mbar_wait(&S.qdo_full[st], (g / NST) & 1, p.err))))
           break;
-        // dS[s] doubled as dQ staging in this stream's previous step: its reduce must have
-        // read it. The issuing thread waits for the read and releases the buffer.
-        if (g >= 2) {
-          if (q4 == 0 && lane == 0) {
-            bulk_wait_read0();
-            mbar_arrive(&S.stage_free[s]);
-          }
-          if (!(ok = __all_sync(0xffffffffu, mbar_wait(&S.stage_free[s], ((g >> 1) - 1) & 1, p.err)))) break;
-        }
         tc_fence_after();
         uint8_t* dsrow = S.ds[s] + r * 128;
         // every query of the tile sees this key (no per-element test needed)?
@@ -336,12 +250,12 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         }
 #pragma unroll
         for (int t4 = 0; t4 < 16; ++t4) {
-          const float4 L = l4[t4], Dl = d4[t4];
+          const float4 L4 = l4[t4], D4 = d4[t4];
 #pragma unroll
           for (int h2 = 0; h2 < 2; ++h2) {
             const int t2 = t4 * 4 + h2 * 2;
-            const float2 lv = h2 ? make_float2(L.z, L.w) : make_float2(L.x, L.y);
-            const float2 dv = h2 ? make_float2(Dl.z, Dl.w) : make_float2(Dl.x, Dl.y);
+            const float2 lv = h2 ? make_float2(L4.z, L4.w) : make_float2(L4.x, L4.y);
+            const float2 dv = h2 ? make_float2(D4.z, D4.w) : make_float2(D4.x, D4.y);
             const float2 x = __ffma2_rn(make_float2(__uint_as_float(sv[t2]), __uint_as_float(sv[t2 + 1])),
                                         make_float2(sl2, sl2), make_float2(-lv.x, -lv.y));
             const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
@@ -351,7 +265,12 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
             dk[t2 / 2] = pack_bf16(dd.x, dd.y);
           }
         }
+        // P^T into the S^T columns (S^T of this step is complete, and dV two steps back,
+        // which read the previous P^T, finished before it on the same issuer)
         tmem_st32(tS, pk);
+        // dS^T into shared memory once dK of this stream's previous step has read it
+        if (g >= 2 && !(ok = __all_sync(0xffffffffu, mbar_wait(&S.dk_done[s], ((g >> 1) - 1) & 1, p.err))))
+          break;
 #pragma unroll
         for (int w = 0; w < 8; ++w) {
           const int chunk = w ^ (r & 7);
@@ -362,37 +281,6 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.ds_ready[s]);
-        // dQ^T of this step: TMEM lane = head dimension r, column = query. Free the
-        // columns once they are in registers, write scale * dQ row-major into the staging
-        // buffer, and add the 64 x 128 tile into the fp32 accumulator with one TMA reduce.
-        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&S.dq_full[s], (g >> 1) & 1, p.err)))) break;
-        tc_fence_after();
-        uint32_t v0[32], v1[32];
-        tmem_ld32(tD, v0);
-        tmem_ld32(tD + 32, v1);
-        tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&S.drain_done[s]);
-        // dS[s] becomes staging: dK of this step (another issuer) must have read it
-        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&S.dk_done[s], (g >> 1) & 1, p.err)))) break;
-        float* lo_half = reinterpret_cast<float*>(S.ds[s]);
-        float* hi_half = S.dq_half[s];
-#pragma unroll
-        for (int t2 = 0; t2 < 32; ++t2) {
-          lo_half[t2 * D + r] = __uint_as_float(v0[t2]) * p.scale;
-          hi_half[t2 * D + r] = __uint_as_float(v1[t2]) * p.scale;
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&S.stage_full[s]);
-        if (q4 == 0 && lane == 0) {  // one thread issues the reduces once all four warps wrote
-          if (mbar_wait(&S.stage_full[s], (g >> 1) & 1, p.err)) {
-            tma_reduce_add_3d(&tmDQ, lo_half, 0, h, i0);
-            if (i0 + BQ / 2 < p.T) tma_reduce_add_3d(&tmDQ, hi_half, 0, h, i0 + BQ / 2);
-            bulk_commit();  // the read is waited for at this stream's next step (or at exit)
-          }
-        }
       }
       // unit epilogue: warps 0-3 add scale * dK, warps 4-7 add dV (one key row per thread)
       ok = __all_sync(0xffffffffu, ok && mbar_wait(&S.mma_done, uit & 1, p.err));
@@ -416,31 +304,209 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
       } else {
         s_abort = 1;
       }
+      g0 += L;
+      ++uit;
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
     }
-    g0 += L;
-    ++uit;
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
+  } else if (warp < kWarpDq) {
+    regs_dec<kRegIssue>();
+    while (true) {
+      Unit U;
+      const int fu = fetch_unit(p, G, &s_unit, &s_abort, false, U);
+      if (fu == 2) break;
+      if (fu == 1) {
+        __syncthreads();
+        continue;
+      }
+      const int kt = U.kt, kvh = U.kvh, b = U.b, L = U.L, qt_lo = U.qt_lo, j0 = kt * BN;
+      (void)kt; (void)j0;
+      if (lane == 0) {
+        constexpr uint32_t id_s = idesc_bf16(BN, BQ, 0, 0);  // S^T, dP^T
+        constexpr uint32_t id_kv = idesc_bf16(BN, D, 0, 1);  // dV, dK (B MN-major)
+        constexpr uint32_t id_dq = idesc_bf16(D, BQ, 1, 1);  // dQ^T (A and B MN-major)
+        const uint32_t kb = smem_u32(S.k), vb = smem_u32(S.v);
+        // one of S^T = K Q^T or dP^T = V dO^T of step g into its stream's columns
+        auto issue_one = [&](int g, bool is_s) -> bool {
+          const int st = g % NST, s = g & 1;
+          if (!mbar_wait(&S.qdo_full[st], (g / NST) & 1, p.err)) return false;
+          tc_fence_after();
+          const uint32_t xb = smem_u32(is_s ? S.q[st] : S.dout[st]), ab = is_s ? kb : vb;
+          const uint32_t d = tmem + s * 128 + (is_s ? 0 : 64);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t ka = (kk >> 2) * kKSub + (kk & 3) * 32, qa = (kk >> 2) * kQSub + (kk & 3) * 32;
+            mma_ss(d, desc_sw128(ab + ka, 16, 1024), desc_sw128(xb + qa, 16, 1024), id_s, kk > 0);
+          }
+          mma_commit(&S.s_full[s]);
+          return true;
+        };
+        bool ok = true;
+        if (warp == kWarpProducer) {
+          if (uit == 0) {
+            prefetch_tmap(&tmK);
+            prefetch_tmap(&tmV);
+            prefetch_tmap(&tmQ);
+            prefetch_tmap(&tmDO);
+          }
+          mbar_arrive_expect_tx(&S.kv_full, 2 * kKTile);
+          tma_load_3d(S.k, &tmK, &S.kv_full, 0, kvh, j0);
+          tma_load_3d(S.k + kKSub, &tmK, &S.kv_full, 64, kvh, j0);
+          tma_load_3d(S.v, &tmV, &S.kv_full, 0, kvh, j0);
+          tma_load_3d(S.v + kKSub, &tmV, &S.kv_full, 64, kvh, j0);
+          // Q_i, dO_i, LSE_i, Delta_i of step g once step g - NST no longer reads the stage
+          auto load_step = [&](int g) -> bool {
+            const int st = g % NST, t = b + (g - g0);
+            if (g >= NST && !mbar_wait(&S.qdo_empty[st], ((g / NST) - 1) & 1, p.err)) return false;
+            const int h = kvh * G + t % G;
+            const int i0 = (qt_lo + t / G) * BQ;
+            mbar_arrive_expect_tx(&S.qdo_full[st], 2 * kQTile + 2 * BQ * 4);
+            tma_load_3d(S.q[st], &tmQ, &S.qdo_full[st], 0, h, i0);
+            tma_load_3d(S.q[st] + kQSub, &tmQ, &S.qdo_full[st], 64, h, i0);
+            tma_load_3d(S.dout[st], &tmDO, &S.qdo_full[st], 0, h, i0);
+            tma_load_3d(S.dout[st] + kQSub, &tmDO, &S.qdo_full[st], 64, h, i0);
+            bulk_load(S.lse2[st], p.lse2 + static_cast<int64_t>(h) * p.T_pad + i0, BQ * 4, &S.qdo_full[st]);
+            bulk_load(S.delta[st], p.delta + static_cast<int64_t>(h) * p.T_pad + i0, BQ * 4, &S.qdo_full[st]);
+            g_loaded = g + 1;
+            return true;
+          };
+          for (int l = 0; ok && l < min(NST, L); ++l) ok = load_step(g0 + l);
+          for (int l = 0; ok && l < L; ++l) {
+            const int g = g0 + l, s = g & 1, st = g % NST;
+            if (!(ok = mbar_wait(&S.ds_ready[s], (g >> 1) & 1, p.err))) break;
+            tc_fence_after();
+            const uint32_t qb = smem_u32(S.q[st]), db = smem_u32(S.ds[s]);
+#pragma unroll
+            for (int kk = 0; kk < BQ / 16; ++kk)  // dK += dS^T Q
+              mma_ss(tmem + kColDK, desc_sw128(db + kk * 32, 16, 1024), desc_sw128(qb + kk * 2048, kQSub, 1024),
+                     id_kv, (l > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(&S.qdo_empty[st]);
+            mma_commit(&S.dk_done[s]);
+            if (l + NST < L) ok = load_step(g + NST);
+          }
+          mma_commit(&S.mma_done);
+        } else if (warp == kWarpMma) {
+          ok = mbar_wait(&S.kv_full, uit & 1, p.err);
+          for (int l = 0; ok && l < min(2, L); ++l) ok = issue_one(g0 + l, true) && issue_one(g0 + l, false);
+          for (int l = 0; ok && l + 2 < L; ++l) {
+            const int g = g0 + l;
+            // dP^T of step g+2 overwrites the columns that held step g's dQ^T
+            if (!(ok = mbar_wait(&S.drain_done[g & 1], (g >> 1) & 1, p.err))) break;
+            tc_fence_after();
+            ok = issue_one(g + 2, false);
+          }
+        } else if (warp == kWarpMma2) {
+          ok = mbar_wait(&S.kv_full, uit & 1, p.err);
+          for (int l = 0; ok && l < L; ++l) {
+            const int g = g0 + l, s = g & 1, st = g % NST;
+            if (!(ok = mbar_wait(&S.ds_ready[s], (g >> 1) & 1, p.err))) break;
+            tc_fence_after();
+            const uint32_t ob = smem_u32(S.dout[st]), tS = tmem + s * 128;
+#pragma unroll
+            for (int kk = 0; kk < BQ / 16; ++kk)  // dV += P^T dO
+              mma_ts(tmem + kColDV, tS + kk * 8, desc_sw128(ob + kk * 2048, kQSub, 1024), id_kv,
+                     (l > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(&S.qdo_empty[st]);
+            // S^T of step g+2 reuses the columns whose P^T the dV above reads (same issuer: ordered)
+            if (l + 2 < L && !(ok = issue_one(g + 2, true))) break;
+          }
+          mma_commit(&S.mma_done);
+        } else {
+          ok = mbar_wait(&S.kv_full, uit & 1, p.err);
+          for (int l = 0; ok && l < L; ++l) {
+            const int g = g0 + l, s = g & 1;
+            if (!(ok = mbar_wait(&S.ds_ready[s], (g >> 1) & 1, p.err))) break;
+            tc_fence_after();
+            const uint32_t db = smem_u32(S.ds[s]), tD = tmem + s * 128 + 64;
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk)  // dQ^T = K^T dS^T
+              mma_ss(tD, desc_sw128(kb + kk * 2048, kKSub, 1024), desc_sw128(db + kk * 2048, kQSub, 1024), id_dq,
+                     kk > 0);
+            mma_commit(&S.dq_full[s]);
+          }
+        }
+        if (!ok) s_abort = 1;
+      }
+      __syncwarp();
+      g0 += L;
+      ++uit;
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
+    }
+  } else {
+    regs_dec<kRegDq>();
+    while (true) {
+      Unit U;
+      const int fu = fetch_unit(p, G, &s_unit, &s_abort, false, U);
+      if (fu == 2) break;
+      if (fu == 1) {
+        __syncthreads();
+        continue;
+      }
+      const int kt = U.kt, kvh = U.kvh, b = U.b, L = U.L, qt_lo = U.qt_lo, j0 = kt * BN;
+      (void)kt; (void)j0;
+      // ------------------------------------------------------ dQ drain (warps 12-15)
+      // TMEM lane = head dimension r, column = query. Free the columns once they are in
+      // registers, then per half tile write scale * dQ row-major into a staging buffer and
+      // add it into the fp32 accumulator with one TMA reduce (one thread issues them all).
+      const int q4 = warp & 3, r = q4 * 32 + lane;
+      const uint32_t lanes = static_cast<uint32_t>(q4 * 32) << 16;
+      const bool leader = warp == kWarpDq && lane == 0;
+      bool ok = true;
+      for (int l = 0; l < L; ++l) {
+        const int g = g0 + l, s = g & 1, t = b + l;
+        const int h = kvh * G + t % G;
+        const int i0 = (qt_lo + t / G) * BQ;
+        // one decision for the four warps: they meet at the staging barriers below
+        if (!(ok = named_bar_and(1, 128, mbar_wait(&S.dq_full[s], (g >> 1) & 1, p.err)))) break;
+        tc_fence_after();
+        uint32_t v[2][32];
+        const uint32_t tD = tmem + lanes + s * 128 + 64;
+        tmem_ld32(tD, v[0]);
+        tmem_ld32(tD + 32, v[1]);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.drain_done[s]);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          // the reduce that last read this half's buffer must be done reading it
+          if (leader) {
+            if (last_stage == half) bulk_wait_read0(); else bulk_wait_read1();
+          }
+          named_bar_sync(1, 128);
+          float* buf = S.dq_stage[half];
+#pragma unroll
+          for (int t2 = 0; t2 < 32; ++t2) buf[t2 * D + r] = __uint_as_float(v[half][t2]) * p.scale;
+          fence_proxy_async_smem();
+          named_bar_sync(1, 128);
+          if (leader && i0 + half * (BQ / 2) < p.T) {
+            tma_reduce_add_3d(&tmDQ, buf, 0, h, i0 + half * (BQ / 2));
+            bulk_commit();
+            last_stage = half;
+          }
+        }
+      }
+      if (!ok) s_abort = 1;
+      g0 += L;
+      ++uit;
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
+    }
   }
-  // The dQ reduces issued last must have read their staging before the CTA exits.
-  if (warp < 8 && (warp & 3) == 0 && lane == 0) bulk_wait_read0();
+  // The last dQ reduces must have read their staging before the CTA exits.
+  if (warp == kWarpDq && lane == 0) bulk_wait_read0();
   // On an early exit, leave no TMA copy or MMA in flight.
-  if (s_abort && threadIdx.x == kWarpProducer * 32) {
-    mbar_wait(&S.kv_full, (uit - 1) & 1, p.err);
-    for (int g = (g0 > NST ? g0 - NST : 0); g < g0; ++g) mbar_wait(&S.qdo_full[g % NST], (g / NST) & 1, p.err);
-  }
-  if (s_abort && threadIdx.x == kWarpMma * 32) {
-    mma_commit(&S.sdp_done);
-    mbar_wait(&S.sdp_done, 0, p.err);
-  }
-  if (s_abort && threadIdx.x == kWarpMma3 * 32) {
-    mma_commit(&S.dq_done_all);
-    mbar_wait(&S.dq_done_all, 0, p.err);
-  }
-  if (s_abort && threadIdx.x == kWarpMma2 * 32) {
-    mma_commit(&S.mma_done);
-    mbar_wait(&S.mma_done, uit & 1, p.err);
+  if (s_abort && warp >= kWarpProducer && warp <= kWarpMma3 && lane == 0) {
+    if (warp == kWarpProducer) {
+      if (uit > 0) mbar_wait(&S.kv_full, (uit - 1) & 1, p.err);
+      for (int g = max(0, g_loaded - NST); g < g_loaded; ++g) mbar_wait(&S.qdo_full[g % NST], (g / NST) & 1, p.err);
+    }
+    mma_commit(&S.fin[warp - kWarpProducer]);
+    mbar_wait(&S.fin[warp - kWarpProducer], 0, p.err);
   }
   tc_fence_before();
   __syncthreads();
@@ -642,6 +708,16 @@ int attn_bwd_tc(const AttnArgs& a, cudaStream_t st) {
   }
   int n_sm = 0;
   if ((rc = sm_count(&n_sm))) return rc;
+  // The warpgroups' register split adds up to exactly the launch's registers per thread.
+  static int launch_regs = -1;
+  if (launch_regs < 0) {
+    cudaFuncAttributes fa{};
+    TREE_CUDA_TRY(cudaFuncGetAttributes(&fa, attn_bwd_tc_kernel));
+    launch_regs = fa.numRegs;
+  }
+  if (launch_regs != kRegLaunch)
+    return fail(TREE_ERR_CUDA, "attn_bwd_tc_kernel: built with %d registers per thread, its warpgroups split %d",
+                launch_regs, kRegLaunch);
   Params p{};
   p.T = static_cast<int>(a.T);
   p.T_pad = static_cast<int>(T_pad);
