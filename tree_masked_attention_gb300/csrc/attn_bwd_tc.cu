@@ -18,17 +18,20 @@
 //   dQ_i^T = K^T dS^T       (M=128 dims, N=64 queries; A = K MN-major, B = dS^T MN-major)
 //   dQ_i += scale dQ_i^T    (fp32 reductions into the workspace accumulator, coalesced
 //                            along the head dimension; a final kernel converts to bf16)
-// Two compute warpgroups own alternate steps (TMEM: S/P and dP/dQ per stream, 2 x 128
-// columns, plus dV and dK, 128 each), so the tensor core works on one stream while the
-// other stream's warps run the softmax backward. A third warpgroup drains dQ^T out of
-// TMEM and into the fp32 accumulator, so the compute warps never wait for those
-// reductions. Roles:
-//   warps 0-3, 4-7   compute streams 0 and 1; at the end of a unit 0-3 add dK, 4-7 dV
-//   warp 8           TMA producer, and issues dK
-//   warps 9, 10, 11  issue S^T/dP^T, dV (+ the next S^T), dQ^T (warp 9 owns TMEM)
-//   warps 12-15      dQ^T drain, staging and TMA reduce
-// A tcgen05.mma issue occupies its thread for about as long as an N<=128 MMA runs, so
-// four issuing threads share a step's 32 MMAs.
+// Both compute warpgroups work on the same step, warpgroup w on queries 32w..32w+31 of
+// the tile, so a step's softmax backward takes half as long. TMEM (512 columns): two
+// S^T/P^T slots used by alternate steps, one dP^T slot, one dQ^T slot (64 each), dV and
+// dK (128 each). While the warps work on step g, the tensor core already computes S^T
+// and dP^T of step g+1 into the free slots, and dQ^T of step g-1 drains through a
+// warpgroup of its own into the fp32 accumulator.
+//   warps 0-7    compute (0-3 and 4-7: query halves); at the end of a unit 0-3 add dK, 4-7 dV
+//   warp 8       TMA producer, and issues dK
+//   warp 9       issues dP^T (owns TMEM)
+//   warp 10      issues dV, then S^T two steps ahead into the slot that dV has just read
+//   warp 11      issues dQ^T
+//   warps 12-15  dQ^T drain, staging and TMA reduce
+// A tcgen05.mma issue occupies its thread for about as long as an N<=128 MMA runs, so the
+// four issuing threads share a step's 32 MMAs about evenly (8 each).
 #include <algorithm>
 #include <cmath>
 
@@ -46,10 +49,6 @@ namespace tcbwd {
 constexpr int BN = 128, BQ = 64, D = 128, NST = 3;
 constexpr int kThreads = 512;
 constexpr int kWarpProducer = 8, kWarpMma = 9, kWarpMma2 = 10, kWarpMma3 = 11, kWarpDq = 12;
-// Registers per thread after the warpgroups re-allocate: the launch gives 512 x 128; the
-// compute warpgroups take 168 each, the issuers 56, the dQ drain 120 (sum 4 x 128).
-constexpr int kRegLaunch = 128, kRegCompute = 168, kRegIssue = 56, kRegDq = 120;
-static_assert(2 * kRegCompute + kRegIssue + kRegDq == 4 * kRegLaunch, "register split exceeds the launch");
 constexpr uint32_t kKSub = 128 * 128;          // 128 key rows x 128 B
 constexpr uint32_t kKTile = 2 * kKSub;         // K or V: 128 x 128 bf16
 constexpr uint32_t kQSub = BQ * 128;           // 64 query rows x 128 B
@@ -67,8 +66,8 @@ struct Smem {
   float dq_stage[2][(BQ / 2) * D];
   float lse2[NST][BQ];
   float delta[NST][BQ];
-  uint64_t kv_full, qdo_full[NST], qdo_empty[NST], s_full[2], ds_ready[2], dq_full[2], drain_done[2], dk_done[2],
-      mma_done, fin[4];
+  uint64_t kv_full, qdo_full[NST], qdo_empty[NST], s_full[2], dp_full, ld_done, ds_ready[2], dk_done[2],
+      dq_full[2], drain_done, mma_done, fin[4];
   uint32_t tmem_base;
 };
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
@@ -171,20 +170,25 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int G = p.Hq / p.Hkv;
 
+  // Barrier phases run over the CTA's whole life, indexed by its step counter g; those
+  // with two copies alternate between steps, so that a step's arrival can never land on
+  // the phase of the step before it before every waiter has seen that one.
   if (threadIdx.x == 0) {
     mbar_init(&S.kv_full, 1);
     for (int s = 0; s < NST; ++s) {
       mbar_init(&S.qdo_full[s], 1);
-      mbar_init(&S.qdo_empty[s], 2);  // dV (warp 10) and dK (warp 8) of the step read Q_i / dO_i
+      mbar_init(&S.qdo_empty[s], 2);  // dV (warp 10) and dK (warp 8) read Q_i / dO_i last
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&S.s_full[s], 2);  // S^T and dP^T of a step may come from two issuers
-      mbar_init(&S.ds_ready[s], 4);
-      mbar_init(&S.dq_full[s], 1);
-      mbar_init(&S.drain_done[s], 4);
+      mbar_init(&S.s_full[s], 1);
+      mbar_init(&S.ds_ready[s], 8);
       mbar_init(&S.dk_done[s], 1);
+      mbar_init(&S.dq_full[s], 1);
     }
-    mbar_init(&S.mma_done, 2);  // dV accumulation (warp 10) and dK accumulation (warp 8)
+    mbar_init(&S.dp_full, 1);
+    mbar_init(&S.ld_done, 8);
+    mbar_init(&S.drain_done, 4);
+    mbar_init(&S.mma_done, 2);  // dV (warp 10) and dK (warp 8) accumulation of a unit
     for (int w = 0; w < 4; ++w) mbar_init(&S.fin[w], 1);
     fence_mbarrier_init();
     s_abort = 0;
@@ -194,15 +198,19 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = S.tmem_base;
-  constexpr uint32_t kColDV = 256, kColDK = 384;
+  // TMEM columns: S^T/P^T of even steps at 0, of odd steps at 64; dP^T 128; dQ^T 192
+  constexpr uint32_t kColDP = 128, kColDQ = 192, kColDV = 256, kColDK = 384;
   int g0 = 0, uit = 0;  // steps and units this CTA has run (every role counts them)
   int g_loaded = 0;     // producer: steps whose Q_i / dO_i loads were issued
   int last_stage = -1;  // dQ drain leader: staging half of the most recent reduce
 
-  // Each role runs its own copy of the unit loop (so that each is compiled under its own
-  // register limit); all of them meet at the same two CTA barriers per unit.
+  // Each role runs its own copy of the unit loop; all meet at two CTA barriers per unit.
   if (warp < 8) {
-    regs_inc<kRegCompute>();
+    // ------------------------------------------------------------ compute warps
+    const int wg = warp >> 2, q4 = warp & 3;
+    const int r = q4 * 32 + lane;  // key row of S^T, dP^T, dK, dV
+    const uint32_t lanes = static_cast<uint32_t>(q4 * 32) << 16;
+    const float sl2 = p.scale_log2;
     while (true) {
       Unit U;
       const int fu = fetch_unit(p, G, &s_unit, &s_abort, threadIdx.x == 0, U);
@@ -211,45 +219,38 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         __syncthreads();
         continue;
       }
-      const int kt = U.kt, kvh = U.kvh, b = U.b, L = U.L, qt_lo = U.qt_lo, j0 = kt * BN;
-      (void)kt; (void)j0;
-      // ---------------------------------------------------------- compute warps
-      const int s = warp >> 2, q4 = warp & 3;
-      const int r = q4 * 32 + lane;  // key row of S^T, dP^T, dK, dV
-      const int j = j0 + r;
-      const int ej = p.endp[j];      // -1 past T
-      const uint32_t lanes = static_cast<uint32_t>(q4 * 32) << 16;
-      const uint32_t tS = tmem + lanes + s * 128, tD = tmem + lanes + s * 128 + 64;
-      const float sl2 = p.scale_log2;
+      const int b = U.b, L = U.L;
+      const int j = U.kt * BN + r;
+      const int ej = p.endp[j];  // -1 past T
       bool ok = true;
-      for (int l = ((g0 & 1) == s) ? 0 : 1; l < L; l += 2) {
+      for (int l = 0; l < L; ++l) {
         const int g = g0 + l, st = g % NST, t = b + l;
-        const int i0 = (qt_lo + t / G) * BQ;
-        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&S.s_full[s], (g >> 1) & 1, p.err) &&
+        const int i0 = (U.qt_lo + t / G) * BQ + wg * 32;  // first query of this half
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&S.s_full[g & 1], (g >> 1) & 1, p.err) &&
+                                               mbar_wait(&S.dp_full, g & 1, p.err) &&
                                                mbar_wait(&S.qdo_full[st], (g / NST) & 1, p.err))))
           break;
         tc_fence_after();
-        uint8_t* dsrow = S.ds[s] + r * 128;
-        // every query of the tile sees this key (no per-element test needed)?
-        const bool all_vis = __all_sync(0xffffffffu, j <= i0 && ej >= i0 + BQ - 1);
-        const float4* l4 = reinterpret_cast<const float4*>(S.lse2[st]);
-        const float4* d4 = reinterpret_cast<const float4*>(S.delta[st]);
-        // all 64 columns of S^T and dP^T in flight at once, one TMEM wait
-        uint32_t sv[64], dp[64], pk[32], dk[32];
-        tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-        tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-        tmem_ld32(tD, *reinterpret_cast<uint32_t(*)[32]>(&dp[0]));
-        tmem_ld32(tD + 32, *reinterpret_cast<uint32_t(*)[32]>(&dp[32]));
+        const uint32_t tS = tmem + lanes + (g & 1) * 64 + wg * 32, tD = tmem + lanes + kColDP + wg * 32;
+        uint32_t sv[32], dp[32];
+        tmem_ld32(tS, sv);
+        tmem_ld32(tD, dp);
         tmem_ld_wait();
-        if (!all_vis) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.ld_done);  // dP^T of the next step may overwrite its slot
+        if (!__all_sync(0xffffffffu, j <= i0 && ej >= i0 + 31)) {
 #pragma unroll
-          for (int t2 = 0; t2 < 64; ++t2) {
+          for (int t2 = 0; t2 < 32; ++t2) {
             const int i = i0 + t2;
             if (!((j <= i) && (i <= ej))) sv[t2] = 0xff800000u;  // -inf: p = 0
           }
         }
+        const float4* l4 = reinterpret_cast<const float4*>(S.lse2[st] + wg * 32);
+        const float4* d4 = reinterpret_cast<const float4*>(S.delta[st] + wg * 32);
+        uint32_t pk[16], dk[16];
 #pragma unroll
-        for (int t4 = 0; t4 < 16; ++t4) {
+        for (int t4 = 0; t4 < 8; ++t4) {
           const float4 L4 = l4[t4], D4 = d4[t4];
 #pragma unroll
           for (int h2 = 0; h2 < 2; ++h2) {
@@ -265,30 +266,32 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
             dk[t2 / 2] = pack_bf16(dd.x, dd.y);
           }
         }
-        // P^T into the S^T columns (S^T of this step is complete, and dV two steps back,
-        // which read the previous P^T, finished before it on the same issuer)
-        tmem_st32(tS, pk);
-        // dS^T into shared memory once dK of this stream's previous step has read it
-        if (g >= 2 && !(ok = __all_sync(0xffffffffu, mbar_wait(&S.dk_done[s], ((g >> 1) - 1) & 1, p.err))))
+        // P^T (bf16 pairs) over the first 16 of this half's S^T columns, which only this
+        // warp has read
+        tmem_st16(tS, pk);
+        // dS^T into shared memory once dK and dQ^T of step g-2 have read the buffer
+        if (g >= 2 && !(ok = __all_sync(0xffffffffu, mbar_wait(&S.dk_done[g & 1], ((g >> 1) - 1) & 1, p.err) &&
+                                                         mbar_wait(&S.dq_full[g & 1], ((g >> 1) - 1) & 1, p.err))))
           break;
+        uint8_t* dsrow = S.ds[g & 1] + r * 128;
 #pragma unroll
-        for (int w = 0; w < 8; ++w) {
-          const int chunk = w ^ (r & 7);
+        for (int w = 0; w < 4; ++w) {
+          const int chunk = (wg * 4 + w) ^ (r & 7);
           *reinterpret_cast<uint4*>(dsrow + chunk * 16) = make_uint4(dk[4 * w], dk[4 * w + 1], dk[4 * w + 2], dk[4 * w + 3]);
         }
         tmem_st_wait();
         tc_fence_before();
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&S.ds_ready[s]);
+        if (lane == 0) mbar_arrive(&S.ds_ready[g & 1]);
       }
       // unit epilogue: warps 0-3 add scale * dK, warps 4-7 add dV (one key row per thread)
       ok = __all_sync(0xffffffffu, ok && mbar_wait(&S.mma_done, uit & 1, p.err));
       tc_fence_after();
       if (ok) {
-        float* acc = (s == 0 ? p.dk_acc : p.dv_acc) + (static_cast<int64_t>(j) * p.Hkv + kvh) * D;
-        const float mul = s == 0 ? p.scale : 1.f;
-        const uint32_t tacc = tmem + lanes + (s == 0 ? kColDK : kColDV);
+        float* acc = (wg == 0 ? p.dk_acc : p.dv_acc) + (static_cast<int64_t>(j) * p.Hkv + U.kvh) * D;
+        const float mul = wg == 0 ? p.scale : 1.f;
+        const uint32_t tacc = tmem + lanes + (wg == 0 ? kColDK : kColDV);
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t v[32];
@@ -311,7 +314,26 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
       tc_fence_after();
     }
   } else if (warp < kWarpDq) {
-    regs_dec<kRegIssue>();
+    // ---------------------------------------------------- producer and MMA issuers
+    constexpr uint32_t id_s = idesc_bf16(BN, BQ, 0, 0);  // S^T, dP^T
+    constexpr uint32_t id_kv = idesc_bf16(BN, D, 0, 1);  // dV, dK (B MN-major)
+    constexpr uint32_t id_dq = idesc_bf16(D, BQ, 1, 1);  // dQ^T (A and B MN-major)
+    const uint32_t kb = smem_u32(S.k), vb = smem_u32(S.v);
+    // S^T = K Q_i^T into the step's slot, or dP^T = V dO_i^T into the dP^T slot
+    auto issue_sdp = [&](int g, bool is_s) -> bool {
+      const int st = g % NST;
+      if (!mbar_wait(&S.qdo_full[st], (g / NST) & 1, p.err)) return false;
+      tc_fence_after();
+      const uint32_t xb = smem_u32(is_s ? S.q[st] : S.dout[st]), ab = is_s ? kb : vb;
+      const uint32_t d = tmem + (is_s ? (g & 1) * 64 : kColDP);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t ka = (kk >> 2) * kKSub + (kk & 3) * 32, qa = (kk >> 2) * kQSub + (kk & 3) * 32;
+        mma_ss(d, desc_sw128(ab + ka, 16, 1024), desc_sw128(xb + qa, 16, 1024), id_s, kk > 0);
+      }
+      mma_commit(is_s ? &S.s_full[g & 1] : &S.dp_full);
+      return true;
+    };
     while (true) {
       Unit U;
       const int fu = fetch_unit(p, G, &s_unit, &s_abort, false, U);
@@ -320,28 +342,8 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         __syncthreads();
         continue;
       }
-      const int kt = U.kt, kvh = U.kvh, b = U.b, L = U.L, qt_lo = U.qt_lo, j0 = kt * BN;
-      (void)kt; (void)j0;
+      const int kvh = U.kvh, b = U.b, L = U.L, j0 = U.kt * BN;
       if (lane == 0) {
-        constexpr uint32_t id_s = idesc_bf16(BN, BQ, 0, 0);  // S^T, dP^T
-        constexpr uint32_t id_kv = idesc_bf16(BN, D, 0, 1);  // dV, dK (B MN-major)
-        constexpr uint32_t id_dq = idesc_bf16(D, BQ, 1, 1);  // dQ^T (A and B MN-major)
-        const uint32_t kb = smem_u32(S.k), vb = smem_u32(S.v);
-        // one of S^T = K Q^T or dP^T = V dO^T of step g into its stream's columns
-        auto issue_one = [&](int g, bool is_s) -> bool {
-          const int st = g % NST, s = g & 1;
-          if (!mbar_wait(&S.qdo_full[st], (g / NST) & 1, p.err)) return false;
-          tc_fence_after();
-          const uint32_t xb = smem_u32(is_s ? S.q[st] : S.dout[st]), ab = is_s ? kb : vb;
-          const uint32_t d = tmem + s * 128 + (is_s ? 0 : 64);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t ka = (kk >> 2) * kKSub + (kk & 3) * 32, qa = (kk >> 2) * kQSub + (kk & 3) * 32;
-            mma_ss(d, desc_sw128(ab + ka, 16, 1024), desc_sw128(xb + qa, 16, 1024), id_s, kk > 0);
-          }
-          mma_commit(&S.s_full[s]);
-          return true;
-        };
         bool ok = true;
         if (warp == kWarpProducer) {
           if (uit == 0) {
@@ -360,7 +362,7 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
             const int st = g % NST, t = b + (g - g0);
             if (g >= NST && !mbar_wait(&S.qdo_empty[st], ((g / NST) - 1) & 1, p.err)) return false;
             const int h = kvh * G + t % G;
-            const int i0 = (qt_lo + t / G) * BQ;
+            const int i0 = (U.qt_lo + t / G) * BQ;
             mbar_arrive_expect_tx(&S.qdo_full[st], 2 * kQTile + 2 * BQ * 4);
             tma_load_3d(S.q[st], &tmQ, &S.qdo_full[st], 0, h, i0);
             tma_load_3d(S.q[st] + kQSub, &tmQ, &S.qdo_full[st], 64, h, i0);
@@ -373,57 +375,59 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
           };
           for (int l = 0; ok && l < min(NST, L); ++l) ok = load_step(g0 + l);
           for (int l = 0; ok && l < L; ++l) {
-            const int g = g0 + l, s = g & 1, st = g % NST;
-            if (!(ok = mbar_wait(&S.ds_ready[s], (g >> 1) & 1, p.err))) break;
+            const int g = g0 + l, st = g % NST;
+            if (!(ok = mbar_wait(&S.ds_ready[g & 1], (g >> 1) & 1, p.err))) break;
             tc_fence_after();
-            const uint32_t qb = smem_u32(S.q[st]), db = smem_u32(S.ds[s]);
+            const uint32_t qb = smem_u32(S.q[st]), db = smem_u32(S.ds[g & 1]);
 #pragma unroll
             for (int kk = 0; kk < BQ / 16; ++kk)  // dK += dS^T Q
               mma_ss(tmem + kColDK, desc_sw128(db + kk * 32, 16, 1024), desc_sw128(qb + kk * 2048, kQSub, 1024),
                      id_kv, (l > 0 || kk > 0) ? 1u : 0u);
             mma_commit(&S.qdo_empty[st]);
-            mma_commit(&S.dk_done[s]);
+            mma_commit(&S.dk_done[g & 1]);
             if (l + NST < L) ok = load_step(g + NST);
           }
           mma_commit(&S.mma_done);
         } else if (warp == kWarpMma) {
-          ok = mbar_wait(&S.kv_full, uit & 1, p.err);
-          for (int l = 0; ok && l < min(2, L); ++l) ok = issue_one(g0 + l, true) && issue_one(g0 + l, false);
-          for (int l = 0; ok && l + 2 < L; ++l) {
+          // dP^T of step g+1 as soon as every compute warp has read step g's
+          ok = mbar_wait(&S.kv_full, uit & 1, p.err) && issue_sdp(g0, false);
+          for (int l = 0; ok && l + 1 < L; ++l) {
             const int g = g0 + l;
-            // dP^T of step g+2 overwrites the columns that held step g's dQ^T
-            if (!(ok = mbar_wait(&S.drain_done[g & 1], (g >> 1) & 1, p.err))) break;
+            if (!(ok = mbar_wait(&S.ld_done, g & 1, p.err))) break;
             tc_fence_after();
-            ok = issue_one(g + 2, false);
+            ok = issue_sdp(g + 1, false);
           }
         } else if (warp == kWarpMma2) {
           ok = mbar_wait(&S.kv_full, uit & 1, p.err);
+          for (int l = 0; ok && l < min(2, L); ++l) ok = issue_sdp(g0 + l, true);
           for (int l = 0; ok && l < L; ++l) {
-            const int g = g0 + l, s = g & 1, st = g % NST;
-            if (!(ok = mbar_wait(&S.ds_ready[s], (g >> 1) & 1, p.err))) break;
+            const int g = g0 + l, st = g % NST;
+            if (!(ok = mbar_wait(&S.ds_ready[g & 1], (g >> 1) & 1, p.err))) break;
             tc_fence_after();
-            const uint32_t ob = smem_u32(S.dout[st]), tS = tmem + s * 128;
+            const uint32_t ob = smem_u32(S.dout[st]), tP = tmem + (g & 1) * 64;
 #pragma unroll
-            for (int kk = 0; kk < BQ / 16; ++kk)  // dV += P^T dO
-              mma_ts(tmem + kColDV, tS + kk * 8, desc_sw128(ob + kk * 2048, kQSub, 1024), id_kv,
-                     (l > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < BQ / 16; ++kk)  // dV += P^T dO; P^T of query half w at column 32w
+              mma_ts(tmem + kColDV, tP + (kk >> 1) * 32 + (kk & 1) * 8, desc_sw128(ob + kk * 2048, kQSub, 1024),
+                     id_kv, (l > 0 || kk > 0) ? 1u : 0u);
             mma_commit(&S.qdo_empty[st]);
-            // S^T of step g+2 reuses the columns whose P^T the dV above reads (same issuer: ordered)
-            if (l + 2 < L && !(ok = issue_one(g + 2, true))) break;
+            // S^T of step g+2 into the slot whose P^T the dV above reads (same issuer: ordered)
+            if (l + 2 < L && !(ok = issue_sdp(g + 2, true))) break;
           }
           mma_commit(&S.mma_done);
         } else {
           ok = mbar_wait(&S.kv_full, uit & 1, p.err);
           for (int l = 0; ok && l < L; ++l) {
-            const int g = g0 + l, s = g & 1;
-            if (!(ok = mbar_wait(&S.ds_ready[s], (g >> 1) & 1, p.err))) break;
+            const int g = g0 + l;
+            if (!(ok = mbar_wait(&S.ds_ready[g & 1], (g >> 1) & 1, p.err))) break;
+            // the dQ^T columns must have been drained (step g-1)
+            if (g >= 1 && !(ok = mbar_wait(&S.drain_done, (g - 1) & 1, p.err))) break;
             tc_fence_after();
-            const uint32_t db = smem_u32(S.ds[s]), tD = tmem + s * 128 + 64;
+            const uint32_t db = smem_u32(S.ds[g & 1]);
 #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk)  // dQ^T = K^T dS^T
-              mma_ss(tD, desc_sw128(kb + kk * 2048, kKSub, 1024), desc_sw128(db + kk * 2048, kQSub, 1024), id_dq,
-                     kk > 0);
-            mma_commit(&S.dq_full[s]);
+              mma_ss(tmem + kColDQ, desc_sw128(kb + kk * 2048, kKSub, 1024), desc_sw128(db + kk * 2048, kQSub, 1024),
+                     id_dq, kk > 0);
+            mma_commit(&S.dq_full[g & 1]);
           }
         }
         if (!ok) s_abort = 1;
@@ -436,7 +440,13 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
       tc_fence_after();
     }
   } else {
-    regs_dec<kRegDq>();
+    // ------------------------------------------------------ dQ drain (warps 12-15)
+    // TMEM lane = head dimension r, column = query. Free the columns once they are in
+    // registers, then per half tile write scale * dQ row-major into a staging buffer and
+    // add it into the fp32 accumulator with one TMA reduce (one thread issues them all).
+    const int q4 = warp & 3, r = q4 * 32 + lane;
+    const uint32_t lanes = static_cast<uint32_t>(q4 * 32) << 16;
+    const bool leader = warp == kWarpDq && lane == 0;
     while (true) {
       Unit U;
       const int fu = fetch_unit(p, G, &s_unit, &s_abort, false, U);
@@ -445,31 +455,22 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         __syncthreads();
         continue;
       }
-      const int kt = U.kt, kvh = U.kvh, b = U.b, L = U.L, qt_lo = U.qt_lo, j0 = kt * BN;
-      (void)kt; (void)j0;
-      // ------------------------------------------------------ dQ drain (warps 12-15)
-      // TMEM lane = head dimension r, column = query. Free the columns once they are in
-      // registers, then per half tile write scale * dQ row-major into a staging buffer and
-      // add it into the fp32 accumulator with one TMA reduce (one thread issues them all).
-      const int q4 = warp & 3, r = q4 * 32 + lane;
-      const uint32_t lanes = static_cast<uint32_t>(q4 * 32) << 16;
-      const bool leader = warp == kWarpDq && lane == 0;
+      const int kvh = U.kvh, b = U.b, L = U.L;
       bool ok = true;
       for (int l = 0; l < L; ++l) {
-        const int g = g0 + l, s = g & 1, t = b + l;
+        const int g = g0 + l, t = b + l;
         const int h = kvh * G + t % G;
-        const int i0 = (qt_lo + t / G) * BQ;
+        const int i0 = (U.qt_lo + t / G) * BQ;
         // one decision for the four warps: they meet at the staging barriers below
-        if (!(ok = named_bar_and(1, 128, mbar_wait(&S.dq_full[s], (g >> 1) & 1, p.err)))) break;
+        if (!(ok = named_bar_and(1, 128, mbar_wait(&S.dq_full[g & 1], (g >> 1) & 1, p.err)))) break;
         tc_fence_after();
         uint32_t v[2][32];
-        const uint32_t tD = tmem + lanes + s * 128 + 64;
-        tmem_ld32(tD, v[0]);
-        tmem_ld32(tD + 32, v[1]);
+        tmem_ld32(tmem + lanes + kColDQ, v[0]);
+        tmem_ld32(tmem + lanes + kColDQ + 32, v[1]);
         tmem_ld_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&S.drain_done[s]);
+        if (lane == 0) mbar_arrive(&S.drain_done);
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           // the reduce that last read this half's buffer must be done reading it
@@ -708,16 +709,6 @@ int attn_bwd_tc(const AttnArgs& a, cudaStream_t st) {
   }
   int n_sm = 0;
   if ((rc = sm_count(&n_sm))) return rc;
-  // The warpgroups' register split adds up to exactly the launch's registers per thread.
-  static int launch_regs = -1;
-  if (launch_regs < 0) {
-    cudaFuncAttributes fa{};
-    TREE_CUDA_TRY(cudaFuncGetAttributes(&fa, attn_bwd_tc_kernel));
-    launch_regs = fa.numRegs;
-  }
-  if (launch_regs != kRegLaunch)
-    return fail(TREE_ERR_CUDA, "attn_bwd_tc_kernel: built with %d registers per thread, its warpgroups split %d",
-                launch_regs, kRegLaunch);
   Params p{};
   p.T = static_cast<int>(a.T);
   p.T_pad = static_cast<int>(T_pad);
