@@ -71,6 +71,13 @@ struct Smem {
   uint32_t tmem_base;
 };
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
+// dK and dV staging at the end of a unit, 64 KB each, over q, dout and ds (contiguous)
+constexpr uint32_t kEpiBytes = BN * D * 4;
+static_assert(offsetof(Smem, dout) == offsetof(Smem, q) + sizeof(Smem::q) &&
+                  offsetof(Smem, ds) == offsetof(Smem, dout) + sizeof(Smem::dout) &&
+                  sizeof(Smem::q) + sizeof(Smem::dout) + sizeof(Smem::ds) >= 2 * kEpiBytes &&
+                  offsetof(Smem, q) % 1024 == 0,
+              "dK / dV staging needs q, dout and ds contiguous and 1024-byte aligned");
 static_assert(kSmemBytes + 64 <= 232448, "backward shared memory exceeds the 227 KB per-block limit");
 
 struct Params {
@@ -162,7 +169,8 @@ __device__ __forceinline__ int fetch_unit(const Params& p, int G, int* s_unit, i
 __global__ void __launch_bounds__(kThreads, 1)
 attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
-                   const __grid_constant__ CUtensorMap tmDQ, Params p) {
+                   const __grid_constant__ CUtensorMap tmDQ, const __grid_constant__ CUtensorMap tmDK,
+                   const __grid_constant__ CUtensorMap tmDV, Params p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_unit, s_abort;
   if (p.err && (*reinterpret_cast<volatile int*>(p.err) & (1 << TREE_ERR_TIMEOUT))) return;
@@ -285,11 +293,17 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.ds_ready[g & 1]);
       }
-      // unit epilogue: warps 0-3 add scale * dK, warps 4-7 add dV (one key row per thread)
-      ok = __all_sync(0xffffffffu, ok && mbar_wait(&S.mma_done, uit & 1, p.err));
+      // Unit epilogue: warps 0-3 add scale * dK, warps 4-7 add dV into the fp32
+      // accumulators (one key row per thread). The rows are staged in the Q_i / dO_i / dS^T
+      // buffers, idle now, as four [128 keys][32 dims] tiles with the 128-byte swizzle, and
+      // added by TMA reduces. dQ^T of the unit's last two steps must have read dS^T first.
+      const int g_end = g0 + L;
+      ok = __all_sync(0xffffffffu, ok && mbar_wait(&S.mma_done, uit & 1, p.err) &&
+                                       mbar_wait(&S.dq_full[(g_end - 1) & 1], ((g_end - 1) >> 1) & 1, p.err) &&
+                                       (L < 2 || mbar_wait(&S.dq_full[g_end & 1], ((g_end - 2) >> 1) & 1, p.err)));
       tc_fence_after();
       if (ok) {
-        float* acc = (wg == 0 ? p.dk_acc : p.dv_acc) + (static_cast<int64_t>(j) * p.Hkv + U.kvh) * D;
+        uint8_t* stage = S.q[0] + wg * kEpiBytes;
         const float mul = wg == 0 ? p.scale : 1.f;
         const uint32_t tacc = tmem + lanes + (wg == 0 ? kColDK : kColDV);
 #pragma unroll 1
@@ -297,12 +311,20 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
           uint32_t v[32];
           tmem_ld32(tacc + c * 32, v);
           tmem_ld_wait();
-          if (j < p.T) {
+          uint8_t* row = stage + c * (kEpiBytes / 4) + r * 128;
 #pragma unroll
-            for (int w = 0; w < 8; ++w)
-              red_add4(acc + c * 32 + 4 * w, __uint_as_float(v[4 * w]) * mul, __uint_as_float(v[4 * w + 1]) * mul,
-                       __uint_as_float(v[4 * w + 2]) * mul, __uint_as_float(v[4 * w + 3]) * mul);
-          }
+          for (int w = 0; w < 8; ++w)
+            *reinterpret_cast<float4*>(row + ((w ^ (r & 7)) * 16)) =
+                make_float4(__uint_as_float(v[4 * w]) * mul, __uint_as_float(v[4 * w + 1]) * mul,
+                            __uint_as_float(v[4 * w + 2]) * mul, __uint_as_float(v[4 * w + 3]) * mul);
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(2 + wg, 128);
+        if (q4 == 0 && lane == 0) {
+          for (int c = 0; c < 4; ++c)
+            tma_reduce_add_3d(wg == 0 ? &tmDK : &tmDV, stage + c * (kEpiBytes / 4), c * 32, U.kvh, U.kt * BN);
+          bulk_commit();
+          bulk_wait_read0();  // the next unit loads into these buffers
         }
       } else {
         s_abort = 1;
@@ -517,114 +539,162 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
   }
 }
 
-// Builds the work units. Every key tile's steps (its 64-row query tiles x the G query
-// heads of the group) are cut into chunks of chunk_q whole query tiles, chunk_q growing
-// with the total work so that there are at most about 1216 + Hkv * n_kt units; the units
-// of all key tiles are then ordered by the first query tile they cover (a counting sort),
-// so the CTAs running at the same time work on nearby query rows and share the Q / dO
-// tiles and the dQ accumulator lines in L2. One block; `bucket` holds n_q64 + 1 ints.
-__global__ void attn_bwd_plan_kernel(const int32_t* __restrict__ kmax, int n_kt, int T, int G, int Hkv,
-                                     int max_units, int4* __restrict__ units, int* __restrict__ n_units,
-                                     int* __restrict__ counter, int* __restrict__ bucket) {
+struct PrepParams {
+  const int32_t* end;  // subtree_end [T]
+  int T, T_pad, n_kt, Hq, Hkv, max_units;
+  int32_t* kmax;       // [n_kt] max subtree_end of each 128-key tile
+  int32_t* kmin;       // [n_kt] min subtree_end of each 128-key tile
+  int32_t* endp;       // [n_kt * 128] subtree_end, -1 past T
+  int4* units;
+  int* n_units;
+  int* counter;
+  int* bucket;         // [T_pad / 64 + 1]
+  const __nv_bfloat16* o;
+  const __nv_bfloat16* dout;
+  const float* lse;    // [Hq, T]
+  float* lse2;         // [Hq, T_pad]
+  float* delta;        // [Hq, T_pad]
+  float* dq_acc;
+  float* dk_acc;
+  float* dv_acc;
+  int* err;
+};
+
+// Block 0 (the planner): per-128-key-tile bounds of subtree_end (checked to lie in
+// [j, T)), the padded copy the main kernel reads, and the work units. Every key tile's
+// steps (its 64-row query tiles x the G query heads of the group) are cut into chunks of
+// chunk_q whole query tiles, chunk_q growing with the total work so that there are at
+// most about 1216 + Hkv * n_kt units; the units of all key tiles are then ordered by the
+// first query tile they cover (a counting sort), so that the CTAs running at the same
+// time work on nearby query rows and share the Q / dO tiles and the dQ accumulator lines
+// in L2.
+// Blocks 1..: Delta = dO . O and LSE * log2(e) per (row, head), padded to T_pad with
+// (0, +inf), and zeroed fp32 dQ, dK and dV accumulators; one warp per (row, head).
+__global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const PrepParams q) {
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (blockIdx.x > 0) {
+    const int64_t w = static_cast<int64_t>(blockIdx.x - 1) * 8 + warp;
+    if (w >= static_cast<int64_t>(q.T_pad) * q.Hq) return;
+    const int64_t i = w / q.Hq;
+    const int h = static_cast<int>(w % q.Hq);
+    float dl = 0.f, l2 = INFINITY;
+    if (i < q.T) {
+      const int64_t off = w * 128 + lane * 4;
+      const uint2 a = *reinterpret_cast<const uint2*>(q.o + off);
+      const uint2 b = *reinterpret_cast<const uint2*>(q.dout + off);
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+      const float2 a0 = __bfloat1622float2(a2[0]), a1 = __bfloat1622float2(a2[1]);
+      const float2 b0 = __bfloat1622float2(b2[0]), b1 = __bfloat1622float2(b2[1]);
+      dl = a0.x * b0.x + a0.y * b0.y + a1.x * b1.x + a1.y * b1.y;
+#pragma unroll
+      for (int s = 16; s > 0; s >>= 1) dl += __shfl_xor_sync(0xffffffffu, dl, s);
+      l2 = q.lse[static_cast<int64_t>(h) * q.T + i] * 1.4426950408889634f;
+      const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+      *reinterpret_cast<float4*>(q.dq_acc + off) = z;
+      if (h < q.Hkv) {
+        const int64_t kv = (i * q.Hkv + h) * 128 + lane * 4;
+        *reinterpret_cast<float4*>(q.dk_acc + kv) = z;
+        *reinterpret_cast<float4*>(q.dv_acc + kv) = z;
+      }
+    }
+    if (lane == 0) {
+      q.lse2[static_cast<int64_t>(h) * q.T_pad + i] = l2;
+      q.delta[static_cast<int64_t>(h) * q.T_pad + i] = dl;
+    }
+    return;
+  }
+  // ---------------------------------------------------------------- planner
   __shared__ long long s_total;
   __shared__ int s_units;
-  const int n_q64 = (T + BQ - 1) / BQ;
+  const int T = q.T, n_q64 = q.T_pad / BQ, G = q.Hq / q.Hkv;
   if (threadIdx.x == 0) {
     s_total = 0;
     s_units = 0;
-    *counter = 0;
+    *q.counter = 0;
   }
-  for (int b = threadIdx.x; b <= n_q64; b += blockDim.x) bucket[b] = 0;
+  for (int b = threadIdx.x; b <= n_q64; b += blockDim.x) q.bucket[b] = 0;
+  for (int kt = warp; kt < q.n_kt; kt += blockDim.x / 32) {
+    int mx = -1, mn = INT32_MAX;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int j = kt * BN + c * 32 + lane;
+      const bool in = j < T;
+      const int e = in ? q.end[j] : -1;
+      if (in && (e < j || e >= T)) raise_error(q.err, TREE_ERR_DEVICE_CHECK);
+      q.endp[j] = e;
+      if (in) {
+        mx = max(mx, e);
+        mn = min(mn, e);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    }
+    if (lane == 0) {
+      q.kmax[kt] = mx;
+      q.kmin[kt] = mn;
+    }
+  }
   __syncthreads();
   auto tiles_of = [&](int kt, int* lo) -> int {
     const int j0 = kt * BN;
-    const int last_row = min(kmax[kt], T - 1);
+    const int last_row = min(q.kmax[kt], T - 1);
     *lo = j0 / BQ;
     return last_row >= j0 ? last_row / BQ - *lo + 1 : 0;
   };
   long long local = 0;
-  for (int kt = threadIdx.x; kt < n_kt; kt += blockDim.x) {
+  for (int kt = threadIdx.x; kt < q.n_kt; kt += blockDim.x) {
     int lo;
     local += tiles_of(kt, &lo);
   }
   atomicAdd(reinterpret_cast<unsigned long long*>(&s_total), static_cast<unsigned long long>(local));
   __syncthreads();
-  const long long steps_all = s_total * G * Hkv;
+  const long long steps_all = s_total * G * q.Hkv;
   // ~8 units per SM on large trees; on small ones the 16-step floor keeps units short
   const int chunk_steps = static_cast<int>(max(16LL, (steps_all + 1215) / 1216));
   const int chunk_q = (chunk_steps + G - 1) / G;
-  // count units per first query tile
-  for (int kt = threadIdx.x; kt < n_kt; kt += blockDim.x) {
+  for (int kt = threadIdx.x; kt < q.n_kt; kt += blockDim.x) {  // units per first query tile
     int lo;
     const int nq = tiles_of(kt, &lo);
-    for (int c = 0; c * chunk_q < nq; ++c) atomicAdd(&bucket[lo + c * chunk_q], 1);
+    for (int c = 0; c * chunk_q < nq; ++c) atomicAdd(&q.bucket[lo + c * chunk_q], 1);
   }
   __syncthreads();
-  if (threadIdx.x == 0) {  // exclusive scan, in units of (key tile, chunk) pairs
+  if (warp == 0) {  // exclusive scan, in units of (key tile, chunk) pairs
     int run = 0;
-    for (int b = 0; b < n_q64; ++b) {
-      const int x = bucket[b];
-      bucket[b] = run;
-      run += x;
+    for (int b0 = 0; b0 <= n_q64; b0 += 32) {
+      const int b = b0 + lane;
+      const int x = b < n_q64 ? q.bucket[b] : 0;
+      int incl = x;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (b <= n_q64) q.bucket[b] = run + incl - x;
+      run += __shfl_sync(0xffffffffu, incl, 31);
     }
-    bucket[n_q64] = run;
-    s_units = run;
+    if (lane == 0) s_units = run;
   }
   __syncthreads();
-  for (int kt = threadIdx.x; kt < n_kt; kt += blockDim.x) {
+  for (int kt = threadIdx.x; kt < q.n_kt; kt += blockDim.x) {
     int lo;
     const int nq = tiles_of(kt, &lo);
     for (int c = 0; c * chunk_q < nq; ++c) {
-      const int pos = atomicAdd(&bucket[lo + c * chunk_q], 1);
+      const int pos = atomicAdd(&q.bucket[lo + c * chunk_q], 1);
       const int b0 = c * chunk_q * G, b1 = min((c + 1) * chunk_q, nq) * G;
-      for (int kvh = 0; kvh < Hkv; ++kvh) {
-        const int idx = pos * Hkv + kvh;
-        if (idx < max_units) units[idx] = make_int4(kt, kvh, b0, b1);
+      for (int kvh = 0; kvh < q.Hkv; ++kvh) {
+        const int idx = pos * q.Hkv + kvh;
+        if (idx < q.max_units) q.units[idx] = make_int4(kt, kvh, b0, b1);
       }
     }
   }
-  if (threadIdx.x == 0) *n_units = min(s_units * Hkv, max_units);
+  if (threadIdx.x == 0) *q.n_units = min(s_units * q.Hkv, q.max_units);
 }
 
 }  // namespace tcbwd
-
-// Delta = dO . O and LSE * log2(e) per (row, head), padded to T_pad with (0, +inf);
-// zeroes the fp32 dQ, dK and dV accumulators. One warp per (row, head), 4 dims per lane.
-__global__ void attn_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
-                                    const float* __restrict__ lse, int64_t T, int64_t T_pad, int Hq, int Hkv,
-                                    float* __restrict__ lse2, float* __restrict__ delta, float* __restrict__ dq_acc,
-                                    float* __restrict__ dk_acc, float* __restrict__ dv_acc) {
-  const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
-  const int lane = threadIdx.x % 32;
-  if (w >= T_pad * Hq) return;
-  const int64_t i = w / Hq;
-  const int h = static_cast<int>(w % Hq);
-  float dl = 0.f, l2 = INFINITY;
-  if (i < T) {
-    const int64_t off = w * 128 + lane * 4;
-    const uint2 a = *reinterpret_cast<const uint2*>(o + off);
-    const uint2 b = *reinterpret_cast<const uint2*>(dout + off);
-    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
-    const float2 a0 = __bfloat1622float2(a2[0]), a1 = __bfloat1622float2(a2[1]);
-    const float2 b0 = __bfloat1622float2(b2[0]), b1 = __bfloat1622float2(b2[1]);
-    dl = a0.x * b0.x + a0.y * b0.y + a1.x * b1.x + a1.y * b1.y;
-#pragma unroll
-    for (int s = 16; s > 0; s >>= 1) dl += __shfl_xor_sync(0xffffffffu, dl, s);
-    l2 = lse[static_cast<int64_t>(h) * T + i] * 1.4426950408889634f;
-    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-    *reinterpret_cast<float4*>(dq_acc + off) = z;
-    if (h < Hkv) {
-      const int64_t kv = (i * Hkv + h) * 128 + lane * 4;
-      *reinterpret_cast<float4*>(dk_acc + kv) = z;
-      *reinterpret_cast<float4*>(dv_acc + kv) = z;
-    }
-  }
-  if (lane == 0) {
-    lse2[static_cast<int64_t>(h) * T_pad + i] = l2;
-    delta[static_cast<int64_t>(h) * T_pad + i] = dl;
-  }
-}
 
 // dQ, dK and dV (bf16) from their fp32 accumulators in one launch, 4 elements per thread.
 __global__ void attn_grads_to_bf16_kernel(const float* __restrict__ aq, __nv_bfloat16* __restrict__ oq, int64_t nq4,
@@ -674,22 +744,39 @@ static int sm_count(int* n) {
 
 int attn_bwd_tc(const AttnArgs& a, cudaStream_t st) {
   using namespace tcbwd;
-  int rc = tile_meta128_launch(a, st);
-  if (rc) return rc;
   const int64_t T_pad = (a.T + BQ - 1) / BQ * BQ;
   const int n_kt = static_cast<int>((a.T + BN - 1) / BN);
   const int max_units = static_cast<int>(attn_bwd_max_units(a.T, a.Hkv));
-  attn_bwd_plan_kernel<<<1, 1024, 0, st>>>(a.ws.kmax128, n_kt, static_cast<int>(a.T), a.Hq / a.Hkv, a.Hkv,
-                                           max_units, reinterpret_cast<int4*>(a.ws.units), a.ws.n_units,
-                                           a.ws.counter, a.ws.bucket);
-  TREE_LAUNCH_CHECK("attn_bwd_plan_kernel");
   {
-    const int64_t warps = T_pad * a.Hq;
-    attn_bwd_pre_kernel<<<static_cast<unsigned>((warps * 32 + 255) / 256), 256, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout), a.lse, a.T, T_pad,
-        a.Hq, a.Hkv, a.ws.lse2_pad, a.ws.delta_pad, a.ws.dq_acc, a.ws.dk_acc, a.ws.dv_acc);
-    TREE_LAUNCH_CHECK("attn_bwd_pre_kernel");
+    PrepParams q{};
+    q.end = a.end;
+    q.T = static_cast<int>(a.T);
+    q.T_pad = static_cast<int>(T_pad);
+    q.n_kt = n_kt;
+    q.Hq = a.Hq;
+    q.Hkv = a.Hkv;
+    q.max_units = max_units;
+    q.kmax = a.ws.kmax128;
+    q.kmin = a.ws.kmin128;
+    q.endp = a.ws.end_pad;
+    q.units = reinterpret_cast<int4*>(a.ws.units);
+    q.n_units = a.ws.n_units;
+    q.counter = a.ws.counter;
+    q.bucket = a.ws.bucket;
+    q.o = static_cast<const __nv_bfloat16*>(a.o);
+    q.dout = static_cast<const __nv_bfloat16*>(a.dout);
+    q.lse = a.lse;
+    q.lse2 = a.ws.lse2_pad;
+    q.delta = a.ws.delta_pad;
+    q.dq_acc = a.ws.dq_acc;
+    q.dk_acc = a.ws.dk_acc;
+    q.dv_acc = a.ws.dv_acc;
+    q.err = device_error_word();
+    const int64_t pre_blocks = (T_pad * a.Hq + 7) / 8;
+    attn_bwd_prep_kernel<<<static_cast<unsigned>(1 + pre_blocks), 256, 0, st>>>(q);
+    TREE_LAUNCH_CHECK("attn_bwd_prep_kernel");
   }
+  int rc = TREE_OK;
   CUtensorMap mk, mv, mq, mdo, mdq;
   if ((rc = rows_map(&mk, a.k, a.T, a.Hkv, 128)) || (rc = rows_map(&mv, a.v, a.T, a.Hkv, 128)) ||
       (rc = rows_map(&mq, a.q, a.T, a.Hq, BQ)) || (rc = rows_map(&mdo, a.dout, a.T, a.Hq, BQ)))
@@ -700,6 +787,16 @@ int attn_bwd_tc(const AttnArgs& a, cudaStream_t st) {
     const uint64_t strides[2] = {128 * 4, static_cast<uint64_t>(a.Hq) * 128 * 4};
     const uint32_t box[3] = {128, 1, BQ / 2};
     if ((rc = make_tmap(&mdq, a.ws.dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, dims, strides, box, false))) return rc;
+  }
+  CUtensorMap mdk, mdv;
+  {
+    // fp32 dK / dV accumulators [T, Hkv, 128] as {d, head, row}, box {32, 1, 128}, 128-byte swizzle
+    const uint64_t dims[3] = {128, static_cast<uint64_t>(a.Hkv), static_cast<uint64_t>(a.T)};
+    const uint64_t strides[2] = {128 * 4, static_cast<uint64_t>(a.Hkv) * 128 * 4};
+    const uint32_t box[3] = {32, 1, BN};
+    if ((rc = make_tmap(&mdk, a.ws.dk_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, dims, strides, box, true)) ||
+        (rc = make_tmap(&mdv, a.ws.dv_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, dims, strides, box, true)))
+      return rc;
   }
   static bool attr_set = false;
   if (!attr_set) {
@@ -728,7 +825,7 @@ int attn_bwd_tc(const AttnArgs& a, cudaStream_t st) {
   p.counter = a.ws.counter;
   p.err = device_error_word();
   const int grid = static_cast<int>(std::min<int64_t>(n_sm, max_units));
-  attn_bwd_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(mk, mv, mq, mdo, mdq, p);
+  attn_bwd_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(mk, mv, mq, mdo, mdq, mdk, mdv, p);
   TREE_LAUNCH_CHECK("attn_bwd_tc_kernel");
   const int64_t nq4 = a.T * a.Hq * a.d / 4, nk4 = a.T * a.Hkv * a.d / 4;
   attn_grads_to_bf16_kernel<<<static_cast<unsigned>((nq4 + 2 * nk4 + 255) / 256), 256, 0, st>>>(
