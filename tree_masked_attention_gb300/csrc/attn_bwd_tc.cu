@@ -14,24 +14,25 @@
 //   P^T  = exp2(S^T scale log2e - LSE_i log2e) on visible pairs, 0 elsewhere
 //   dS^T = P^T (dP^T - Delta_i)                              (compute warps, one key row each)
 //   dV  += P^T dO_i         (A = P^T bf16 from TMEM, B = dO_i MN-major)
-//   dK  += dS^T Q_i         (A = dS^T bf16 in shared memory, B = Q_i MN-major)
+//   dK  += dS^T Q_i         (A = dS^T bf16 from TMEM, B = Q_i MN-major)
 //   dQ_i^T = K^T dS^T       (M=128 dims, N=64 queries; A = K MN-major, B = dS^T MN-major)
 //   dQ_i += scale dQ_i^T    (fp32 reductions into the workspace accumulator, coalesced
 //                            along the head dimension; a final kernel converts to bf16)
 // Both compute warpgroups work on the same step, warpgroup w on queries 32w..32w+31 of
 // the tile, so a step's softmax backward takes half as long. TMEM (512 columns): two
-// S^T/P^T slots used by alternate steps, one dP^T slot, one dQ^T slot (64 each), dV and
-// dK (128 each). While the warps work on step g, the tensor core already computes S^T
-// and dP^T of step g+1 into the free slots, and dQ^T of step g-1 drains through a
-// warpgroup of its own into the fp32 accumulator.
+// slots used by alternate steps (S^T, then P^T and dS^T as bf16 pairs), one dP^T slot,
+// one dQ^T slot (64 each), dV and dK (128 each). While the warps work on step g, the
+// tensor core already computes S^T and dP^T of step g+1 into the free slots, and dQ^T
+// of step g-1 drains through a warpgroup of its own into the fp32 accumulator.
 //   warps 0-7    compute (0-3 and 4-7: query halves); at the end of a unit 0-3 add dK, 4-7 dV
 //   warp 8       TMA producer, and issues dK
 //   warp 9       issues dP^T (owns TMEM)
-//   warp 10      issues dV, then S^T two steps ahead into the slot that dV has just read
+//   warp 10      issues dV, then S^T two steps ahead into the slot that dV and dK have read
 //   warp 11      issues dQ^T
 //   warps 12-15  dQ^T drain, staging and TMA reduce
 // A tcgen05.mma issue occupies its thread for about as long as an N<=128 MMA runs, so the
-// four issuing threads share a step's 32 MMAs about evenly (8 each).
+// four issuing threads share a step's 32 MMAs. The operands that stay in TMEM (P^T and
+// dS^T) spare shared-memory bandwidth, which the MMAs' operand reads otherwise saturate.
 #include <algorithm>
 #include <cmath>
 
@@ -274,12 +275,13 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
             dk[t2 / 2] = pack_bf16(dd.x, dd.y);
           }
         }
-        // P^T (bf16 pairs) over the first 16 of this half's S^T columns, which only this
-        // warp has read
+        // P^T and dS^T (bf16 pairs) over this half's S^T columns, which only this warp has
+        // read: P^T (the A operand of dV) in the first 16, dS^T (that of dK) in the last 16
         tmem_st16(tS, pk);
-        // dS^T into shared memory once dK and dQ^T of step g-2 have read the buffer
-        if (g >= 2 && !(ok = __all_sync(0xffffffffu, mbar_wait(&S.dk_done[g & 1], ((g >> 1) - 1) & 1, p.err) &&
-                                                         mbar_wait(&S.dq_full[g & 1], ((g >> 1) - 1) & 1, p.err))))
+        tmem_st16(tS + 16, dk);
+        // dS^T into shared memory too (the B operand of dQ^T) once dQ^T of step g-2 has
+        // read the buffer
+        if (g >= 2 && !(ok = __all_sync(0xffffffffu, mbar_wait(&S.dq_full[g & 1], ((g >> 1) - 1) & 1, p.err))))
           break;
         uint8_t* dsrow = S.ds[g & 1] + r * 128;
 #pragma unroll
@@ -400,10 +402,10 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
             const int g = g0 + l, st = g % NST;
             if (!(ok = mbar_wait(&S.ds_ready[g & 1], (g >> 1) & 1, p.err))) break;
             tc_fence_after();
-            const uint32_t qb = smem_u32(S.q[st]), db = smem_u32(S.ds[g & 1]);
+            const uint32_t qb = smem_u32(S.q[st]), tDS = tmem + (g & 1) * 64 + 16;
 #pragma unroll
-            for (int kk = 0; kk < BQ / 16; ++kk)  // dK += dS^T Q
-              mma_ss(tmem + kColDK, desc_sw128(db + kk * 32, 16, 1024), desc_sw128(qb + kk * 2048, kQSub, 1024),
+            for (int kk = 0; kk < BQ / 16; ++kk)  // dK += dS^T Q; dS^T of query half w at column 32w + 16
+              mma_ts(tmem + kColDK, tDS + (kk >> 1) * 32 + (kk & 1) * 8, desc_sw128(qb + kk * 2048, kQSub, 1024),
                      id_kv, (l > 0 || kk > 0) ? 1u : 0u);
             mma_commit(&S.qdo_empty[st]);
             mma_commit(&S.dk_done[g & 1]);
@@ -432,8 +434,13 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
               mma_ts(tmem + kColDV, tP + (kk >> 1) * 32 + (kk & 1) * 8, desc_sw128(ob + kk * 2048, kQSub, 1024),
                      id_kv, (l > 0 || kk > 0) ? 1u : 0u);
             mma_commit(&S.qdo_empty[st]);
-            // S^T of step g+2 into the slot whose P^T the dV above reads (same issuer: ordered)
-            if (l + 2 < L && !(ok = issue_sdp(g + 2, true))) break;
+            // S^T of step g+2 into the slot whose P^T the dV above reads (same issuer:
+            // ordered) and whose dS^T dK (warp 8) reads
+            if (l + 2 < L) {
+              if (!(ok = mbar_wait(&S.dk_done[g & 1], (g >> 1) & 1, p.err))) break;
+              tc_fence_after();
+              if (!(ok = issue_sdp(g + 2, true))) break;
+            }
           }
           mma_commit(&S.mma_done);
         } else {
