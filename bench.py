@@ -206,6 +206,8 @@ def describe(name, T, P, n_seqs, n_tokens, c):
         "unpacked_tokens": int(n_tokens), "por": round(1.0 - T / n_tokens, 4),
         "Hq": c["Hq"], "Hkv": c["Hkv"], "d": c["d"],
         "l2": "flushed before every timed step (256 MiB write)",
+        "step": "tree_rope(q, k) -> tree_attn_fwd -> tree_attn_bwd_rope (backward, and the inverse "
+                "rotation of dq, dk fused into the kernel that writes them)",
     }
 
 
@@ -254,10 +256,9 @@ def run_ours(args):
         if ev: ev[1].record(stream)
         tma.tree_attn_fwd(q, k, v, end, workspace=ws, out=o, lse=lse)
         if ev: ev[2].record(stream)
-        tma.tree_attn_bwd(q, k, v, o, do, lse, end, workspace=ws, grads=(dq, dk, dv))
+        # backward with the inverse rotation of dq, dk fused into the kernel that writes them
+        tma.tree_attn_bwd_rope(q, k, v, o, do, lse, end, pos, workspace=ws, grads=(dq, dk, dv))
         if ev: ev[3].record(stream)
-        tma.tree_rope(dq, dk, pos, inverse=True)
-        if ev: ev[4].record(stream)
 
     clocks = ClockSampler(local).start()
     for _ in range(max(args.warmup, 0)):
@@ -269,7 +270,7 @@ def run_ours(args):
     K = args.steps
     # Per-call split: K eager steps with CUDA events between the calls, on the launching
     # stream (these give the roofline's per-kernel-call durations).
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
     barrier(world)
     torch.cuda.synchronize()
     n0 = tma.tree_launch_count()
@@ -278,7 +279,7 @@ def run_ours(args):
         step(evs[s])
     torch.cuda.synchronize()
     launches_per_step = (tma.tree_launch_count() - n0) / K
-    op_ms = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(4)] for e in evs])  # [K, 4]
+    op_ms = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(3)] for e in evs])  # [K, 3]
     graph = None
     if not args.no_graph:
         # The step's launches captured once into a CUDA graph (static shapes and buffers),
@@ -320,11 +321,11 @@ def run_ours(args):
     peak = float(peaks["bf16_tflops"])
 
     # dominant kernel call: the op with the largest share of the step
-    names = ["tree_rope", "tree_attn_fwd", "tree_attn_bwd", "tree_rope_inverse"]
+    names = ["tree_rope", "tree_attn_fwd", "tree_attn_bwd_rope"]
     avg = op_ms.mean(axis=0)
     dom = int(np.argmax(avg))
     esize = 2 if td == torch.bfloat16 else 4
-    rope_bytes = 2.0 * (T * Hq * d + T * Hkv * d) * esize
+    rope_bytes = 2.0 * (T * Hq * d + T * Hkv * d) * esize  # read and write q, k once
     if dom in (1, 2):
         fl = f_fwd if dom == 1 else f_bwd
         achieved = fl / (avg[dom] / 1e3) / 1e12

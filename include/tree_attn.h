@@ -210,6 +210,23 @@ int tree_attn_bwd(const void* q, const void* k, const void* v, const void* o,
                   float softmax_scale, int deterministic, void* workspace,
                   size_t workspace_bytes, tree_stream_t stream);
 
+/*
+ * tree_attn_bwd_rope -- tree_attn_bwd, then the backward of the depth rotation
+ * (tree_rope with inverse = 1) on dq and dk, in one pass: when q = R q0 and
+ * k = R k0 came from tree_rope, it returns dL/dq0 = R^T dL/dq and dL/dk0 =
+ * R^T dL/dk (dv unchanged). On the tensor-core path the rotation is applied to
+ * the fp32 sums before their one rounding to dtype, inside the kernel that
+ * writes dq and dk; elsewhere it is a tree_rope call after the backward.
+ * Arguments as tree_attn_bwd, plus position_ids (device int32 [T], >= 0) and
+ * theta_base (finite, > 1) as in tree_rope.
+ */
+int tree_attn_bwd_rope(const void* q, const void* k, const void* v, const void* o,
+                       const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                       const int32_t* subtree_end, const int32_t* position_ids, int64_t T,
+                       int Hq, int Hkv, int d, int dtype, float softmax_scale,
+                       float theta_base, int deterministic, void* workspace,
+                       size_t workspace_bytes, tree_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Shared-logit log-probs                                                    */
 /* ------------------------------------------------------------------------ */

@@ -25,7 +25,7 @@ from ._lib import PackOut, PackSizes, TreeError, check, lib
 
 __all__ = [
     "tree_pack", "tree_validate_subtree_end", "tree_rope", "tree_attn_workspace_size",
-    "tree_attn_fwd", "tree_attn_bwd", "tree_logprob_workspace_size", "tree_logprob_fwd",
+    "tree_attn_fwd", "tree_attn_bwd", "tree_attn_bwd_rope", "tree_logprob_workspace_size", "tree_logprob_fwd",
     "tree_logprob_bwd", "tree_check_device_status", "tree_kernel_path", "tree_launch_count", "TreeError", "lib",
     "DTYPE_F32", "DTYPE_BF16",
 ]
@@ -184,6 +184,32 @@ def tree_attn_bwd(q, k, v, o, dout, lse, subtree_end, softmax_scale: float = 0.0
                               float(softmax_scale), int(bool(deterministic)),
                               C.c_void_p(ws.data_ptr()), ws.numel() * ws.element_size(), _stream(q)),
           "tree_attn_bwd")
+    return dq, dk, dv
+
+
+def tree_attn_bwd_rope(q, k, v, o, dout, lse, subtree_end, position_ids, theta_base: float = 10000.0,
+                       softmax_scale: float = 0.0, deterministic: bool = False, workspace=None, grads=None):
+    """tree_attn_bwd followed by the inverse depth rotation on dq and dk (one fused pass):
+    for q, k rotated by tree_rope, returns the gradients of the unrotated q, k, and dv."""
+    torch = _torch()
+    T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    dt = _dtype_code(q)
+    if grads is None:
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    else:
+        dq, dk, dv = grads
+    nbytes = tree_attn_workspace_size(T, Hq, Hkv, d, dt)
+    ws = _workspace(nbytes, q.device, workspace)
+    check(lib().tree_attn_bwd_rope(_dev(q, "q"), _dev(k, "k", q.dtype), _dev(v, "v", q.dtype),
+                                   _dev(o, "o", q.dtype), _dev(dout, "dout", q.dtype),
+                                   _dev(lse, "lse", torch.float32), _dev(dq, "dq", q.dtype),
+                                   _dev(dk, "dk", q.dtype), _dev(dv, "dv", q.dtype),
+                                   _dev(subtree_end, "subtree_end", torch.int32),
+                                   _dev(position_ids, "position_ids", torch.int32), T, Hq, Hkv, d, dt,
+                                   float(softmax_scale), float(theta_base), int(bool(deterministic)),
+                                   C.c_void_p(ws.data_ptr()), ws.numel() * ws.element_size(), _stream(q)),
+          "tree_attn_bwd_rope")
     return dq, dk, dv
 
 

@@ -132,21 +132,21 @@ extern "C" int tree_attn_fwd(const void* q, const void* k, const void* v, void* 
   return attn_fwd_simt(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
-extern "C" int tree_attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
-                             const float* lse, void* dq, void* dk, void* dv, const int32_t* subtree_end,
-                             int64_t T, int Hq, int Hkv, int d, int dtype, float softmax_scale,
-                             int deterministic, void* workspace, size_t workspace_bytes,
-                             tree_stream_t stream) {
+static int attn_bwd_common(const char* name, const void* q, const void* k, const void* v, const void* o,
+                           const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                           const int32_t* subtree_end, int64_t T, int Hq, int Hkv, int d, int dtype,
+                           float softmax_scale, int deterministic, const int32_t* rope_pos, float rope_theta,
+                           void* workspace, size_t workspace_bytes, tree_stream_t stream) {
   clear_error();
   int rc = check_attn_shape(T, Hq, Hkv, d, dtype);
   if (rc) return rc;
   if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !subtree_end)
-    return fail(TREE_ERR_INVALID_ARG, "tree_attn_bwd: null tensor pointer");
+    return fail(TREE_ERR_INVALID_ARG, "%s: null tensor pointer", name);
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
-    return fail(TREE_ERR_ALIGNMENT, "tree_attn_bwd: tensors not 16-byte aligned");
+    return fail(TREE_ERR_ALIGNMENT, "%s: tensors not 16-byte aligned", name);
   if (deterministic != 0 && deterministic != 1)
-    return fail(TREE_ERR_INVALID_ARG, "tree_attn_bwd: deterministic must be 0 or 1");
+    return fail(TREE_ERR_INVALID_ARG, "%s: deterministic must be 0 or 1", name);
   const size_t need = attn_ws_layout(T, Hq, Hkv, d, dtype, nullptr, nullptr);
   if ((rc = check_ws(workspace, workspace_bytes, need))) return rc;
   AttnArgs a{};
@@ -155,8 +155,41 @@ extern "C" int tree_attn_bwd(const void* q, const void* k, const void* v, const 
   a.T = T; a.Hq = Hq; a.Hkv = Hkv; a.d = d; a.dtype = dtype; a.deterministic = deterministic;
   a.scale = softmax_scale > 0.f ? softmax_scale : static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
   attn_ws_layout(T, Hq, Hkv, d, dtype, workspace, &a.ws);
-  if (attn_bwd_tc_supported(dtype, d, deterministic)) return attn_bwd_tc(a, reinterpret_cast<cudaStream_t>(stream));
-  return attn_bwd_simt(a, reinterpret_cast<cudaStream_t>(stream));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (attn_bwd_tc_supported(dtype, d, deterministic)) {
+    a.rope_pos = rope_pos;  // fused into the conversion of the fp32 sums
+    a.rope_theta = rope_theta;
+    return attn_bwd_tc(a, st);
+  }
+  if ((rc = attn_bwd_simt(a, st)) || !rope_pos) return rc;
+  return tree_rope(dq, dk, rope_pos, T, Hq, Hkv, d, rope_theta, dtype, 1, stream);
+}
+
+extern "C" int tree_attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                             const float* lse, void* dq, void* dk, void* dv, const int32_t* subtree_end,
+                             int64_t T, int Hq, int Hkv, int d, int dtype, float softmax_scale,
+                             int deterministic, void* workspace, size_t workspace_bytes,
+                             tree_stream_t stream) {
+  return attn_bwd_common("tree_attn_bwd", q, k, v, o, dout, lse, dq, dk, dv, subtree_end, T, Hq, Hkv, d, dtype,
+                         softmax_scale, deterministic, nullptr, 0.f, workspace, workspace_bytes, stream);
+}
+
+extern "C" int tree_attn_bwd_rope(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                                  const float* lse, void* dq, void* dk, void* dv, const int32_t* subtree_end,
+                                  const int32_t* position_ids, int64_t T, int Hq, int Hkv, int d, int dtype,
+                                  float softmax_scale, float theta_base, int deterministic, void* workspace,
+                                  size_t workspace_bytes, tree_stream_t stream) {
+  if (!position_ids) {
+    clear_error();
+    return fail(TREE_ERR_INVALID_ARG, "tree_attn_bwd_rope: position_ids is null");
+  }
+  if (!(theta_base > 1.f) || !std::isfinite(theta_base)) {
+    clear_error();
+    return fail(TREE_ERR_INVALID_ARG, "tree_attn_bwd_rope: theta_base must be finite and > 1");
+  }
+  return attn_bwd_common("tree_attn_bwd_rope", q, k, v, o, dout, lse, dq, dk, dv, subtree_end, T, Hq, Hkv, d,
+                         dtype, softmax_scale, deterministic, position_ids, theta_base, workspace,
+                         workspace_bytes, stream);
 }
 
 static int check_lm(const void* h, const void* w, const int32_t* row_ptr, const int32_t* perm,

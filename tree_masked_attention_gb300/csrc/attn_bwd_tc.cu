@@ -726,6 +726,62 @@ __global__ void attn_grads_to_bf16_kernel(const float* __restrict__ aq, __nv_bfl
   reinterpret_cast<uint2*>(o)[t] = u;
 }
 
+// The same conversion with the backward of the depth rotation (tree_rope, inverse) on dQ
+// and dK, applied to the fp32 sums before the one rounding: rotate-half pairs
+// (x[f], x[f + 64]) turned by -pos * theta^(-2f/128). One thread owns one row, 4
+// consecutive frequencies and 4 heads (of dQ, then dK), so each (cos, sin) serves 4
+// heads; then dV, 4 elements per thread.
+__global__ void attn_grads_rope_to_bf16_kernel(const float* __restrict__ aq, __nv_bfloat16* __restrict__ oq,
+                                               const float* __restrict__ ak, __nv_bfloat16* __restrict__ ok,
+                                               const float* __restrict__ av, __nv_bfloat16* __restrict__ ov,
+                                               const int32_t* __restrict__ pos, int64_t T, int Hq, int Hkv,
+                                               float neg2_log2base_over_d, int* err) {
+  constexpr int kGroups = 16, kHeads = 4;  // 16 groups of 4 frequencies per 128-wide row
+  const int n_heads = Hq + Hkv, chunks = (n_heads + kHeads - 1) / kHeads;
+  const int64_t n_rot = T * chunks * kGroups;
+  int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= n_rot) {  // dV: plain conversion
+    t -= n_rot;
+    if (t >= T * Hkv * 32) return;
+    const float4 v = reinterpret_cast<const float4*>(av)[t];
+    uint2 u;
+    u.x = sm100::pack_bf16(v.x, v.y);
+    u.y = sm100::pack_bf16(v.z, v.w);
+    reinterpret_cast<uint2*>(ov)[t] = u;
+    return;
+  }
+  const int g = static_cast<int>(t % kGroups);
+  const int chunk = static_cast<int>((t / kGroups) % chunks);
+  const int64_t row = t / (kGroups * chunks);
+  const int p0 = pos[row];
+  if (p0 < 0) {
+    raise_error(err, TREE_ERR_DEVICE_CHECK);
+    return;
+  }
+  float c[4], s[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float inv_freq = exp2f(static_cast<float>(g * 4 + i) * neg2_log2base_over_d);
+    sincosf(static_cast<float>(p0) * inv_freq, &s[i], &c[i]);
+  }
+  for (int hh = chunk * kHeads; hh < min(n_heads, (chunk + 1) * kHeads); ++hh) {
+    const bool is_q = hh < Hq;
+    const int H = is_q ? Hq : Hkv, h = is_q ? hh : hh - Hq;
+    const int64_t off = (row * H + h) * 128 + g * 4;
+    const float* a = (is_q ? aq : ak) + off;
+    __nv_bfloat16* o = (is_q ? oq : ok) + off;
+    const float4 x1 = *reinterpret_cast<const float4*>(a), x2 = *reinterpret_cast<const float4*>(a + 64);
+    // inverse rotation: y1 = x1 c + x2 s, y2 = x2 c - x1 s
+    uint2 u1, u2;
+    u1.x = sm100::pack_bf16(x1.x * c[0] + x2.x * s[0], x1.y * c[1] + x2.y * s[1]);
+    u1.y = sm100::pack_bf16(x1.z * c[2] + x2.z * s[2], x1.w * c[3] + x2.w * s[3]);
+    u2.x = sm100::pack_bf16(x2.x * c[0] - x1.x * s[0], x2.y * c[1] - x1.y * s[1]);
+    u2.y = sm100::pack_bf16(x2.z * c[2] - x1.z * s[2], x2.w * c[3] - x1.w * s[3]);
+    *reinterpret_cast<uint2*>(o) = u1;
+    *reinterpret_cast<uint2*>(o + 64) = u2;
+  }
+}
+
 static int rows_map(CUtensorMap* m, const void* base, int64_t T, int H, uint32_t rows) {
   const uint64_t dims[3] = {128, static_cast<uint64_t>(H), static_cast<uint64_t>(T)};
   const uint64_t strides[2] = {128 * 2, static_cast<uint64_t>(H) * 128 * 2};
@@ -834,6 +890,15 @@ int attn_bwd_tc(const AttnArgs& a, cudaStream_t st) {
   const int grid = static_cast<int>(std::min<int64_t>(n_sm, max_units));
   attn_bwd_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(mk, mv, mq, mdo, mdq, mdk, mdv, p);
   TREE_LAUNCH_CHECK("attn_bwd_tc_kernel");
+  if (a.rope_pos) {
+    const int64_t n = a.T * ((a.Hq + a.Hkv + 3) / 4) * 16 + a.T * a.Hkv * 32;
+    const float e = static_cast<float>(-2.0 * std::log2(static_cast<double>(a.rope_theta)) / a.d);
+    attn_grads_rope_to_bf16_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(
+        a.ws.dq_acc, static_cast<__nv_bfloat16*>(a.dq), a.ws.dk_acc, static_cast<__nv_bfloat16*>(a.dk),
+        a.ws.dv_acc, static_cast<__nv_bfloat16*>(a.dv), a.rope_pos, a.T, a.Hq, a.Hkv, e, device_error_word());
+    TREE_LAUNCH_CHECK("attn_grads_rope_to_bf16_kernel");
+    return TREE_OK;
+  }
   const int64_t nq4 = a.T * a.Hq * a.d / 4, nk4 = a.T * a.Hkv * a.d / 4;
   attn_grads_to_bf16_kernel<<<static_cast<unsigned>((nq4 + 2 * nk4 + 255) / 256), 256, 0, st>>>(
       a.ws.dq_acc, static_cast<__nv_bfloat16*>(a.dq), nq4, a.ws.dk_acc, static_cast<__nv_bfloat16*>(a.dk), nk4,

@@ -41,6 +41,8 @@ struct AttnArgs {
   int Hq, Hkv, d, dtype;
   float scale;
   int deterministic;
+  const int32_t* rope_pos;  // backward only: when set, dq/dk get the inverse depth rotation
+  float rope_theta;
   AttnWs ws;
 };
 
