@@ -287,6 +287,14 @@ int tree_kernel_path(int op, int dtype, int d);
  * threads), for launch accounting by benchmarks. */
 uint64_t tree_launch_count(void);
 
+/* Kernel timing for benchmarks. With tree_kernel_timing(1), each attention call
+ * brackets its main kernel with CUDA events on its stream (which = 0: the
+ * forward's, 1: the backward's); tree_kernel_last_ms(which) waits for the latest
+ * bracket on the current device and returns its duration in ms, or -1 if there
+ * is none. Off by default; leave it off while a stream is being captured. */
+int tree_kernel_timing(int enable);
+float tree_kernel_last_ms(int which);
+
 const char* tree_version(void);
 
 #ifdef __cplusplus

@@ -101,3 +101,10 @@ def test_host_argument_errors(tma):
     assert L.tree_rope(None, None, None, 4, 1, 1, 7, 10000.0, 1, 0, None) == 2
     assert L.tree_attn_workspace_size(4096, 32, 8, 128, 1) > 0
     assert L.tree_logprob_workspace_size(64, 64, 512, 100, 0) > 0
+
+
+def test_kernel_timing_without_brackets(tma):
+    """Without a recorded bracket (or a device) the timing query answers -1."""
+    tma.tree_kernel_timing(False)
+    assert tma.tree_kernel_last_ms(5) == -1
+    assert tma.tree_kernel_last_ms(-1) == -1

@@ -147,3 +147,24 @@ def test_bad_subtree_end_sets_device_flag():
         m.tree_check_device_status()
     assert ei.value.status == 7
     m.tree_check_device_status()   # cleared
+
+
+def test_kernel_timing_brackets():
+    """tree_kernel_timing brackets the main kernels; durations come back positive."""
+    need_cuda()
+    m = tma()
+    t = synth.galton_watson(seed=3, budget=400, seg=(5, 90), vocab=1000)
+    pk = m.tree_pack(t.seqs)
+    T = pk["T"]
+    q, k, v, do = (dev(synth.normal(s, (T, h, 128), bf16=True), torch.bfloat16)
+                   for s, h in ((1, 4), (2, 2), (3, 2), (4, 4)))
+    end = dev(pk["subtree_end"])
+    m.tree_kernel_timing(True)
+    try:
+        o, lse = m.tree_attn_fwd(q, k, v, end)
+        m.tree_attn_bwd(q, k, v, o, do, lse, end)
+        assert m.tree_kernel_last_ms(0) > 0 and m.tree_kernel_last_ms(1) > 0
+        assert m.tree_kernel_last_ms(2) == -1
+    finally:
+        m.tree_kernel_timing(False)
+    m.tree_check_device_status()

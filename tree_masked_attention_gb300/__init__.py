@@ -25,7 +25,7 @@ from ._lib import PackOut, PackSizes, TreeError, check, lib
 
 __all__ = [
     "tree_pack", "tree_validate_subtree_end", "tree_rope", "tree_attn_workspace_size",
-    "tree_attn_fwd", "tree_attn_bwd", "tree_attn_bwd_rope", "tree_logprob_workspace_size", "tree_logprob_fwd",
+    "tree_attn_fwd", "tree_attn_bwd", "tree_attn_bwd_rope", "tree_kernel_timing", "tree_kernel_last_ms", "tree_logprob_workspace_size", "tree_logprob_fwd",
     "tree_logprob_bwd", "tree_check_device_status", "tree_kernel_path", "tree_launch_count", "TreeError", "lib",
     "DTYPE_F32", "DTYPE_BF16",
 ]
@@ -211,6 +211,16 @@ def tree_attn_bwd_rope(q, k, v, o, dout, lse, subtree_end, position_ids, theta_b
                                    C.c_void_p(ws.data_ptr()), ws.numel() * ws.element_size(), _stream(q)),
           "tree_attn_bwd_rope")
     return dq, dk, dv
+
+
+def tree_kernel_timing(enable: bool) -> None:
+    """Bracket each attention call's main kernel with CUDA events (for benchmarks)."""
+    lib().tree_kernel_timing(int(bool(enable)))
+
+
+def tree_kernel_last_ms(which: int) -> float:
+    """Duration of the latest bracketed main kernel (0: forward, 1: backward), or -1."""
+    return float(lib().tree_kernel_last_ms(int(which)))
 
 
 def tree_logprob_workspace_size(T, K_h, V, n_occ, dtype_code) -> int:

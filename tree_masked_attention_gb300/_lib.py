@@ -54,6 +54,8 @@ SIGNATURES = {
     "tree_attn_fwd_noalloc": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _int, _int, _int, _int, _f, _vp]),
     "tree_attn_bwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _int, _int,
                              _int, _int, _f, _int, _vp, _sz, _vp]),
+    "tree_kernel_timing": (_int, [_int]),
+    "tree_kernel_last_ms": (C.c_float, [_int]),
     "tree_attn_bwd_rope": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _int,
                                   _int, _int, _int, _f, _f, _int, _vp, _sz, _vp]),
     "tree_logprob_workspace_size": (_sz, [_i64, _i64, _i64, _i64, _int]),

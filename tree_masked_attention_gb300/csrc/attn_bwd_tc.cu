@@ -888,8 +888,10 @@ int attn_bwd_tc(const AttnArgs& a, cudaStream_t st) {
   p.counter = a.ws.counter;
   p.err = device_error_word();
   const int grid = static_cast<int>(std::min<int64_t>(n_sm, max_units));
+  timing_begin(1, st);
   attn_bwd_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(mk, mv, mq, mdo, mdq, mdk, mdv, p);
   TREE_LAUNCH_CHECK("attn_bwd_tc_kernel");
+  timing_end(1, st);
   if (a.rope_pos) {
     const int64_t n = a.T * ((a.Hq + a.Hkv + 3) / 4) * 16 + a.T * a.Hkv * 32;
     const float e = static_cast<float>(-2.0 * std::log2(static_cast<double>(a.rope_theta)) / a.d);

@@ -429,8 +429,10 @@ int attn_fwd_tc(const AttnArgs& a, cudaStream_t st) {
   p.lse = a.lse;
   p.err = device_error_word();
   dim3 grid(a.Hq / 2, p.n_qt);
+  timing_begin(0, st);
   attn_fwd_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(mq, mk, mv, mo, p);
   TREE_LAUNCH_CHECK("attn_fwd_tc_kernel");
+  timing_end(0, st);
   return TREE_OK;
 }
 

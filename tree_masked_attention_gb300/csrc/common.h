@@ -20,6 +20,12 @@ int* device_error_word();
 // Counts one kernel launch (reported by tree_launch_count()).
 void count_launch();
 
+// CUDA-event brackets around a call's main kernel, when tree_kernel_timing(1) is on:
+// 0 = attention forward, 1 = attention backward (tree_kernel_last_ms reads them).
+constexpr int kTimedKernels = 2;
+void timing_begin(int which, void* stream);
+void timing_end(int which, void* stream);
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
 inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }

@@ -67,4 +67,47 @@ extern "C" const char* tree_last_error(void) { return tree::g_msg.c_str(); }
 
 extern "C" uint64_t tree_launch_count(void) { return tree::g_launches.load(); }
 
+namespace tree {
+static std::atomic<int> g_timing{0};
+static cudaEvent_t g_tev[128][kTimedKernels][2];
+static bool g_trecorded[128][kTimedKernels];
+
+static void timing_record(int which, void* stream, int edge) {
+  if (!g_timing.load(std::memory_order_relaxed) || which < 0 || which >= kTimedKernels) return;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return;
+  std::lock_guard<std::mutex> lock(g_err_mu);
+  cudaEvent_t& e = g_tev[dev][which][edge];
+  if (!e && cudaEventCreate(&e) != cudaSuccess) {
+    e = nullptr;
+    return;
+  }
+  if (cudaEventRecord(e, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess && edge == 1)
+    g_trecorded[dev][which] = true;
+}
+void timing_begin(int which, void* stream) { timing_record(which, stream, 0); }
+void timing_end(int which, void* stream) { timing_record(which, stream, 1); }
+}  // namespace tree
+
+extern "C" int tree_kernel_timing(int enable) {
+  tree::g_timing.store(enable ? 1 : 0);
+  return TREE_OK;
+}
+
+extern "C" float tree_kernel_last_ms(int which) {
+  int dev = 0;
+  if (which < 0 || which >= tree::kTimedKernels || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128)
+    return -1.f;
+  cudaEvent_t b, e;
+  {
+    std::lock_guard<std::mutex> lock(tree::g_err_mu);
+    if (!tree::g_trecorded[dev][which]) return -1.f;
+    b = tree::g_tev[dev][which][0];
+    e = tree::g_tev[dev][which][1];
+  }
+  float ms = -1.f;
+  if (cudaEventSynchronize(e) != cudaSuccess || cudaEventElapsedTime(&ms, b, e) != cudaSuccess) return -1.f;
+  return ms;
+}
+
 extern "C" const char* tree_version(void) { return "tree_masked_attention_gb300 0.1 (sm_103a)"; }
