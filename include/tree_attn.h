@@ -295,6 +295,11 @@ uint64_t tree_launch_count(void);
 int tree_kernel_timing(int enable);
 float tree_kernel_last_ms(int which);
 
+/* Evaluates the FMA-pipe 2^x that the attention softmax uses for part of its
+ * exponentials on x [n] (device fp32) into y [n] (device fp32), for tests against
+ * the hardware exp2. Inputs below -125 give 2^-125. */
+int tree_selftest_exp2(const float* x, float* y, int64_t n, tree_stream_t stream);
+
 const char* tree_version(void);
 
 #ifdef __cplusplus

@@ -168,3 +168,25 @@ def test_kernel_timing_brackets():
     finally:
         m.tree_kernel_timing(False)
     m.tree_check_device_status()
+
+
+def test_fma_exp2_matches_hardware_exp2():
+    """The FMA-pipe 2^x used for part of the forward softmax's exponentials: relative error
+    within 1e-5 of CUDA's exp2 over the softmax's range, exact powers of two at integers,
+    and 2^-125 below -125 (where the SFU's ftz ex2 gives 0 or a denormal)."""
+    need_cuda()
+    m = tma()
+    rng = np.random.default_rng(3)
+    x = np.concatenate([rng.uniform(-125.0, 0.0, 200000), rng.uniform(-2.0, 2.0, 50000),
+                        np.arange(-125, 21, dtype=np.float64), np.arange(-125, 20) + 0.5,
+                        [-0.5, 0.5, -1e-7, 1e-7, 0.0]]).astype(np.float32)
+    tx = torch.from_numpy(x).cuda()
+    y = m.tree_selftest_exp2(tx)
+    ref = torch.exp2(tx.double())
+    rel = ((y.double() - ref).abs() / ref).cpu().numpy()
+    assert rel.max() <= 1e-5, float(rel.max())
+    ints = np.arange(-125, 21)
+    yi = m.tree_selftest_exp2(torch.from_numpy(ints.astype(np.float32)).cuda()).cpu().numpy()
+    assert np.allclose(yi, 2.0 ** ints, rtol=3e-6, atol=0)
+    low = m.tree_selftest_exp2(torch.tensor([-126.0, -200.0, -float("inf")], device="cuda")).cpu().numpy()
+    assert np.allclose(low, 2.0 ** -125, rtol=1e-5, atol=0)

@@ -218,6 +218,15 @@ def tree_kernel_timing(enable: bool) -> None:
     lib().tree_kernel_timing(int(bool(enable)))
 
 
+def tree_selftest_exp2(x):
+    """The library's FMA-pipe 2^x on a device fp32 tensor (for tests)."""
+    torch = _torch()
+    y = torch.empty_like(x)
+    check(lib().tree_selftest_exp2(_dev(x, "x", torch.float32), _dev(y, "y", torch.float32), x.numel(), _stream(x)),
+          "tree_selftest_exp2")
+    return y
+
+
 def tree_kernel_last_ms(which: int) -> float:
     """Duration of the latest bracketed main kernel (0: forward, 1: backward), or -1."""
     return float(lib().tree_kernel_last_ms(int(which)))

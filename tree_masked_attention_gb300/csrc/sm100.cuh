@@ -119,6 +119,15 @@ __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const 
       : "memory");
 }
 
+// 1-D bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16),
+// completing `bytes` of transaction count on `bar`.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read0() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
@@ -269,6 +278,31 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// 2^x for a pair of values on the FMA pipes, to take part of the softmax's exponentials off
+// the SFU (which issues one ex2 per lane every 8 clocks per sub-partition): x = j + f with
+// j = round(x), obtained by adding 1.5 * 2^23 (j lands in the low mantissa bits), f in
+// [-1/2, 1/2]; 2^f from a degree-4 polynomial fitted here to 2^f on that interval (least
+// squares on Chebyshev nodes, reweighted towards equal relative error: max relative error
+// 7.6e-6, below the bf16 rounding P gets); j is then added to the exponent field. x is
+// clamped at -125 so that the result stays a normal number (2^-125 where ex2 would give 0:
+// such p only ever multiply masked scores and vanish against the row sum).
+__device__ __forceinline__ float2 exp2_fma2(float2 x) {
+  constexpr float kMagic = 12582912.f;  // 1.5 * 2^23
+  constexpr float c0 = 0.9999978542327881f, c1 = 0.6931295394897461f, c2 = 0.2403089553117752f,
+                  c3 = 0.05586502328515053f, c4 = 0.009278289042413235f;
+  x = make_float2(fmaxf(x.x, -125.f), fmaxf(x.y, -125.f));
+  const float2 t = __fadd2_rn(x, make_float2(kMagic, kMagic));
+  const float2 j = __fadd2_rn(t, make_float2(-kMagic, -kMagic));
+  const float2 f = __ffma2_rn(j, make_float2(-1.f, -1.f), x);
+  float2 q = __ffma2_rn(make_float2(c4, c4), f, make_float2(c3, c3));
+  q = __ffma2_rn(q, f, make_float2(c2, c2));
+  q = __ffma2_rn(q, f, make_float2(c1, c1));
+  q = __ffma2_rn(q, f, make_float2(c0, c0));
+  // the low 9 bits of t's pattern are j (two's complement); shifted into the exponent field
+  return make_float2(__uint_as_float(__float_as_uint(q.x) + (__float_as_uint(t.x) << 23)),
+                     __uint_as_float(__float_as_uint(q.y) + (__float_as_uint(t.y) << 23)));
 }
 
 __device__ __forceinline__ bool elect_one() {

@@ -5,6 +5,7 @@
 #include <mutex>
 
 #include "common.h"
+#include "sm100.cuh"
 
 namespace tree {
 
@@ -108,6 +109,30 @@ extern "C" float tree_kernel_last_ms(int which) {
   float ms = -1.f;
   if (cudaEventSynchronize(e) != cudaSuccess || cudaEventElapsedTime(&ms, b, e) != cudaSuccess) return -1.f;
   return ms;
+}
+
+namespace tree {
+__global__ void selftest_exp2_kernel(const float* __restrict__ x, float* __restrict__ y, int64_t n) {
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (2 * t + 1 < n) {
+    const float2 r = sm100::exp2_fma2(make_float2(x[2 * t], x[2 * t + 1]));
+    y[2 * t] = r.x;
+    y[2 * t + 1] = r.y;
+  } else if (2 * t < n) {
+    y[2 * t] = sm100::exp2_fma2(make_float2(x[2 * t], 0.f)).x;
+  }
+}
+}  // namespace tree
+
+extern "C" int tree_selftest_exp2(const float* x, float* y, int64_t n, tree_stream_t stream) {
+  tree::clear_error();
+  if (n < 0 || (n > 0 && (!x || !y))) return tree::fail(TREE_ERR_INVALID_ARG, "tree_selftest_exp2: bad arguments");
+  if (n == 0) return TREE_OK;
+  const int64_t pairs = (n + 1) / 2;
+  tree::selftest_exp2_kernel<<<static_cast<unsigned>((pairs + 255) / 256), 256, 0,
+                               reinterpret_cast<cudaStream_t>(stream)>>>(x, y, n);
+  TREE_LAUNCH_CHECK("selftest_exp2_kernel");
+  return TREE_OK;
 }
 
 extern "C" const char* tree_version(void) { return "tree_masked_attention_gb300 0.1 (sm_103a)"; }
