@@ -67,7 +67,7 @@ struct Smem {
   float dq_stage[2][(BQ / 2) * D];
   float lse2[NST][BQ];
   float delta[NST][BQ];
-  uint64_t kv_full, qdo_full[NST], qdo_empty[NST], s_full[2], dp_full, ld_done, ds_ready[2], dk_done[2],
+  uint64_t stage_read, kv_full, qdo_full[NST], qdo_empty[NST], s_full[2], dp_full, ld_done, ds_ready[2], dk_done[2],
       dq_full[2], drain_done, mma_done, fin[4];
   uint32_t tmem_base;
 };
@@ -192,6 +192,7 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
     mbar_init(&S.ld_done, 8);
     mbar_init(&S.drain_done, 4);
     mbar_init(&S.mma_done, 2);  // dV (warp 10) and dK (warp 8) accumulation of a unit
+    mbar_init(&S.stage_read, 2);  // the dK / dV reduces of a unit have read their staging
     for (int w = 0; w < 4; ++w) mbar_init(&S.fin[w], 1);
     fence_mbarrier_init();
     s_abort = 0;
@@ -225,6 +226,12 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
       const int b = U.b, L = U.L;
       const int j = U.kt * BN + r;
       const int ej = p.endp[j];  // -1 past T
+      // the previous unit's dK / dV reduces must have read their staging (the Q / dO / dS
+      // buffers) before this unit's loads reuse them; the producer waits for this
+      if (uit > 0 && q4 == 0 && lane == 0) {
+        bulk_wait_read0();
+        mbar_arrive(&S.stage_read);
+      }
       bool ok = true;
       for (int l = 0; l < L; ++l) {
         const int g = g0 + l, st = g % NST, t = b + l;
@@ -319,8 +326,7 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         if (q4 == 0 && lane == 0) {
           for (int c = 0; c < 4; ++c)
             tma_reduce_add_3d(wg == 0 ? &tmDK : &tmDV, stage + c * (kEpiBytes / 4), c * 32, U.kvh, U.kt * BN);
-          bulk_commit();
-          bulk_wait_read0();  // the next unit loads into these buffers
+          bulk_commit();  // read completion is waited for at the next unit's start
         }
       } else {
         s_abort = 1;
@@ -331,6 +337,8 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
       __syncthreads();
       tc_fence_after();
     }
+    // the last unit's dK / dV reduces must have read their staging before the CTA exits
+    if (q4 == 0 && lane == 0) bulk_wait_read0();
   } else if (warp < kWarpDq) {
     // ---------------------------------------------------- producer and MMA issuers
     constexpr uint32_t id_s = idesc_bf16(BN, BQ, 0, 0);  // S^T, dP^T
@@ -391,6 +399,8 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
             g_loaded = g + 1;
             return true;
           };
+          // Q / dO go where the previous unit's dK / dV were staged
+          if (uit > 0) ok = mbar_wait(&S.stage_read, (uit - 1) & 1, p.err);
           for (int l = 0; ok && l < min(NST, L); ++l) ok = load_step(g0 + l);
           for (int l = 0; ok && l < L; ++l) {
             const int g = g0 + l, st = g % NST;
