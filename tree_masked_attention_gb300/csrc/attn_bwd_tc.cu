@@ -762,25 +762,40 @@ __global__ void attn_grads_rope_to_bf16_kernel(const float* __restrict__ aq, __n
     raise_error(err, TREE_ERR_DEVICE_CHECK);
     return;
   }
+  // all of the thread's loads first (8 in flight), then the rotation and the stores
+  float4 x1[kHeads], x2[kHeads];
+  int64_t off[kHeads];
+  bool isq[kHeads], valid[kHeads];
+#pragma unroll
+  for (int u = 0; u < kHeads; ++u) {
+    const int hh = chunk * kHeads + u;
+    valid[u] = hh < n_heads;
+    isq[u] = hh < Hq;
+    const int H = isq[u] ? Hq : Hkv, h = isq[u] ? hh : hh - Hq;
+    off[u] = (row * H + h) * 128 + g * 4;
+    if (valid[u]) {
+      const float* a = (isq[u] ? aq : ak) + off[u];
+      x1[u] = *reinterpret_cast<const float4*>(a);
+      x2[u] = *reinterpret_cast<const float4*>(a + 64);
+    }
+  }
   float c[4], s[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const float inv_freq = exp2f(static_cast<float>(g * 4 + i) * neg2_log2base_over_d);
     sincosf(static_cast<float>(p0) * inv_freq, &s[i], &c[i]);
   }
-  for (int hh = chunk * kHeads; hh < min(n_heads, (chunk + 1) * kHeads); ++hh) {
-    const bool is_q = hh < Hq;
-    const int H = is_q ? Hq : Hkv, h = is_q ? hh : hh - Hq;
-    const int64_t off = (row * H + h) * 128 + g * 4;
-    const float* a = (is_q ? aq : ak) + off;
-    __nv_bfloat16* o = (is_q ? oq : ok) + off;
-    const float4 x1 = *reinterpret_cast<const float4*>(a), x2 = *reinterpret_cast<const float4*>(a + 64);
+#pragma unroll
+  for (int u = 0; u < kHeads; ++u) {
+    if (!valid[u]) continue;
+    __nv_bfloat16* o = (isq[u] ? oq : ok) + off[u];
+    const float4 a1 = x1[u], a2 = x2[u];
     // inverse rotation: y1 = x1 c + x2 s, y2 = x2 c - x1 s
     uint2 u1, u2;
-    u1.x = sm100::pack_bf16(x1.x * c[0] + x2.x * s[0], x1.y * c[1] + x2.y * s[1]);
-    u1.y = sm100::pack_bf16(x1.z * c[2] + x2.z * s[2], x1.w * c[3] + x2.w * s[3]);
-    u2.x = sm100::pack_bf16(x2.x * c[0] - x1.x * s[0], x2.y * c[1] - x1.y * s[1]);
-    u2.y = sm100::pack_bf16(x2.z * c[2] - x1.z * s[2], x2.w * c[3] - x1.w * s[3]);
+    u1.x = sm100::pack_bf16(a1.x * c[0] + a2.x * s[0], a1.y * c[1] + a2.y * s[1]);
+    u1.y = sm100::pack_bf16(a1.z * c[2] + a2.z * s[2], a1.w * c[3] + a2.w * s[3]);
+    u2.x = sm100::pack_bf16(a2.x * c[0] - a1.x * s[0], a2.y * c[1] - a1.y * s[1]);
+    u2.y = sm100::pack_bf16(a2.z * c[2] - a1.z * s[2], a2.w * c[3] - a1.w * s[3]);
     *reinterpret_cast<uint2*>(o) = u1;
     *reinterpret_cast<uint2*>(o + 64) = u2;
   }
