@@ -27,6 +27,10 @@ The oracle follows the plain definitions on the pages:
                    gradient of the weighted loss scattered back to rows
                    (Trie packing "Share logits, preserve every prediction" and
                    "Same chain rule, shared computation graph", Step 1).
+* ``policy``    -- the per-occurrence clipped policy objective and its gradient
+                   with respect to each occurrence's log-probability (Trie
+                   packing, "The training-loop change is small"; Tree Training
+                   §3.1 eq. 1).
 * ``metrics``   -- potential overlap ratio (Tree Training §4.1 eq. 12).
 
 Pins (tests/test_oracle_*.py) tie every function to values printed on the
@@ -41,9 +45,11 @@ from .rope import rope_ref
 from .logprob import logprob_ref_fwd, logprob_ref_bwd, logprob_ref_gz
 from .metrics import por, token_ratio, allowed_pairs_from_paths
 
+from .policy import policy_loss_ref
+
 __all__ = [
     "pack_ref", "brute_force_prefixes", "attn_ref_fwd", "attn_ref_bwd", "attn_ref_rows",
     "attn_ref_dq_rows", "attn_ref_dkdv_rows", "dense_mask_from_chunks", "mask_from_paths",
     "leaf_paths_from_parents", "rope_ref", "logprob_ref_fwd", "logprob_ref_bwd",
-    "logprob_ref_gz", "por", "token_ratio", "allowed_pairs_from_paths",
+    "logprob_ref_gz", "por", "token_ratio", "allowed_pairs_from_paths", "policy_loss_ref",
 ]
