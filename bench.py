@@ -449,26 +449,35 @@ def run_lm_head(args, dev, peaks, peak_src):
     f_gemm = 2.0 * rows * K * V
     stream = torch.cuda.current_stream(dev)
 
+    # a policy-gradient step: per-occurrence advantages and old log-probs (the current
+    # ones perturbed), the clipped objective's gradient feeds the backward
+    tma.tree_logprob_fwd(h, w, rp, pm, tg, workspace=ws, lse=lse, logp=logp)
+    adv = torch.randn(n_occ, generator=g, device=dev, dtype=torch.float32)
+    old_lp = logp + 0.3 * torch.randn(n_occ, generator=g, device=dev, dtype=torch.float32)
+
     def step(ev=None):
         if ev: ev[0].record(stream)
         tma.tree_logprob_fwd(h, w, rp, pm, tg, workspace=ws, lse=lse, logp=logp)
         if ev: ev[1].record(stream)
-        tma.tree_logprob_bwd(h, w, lse, rp, pm, tg, gl, workspace=ws, grads=(dh, dw))
+        tma.tree_policy_loss(logp, old_lp, adv, eps_low=0.2, grad=gl)
         if ev: ev[2].record(stream)
+        tma.tree_logprob_bwd(h, w, lse, rp, pm, tg, gl, workspace=ws, grads=(dh, dw))
+        if ev: ev[3].record(stream)
 
     step()
     torch.cuda.synchronize()
     n = max(args.lm_steps, 1)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
     for s in range(n):
         step(evs[s])
     torch.cuda.synchronize()
     tma.tree_check_device_status()
-    ms = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2])] for e in evs]).mean(axis=0)
+    ms3 = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(3)] for e in evs]).mean(axis=0)
+    ms = np.array([ms3[0], ms3[2]])  # the two GEMM phases; the objective is reported apart
     peak = float(peaks["bf16_tflops"])
     fwd_t = f_gemm / (ms[0] / 1e3) / 1e12
     bwd_t = 3 * f_gemm / (ms[1] / 1e3) / 1e12
-    tot = 4 * f_gemm / ((ms[0] + ms[1]) / 1e3) / 1e12
+    tot = 4 * f_gemm / (float(ms3.sum()) / 1e3) / 1e12  # whole step, objective included
     dom = 1 if ms[1] >= ms[0] else 0
     ach = bwd_t if dom else fwd_t
     return {
@@ -476,6 +485,8 @@ def run_lm_head(args, dev, peaks, peak_src):
                     "(source rows from a Galton-Watson tree of 8192 tokens), targets U[0,V), weights U(0,1]",
         "value": round(tot, 3), "unit": "TFLOP/s", "steps": n,
         "ms_fwd": round(float(ms[0]), 3), "ms_bwd": round(float(ms[1]), 3),
+        "ms_policy_loss": round(float(ms3[1]), 4),
+        "step": "tree_logprob_fwd -> tree_policy_loss (clipped objective, eps 0.2) -> tree_logprob_bwd",
         "flops_per_step": 4 * f_gemm, "pct_bf16_peak": round(100 * tot / peak, 2),
         "roofline": {"bound": "tensor", "achieved": round(ach, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(ach / peak, 4), "of": peak_src,

@@ -268,6 +268,27 @@ int tree_logprob_bwd(const void* hidden, const void* w_lm, const float* lse,
 /* ------------------------------------------------------------------------ */
 /* Status                                                                    */
 /* ------------------------------------------------------------------------ */
+/* ------------------------------------------------------------------------ */
+/* Per-occurrence clipped policy objective                                   */
+/* ------------------------------------------------------------------------ */
+/*
+ * [TP] "The training-loop change is small": for PPO/GRPO every occurrence keeps its
+ * own advantage, old log-probability, clipping rule, mask and weight (advantages
+ * are not averaged before the clipped loss); [TT] §3.1 eq. 1 is the ratio-1 case
+ * -A log p. With r_o = exp(logp_o - old_logp_o):
+ *   loss[o]      = -w_o m_o min(r_o A_o, clip(r_o, 1 - eps_low, 1 + eps_high) A_o)
+ *   grad_logp[o] = dL/dlogp_o = -w_o m_o A_o r_o where the unclipped term is the
+ *                  minimum, 0 where the clipped one is (the input of tree_logprob_bwd)
+ *   *loss_sum    = sum_o loss[o], summed in a fixed order (deterministic).
+ * logp, old_logp, advantage: device fp32 [n_occ]; weight (fp32) and mask (uint8,
+ * 0 = dropped) may be NULL (all ones). loss may be NULL unless loss_sum is wanted;
+ * loss_sum: device fp32 scalar or NULL. 0 <= eps_low < 1, eps_high >= 0 finite.
+ */
+int tree_policy_loss(const float* logp, const float* old_logp, const float* advantage,
+                     const float* weight, const uint8_t* mask, int64_t n_occ, float eps_low,
+                     float eps_high, float* loss, float* grad_logp, float* loss_sum,
+                     tree_stream_t stream);
+
 /* Synchronises `stream`, reads and clears the device error word of the current
  * device: TREE_OK, TREE_ERR_DEVICE_CHECK or TREE_ERR_TIMEOUT (a bounded
  * pipeline wait gave up; the kernel then returned early and its outputs are

@@ -108,3 +108,11 @@ def test_kernel_timing_without_brackets(tma):
     tma.tree_kernel_timing(False)
     assert tma.tree_kernel_last_ms(5) == -1
     assert tma.tree_kernel_last_ms(-1) == -1
+
+
+def test_policy_loss_rejects_bad_clip_range(tma):
+    """Argument checks run before any device work."""
+    L = tma.lib()
+    assert L.tree_policy_loss(None, None, None, None, None, 4, 1.5, 0.2, None, None, None, None) != 0
+    assert L.tree_policy_loss(None, None, None, None, None, 4, 0.2, float("inf"), None, None, None, None) != 0
+    assert L.tree_policy_loss(None, None, None, None, None, -1, 0.2, 0.2, None, None, None, None) != 0

@@ -25,7 +25,7 @@ from ._lib import PackOut, PackSizes, TreeError, check, lib
 
 __all__ = [
     "tree_pack", "tree_validate_subtree_end", "tree_rope", "tree_attn_workspace_size",
-    "tree_attn_fwd", "tree_attn_bwd", "tree_attn_bwd_rope", "tree_kernel_timing", "tree_kernel_last_ms", "tree_logprob_workspace_size", "tree_logprob_fwd",
+    "tree_attn_fwd", "tree_attn_bwd", "tree_attn_bwd_rope", "tree_kernel_timing", "tree_kernel_last_ms", "tree_logprob_workspace_size", "tree_logprob_fwd", "tree_policy_loss",
     "tree_logprob_bwd", "tree_check_device_status", "tree_kernel_path", "tree_launch_count", "TreeError", "lib",
     "DTYPE_F32", "DTYPE_BF16",
 ]
@@ -230,6 +230,26 @@ def tree_selftest_exp2(x):
 def tree_kernel_last_ms(which: int) -> float:
     """Duration of the latest bracketed main kernel (0: forward, 1: backward), or -1."""
     return float(lib().tree_kernel_last_ms(int(which)))
+
+
+def tree_policy_loss(logp, old_logp, advantage, weight=None, mask=None, eps_low: float = 0.2,
+                     eps_high=None, grad=None):
+    """Per-occurrence clipped policy objective: returns (loss [n_occ], grad_logp [n_occ],
+    loss_sum [1]), all fp32 on the device; grad_logp feeds tree_logprob_bwd."""
+    torch = _torch()
+    n = logp.shape[0]
+    f32 = torch.float32
+    loss = torch.empty(n, dtype=f32, device=logp.device)
+    g = torch.empty(n, dtype=f32, device=logp.device) if grad is None else grad
+    total = torch.empty(1, dtype=f32, device=logp.device)
+    check(lib().tree_policy_loss(_dev(logp, "logp", f32), _dev(old_logp, "old_logp", f32),
+                                 _dev(advantage, "advantage", f32), _dev(weight, "weight", f32),
+                                 _dev(mask, "mask", torch.uint8), n, float(eps_low),
+                                 float(eps_low if eps_high is None else eps_high),
+                                 _dev(loss, "loss", f32), _dev(g, "grad_logp", f32),
+                                 _dev(total, "loss_sum", f32), _stream(logp)),
+          "tree_policy_loss")
+    return loss, g, total
 
 
 def tree_logprob_workspace_size(T, K_h, V, n_occ, dtype_code) -> int:

@@ -55,6 +55,7 @@ SIGNATURES = {
     "tree_attn_bwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _int, _int,
                              _int, _int, _f, _int, _vp, _sz, _vp]),
     "tree_kernel_timing": (_int, [_int]),
+    "tree_policy_loss": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _f, _f, _vp, _vp, _vp, _vp]),
     "tree_selftest_exp2": (_int, [_vp, _vp, _i64, _vp]),
     "tree_kernel_last_ms": (C.c_float, [_int]),
     "tree_attn_bwd_rope": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _int,
