@@ -48,10 +48,24 @@ struct Smem {
 };
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
 
+#ifndef LM_RASTER_GROUP_DEFAULT
+#define LM_RASTER_GROUP_DEFAULT (1 << 30)  // one slab: M fastest over the whole grid
+#endif
+#ifndef LM_RASTER_GROUP_DW
+#define LM_RASTER_GROUP_DW 16  // dW = H^T G_z: 16 M blocks (32 MB of H) stay in L2 per pass over G_z
+#endif
+#ifndef LM_RASTER_GROUP_DH
+#define LM_RASTER_GROUP_DH 8  // dH = G_z W^T
+#endif
+#ifndef LM_RASTER_GROUP_GZ
+#define LM_RASTER_GROUP_GZ 16  // z again for G_z
+#endif
+
 struct Params {
   int M, N, K;
   int a_mn, b_mn;        // operand majorness (1 = MN-major)
-  int raster_m_fast;     // tile t -> (t % n_mb, t / n_mb) when 1, else (t / n_nb, t % n_nb)
+  int raster_group;      // tiles walk slabs of this many M blocks, M fastest within a slab
+                         // (0: N fastest over the whole grid)
   int epi;
   // EPI_LSE / EPI_GZ
   const int32_t* row_ptr;
@@ -98,13 +112,16 @@ __device__ __forceinline__ void load_stage(const Params& p, const CUtensorMap* t
 }
 
 __device__ __forceinline__ void tile_coords(const Params& p, int t, int n_mb, int n_nb, int* mb, int* nb) {
-  if (p.raster_m_fast) {
-    *mb = t % n_mb;
-    *nb = t / n_mb;
-  } else {
+  const int g = min(p.raster_group, n_mb);
+  if (g <= 0) {
     *mb = t / n_nb;
     *nb = t % n_nb;
+    return;
   }
+  const int slab = t / (g * n_nb), local = t - slab * g * n_nb;
+  const int rows = min(g, n_mb - slab * g);  // the last slab may be shorter
+  *mb = slab * g + local % rows;
+  *nb = local / rows;
 }
 
 // Occurrence range of row m, or an empty range (and the error flag) when the CSR is bad.
@@ -482,7 +499,7 @@ int logprob_fwd_tc(const LogprobArgs& a, cudaStream_t st) {
   p.K = static_cast<int>(a.K);
   p.a_mn = 0;
   p.b_mn = 1;
-  p.raster_m_fast = 1;
+  p.raster_group = LM_RASTER_GROUP_DEFAULT;
   p.epi = EPI_LSE;
   p.row_ptr = a.row_ptr;
   p.perm = a.perm;
@@ -526,7 +543,7 @@ int logprob_bwd_tc(const LogprobArgs& a, cudaStream_t st) {
     p.K = static_cast<int>(a.K);
     p.a_mn = 0;
     p.b_mn = 1;
-    p.raster_m_fast = 1;
+    p.raster_group = LM_RASTER_GROUP_GZ;
     p.epi = EPI_GZ;
     p.row_ptr = a.row_ptr;
     p.perm = a.perm;
@@ -550,7 +567,7 @@ int logprob_bwd_tc(const LogprobArgs& a, cudaStream_t st) {
     p.K = static_cast<int>(a.V);
     p.a_mn = 0;
     p.b_mn = 0;
-    p.raster_m_fast = 1;
+    p.raster_group = LM_RASTER_GROUP_DH;
     p.epi = EPI_STORE;
     p.out = static_cast<__nv_bfloat16*>(a.dh);
     p.err = device_error_word();
@@ -566,7 +583,7 @@ int logprob_bwd_tc(const LogprobArgs& a, cudaStream_t st) {
     p.K = static_cast<int>(a.T);
     p.a_mn = 1;
     p.b_mn = 1;
-    p.raster_m_fast = 1;
+    p.raster_group = LM_RASTER_GROUP_DW;
     p.epi = EPI_DW;
     p.out = static_cast<__nv_bfloat16*>(a.dw);
     p.targets = a.targets;
