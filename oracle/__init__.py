@@ -31,6 +31,9 @@ The oracle follows the plain definitions on the pages:
                    with respect to each occurrence's log-probability (Trie
                    packing, "The training-loop change is small"; Tree Training
                    §3.1 eq. 1).
+* ``conv``      -- tree-correct causal depthwise conv1d: per-path convolution with
+                   the parent's tokens as left context (Tree Training §3.2
+                   "(ii) Causal convolution", eq. 11, Fig. 4).
 * ``metrics``   -- potential overlap ratio (Tree Training §4.1 eq. 12).
 
 Pins (tests/test_oracle_*.py) tie every function to values printed on the
@@ -46,10 +49,12 @@ from .logprob import logprob_ref_fwd, logprob_ref_bwd, logprob_ref_gz
 from .metrics import por, token_ratio, allowed_pairs_from_paths
 
 from .policy import policy_loss_ref
+from .conv import conv1d_ref_fwd, conv1d_ref_bwd, conv1d_ref_rows
 
 __all__ = [
     "pack_ref", "brute_force_prefixes", "attn_ref_fwd", "attn_ref_bwd", "attn_ref_rows",
     "attn_ref_dq_rows", "attn_ref_dkdv_rows", "dense_mask_from_chunks", "mask_from_paths",
     "leaf_paths_from_parents", "rope_ref", "logprob_ref_fwd", "logprob_ref_bwd",
     "logprob_ref_gz", "por", "token_ratio", "allowed_pairs_from_paths", "policy_loss_ref",
+    "conv1d_ref_fwd", "conv1d_ref_bwd", "conv1d_ref_rows",
 ]
