@@ -55,6 +55,8 @@ def parse_args(argv=None):
                     choices=["agentic_short", "agentic_long", "galton_watson", "tiny_fp32"])
     ap.add_argument("--lm-steps", type=int, default=3)
     ap.add_argument("--no-lm", action="store_true")
+    ap.add_argument("--conv-steps", type=int, default=10)
+    ap.add_argument("--no-conv", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of graph replays")
@@ -407,6 +409,8 @@ def run_ours(args):
 
     if not args.no_lm and rank == 0:
         out["lm_head"] = run_lm_head(args, dev, peaks, peak_src)
+    if not args.no_conv and rank == 0:
+        out["conv1d"] = run_conv1d(args, dev, peaks, peak_src, flush)
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(args.workload, tree, (qh, kh, vh, doh), P, budget_s=25.0)
@@ -492,6 +496,71 @@ def run_lm_head(args, dev, peaks, peak_src):
                      "frac": round(ach / peak, 4), "of": peak_src,
                      "kernel": "tree_logprob_bwd" if dom else "tree_logprob_fwd", "traffic": None},
         "kernel_family": {"fwd": tma.tree_kernel_path(2, 1, 128), "bwd": tma.tree_kernel_path(3, 1, 128)},
+        "data": "synthetic (seeded torch generator on device)",
+    }
+
+
+def run_conv1d(args, dev, peaks, peak_src, flush):
+    """Tree-correct causal depthwise conv1d (kernel size 4) forward and backward on the
+    16384-row Galton-Watson tree at 8192 channels (bf16): the short convolution of an
+    SSM layer. HBM-bound; L2 flushed before every call, CUDA events on the stream."""
+    import torch
+    import tree_masked_attention_gb300 as tma
+    tree = synth.galton_watson()
+    pk = tma.tree_pack(tree.seqs)
+    T, C, K = pk["T"], 8192, 4
+    g = torch.Generator(device=dev)
+    g.manual_seed(9)
+    x = torch.randn((T, C), generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    dy = torch.randn((T, C), generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    w = (0.5 * torch.randn((C, K), generator=g, device=dev, dtype=torch.float32)).to(torch.bfloat16)
+    b = (0.1 * torch.randn(C, generator=g, device=dev, dtype=torch.float32)).to(torch.bfloat16)
+    par = torch.from_numpy(pk["parent_row"]).to(dev)
+    end = torch.from_numpy(pk["subtree_end"]).to(dev)
+    pos = torch.from_numpy(pk["position_ids"]).to(dev)
+    y, dx = torch.empty_like(x), torch.empty_like(x)
+    dw = torch.empty((C, K), dtype=torch.float32, device=dev)
+    db = torch.empty(C, dtype=torch.float32, device=dev)
+    ws = torch.empty(tma.tree_conv1d_workspace_size(T, C, K), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    n = max(args.conv_steps, 1)
+    for _ in range(3):
+        tma.tree_conv1d_fwd(x, w, par, bias=b, out=y)
+        tma.tree_conv1d_bwd(x, w, dy, end, pos, workspace=ws, grads=(dx, dw, db))
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
+    for s in range(n):
+        flush.zero_()
+        evs[s][0].record(stream)
+        tma.tree_conv1d_fwd(x, w, par, bias=b, out=y)
+        evs[s][1].record(stream)
+        flush.zero_()
+        evs[s][2].record(stream)
+        tma.tree_conv1d_bwd(x, w, dy, end, pos, workspace=ws, grads=(dx, dw, db))
+        evs[s][3].record(stream)
+    torch.cuda.synchronize()
+    tma.tree_check_device_status()
+    f_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
+    b_ms = float(np.mean([e[2].elapsed_time(e[3]) for e in evs]))
+    el = 2
+    # algorithmic bytes: forward reads x and writes y once, reads parent_row and the taps;
+    # backward reads x and dy and writes dx once, reads subtree_end, positions and the
+    # taps, writes dw and dbias (the per-tile partial sums are not counted)
+    f_bytes = 2.0 * T * C * el + 4.0 * T + C * (K + 1) * el
+    b_bytes = 3.0 * T * C * el + 8.0 * T + C * K * el + 4.0 * C * (K + 1)
+    hbm = float(peaks["hbm_gbs"])
+    fg, bg = f_bytes / (f_ms / 1e3) / 1e9, b_bytes / (b_ms / 1e3) / 1e9
+    dom_b = b_ms >= f_ms
+    return {
+        "workload": f"conv1d: Galton-Watson tree of {T} rows, {C} channels, kernel size {K}, bf16, with bias",
+        "value": round((f_bytes + b_bytes) / ((f_ms + b_ms) / 1e3) / 1e9, 1), "unit": "GB/s",
+        "ms_fwd": round(f_ms, 4), "ms_bwd": round(b_ms, 4), "steps": n,
+        "gbs_fwd": round(fg, 1), "gbs_bwd": round(bg, 1),
+        "step": "tree_conv1d_fwd -> tree_conv1d_bwd (dx, dw, dbias), L2 flushed before each call",
+        "roofline": {"bound": "hbm", "achieved": round(bg if dom_b else fg, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round((bg if dom_b else fg) / hbm, 4), "of": peak_src,
+                     "kernel": "tree_conv1d_bwd" if dom_b else "tree_conv1d_fwd",
+                     "bytes_per_launch": b_bytes if dom_b else f_bytes, "traffic": None},
         "data": "synthetic (seeded torch generator on device)",
     }
 

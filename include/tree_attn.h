@@ -289,6 +289,52 @@ int tree_policy_loss(const float* logp, const float* old_logp, const float* adva
                      float eps_high, float* loss, float* grad_logp, float* loss_sum,
                      tree_stream_t stream);
 
+/* ------------------------------------------------------------------------ */
+/* Tree-correct causal depthwise conv1d (short convolution of SSM layers)    */
+/* ------------------------------------------------------------------------ */
+/*
+ * [TT] §3.2 "(ii) Causal convolution", eq. 11 and Fig. 4: a causal conv of kernel
+ * size K reads the K-1 tokens before each token; in the preorder serialisation
+ * those rows may belong to a sibling branch, so the left context of a row is its
+ * nearest ancestors (reaching past a short parent chunk into the grandparent),
+ * zero above the root -- exactly what the row sees in a per-branch pass with zero
+ * left padding. With a_0(i) = i and a_{m+1}(i) = parent_row[a_m(i)]:
+ *   y[i, c] = bias[c] + sum_{m=0}^{K-1} w[c, K-1-m] * x[a_m(i), c]
+ * (tap K-1 multiplies the row itself, tap 0 the farthest ancestor). No activation.
+ *
+ * x, y, dy, dx: device [T, C] in `dtype`, row-major, 16-byte aligned; w: device
+ * [C, K] in `dtype`; bias: device [C] in `dtype` or NULL (no bias); C a multiple
+ * of 8, 1 <= K <= 8. parent_row: device int32 [T] from tree_pack_emit (-1 for a
+ * root, otherwise an earlier row). Arithmetic in fp32; y, dx rounded once.
+ * A parent_row entry that is not an earlier row (or -1) sets the device error word
+ * (TREE_ERR_DEVICE_CHECK) and is read as -1.
+ */
+int tree_conv1d_fwd(const void* x, const void* w, const void* bias, void* y,
+                    const int32_t* parent_row, int64_t T, int C, int K, int dtype,
+                    tree_stream_t stream);
+
+/* Bytes of workspace tree_conv1d_bwd needs (per-tile partial sums of dw and
+ * dbias, fp32); 0 for invalid sizes. */
+size_t tree_conv1d_workspace_size(int64_t T, int C, int K);
+
+/*
+ * Gradients of L = sum(dy * y) for tree_conv1d_fwd: with D_m[j] the sum of dy over
+ * the rows whose m-th ancestor is j (the descendants of j at depth m below it),
+ *   dx[j, c]     = sum_m w[c, K-1-m] D_m[j, c]        (written in `dtype`)
+ *   dw[c, K-1-m] = sum_j x[j, c] D_m[j, c]            (device fp32 [C, K], written)
+ *   dbias[c]     = sum_i dy[i, c]                     (device fp32 [C], written)
+ * dw and dbias may be NULL (not computed). The descendants are found from the
+ * preorder intervals: subtree_end (device int32 [T]) and position_ids (device
+ * int32 [T], depth of each row), both from tree_pack_emit. dw and dbias are summed
+ * in a fixed order (deterministic). Entries inconsistent with a preorder forest
+ * set the device error word. workspace: device, >= tree_conv1d_workspace_size(T,
+ * C, K) bytes, 256-byte aligned. T = 0 writes zero dw and dbias.
+ */
+int tree_conv1d_bwd(const void* x, const void* w, const void* dy, void* dx, float* dw,
+                    float* dbias, const int32_t* subtree_end, const int32_t* position_ids,
+                    int64_t T, int C, int K, int dtype, void* workspace,
+                    size_t workspace_bytes, tree_stream_t stream);
+
 /* Synchronises `stream`, reads and clears the device error word of the current
  * device: TREE_OK, TREE_ERR_DEVICE_CHECK or TREE_ERR_TIMEOUT (a bounded
  * pipeline wait gave up; the kernel then returned early and its outputs are

@@ -21,7 +21,7 @@ import numpy as np
 __all__ = [
     "bf16_round", "normal", "SynthTree", "tiny_tree", "agentic_short", "agentic_long",
     "galton_watson", "lm_head_tree", "random_sequences", "attention_config",
-    "lm_head_config", "CONFIGS",
+    "lm_head_config", "conv1d_config", "CONFIGS",
 ]
 
 
@@ -257,3 +257,11 @@ def lm_head_config(T: int, K_h: int, V: int, n_occ: int, bf16: bool, seed: int =
     tg = rng.integers(0, V, size=n_occ).astype(np.int32) if random_targets else None
     wt = (1.0 - rng.random(n_occ)).astype(np.float32)     # (0, 1]
     return h, w, tg, wt
+
+
+def conv1d_config(T: int, C: int, K: int, bf16: bool, seed: int = 0):
+    """Inputs of the depthwise conv1d: x [T, C] ~ N(0,1), taps w [C, K] ~ N(0, 0.5^2),
+    bias [C] ~ N(0, 0.1^2), output gradient dy [T, C] ~ N(0,1) (float32, bf16-rounded
+    when ``bf16``)."""
+    return (normal(seed * 4 + 1, (T, C), bf16=bf16), normal(seed * 4 + 2, (C, K), 0.5, bf16=bf16),
+            normal(seed * 4 + 3, (C,), 0.1, bf16=bf16), normal(seed * 4 + 4, (T, C), bf16=bf16))

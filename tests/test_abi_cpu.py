@@ -116,3 +116,15 @@ def test_policy_loss_rejects_bad_clip_range(tma):
     assert L.tree_policy_loss(None, None, None, None, None, 4, 1.5, 0.2, None, None, None, None) != 0
     assert L.tree_policy_loss(None, None, None, None, None, 4, 0.2, float("inf"), None, None, None, None) != 0
     assert L.tree_policy_loss(None, None, None, None, None, -1, 0.2, 0.2, None, None, None, None) != 0
+
+
+def test_conv1d_rejects_bad_sizes(tma):
+    """Channel count, kernel size, dtype and workspace are checked before any device work."""
+    L = tma.lib()
+    assert L.tree_conv1d_fwd(None, None, None, None, None, 16, 12, 4, 1, None) == 2   # C not a multiple of 8
+    assert L.tree_conv1d_fwd(None, None, None, None, None, 16, 16, 9, 1, None) == 2   # K > 8
+    assert L.tree_conv1d_fwd(None, None, None, None, None, 16, 16, 4, 5, None) == 3   # dtype
+    assert L.tree_conv1d_fwd(None, None, None, None, None, 16, 16, 4, 1, None) == 1   # null pointers
+    assert L.tree_conv1d_bwd(None, None, None, None, None, None, None, None, 16, 16, 0, 1, None, 0, None) == 2
+    assert L.tree_conv1d_workspace_size(16384, 8192, 4) == 256 * 5 * 8192 * 4
+    assert L.tree_conv1d_workspace_size(16, 16, 9) == 0

@@ -14,6 +14,9 @@ Functions (same names as the C ABI):
   tree_logprob_fwd(hidden, w_lm, occ_row_ptr, occ_perm, occ_targets, ...) -> (lse, logp)
   tree_logprob_bwd(hidden, w_lm, lse, occ_row_ptr, occ_perm, occ_targets, grad_logp, ...)
                                                     -> (d_hidden, d_w)
+  tree_policy_loss(logp, old_logp, advantage, ...)  -> (loss, grad_logp, loss_sum)
+  tree_conv1d_fwd(x, w, parent_row, bias)           -> y
+  tree_conv1d_bwd(x, w, dy, subtree_end, position_ids) -> (dx, dw, dbias)
 """
 from __future__ import annotations
 
@@ -26,6 +29,7 @@ from ._lib import PackOut, PackSizes, TreeError, check, lib
 __all__ = [
     "tree_pack", "tree_validate_subtree_end", "tree_rope", "tree_attn_workspace_size",
     "tree_attn_fwd", "tree_attn_bwd", "tree_attn_bwd_rope", "tree_kernel_timing", "tree_kernel_last_ms", "tree_logprob_workspace_size", "tree_logprob_fwd", "tree_policy_loss",
+    "tree_conv1d_fwd", "tree_conv1d_bwd", "tree_conv1d_workspace_size",
     "tree_logprob_bwd", "tree_check_device_status", "tree_kernel_path", "tree_launch_count", "TreeError", "lib",
     "DTYPE_F32", "DTYPE_BF16",
 ]
@@ -250,6 +254,47 @@ def tree_policy_loss(logp, old_logp, advantage, weight=None, mask=None, eps_low:
                                  _dev(total, "loss_sum", f32), _stream(logp)),
           "tree_policy_loss")
     return loss, g, total
+
+
+def tree_conv1d_fwd(x, w, parent_row, bias=None, out=None):
+    """Tree-correct causal depthwise conv1d: x [T, C], w [C, K] (x's dtype), parent_row
+    int32 [T], bias [C] or None; returns y [T, C] in x's dtype."""
+    torch = _torch()
+    T, Cc = x.shape
+    K = w.shape[1]
+    y = torch.empty_like(x) if out is None else out
+    check(lib().tree_conv1d_fwd(_dev(x, "x"), _dev(w, "w", x.dtype), _dev(bias, "bias", x.dtype),
+                                _dev(y, "y", x.dtype), _dev(parent_row, "parent_row", torch.int32), T, Cc, K,
+                                _dtype_code(x), _stream(x)), "tree_conv1d_fwd")
+    return y
+
+
+def tree_conv1d_workspace_size(T, C_, K) -> int:
+    return int(lib().tree_conv1d_workspace_size(T, C_, K))
+
+
+def tree_conv1d_bwd(x, w, dy, subtree_end, position_ids, workspace=None, grads=None, want_dw: bool = True,
+                    want_dbias: bool = True):
+    """Gradients of tree_conv1d_fwd: returns (dx [T, C] in x's dtype, dw [C, K] fp32 or None,
+    dbias [C] fp32 or None)."""
+    torch = _torch()
+    T, Cc = x.shape
+    K = w.shape[1]
+    f32 = torch.float32
+    if grads is None:
+        dx = torch.empty_like(x)
+        dw = torch.empty((Cc, K), dtype=f32, device=x.device) if want_dw else None
+        db = torch.empty(Cc, dtype=f32, device=x.device) if want_dbias else None
+    else:
+        dx, dw, db = grads
+    ws = _workspace(tree_conv1d_workspace_size(T, Cc, K), x.device, workspace)
+    i32 = torch.int32
+    check(lib().tree_conv1d_bwd(_dev(x, "x"), _dev(w, "w", x.dtype), _dev(dy, "dy", x.dtype),
+                                _dev(dx, "dx", x.dtype), _dev(dw, "dw", f32), _dev(db, "dbias", f32),
+                                _dev(subtree_end, "subtree_end", i32), _dev(position_ids, "position_ids", i32),
+                                T, Cc, K, _dtype_code(x), C.c_void_p(ws.data_ptr()),
+                                ws.numel() * ws.element_size(), _stream(x)), "tree_conv1d_bwd")
+    return dx, dw, db
 
 
 def tree_logprob_workspace_size(T, K_h, V, n_occ, dtype_code) -> int:

@@ -1,0 +1,419 @@
+// tree_conv1d_fwd / tree_conv1d_bwd: tree-correct causal depthwise conv1d (the short
+// convolution of SSM / linear-attention layers) over a packed prefix tree.
+//
+// Tree Training (arXiv 2511.00413) §3.2 "(ii) Causal convolution", eq. 11 and Fig. 4: a
+// causal conv of kernel size K reads the K-1 tokens before a token; in the preorder
+// serialisation the rows just before a child chunk belong to a sibling, so the left
+// context of a row is taken from its ancestors instead, which reproduces what the row
+// sees in an independent per-branch pass. Row i's m-th ancestor a_m(i) (a_0 = i,
+// a_{m+1} = parent_row[a_m], none above a root) gets tap K-1-m:
+//   y[i, c] = bias[c] + sum_{m<K} w[c, K-1-m] x[a_m(i), c]          (zero past the root)
+// Backward, with D_m[j] = sum of dy[i] over the rows i whose m-th ancestor is j:
+//   dx[j, c] = sum_{m<K} w[c, K-1-m] D_m[j, c]
+//   dw[c, K-1-m] = sum_j x[j, c] D_m[j, c],     dbias[c] = sum_i dy[i, c].
+//
+// Both directions are HBM-bound (read x / write y; read x, dy / write dx) and use no
+// atomics. A CTA owns a tile of consecutive rows and 512 channels (4 per thread, so
+// one warp reads 256 contiguous bytes of a bf16 row); every thread of the CTA walks
+// the same rows, so the tree logic is uniform and only the channel data differ.
+//  - Forward, rows in increasing order: a register window holds x at the current
+//    row's K ancestors. When parent_row[i] == i-1 (inside a chunk, or the first
+//    child of a chunk's last row) the window shifts by one; at other rows (a later
+//    sibling, the tile's first row) it is refilled by walking parent links.
+//  - Backward, rows in decreasing order: a window holds D_0..D_{K-1} of the current
+//    row. When j's only child is j+1 (subtree_end[j+1] == subtree_end[j]) the window
+//    of j+1 shifts by one; a leaf has D_m = 0 for m > 0; otherwise (a fork, the
+//    tile's last row) the descendants within depth K-1 are enumerated in preorder
+//    from subtree_end and the depth positions. dw and dbias are summed per tile in
+//    fp32, then a second kernel adds the tiles in a fixed order in fp64.
+#include <algorithm>
+
+#include "common.h"
+#include "device_common.cuh"
+
+namespace tree {
+namespace {
+
+constexpr int kConvThreads = 128;
+constexpr int kConvVec = 4;                             // channels per thread
+constexpr int kConvChan = kConvThreads * kConvVec;      // channels per CTA
+constexpr int kFwdRows = 32;                            // rows per forward CTA
+constexpr int kBwdRows = 64;                            // rows per backward CTA
+constexpr int kPrefetch = 4;                            // rows loaded ahead
+constexpr int kConvMaxK = 8;                            // largest kernel size
+
+// 4 consecutive elements <-> 4 floats (8-byte access for bf16, 16-byte for fp32).
+__device__ __forceinline__ void ld4(const __nv_bfloat16* p, float* f) {
+  uint2 u = *reinterpret_cast<const uint2*>(p);
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+  float2 a = __bfloat1622float2(h[0]), b = __bfloat1622float2(h[1]);
+  f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+}
+__device__ __forceinline__ void ld4(const float* p, float* f) {
+  float4 a = *reinterpret_cast<const float4*>(p);
+  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+}
+__device__ __forceinline__ void st4(__nv_bfloat16* p, const float* f) {
+  uint2 u;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+  h[0] = __floats2bfloat162_rn(f[0], f[1]);
+  h[1] = __floats2bfloat162_rn(f[2], f[3]);
+  *reinterpret_cast<uint2*>(p) = u;
+}
+__device__ __forceinline__ void st4(float* p, const float* f) {
+  *reinterpret_cast<float4*>(p) = make_float4(f[0], f[1], f[2], f[3]);
+}
+
+// Taps of this thread's channels: wt[k][v] = w[c0 + v, k]; bias in b (0 if none).
+template <typename T, int K>
+__device__ __forceinline__ void load_taps(const T* __restrict__ w, const T* __restrict__ bias, int c0,
+                                          bool active, float (&wt)[K][kConvVec], float* b) {
+#pragma unroll
+  for (int v = 0; v < kConvVec; ++v) {
+    b[v] = (active && bias) ? to_f32(bias[c0 + v]) : 0.f;
+#pragma unroll
+    for (int k = 0; k < K; ++k) wt[k][v] = active ? to_f32(w[static_cast<int64_t>(c0 + v) * K + k]) : 0.f;
+  }
+}
+
+template <typename T, int K>
+__global__ void __launch_bounds__(kConvThreads) conv1d_fwd_kernel(
+    const T* __restrict__ x, const T* __restrict__ w, const T* __restrict__ bias, T* __restrict__ y,
+    const int32_t* __restrict__ parent, int64_t n_rows, int C, int* err) {
+  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kFwdRows;
+  const int64_t r1 = min(r0 + kFwdRows, n_rows);
+  const int c0 = blockIdx.y * kConvChan + threadIdx.x * kConvVec;
+  const bool active = c0 < C;
+  float wt[K][kConvVec], b[kConvVec];
+  load_taps<T, K>(w, bias, c0, active, wt, b);
+  float win[K][kConvVec];  // win[m] = x at the m-th ancestor of the current row
+#pragma unroll
+  for (int m = 0; m < K; ++m)
+#pragma unroll
+    for (int v = 0; v < kConvVec; ++v) win[m][v] = 0.f;
+
+  for (int64_t i0 = r0; i0 < r1; i0 += kPrefetch) {
+    float xb[kPrefetch][kConvVec];
+    int pb[kPrefetch];
+#pragma unroll
+    for (int u = 0; u < kPrefetch; ++u) {
+      const int64_t i = i0 + u;
+      pb[u] = i < r1 ? parent[i] : -1;
+      if (active && i < r1) {
+        ld4(x + i * C + c0, xb[u]);
+      } else {
+#pragma unroll
+        for (int v = 0; v < kConvVec; ++v) xb[u][v] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kPrefetch; ++u) {
+      const int64_t i = i0 + u;
+      if (i >= r1) break;
+      int p = pb[u];
+      if (p < -1 || p >= i) {  // a parent must be an earlier row (or -1 for a root)
+        raise_error(err, TREE_ERR_DEVICE_CHECK);
+        p = -1;
+      }
+      if (i > r0 && p == i - 1) {
+#pragma unroll
+        for (int m = K - 1; m > 0; --m)
+#pragma unroll
+          for (int v = 0; v < kConvVec; ++v) win[m][v] = win[m - 1][v];
+      } else {
+        int64_t a = p;
+#pragma unroll
+        for (int m = 1; m < K; ++m) {
+          if (a >= 0) {
+            if (active) ld4(x + a * C + c0, win[m]);
+            int64_t pa = parent[a];
+            if (pa < -1 || pa >= a) {
+              raise_error(err, TREE_ERR_DEVICE_CHECK);
+              pa = -1;
+            }
+            a = pa;
+          } else {
+#pragma unroll
+            for (int v = 0; v < kConvVec; ++v) win[m][v] = 0.f;
+          }
+        }
+      }
+#pragma unroll
+      for (int v = 0; v < kConvVec; ++v) win[0][v] = xb[u][v];
+      float out[kConvVec];
+#pragma unroll
+      for (int v = 0; v < kConvVec; ++v) {
+        float acc = b[v];
+#pragma unroll
+        for (int m = 0; m < K; ++m) acc = fmaf(wt[K - 1 - m][v], win[m][v], acc);
+        out[v] = acc;
+      }
+      if (active) st4(y + i * C + c0, out);
+    }
+  }
+}
+
+template <typename T, int K>
+__global__ void __launch_bounds__(kConvThreads) conv1d_bwd_kernel(
+    const T* __restrict__ x, const T* __restrict__ w, const T* __restrict__ dy, T* __restrict__ dx,
+    const int32_t* __restrict__ end, const int32_t* __restrict__ pos, int64_t n_rows, int C,
+    float* __restrict__ part, int* err) {
+  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kBwdRows;
+  const int64_t r1 = min(r0 + kBwdRows, n_rows);
+  const int c0 = blockIdx.y * kConvChan + threadIdx.x * kConvVec;
+  const bool active = c0 < C;
+  float wt[K][kConvVec], unused_b[kConvVec];
+  load_taps<T, K>(w, static_cast<const T*>(nullptr), c0, active, wt, unused_b);
+  float D[K][kConvVec];           // D[m] = sum of dy over the current row's depth-m descendants
+  float dwacc[K][kConvVec], dbacc[kConvVec];
+#pragma unroll
+  for (int v = 0; v < kConvVec; ++v) {
+    dbacc[v] = 0.f;
+#pragma unroll
+    for (int m = 0; m < K; ++m) D[m][v] = dwacc[m][v] = 0.f;
+  }
+  int64_t end_next = -1;  // subtree_end of the row processed just before (j + 1)
+
+  for (int64_t j0 = r1 - 1; j0 >= r0; j0 -= kPrefetch) {
+    float xb[kPrefetch][kConvVec], gb[kPrefetch][kConvVec];
+    int eb[kPrefetch];
+#pragma unroll
+    for (int u = 0; u < kPrefetch; ++u) {
+      const int64_t j = j0 - u;
+      eb[u] = j >= r0 ? end[j] : 0;
+      if (active && j >= r0) {
+        ld4(x + j * C + c0, xb[u]);
+        ld4(dy + j * C + c0, gb[u]);
+      } else {
+#pragma unroll
+        for (int v = 0; v < kConvVec; ++v) xb[u][v] = gb[u][v] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kPrefetch; ++u) {
+      const int64_t j = j0 - u;
+      if (j < r0) break;
+      int64_t e = eb[u];
+      if (e < j || e >= n_rows) {  // a subtree holds its root and ends inside the tree
+        raise_error(err, TREE_ERR_DEVICE_CHECK);
+        e = j;
+      }
+      if (j + 1 < r1 && j + 1 <= e && end_next == e) {
+        // j's only child is j + 1, processed just before: its window, one level down
+#pragma unroll
+        for (int m = K - 1; m > 0; --m)
+#pragma unroll
+          for (int v = 0; v < kConvVec; ++v) D[m][v] = D[m - 1][v];
+      } else {
+#pragma unroll
+        for (int m = 1; m < K; ++m)
+#pragma unroll
+          for (int v = 0; v < kConvVec; ++v) D[m][v] = 0.f;
+        if (K > 1 && e > j) {
+          // descendants of j within depth K-1, in preorder: a row at depth K-1 below j
+          // is added and its subtree skipped; a shallower row steps to the next row
+          const int pj = pos[j];
+          int64_t r = j + 1;
+          while (r <= e) {
+            const int dr = pos[r] - pj;
+            int64_t er = end[r];
+            if (er < r) {
+              raise_error(err, TREE_ERR_DEVICE_CHECK);
+              er = r;
+            }
+            if (dr < 1 || dr >= K) {  // depths inconsistent with the subtree intervals
+              raise_error(err, TREE_ERR_DEVICE_CHECK);
+              r = er + 1;
+              continue;
+            }
+            if (active) {
+              float g[kConvVec];
+              ld4(dy + r * C + c0, g);
+#pragma unroll
+              for (int m = 1; m < K; ++m)
+                if (dr == m) {
+#pragma unroll
+                  for (int v = 0; v < kConvVec; ++v) D[m][v] += g[v];
+                }
+            }
+            r = dr == K - 1 ? er + 1 : r + 1;
+          }
+        }
+      }
+#pragma unroll
+      for (int v = 0; v < kConvVec; ++v) D[0][v] = gb[u][v];
+      end_next = e;
+      float out[kConvVec];
+#pragma unroll
+      for (int v = 0; v < kConvVec; ++v) {
+        float acc = 0.f;
+#pragma unroll
+        for (int m = 0; m < K; ++m) {
+          acc = fmaf(wt[K - 1 - m][v], D[m][v], acc);
+          dwacc[K - 1 - m][v] = fmaf(xb[u][v], D[m][v], dwacc[K - 1 - m][v]);
+        }
+        out[v] = acc;
+        dbacc[v] += gb[u][v];
+      }
+      if (active) st4(dx + j * C + c0, out);
+    }
+  }
+  if (active) {
+    float* pt = part + static_cast<int64_t>(blockIdx.x) * (K + 1) * C + c0;
+#pragma unroll
+    for (int k = 0; k < K; ++k) st4(pt + static_cast<int64_t>(k) * C, dwacc[k]);
+    st4(pt + static_cast<int64_t>(K) * C, dbacc);
+  }
+}
+
+// dw[c, k] (k < K) and dbias[c] (k == K) from the per-tile partials part[tile][k][c]:
+// 32 channels x 8 tile strides per CTA, each thread sums its tiles in fp64, then the 8
+// sums are added in a fixed order (the result does not depend on scheduling).
+constexpr int kRedC = 32, kRedT = 8;
+__global__ void __launch_bounds__(kRedC * kRedT) conv1d_reduce_kernel(const float* __restrict__ part,
+                                                                    int64_t n_tiles, int C, int K,
+                                                                    float* __restrict__ dw,
+                                                                    float* __restrict__ dbias) {
+  __shared__ double acc[kRedT][kRedC];
+  const int c = blockIdx.x * kRedC + threadIdx.x;
+  const int k = blockIdx.y;
+  double s = 0.0;
+  if (c < C)
+    for (int64_t t = threadIdx.y; t < n_tiles; t += kRedT) s += part[(t * (K + 1) + k) * C + c];
+  acc[threadIdx.y][threadIdx.x] = s;
+  __syncthreads();
+  if (threadIdx.y == 0 && c < C) {
+    double tot = 0.0;
+#pragma unroll
+    for (int q = 0; q < kRedT; ++q) tot += acc[q][threadIdx.x];
+    if (k < K) {
+      if (dw) dw[static_cast<int64_t>(c) * K + k] = static_cast<float>(tot);
+    } else if (dbias) {
+      dbias[c] = static_cast<float>(tot);
+    }
+  }
+}
+
+template <typename T, int K>
+int launch_fwd(const void* x, const void* w, const void* bias, void* y, const int32_t* parent, int64_t T_,
+               int C, cudaStream_t st) {
+  dim3 grid(static_cast<unsigned>((T_ + kFwdRows - 1) / kFwdRows), static_cast<unsigned>((C + kConvChan - 1) / kConvChan));
+  conv1d_fwd_kernel<T, K><<<grid, kConvThreads, 0, st>>>(static_cast<const T*>(x), static_cast<const T*>(w),
+                                                         static_cast<const T*>(bias), static_cast<T*>(y), parent,
+                                                         T_, C, device_error_word());
+  TREE_LAUNCH_CHECK("conv1d_fwd_kernel");
+  return TREE_OK;
+}
+
+template <typename T, int K>
+int launch_bwd(const void* x, const void* w, const void* dy, void* dx, float* dw, float* dbias,
+               const int32_t* end, const int32_t* pos, int64_t T_, int C, float* part, cudaStream_t st) {
+  const int64_t n_tiles = (T_ + kBwdRows - 1) / kBwdRows;
+  dim3 grid(static_cast<unsigned>(n_tiles), static_cast<unsigned>((C + kConvChan - 1) / kConvChan));
+  int* err = device_error_word();
+  conv1d_bwd_kernel<T, K><<<grid, kConvThreads, 0, st>>>(static_cast<const T*>(x), static_cast<const T*>(w),
+                                                         static_cast<const T*>(dy), static_cast<T*>(dx), end, pos,
+                                                         T_, C, part, err);
+  TREE_LAUNCH_CHECK("conv1d_bwd_kernel");
+  if (dw || dbias) {
+    dim3 rgrid(static_cast<unsigned>((C + kRedC - 1) / kRedC), static_cast<unsigned>(K + 1));
+    conv1d_reduce_kernel<<<rgrid, dim3(kRedC, kRedT), 0, st>>>(part, n_tiles, C, K, dw, dbias);
+    TREE_LAUNCH_CHECK("conv1d_reduce_kernel");
+  }
+  return TREE_OK;
+}
+
+template <typename T>
+int dispatch_fwd(int K, const void* x, const void* w, const void* bias, void* y, const int32_t* parent,
+                 int64_t T_, int C, cudaStream_t st) {
+  switch (K) {
+    case 1: return launch_fwd<T, 1>(x, w, bias, y, parent, T_, C, st);
+    case 2: return launch_fwd<T, 2>(x, w, bias, y, parent, T_, C, st);
+    case 3: return launch_fwd<T, 3>(x, w, bias, y, parent, T_, C, st);
+    case 4: return launch_fwd<T, 4>(x, w, bias, y, parent, T_, C, st);
+    case 5: return launch_fwd<T, 5>(x, w, bias, y, parent, T_, C, st);
+    case 6: return launch_fwd<T, 6>(x, w, bias, y, parent, T_, C, st);
+    case 7: return launch_fwd<T, 7>(x, w, bias, y, parent, T_, C, st);
+    default: return launch_fwd<T, 8>(x, w, bias, y, parent, T_, C, st);
+  }
+}
+
+template <typename T>
+int dispatch_bwd(int K, const void* x, const void* w, const void* dy, void* dx, float* dw, float* dbias,
+                 const int32_t* end, const int32_t* pos, int64_t T_, int C, float* part, cudaStream_t st) {
+  switch (K) {
+    case 1: return launch_bwd<T, 1>(x, w, dy, dx, dw, dbias, end, pos, T_, C, part, st);
+    case 2: return launch_bwd<T, 2>(x, w, dy, dx, dw, dbias, end, pos, T_, C, part, st);
+    case 3: return launch_bwd<T, 3>(x, w, dy, dx, dw, dbias, end, pos, T_, C, part, st);
+    case 4: return launch_bwd<T, 4>(x, w, dy, dx, dw, dbias, end, pos, T_, C, part, st);
+    case 5: return launch_bwd<T, 5>(x, w, dy, dx, dw, dbias, end, pos, T_, C, part, st);
+    case 6: return launch_bwd<T, 6>(x, w, dy, dx, dw, dbias, end, pos, T_, C, part, st);
+    case 7: return launch_bwd<T, 7>(x, w, dy, dx, dw, dbias, end, pos, T_, C, part, st);
+    default: return launch_bwd<T, 8>(x, w, dy, dx, dw, dbias, end, pos, T_, C, part, st);
+  }
+}
+
+int check_conv_args(int64_t T_, int C, int K, int dtype, const char* who) {
+  if (dtype != TREE_DTYPE_F32 && dtype != TREE_DTYPE_BF16) return fail(TREE_ERR_DTYPE, "%s: bad dtype %d", who, dtype);
+  if (T_ < 0 || T_ > INT32_MAX) return fail(TREE_ERR_SHAPE, "%s: T = %lld outside [0, 2^31)", who, (long long)T_);
+  if (C < 8 || C % 8 != 0 || C > (1 << 24))
+    return fail(TREE_ERR_SHAPE, "%s: channels C = %d must be a positive multiple of 8 (<= 2^24)", who, C);
+  if (K < 1 || K > kConvMaxK) return fail(TREE_ERR_SHAPE, "%s: kernel size K = %d outside [1, %d]", who, K, kConvMaxK);
+  return TREE_OK;
+}
+
+}  // namespace
+
+size_t conv1d_ws_bytes(int64_t T_, int C, int K) {
+  const int64_t n_tiles = (T_ + kBwdRows - 1) / kBwdRows;
+  return round_up(static_cast<size_t>(std::max<int64_t>(n_tiles, 1)) * (K + 1) * C * sizeof(float), 256);
+}
+
+}  // namespace tree
+
+using namespace tree;
+
+extern "C" size_t tree_conv1d_workspace_size(int64_t T, int C, int K) {
+  if (T < 0 || C < 1 || K < 1 || K > kConvMaxK) return 0;
+  return conv1d_ws_bytes(T, C, K);
+}
+
+extern "C" int tree_conv1d_fwd(const void* x, const void* w, const void* bias, void* y, const int32_t* parent_row,
+                               int64_t T, int C, int K, int dtype, tree_stream_t stream) {
+  clear_error();
+  int rc = check_conv_args(T, C, K, dtype, "tree_conv1d_fwd");
+  if (rc) return rc;
+  if (T == 0) return TREE_OK;
+  if (!x || !w || !y || !parent_row) return fail(TREE_ERR_INVALID_ARG, "tree_conv1d_fwd: null pointer");
+  if (!aligned16(x) || !aligned16(y)) return fail(TREE_ERR_ALIGNMENT, "tree_conv1d_fwd: x / y not 16-byte aligned");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (dtype == TREE_DTYPE_BF16) return dispatch_fwd<__nv_bfloat16>(K, x, w, bias, y, parent_row, T, C, st);
+  return dispatch_fwd<float>(K, x, w, bias, y, parent_row, T, C, st);
+}
+
+extern "C" int tree_conv1d_bwd(const void* x, const void* w, const void* dy, void* dx, float* dw, float* dbias,
+                               const int32_t* subtree_end, const int32_t* position_ids, int64_t T, int C, int K,
+                               int dtype, void* workspace, size_t workspace_bytes, tree_stream_t stream) {
+  clear_error();
+  int rc = check_conv_args(T, C, K, dtype, "tree_conv1d_bwd");
+  if (rc) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (T == 0) {  // no rows: the weight and bias gradients are zero
+    if (dw) TREE_CUDA_TRY(cudaMemsetAsync(dw, 0, sizeof(float) * C * K, st));
+    if (dbias) TREE_CUDA_TRY(cudaMemsetAsync(dbias, 0, sizeof(float) * C, st));
+    return TREE_OK;
+  }
+  if (!x || !w || !dy || !dx || !subtree_end || !position_ids)
+    return fail(TREE_ERR_INVALID_ARG, "tree_conv1d_bwd: null pointer");
+  if (!aligned16(x) || !aligned16(dy) || !aligned16(dx))
+    return fail(TREE_ERR_ALIGNMENT, "tree_conv1d_bwd: x / dy / dx not 16-byte aligned");
+  const size_t need = conv1d_ws_bytes(T, C, K);
+  if (workspace_bytes < need)
+    return fail(TREE_ERR_WORKSPACE, "tree_conv1d_bwd: workspace of %zu bytes, %zu needed", workspace_bytes, need);
+  if (!workspace) return fail(TREE_ERR_INVALID_ARG, "tree_conv1d_bwd: workspace is null");
+  if (!aligned256(workspace)) return fail(TREE_ERR_ALIGNMENT, "tree_conv1d_bwd: workspace not 256-byte aligned");
+  float* part = static_cast<float*>(workspace);
+  if (dtype == TREE_DTYPE_BF16)
+    return dispatch_bwd<__nv_bfloat16>(K, x, w, dy, dx, dw, dbias, subtree_end, position_ids, T, C, part, st);
+  return dispatch_bwd<float>(K, x, w, dy, dx, dw, dbias, subtree_end, position_ids, T, C, part, st);
+}
