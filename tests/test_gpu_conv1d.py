@@ -35,7 +35,7 @@ def _run(m, seqs, C, K, bf16, seed, bias=True, channels=None):
     # dw and dbias are sums over all T rows: fp32 sums of 64 rows per tile, then fp64
     # over tiles, so their rounding is at most (64 + 2) * 2^-24 * (sum of |terms|); the
     # sum of |terms| is the same gradient taken on |x| and |dy|
-    adw, _, adb = oracle.conv1d_ref_bwd(np.abs(xs), ws_, np.abs(dys), ref["paths"])
+    _, adw, adb = oracle.conv1d_ref_bwd(np.abs(xs), ws_, np.abs(dys), ref["paths"])
     u = 66 * 2.0 ** -24
     gdw, gdb = host(dw[tcs]), host(db[tcs])
     assert np.all(np.abs(gdw - rdw) <= F32_TOL + u * adw), float(np.abs(gdw - rdw).max())
