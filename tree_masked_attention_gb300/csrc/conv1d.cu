@@ -30,17 +30,42 @@
 
 #include "common.h"
 #include "device_common.cuh"
+#include "sm100.cuh"
 
 namespace tree {
 namespace {
 
-constexpr int kConvThreads = 128;
+using namespace sm100;
+
+constexpr int kConvThreads = 256;
 constexpr int kConvVec = 4;                             // channels per thread
-constexpr int kConvChan = kConvThreads * kConvVec;      // channels per CTA
-constexpr int kFwdRows = 32;                            // rows per forward CTA
-constexpr int kBwdRows = 64;                            // rows per backward CTA
-constexpr int kPrefetch = 4;                            // rows loaded ahead
+constexpr int kConvChan = kConvThreads * kConvVec;      // channels per CTA (one row segment)
+constexpr int kStageRows = 8;                           // rows per pipeline stage
+constexpr int kFwdStages = 4;                           // x:      4 x 8 rows x 2 KB (bf16) = 64 KB
+constexpr int kBwdStages = 3;                           // x, dy:  3 x 8 rows x 4 KB (bf16) = 96 KB
+// One wave of CTAs on GB300's 152 SMs: 3 forward / 2 backward CTAs fit per SM by shared memory.
+constexpr int kFwdTargetCtas = 152 * 3;
+constexpr int kBwdTargetCtas = 152 * 2;
 constexpr int kConvMaxK = 8;                            // largest kernel size
+
+template <typename T> constexpr size_t fwd_smem() { return sizeof(T) * kFwdStages * kStageRows * kConvChan; }
+template <typename T> constexpr size_t bwd_smem() { return sizeof(T) * kBwdStages * 2 * kStageRows * kConvChan; }
+
+// Rows are split into groups of whole stages; grid = (groups, channel tiles).
+struct ConvGrid {
+  int64_t rows_per_group, groups;
+  int ctiles;
+};
+ConvGrid conv_grid(int64_t n_rows, int C, int target_ctas) {
+  ConvGrid g;
+  g.ctiles = (C + kConvChan - 1) / kConvChan;
+  const int64_t chunks = std::max<int64_t>((n_rows + kStageRows - 1) / kStageRows, 1);
+  int64_t groups = std::max<int64_t>(1, std::min<int64_t>(chunks, (target_ctas + g.ctiles - 1) / g.ctiles));
+  const int64_t per = (chunks + groups - 1) / groups;
+  g.rows_per_group = per * kStageRows;
+  g.groups = (chunks + per - 1) / per;
+  return g;
+}
 
 // 4 consecutive elements <-> 4 floats (8-byte access for bf16, 16-byte for fp32).
 __device__ __forceinline__ void ld4(const __nv_bfloat16* p, float* f) {
@@ -76,14 +101,53 @@ __device__ __forceinline__ void load_taps(const T* __restrict__ w, const T* __re
   }
 }
 
+// Thread 0: one bulk copy per row of `rows` rows starting at `r`, each `row_bytes` long
+// (the CTA's channel slice), into `dst` (rows kConvChan elements apart), completing on `bar`.
+template <typename T>
+__device__ __forceinline__ void stage_rows(T* dst, const T* src, int64_t r, int rows, int C, int ct0,
+                                           uint32_t row_bytes, uint64_t* bar) {
+  for (int q = 0; q < rows; ++q)
+    bulk_load(dst + q * kConvChan, src + (r + q) * C + ct0, row_bytes, bar);
+}
+
+// After a timed-out wait: thread 0 waits (bounded) for the stages still being filled, so
+// no copy lands in shared memory after the CTA has left.
+__device__ __forceinline__ void drain_stages(uint64_t* full, int n_stages, int first, int last_issued,
+                                             int* err) {
+  for (int c = first; c <= last_issued; ++c) mbar_wait(&full[c % n_stages], (c / n_stages) & 1, err);
+}
+
 template <typename T, int K>
 __global__ void __launch_bounds__(kConvThreads) conv1d_fwd_kernel(
     const T* __restrict__ x, const T* __restrict__ w, const T* __restrict__ bias, T* __restrict__ y,
-    const int32_t* __restrict__ parent, int64_t n_rows, int C, int* err) {
-  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kFwdRows;
-  const int64_t r1 = min(r0 + kFwdRows, n_rows);
-  const int c0 = blockIdx.y * kConvChan + threadIdx.x * kConvVec;
+    const int32_t* __restrict__ parent, int64_t n_rows, int C, int64_t rows_per_group, int* err) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  __shared__ uint64_t full[kFwdStages];
+  T* stage = reinterpret_cast<T*>(smem_raw);  // [kFwdStages][kStageRows][kConvChan]
+  const int64_t g0 = static_cast<int64_t>(blockIdx.x) * rows_per_group;
+  const int64_t g1 = min(g0 + rows_per_group, n_rows);
+  const int ct0 = blockIdx.y * kConvChan;
+  const uint32_t row_bytes = static_cast<uint32_t>(min(kConvChan, C - ct0) * sizeof(T));
+  const int c0 = ct0 + threadIdx.x * kConvVec;
   const bool active = c0 < C;
+  const int n_chunks = static_cast<int>((g1 - g0 + kStageRows - 1) / kStageRows);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kFwdStages; ++s) mbar_init(&full[s], 1);
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+  int issued = -1;  // last chunk whose copies thread 0 has issued
+  auto issue = [&](int c) {
+    const int s = c % kFwdStages;
+    const int64_t r = g0 + static_cast<int64_t>(c) * kStageRows;
+    const int rows = static_cast<int>(min(static_cast<int64_t>(kStageRows), g1 - r));
+    mbar_arrive_expect_tx(&full[s], rows * row_bytes);
+    stage_rows(stage + s * kStageRows * kConvChan, x, r, rows, C, ct0, row_bytes, &full[s]);
+    issued = c;
+  };
+  if (threadIdx.x == 0)
+    for (int c = 0; c < min(kFwdStages - 1, n_chunks); ++c) issue(c);
+
   float wt[K][kConvVec], b[kConvVec];
   load_taps<T, K>(w, bias, c0, active, wt, b);
   float win[K][kConvVec];  // win[m] = x at the m-th ancestor of the current row
@@ -92,63 +156,64 @@ __global__ void __launch_bounds__(kConvThreads) conv1d_fwd_kernel(
 #pragma unroll
     for (int v = 0; v < kConvVec; ++v) win[m][v] = 0.f;
 
-  for (int64_t i0 = r0; i0 < r1; i0 += kPrefetch) {
-    float xb[kPrefetch][kConvVec];
-    int pb[kPrefetch];
+  for (int c = 0; c < n_chunks; ++c) {
+    // the stage of chunk c + kFwdStages - 1 was read in iteration c - 1 (barrier below)
+    if (threadIdx.x == 0 && c + kFwdStages - 1 < n_chunks) issue(c + kFwdStages - 1);
+    const bool ok = mbar_wait(&full[c % kFwdStages], (c / kFwdStages) & 1, err);
+    if (ok) {
+      const T* sx = stage + (c % kFwdStages) * kStageRows * kConvChan + threadIdx.x * kConvVec;
+      const int64_t r = g0 + static_cast<int64_t>(c) * kStageRows;
+      const int rows = static_cast<int>(min(static_cast<int64_t>(kStageRows), g1 - r));
+      int pb[kStageRows];  // the chunk's parent links, loaded together
 #pragma unroll
-    for (int u = 0; u < kPrefetch; ++u) {
-      const int64_t i = i0 + u;
-      pb[u] = i < r1 ? parent[i] : -1;
-      if (active && i < r1) {
-        ld4(x + i * C + c0, xb[u]);
-      } else {
+      for (int q = 0; q < kStageRows; ++q) pb[q] = q < rows ? parent[r + q] : -1;
 #pragma unroll
-        for (int v = 0; v < kConvVec; ++v) xb[u][v] = 0.f;
-      }
-    }
+      for (int q = 0; q < kStageRows; ++q) {
+        const int64_t i = r + q;
+        if (q >= rows) break;
+        int p = pb[q];
+        if (p < -1 || p >= i) {  // a parent must be an earlier row (or -1 for a root)
+          raise_error(err, TREE_ERR_DEVICE_CHECK);
+          p = -1;
+        }
+        if (i > g0 && p == i - 1) {
 #pragma unroll
-    for (int u = 0; u < kPrefetch; ++u) {
-      const int64_t i = i0 + u;
-      if (i >= r1) break;
-      int p = pb[u];
-      if (p < -1 || p >= i) {  // a parent must be an earlier row (or -1 for a root)
-        raise_error(err, TREE_ERR_DEVICE_CHECK);
-        p = -1;
-      }
-      if (i > r0 && p == i - 1) {
+          for (int m = K - 1; m > 0; --m)
 #pragma unroll
-        for (int m = K - 1; m > 0; --m)
+            for (int v = 0; v < kConvVec; ++v) win[m][v] = win[m - 1][v];
+        } else {
+          int64_t a = p;
 #pragma unroll
-          for (int v = 0; v < kConvVec; ++v) win[m][v] = win[m - 1][v];
-      } else {
-        int64_t a = p;
+          for (int m = 1; m < K; ++m) {
+            if (a >= 0) {
+              if (active) ld4(x + a * C + c0, win[m]);
+              int64_t pa = parent[a];
+              if (pa < -1 || pa >= a) {
+                raise_error(err, TREE_ERR_DEVICE_CHECK);
+                pa = -1;
+              }
+              a = pa;
+            } else {
 #pragma unroll
-        for (int m = 1; m < K; ++m) {
-          if (a >= 0) {
-            if (active) ld4(x + a * C + c0, win[m]);
-            int64_t pa = parent[a];
-            if (pa < -1 || pa >= a) {
-              raise_error(err, TREE_ERR_DEVICE_CHECK);
-              pa = -1;
+              for (int v = 0; v < kConvVec; ++v) win[m][v] = 0.f;
             }
-            a = pa;
-          } else {
-#pragma unroll
-            for (int v = 0; v < kConvVec; ++v) win[m][v] = 0.f;
           }
         }
+        if (active) ld4(sx + q * kConvChan, win[0]);
+        float out[kConvVec];
+#pragma unroll
+        for (int v = 0; v < kConvVec; ++v) {
+          float acc = b[v];
+#pragma unroll
+          for (int m = 0; m < K; ++m) acc = fmaf(wt[K - 1 - m][v], win[m][v], acc);
+          out[v] = acc;
+        }
+        if (active) st4(y + i * C + c0, out);
       }
-#pragma unroll
-      for (int v = 0; v < kConvVec; ++v) win[0][v] = xb[u][v];
-      float out[kConvVec];
-#pragma unroll
-      for (int v = 0; v < kConvVec; ++v) {
-        float acc = b[v];
-#pragma unroll
-        for (int m = 0; m < K; ++m) acc = fmaf(wt[K - 1 - m][v], win[m][v], acc);
-        out[v] = acc;
-      }
-      if (active) st4(y + i * C + c0, out);
+    }
+    if (!__syncthreads_and(ok)) {
+      if (threadIdx.x == 0) drain_stages(full, kFwdStages, c + 1, issued, err);
+      return;
     }
   }
 }
@@ -157,14 +222,40 @@ template <typename T, int K>
 __global__ void __launch_bounds__(kConvThreads) conv1d_bwd_kernel(
     const T* __restrict__ x, const T* __restrict__ w, const T* __restrict__ dy, T* __restrict__ dx,
     const int32_t* __restrict__ end, const int32_t* __restrict__ pos, int64_t n_rows, int C,
-    float* __restrict__ part, int* err) {
-  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kBwdRows;
-  const int64_t r1 = min(r0 + kBwdRows, n_rows);
-  const int c0 = blockIdx.y * kConvChan + threadIdx.x * kConvVec;
+    int64_t rows_per_group, float* __restrict__ part, int* err) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  __shared__ uint64_t full[kBwdStages];
+  T* stage = reinterpret_cast<T*>(smem_raw);  // [kBwdStages][x, dy][kStageRows][kConvChan]
+  const int64_t g0 = static_cast<int64_t>(blockIdx.x) * rows_per_group;
+  const int64_t g1 = min(g0 + rows_per_group, n_rows);
+  const int ct0 = blockIdx.y * kConvChan;
+  const uint32_t row_bytes = static_cast<uint32_t>(min(kConvChan, C - ct0) * sizeof(T));
+  const int c0 = ct0 + threadIdx.x * kConvVec;
   const bool active = c0 < C;
+  const int n_chunks = static_cast<int>((g1 - g0 + kStageRows - 1) / kStageRows);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kBwdStages; ++s) mbar_init(&full[s], 1);
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+  // chunks are consumed last row first: consumption step c reads chunk n_chunks - 1 - c
+  int issued = -1;
+  auto issue = [&](int c) {
+    const int s = c % kBwdStages;
+    const int64_t r = g0 + static_cast<int64_t>(n_chunks - 1 - c) * kStageRows;
+    const int rows = static_cast<int>(min(static_cast<int64_t>(kStageRows), g1 - r));
+    T* dst = stage + s * 2 * kStageRows * kConvChan;
+    mbar_arrive_expect_tx(&full[s], 2 * rows * row_bytes);
+    stage_rows(dst, x, r, rows, C, ct0, row_bytes, &full[s]);
+    stage_rows(dst + kStageRows * kConvChan, dy, r, rows, C, ct0, row_bytes, &full[s]);
+    issued = c;
+  };
+  if (threadIdx.x == 0)
+    for (int c = 0; c < min(kBwdStages - 1, n_chunks); ++c) issue(c);
+
   float wt[K][kConvVec], unused_b[kConvVec];
   load_taps<T, K>(w, static_cast<const T*>(nullptr), c0, active, wt, unused_b);
-  float D[K][kConvVec];           // D[m] = sum of dy over the current row's depth-m descendants
+  float D[K][kConvVec];  // D[m] = sum of dy over the current row's depth-m descendants
   float dwacc[K][kConvVec], dbacc[kConvVec];
 #pragma unroll
   for (int v = 0; v < kConvVec; ++v) {
@@ -174,88 +265,95 @@ __global__ void __launch_bounds__(kConvThreads) conv1d_bwd_kernel(
   }
   int64_t end_next = -1;  // subtree_end of the row processed just before (j + 1)
 
-  for (int64_t j0 = r1 - 1; j0 >= r0; j0 -= kPrefetch) {
-    float xb[kPrefetch][kConvVec], gb[kPrefetch][kConvVec];
-    int eb[kPrefetch];
+  for (int c = 0; c < n_chunks; ++c) {
+    if (threadIdx.x == 0 && c + kBwdStages - 1 < n_chunks) issue(c + kBwdStages - 1);
+    const bool ok = mbar_wait(&full[c % kBwdStages], (c / kBwdStages) & 1, err);
+    if (ok) {
+      const T* sx = stage + (c % kBwdStages) * 2 * kStageRows * kConvChan + threadIdx.x * kConvVec;
+      const T* sg = sx + kStageRows * kConvChan;
+      const int64_t r = g0 + static_cast<int64_t>(n_chunks - 1 - c) * kStageRows;
+      const int rows = static_cast<int>(min(static_cast<int64_t>(kStageRows), g1 - r));
+      int eb[kStageRows];  // the chunk's subtree ends, loaded together
 #pragma unroll
-    for (int u = 0; u < kPrefetch; ++u) {
-      const int64_t j = j0 - u;
-      eb[u] = j >= r0 ? end[j] : 0;
-      if (active && j >= r0) {
-        ld4(x + j * C + c0, xb[u]);
-        ld4(dy + j * C + c0, gb[u]);
-      } else {
+      for (int q = 0; q < kStageRows; ++q) eb[q] = q < rows ? end[r + q] : 0;
 #pragma unroll
-        for (int v = 0; v < kConvVec; ++v) xb[u][v] = gb[u][v] = 0.f;
-      }
-    }
+      for (int q = kStageRows - 1; q >= 0; --q) {
+        const int64_t j = r + q;
+        if (q >= rows) continue;
+        int64_t e = eb[q];
+        if (e < j || e >= n_rows) {  // a subtree holds its root and ends inside the tree
+          raise_error(err, TREE_ERR_DEVICE_CHECK);
+          e = j;
+        }
+        if (j + 1 < g1 && j + 1 <= e && end_next == e) {
+          // j's only child is j + 1, processed just before: its window, one level down
 #pragma unroll
-    for (int u = 0; u < kPrefetch; ++u) {
-      const int64_t j = j0 - u;
-      if (j < r0) break;
-      int64_t e = eb[u];
-      if (e < j || e >= n_rows) {  // a subtree holds its root and ends inside the tree
-        raise_error(err, TREE_ERR_DEVICE_CHECK);
-        e = j;
-      }
-      if (j + 1 < r1 && j + 1 <= e && end_next == e) {
-        // j's only child is j + 1, processed just before: its window, one level down
+          for (int m = K - 1; m > 0; --m)
 #pragma unroll
-        for (int m = K - 1; m > 0; --m)
+            for (int v = 0; v < kConvVec; ++v) D[m][v] = D[m - 1][v];
+        } else {
 #pragma unroll
-          for (int v = 0; v < kConvVec; ++v) D[m][v] = D[m - 1][v];
-      } else {
+          for (int m = 1; m < K; ++m)
 #pragma unroll
-        for (int m = 1; m < K; ++m)
+            for (int v = 0; v < kConvVec; ++v) D[m][v] = 0.f;
+          if (K > 1 && e > j) {
+            // descendants of j within depth K-1, in preorder: a row at depth K-1 below j
+            // is added and its subtree skipped; a shallower row steps to the next row
+            const int pj = pos[j];
+            int64_t rr = j + 1;
+            while (rr <= e) {
+              const int dr = pos[rr] - pj;
+              int64_t er = end[rr];
+              if (er < rr) {
+                raise_error(err, TREE_ERR_DEVICE_CHECK);
+                er = rr;
+              }
+              if (dr < 1 || dr >= K) {  // depths inconsistent with the subtree intervals
+                raise_error(err, TREE_ERR_DEVICE_CHECK);
+                rr = er + 1;
+                continue;
+              }
+              if (active) {
+                float g[kConvVec];
+                ld4(dy + rr * C + c0, g);
 #pragma unroll
-          for (int v = 0; v < kConvVec; ++v) D[m][v] = 0.f;
-        if (K > 1 && e > j) {
-          // descendants of j within depth K-1, in preorder: a row at depth K-1 below j
-          // is added and its subtree skipped; a shallower row steps to the next row
-          const int pj = pos[j];
-          int64_t r = j + 1;
-          while (r <= e) {
-            const int dr = pos[r] - pj;
-            int64_t er = end[r];
-            if (er < r) {
-              raise_error(err, TREE_ERR_DEVICE_CHECK);
-              er = r;
+                for (int m = 1; m < K; ++m)
+                  if (dr == m) {
+#pragma unroll
+                    for (int v = 0; v < kConvVec; ++v) D[m][v] += g[v];
+                  }
+              }
+              rr = dr == K - 1 ? er + 1 : rr + 1;
             }
-            if (dr < 1 || dr >= K) {  // depths inconsistent with the subtree intervals
-              raise_error(err, TREE_ERR_DEVICE_CHECK);
-              r = er + 1;
-              continue;
-            }
-            if (active) {
-              float g[kConvVec];
-              ld4(dy + r * C + c0, g);
-#pragma unroll
-              for (int m = 1; m < K; ++m)
-                if (dr == m) {
-#pragma unroll
-                  for (int v = 0; v < kConvVec; ++v) D[m][v] += g[v];
-                }
-            }
-            r = dr == K - 1 ? er + 1 : r + 1;
           }
         }
-      }
+        end_next = e;
+        float xv[kConvVec];
+        if (active) {
+          ld4(sg + q * kConvChan, D[0]);
+          ld4(sx + q * kConvChan, xv);
+        } else {
 #pragma unroll
-      for (int v = 0; v < kConvVec; ++v) D[0][v] = gb[u][v];
-      end_next = e;
-      float out[kConvVec];
-#pragma unroll
-      for (int v = 0; v < kConvVec; ++v) {
-        float acc = 0.f;
-#pragma unroll
-        for (int m = 0; m < K; ++m) {
-          acc = fmaf(wt[K - 1 - m][v], D[m][v], acc);
-          dwacc[K - 1 - m][v] = fmaf(xb[u][v], D[m][v], dwacc[K - 1 - m][v]);
+          for (int v = 0; v < kConvVec; ++v) D[0][v] = xv[v] = 0.f;
         }
-        out[v] = acc;
-        dbacc[v] += gb[u][v];
+        float out[kConvVec];
+#pragma unroll
+        for (int v = 0; v < kConvVec; ++v) {
+          float acc = 0.f;
+#pragma unroll
+          for (int m = 0; m < K; ++m) {
+            acc = fmaf(wt[K - 1 - m][v], D[m][v], acc);
+            dwacc[K - 1 - m][v] = fmaf(xv[v], D[m][v], dwacc[K - 1 - m][v]);
+          }
+          out[v] = acc;
+          dbacc[v] += D[0][v];
+        }
+        if (active) st4(dx + j * C + c0, out);
       }
-      if (active) st4(dx + j * C + c0, out);
+    }
+    if (!__syncthreads_and(ok)) {
+      if (threadIdx.x == 0) drain_stages(full, kBwdStages, c + 1, issued, err);
+      return;
     }
   }
   if (active) {
@@ -266,41 +364,37 @@ __global__ void __launch_bounds__(kConvThreads) conv1d_bwd_kernel(
   }
 }
 
-// dw[c, k] (k < K) and dbias[c] (k == K) from the per-tile partials part[tile][k][c]:
-// 32 channels x 8 tile strides per CTA, each thread sums its tiles in fp64, then the 8
-// sums are added in a fixed order (the result does not depend on scheduling).
-constexpr int kRedC = 32, kRedT = 8;
-__global__ void __launch_bounds__(kRedC * kRedT) conv1d_reduce_kernel(const float* __restrict__ part,
-                                                                    int64_t n_tiles, int C, int K,
-                                                                    float* __restrict__ dw,
-                                                                    float* __restrict__ dbias) {
-  __shared__ double acc[kRedT][kRedC];
-  const int c = blockIdx.x * kRedC + threadIdx.x;
+// dw[c, k] (k < K) and dbias[c] (k == K) from the per-group partials part[group][k][c]:
+// one thread per (channel, k) adds the groups in order in fp64 (deterministic).
+__global__ void __launch_bounds__(256) conv1d_reduce_kernel(const float* __restrict__ part, int64_t n_groups,
+                                                            int C, int K, float* __restrict__ dw,
+                                                            float* __restrict__ dbias) {
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
   const int k = blockIdx.y;
+  if (c >= C) return;
   double s = 0.0;
-  if (c < C)
-    for (int64_t t = threadIdx.y; t < n_tiles; t += kRedT) s += part[(t * (K + 1) + k) * C + c];
-  acc[threadIdx.y][threadIdx.x] = s;
-  __syncthreads();
-  if (threadIdx.y == 0 && c < C) {
-    double tot = 0.0;
-#pragma unroll
-    for (int q = 0; q < kRedT; ++q) tot += acc[q][threadIdx.x];
-    if (k < K) {
-      if (dw) dw[static_cast<int64_t>(c) * K + k] = static_cast<float>(tot);
-    } else if (dbias) {
-      dbias[c] = static_cast<float>(tot);
-    }
+  for (int64_t g = 0; g < n_groups; ++g) s += part[(g * (K + 1) + k) * C + c];
+  if (k < K) {
+    if (dw) dw[static_cast<int64_t>(c) * K + k] = static_cast<float>(s);
+  } else if (dbias) {
+    dbias[c] = static_cast<float>(s);
   }
 }
 
 template <typename T, int K>
 int launch_fwd(const void* x, const void* w, const void* bias, void* y, const int32_t* parent, int64_t T_,
                int C, cudaStream_t st) {
-  dim3 grid(static_cast<unsigned>((T_ + kFwdRows - 1) / kFwdRows), static_cast<unsigned>((C + kConvChan - 1) / kConvChan));
-  conv1d_fwd_kernel<T, K><<<grid, kConvThreads, 0, st>>>(static_cast<const T*>(x), static_cast<const T*>(w),
-                                                         static_cast<const T*>(bias), static_cast<T*>(y), parent,
-                                                         T_, C, device_error_word());
+  static bool attr_set = false;
+  if (!attr_set) {
+    TREE_CUDA_TRY(cudaFuncSetAttribute(conv1d_fwd_kernel<T, K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(fwd_smem<T>())));
+    attr_set = true;
+  }
+  const ConvGrid g = conv_grid(T_, C, kFwdTargetCtas);
+  dim3 grid(static_cast<unsigned>(g.groups), static_cast<unsigned>(g.ctiles));
+  conv1d_fwd_kernel<T, K><<<grid, kConvThreads, fwd_smem<T>(), st>>>(
+      static_cast<const T*>(x), static_cast<const T*>(w), static_cast<const T*>(bias), static_cast<T*>(y), parent,
+      T_, C, g.rows_per_group, device_error_word());
   TREE_LAUNCH_CHECK("conv1d_fwd_kernel");
   return TREE_OK;
 }
@@ -308,16 +402,22 @@ int launch_fwd(const void* x, const void* w, const void* bias, void* y, const in
 template <typename T, int K>
 int launch_bwd(const void* x, const void* w, const void* dy, void* dx, float* dw, float* dbias,
                const int32_t* end, const int32_t* pos, int64_t T_, int C, float* part, cudaStream_t st) {
-  const int64_t n_tiles = (T_ + kBwdRows - 1) / kBwdRows;
-  dim3 grid(static_cast<unsigned>(n_tiles), static_cast<unsigned>((C + kConvChan - 1) / kConvChan));
+  static bool attr_set = false;
+  if (!attr_set) {
+    TREE_CUDA_TRY(cudaFuncSetAttribute(conv1d_bwd_kernel<T, K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(bwd_smem<T>())));
+    attr_set = true;
+  }
+  const ConvGrid g = conv_grid(T_, C, kBwdTargetCtas);
+  dim3 grid(static_cast<unsigned>(g.groups), static_cast<unsigned>(g.ctiles));
   int* err = device_error_word();
-  conv1d_bwd_kernel<T, K><<<grid, kConvThreads, 0, st>>>(static_cast<const T*>(x), static_cast<const T*>(w),
-                                                         static_cast<const T*>(dy), static_cast<T*>(dx), end, pos,
-                                                         T_, C, part, err);
+  conv1d_bwd_kernel<T, K><<<grid, kConvThreads, bwd_smem<T>(), st>>>(
+      static_cast<const T*>(x), static_cast<const T*>(w), static_cast<const T*>(dy), static_cast<T*>(dx), end, pos,
+      T_, C, g.rows_per_group, part, err);
   TREE_LAUNCH_CHECK("conv1d_bwd_kernel");
   if (dw || dbias) {
-    dim3 rgrid(static_cast<unsigned>((C + kRedC - 1) / kRedC), static_cast<unsigned>(K + 1));
-    conv1d_reduce_kernel<<<rgrid, dim3(kRedC, kRedT), 0, st>>>(part, n_tiles, C, K, dw, dbias);
+    dim3 rgrid(static_cast<unsigned>((C + 255) / 256), static_cast<unsigned>(K + 1));
+    conv1d_reduce_kernel<<<rgrid, 256, 0, st>>>(part, g.groups, C, K, dw, dbias);
     TREE_LAUNCH_CHECK("conv1d_reduce_kernel");
   }
   return TREE_OK;
@@ -365,8 +465,8 @@ int check_conv_args(int64_t T_, int C, int K, int dtype, const char* who) {
 }  // namespace
 
 size_t conv1d_ws_bytes(int64_t T_, int C, int K) {
-  const int64_t n_tiles = (T_ + kBwdRows - 1) / kBwdRows;
-  return round_up(static_cast<size_t>(std::max<int64_t>(n_tiles, 1)) * (K + 1) * C * sizeof(float), 256);
+  const ConvGrid g = conv_grid(T_, C, kBwdTargetCtas);
+  return round_up(static_cast<size_t>(g.groups) * (K + 1) * C * sizeof(float), 256);
 }
 
 }  // namespace tree
