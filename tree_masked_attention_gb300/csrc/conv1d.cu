@@ -13,19 +13,27 @@
 //   dw[c, K-1-m] = sum_j x[j, c] D_m[j, c],     dbias[c] = sum_i dy[i, c].
 //
 // Both directions are HBM-bound (read x / write y; read x, dy / write dx) and use no
-// atomics. A CTA owns a tile of consecutive rows and 512 channels (4 per thread, so
-// one warp reads 256 contiguous bytes of a bf16 row); every thread of the CTA walks
-// the same rows, so the tree logic is uniform and only the channel data differ.
-//  - Forward, rows in increasing order: a register window holds x at the current
-//    row's K ancestors. When parent_row[i] == i-1 (inside a chunk, or the first
-//    child of a chunk's last row) the window shifts by one; at other rows (a later
-//    sibling, the tile's first row) it is refilled by walking parent links.
+// atomics. A CTA of 256 threads owns 1024 channels (4 per thread, so a warp touches 256
+// contiguous bytes of a bf16 row) and a group of consecutive rows; the grid is one wave
+// on GB300 (3 forward / 2 backward CTAs per SM). Thread 0 stages the group's rows in
+// chunks of 8 through a ring of shared-memory buffers filled by bulk asynchronous copies
+// (one cp.async.bulk per row segment, completion on an mbarrier), so each SM keeps
+// >100 KB of loads in flight without spending registers on them. Every thread of a CTA
+// walks the same rows: the tree logic is uniform, only the channel data differ.
+//  - Forward, rows in increasing order: a register window holds x at the current row's
+//    K ancestors. A chunk whose rows all continue the previous row (parent_row[i] ==
+//    i-1, the common case inside a chunk of the tree) takes a fast path whose window
+//    indices are compile-time constants (the chunk's own rows plus the window carried
+//    from the row before it). Otherwise each row either shifts the window by one or, at
+//    a later sibling or the group's first row, refills it by walking parent links.
 //  - Backward, rows in decreasing order: a window holds D_0..D_{K-1} of the current
-//    row. When j's only child is j+1 (subtree_end[j+1] == subtree_end[j]) the window
-//    of j+1 shifts by one; a leaf has D_m = 0 for m > 0; otherwise (a fork, the
-//    tile's last row) the descendants within depth K-1 are enumerated in preorder
-//    from subtree_end and the depth positions. dw and dbias are summed per tile in
-//    fp32, then a second kernel adds the tiles in a fixed order in fp64.
+//    row. A chunk in which every row's only child is the next row takes the fast path
+//    (D_m of row q is dy of row q+m, or the carried window of the row after the chunk).
+//    Otherwise a row whose only child is j+1 (subtree_end[j+1] == subtree_end[j])
+//    shifts the window, a leaf has D_m = 0 for m > 0, and a fork (or the group's last
+//    row) enumerates its descendants within depth K-1 in preorder from subtree_end and
+//    the depth positions. dw and dbias are summed per group in fp32, then a second
+//    kernel adds the groups in a fixed order in fp64.
 #include <algorithm>
 
 #include "common.h"
@@ -47,6 +55,7 @@ constexpr int kBwdStages = 3;                           // x, dy:  3 x 8 rows x 
 constexpr int kFwdTargetCtas = 152 * 3;
 constexpr int kBwdTargetCtas = 152 * 2;
 constexpr int kConvMaxK = 8;                            // largest kernel size
+static_assert(kStageRows >= kConvMaxK, "the chain fast paths take a window of K rows from one stage");
 
 template <typename T> constexpr size_t fwd_smem() { return sizeof(T) * kFwdStages * kStageRows * kConvChan; }
 template <typename T> constexpr size_t bwd_smem() { return sizeof(T) * kBwdStages * 2 * kStageRows * kConvChan; }
@@ -118,7 +127,7 @@ __device__ __forceinline__ void drain_stages(uint64_t* full, int n_stages, int f
 }
 
 template <typename T, int K>
-__global__ void __launch_bounds__(kConvThreads) conv1d_fwd_kernel(
+__global__ void __launch_bounds__(kConvThreads, K <= 4 ? 3 : 2) conv1d_fwd_kernel(
     const T* __restrict__ x, const T* __restrict__ w, const T* __restrict__ bias, T* __restrict__ y,
     const int32_t* __restrict__ parent, int64_t n_rows, int C, int64_t rows_per_group, int* err) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -167,6 +176,40 @@ __global__ void __launch_bounds__(kConvThreads) conv1d_fwd_kernel(
       int pb[kStageRows];  // the chunk's parent links, loaded together
 #pragma unroll
       for (int q = 0; q < kStageRows; ++q) pb[q] = q < rows ? parent[r + q] : -1;
+      bool chain = rows == kStageRows && r > g0;
+#pragma unroll
+      for (int q = 0; q < kStageRows; ++q) chain = chain && pb[q] == r + q - 1;
+      if (chain) {
+        // Every row of the chunk continues the previous one: row q's m-th ancestor is
+        // row q - m of the chunk, or (q < m) the (m - q - 1)-th ancestor of the row
+        // before the chunk, which win holds. All indices are fixed at compile time.
+        float xr[kStageRows][kConvVec];
+#pragma unroll
+        for (int q = 0; q < kStageRows; ++q) {
+          if (active) {
+            ld4(sx + q * kConvChan, xr[q]);
+          } else {
+#pragma unroll
+            for (int v = 0; v < kConvVec; ++v) xr[q][v] = 0.f;
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < kStageRows; ++q) {
+          float out[kConvVec];
+#pragma unroll
+          for (int v = 0; v < kConvVec; ++v) {
+            float acc = b[v];
+#pragma unroll
+            for (int m = 0; m < K; ++m) acc = fmaf(wt[K - 1 - m][v], q >= m ? xr[q - m][v] : win[m - q - 1][v], acc);
+            out[v] = acc;
+          }
+          if (active) st4(y + (r + q) * C + c0, out);
+        }
+#pragma unroll
+        for (int m = 0; m < K; ++m)
+#pragma unroll
+          for (int v = 0; v < kConvVec; ++v) win[m][v] = xr[kStageRows - 1 - m][v];
+      } else {
 #pragma unroll
       for (int q = 0; q < kStageRows; ++q) {
         const int64_t i = r + q;
@@ -210,6 +253,7 @@ __global__ void __launch_bounds__(kConvThreads) conv1d_fwd_kernel(
         }
         if (active) st4(y + i * C + c0, out);
       }
+      }
     }
     if (!__syncthreads_and(ok)) {
       if (threadIdx.x == 0) drain_stages(full, kFwdStages, c + 1, issued, err);
@@ -219,7 +263,7 @@ __global__ void __launch_bounds__(kConvThreads) conv1d_fwd_kernel(
 }
 
 template <typename T, int K>
-__global__ void __launch_bounds__(kConvThreads) conv1d_bwd_kernel(
+__global__ void __launch_bounds__(kConvThreads, K <= 4 ? 2 : 1) conv1d_bwd_kernel(
     const T* __restrict__ x, const T* __restrict__ w, const T* __restrict__ dy, T* __restrict__ dx,
     const int32_t* __restrict__ end, const int32_t* __restrict__ pos, int64_t n_rows, int C,
     int64_t rows_per_group, float* __restrict__ part, int* err) {
@@ -276,6 +320,53 @@ __global__ void __launch_bounds__(kConvThreads) conv1d_bwd_kernel(
       int eb[kStageRows];  // the chunk's subtree ends, loaded together
 #pragma unroll
       for (int q = 0; q < kStageRows; ++q) eb[q] = q < rows ? end[r + q] : 0;
+      bool chain = rows == kStageRows && r + kStageRows < g1;
+#pragma unroll
+      for (int q = 0; q < kStageRows; ++q)
+        chain = chain && eb[q] > r + q && eb[q] == (q + 1 < kStageRows ? static_cast<int64_t>(eb[q + 1]) : end_next);
+      if (chain) {
+        // Every row's only child is the next row: row q's depth-m descendant is row q + m
+        // of the chunk, or (q + m >= kStageRows) D[q + m - kStageRows] of the row after the
+        // chunk, which D holds. All indices are fixed at compile time.
+        float gr[kStageRows][kConvVec];
+#pragma unroll
+        for (int q = 0; q < kStageRows; ++q) {
+          if (active) {
+            ld4(sg + q * kConvChan, gr[q]);
+          } else {
+#pragma unroll
+            for (int v = 0; v < kConvVec; ++v) gr[q][v] = 0.f;
+          }
+        }
+#pragma unroll
+        for (int q = kStageRows - 1; q >= 0; --q) {
+          float xv[kConvVec], out[kConvVec];
+          if (active) {
+            ld4(sx + q * kConvChan, xv);
+          } else {
+#pragma unroll
+            for (int v = 0; v < kConvVec; ++v) xv[v] = 0.f;
+          }
+#pragma unroll
+          for (int v = 0; v < kConvVec; ++v) {
+            float acc = 0.f;
+#pragma unroll
+            for (int m = 0; m < K; ++m) {
+              const float d = q + m < kStageRows ? gr[q + m][v] : D[q + m - kStageRows][v];
+              acc = fmaf(wt[K - 1 - m][v], d, acc);
+              dwacc[K - 1 - m][v] = fmaf(xv[v], d, dwacc[K - 1 - m][v]);
+            }
+            out[v] = acc;
+            dbacc[v] += gr[q][v];
+          }
+          if (active) st4(dx + (r + q) * C + c0, out);
+        }
+#pragma unroll
+        for (int m = 0; m < K; ++m)
+#pragma unroll
+          for (int v = 0; v < kConvVec; ++v) D[m][v] = gr[m][v];
+        end_next = eb[0];
+      } else {
 #pragma unroll
       for (int q = kStageRows - 1; q >= 0; --q) {
         const int64_t j = r + q;
@@ -350,6 +441,7 @@ __global__ void __launch_bounds__(kConvThreads) conv1d_bwd_kernel(
         }
         if (active) st4(dx + j * C + c0, out);
       }
+      }
     }
     if (!__syncthreads_and(ok)) {
       if (threadIdx.x == 0) drain_stages(full, kBwdStages, c + 1, issued, err);
@@ -365,19 +457,33 @@ __global__ void __launch_bounds__(kConvThreads) conv1d_bwd_kernel(
 }
 
 // dw[c, k] (k < K) and dbias[c] (k == K) from the per-group partials part[group][k][c]:
-// one thread per (channel, k) adds the groups in order in fp64 (deterministic).
-__global__ void __launch_bounds__(256) conv1d_reduce_kernel(const float* __restrict__ part, int64_t n_groups,
-                                                            int C, int K, float* __restrict__ dw,
-                                                            float* __restrict__ dbias) {
-  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+// a CTA covers 32 channels with 8 threads per channel, each adding every 8th group in
+// fp64; the 8 sums are then added in a fixed order (the result does not depend on
+// scheduling).
+constexpr int kRedC = 32, kRedG = 8;
+__global__ void __launch_bounds__(kRedC * kRedG) conv1d_reduce_kernel(const float* __restrict__ part,
+                                                                    int64_t n_groups, int C, int K,
+                                                                    float* __restrict__ dw,
+                                                                    float* __restrict__ dbias) {
+  __shared__ double acc[kRedG][kRedC];
+  const int c = blockIdx.x * kRedC + threadIdx.x;
   const int k = blockIdx.y;
-  if (c >= C) return;
   double s = 0.0;
-  for (int64_t g = 0; g < n_groups; ++g) s += part[(g * (K + 1) + k) * C + c];
-  if (k < K) {
-    if (dw) dw[static_cast<int64_t>(c) * K + k] = static_cast<float>(s);
-  } else if (dbias) {
-    dbias[c] = static_cast<float>(s);
+  if (c < C) {
+#pragma unroll 4
+    for (int64_t g = threadIdx.y; g < n_groups; g += kRedG) s += part[(g * (K + 1) + k) * C + c];
+  }
+  acc[threadIdx.y][threadIdx.x] = s;
+  __syncthreads();
+  if (threadIdx.y == 0 && c < C) {
+    double tot = 0.0;
+#pragma unroll
+    for (int q = 0; q < kRedG; ++q) tot += acc[q][threadIdx.x];
+    if (k < K) {
+      if (dw) dw[static_cast<int64_t>(c) * K + k] = static_cast<float>(tot);
+    } else if (dbias) {
+      dbias[c] = static_cast<float>(tot);
+    }
   }
 }
 
@@ -416,8 +522,8 @@ int launch_bwd(const void* x, const void* w, const void* dy, void* dx, float* dw
       T_, C, g.rows_per_group, part, err);
   TREE_LAUNCH_CHECK("conv1d_bwd_kernel");
   if (dw || dbias) {
-    dim3 rgrid(static_cast<unsigned>((C + 255) / 256), static_cast<unsigned>(K + 1));
-    conv1d_reduce_kernel<<<rgrid, 256, 0, st>>>(part, g.groups, C, K, dw, dbias);
+    dim3 rgrid(static_cast<unsigned>((C + kRedC - 1) / kRedC), static_cast<unsigned>(K + 1));
+    conv1d_reduce_kernel<<<rgrid, dim3(kRedC, kRedG), 0, st>>>(part, g.groups, C, K, dw, dbias);
     TREE_LAUNCH_CHECK("conv1d_reduce_kernel");
   }
   return TREE_OK;
