@@ -560,7 +560,9 @@ def run_conv1d(args, dev, peaks, peak_src, flush):
         "roofline": {"bound": "hbm", "achieved": round(bg if dom_b else fg, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round((bg if dom_b else fg) / hbm, 4), "of": peak_src,
                      "kernel": "tree_conv1d_bwd" if dom_b else "tree_conv1d_fwd",
-                     "bytes_per_launch": b_bytes if dom_b else f_bytes, "traffic": None},
+                     "bytes_per_launch": b_bytes if dom_b else f_bytes,
+                     "traffic": profiled_traffic(("conv1d_bwd" if dom_b else "conv1d_fwd") + ":galton_watson_c8192_k4",
+                                                 ["conv1d.cu"])},
         "data": "synthetic (seeded torch generator on device)",
     }
 
