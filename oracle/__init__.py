@@ -34,6 +34,11 @@ The oracle follows the plain definitions on the pages:
 * ``conv``      -- tree-correct causal depthwise conv1d: per-path convolution with
                    the parent's tokens as left context (Tree Training §3.2
                    "(ii) Causal convolution", eq. 11, Fig. 4).
+* ``gateway``   -- partition-gateway attention: a child partition's queries over the
+                   parent's accumulated keys (ancestor bias) and its own rows (tree
+                   mask), dense masked softmax forward and backward (Tree Training
+                   §3.3 "Differentiable partition boundaries", Appendix B.1-B.5,
+                   eq. 14-17).
 * ``metrics``   -- potential overlap ratio (Tree Training §4.1 eq. 12).
 
 Pins (tests/test_oracle_*.py) tie every function to values printed on the
@@ -50,11 +55,14 @@ from .metrics import por, token_ratio, allowed_pairs_from_paths
 
 from .policy import policy_loss_ref
 from .conv import conv1d_ref_fwd, conv1d_ref_bwd, conv1d_ref_rows
+from .gateway import (gateway_mask_ref, gateway_attn_ref_fwd, gateway_attn_ref_bwd, gateway_for_child,
+                      local_subtree_end, is_ancestor_or_self)
 
 __all__ = [
     "pack_ref", "brute_force_prefixes", "attn_ref_fwd", "attn_ref_bwd", "attn_ref_rows",
     "attn_ref_dq_rows", "attn_ref_dkdv_rows", "dense_mask_from_chunks", "mask_from_paths",
     "leaf_paths_from_parents", "rope_ref", "logprob_ref_fwd", "logprob_ref_bwd",
     "logprob_ref_gz", "por", "token_ratio", "allowed_pairs_from_paths", "policy_loss_ref",
-    "conv1d_ref_fwd", "conv1d_ref_bwd", "conv1d_ref_rows",
+    "conv1d_ref_fwd", "conv1d_ref_bwd", "conv1d_ref_rows", "gateway_mask_ref", "gateway_attn_ref_fwd",
+    "gateway_attn_ref_bwd", "gateway_for_child", "local_subtree_end", "is_ancestor_or_self",
 ]
