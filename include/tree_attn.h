@@ -290,6 +290,43 @@ int tree_policy_loss(const float* logp, const float* old_logp, const float* adva
                      tree_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* Partition-gateway attention                                               */
+/* ------------------------------------------------------------------------ */
+/*
+ * [TT] §3.3 "Differentiable partition boundaries", Appendix B.2-B.5: a tree too
+ * large for one pass is cut into partitions. A child partition C (T rows, its own
+ * preorder subtree_end, local to C) attends to the keys/values its parent partition
+ * accumulated up to the cut node -- the past, past_len rows -- under an additive
+ * bias, 0 at the cut node's ancestors and -INFINITY elsewhere (eq. 15-16), and to
+ * its own rows under the ordinary tree mask (eq. 14). Positions of C continue from
+ * pos_offset (eq. 17): rotate q and the own rows of k with tree_rope beforehand.
+ *
+ * q, o, dout, dq: device [T, Hq, d]; k, v: device [past_len + T, Hkv, d], the past
+ * rows first (the key/value cache a model holds); dk, dv: device [T, Hkv, d], the
+ * gradients of C's own key/value rows (written). lse: device fp32 [Hq, T].
+ * attn_bias: device fp32 [past_len], each 0 or -INFINITY (any other value sets the
+ * device error word and is read as -INFINITY); may be NULL when past_len = 0.
+ * dk_past, dv_past: device fp32 [past_len, Hkv, d]: the past rows' gradients are
+ * ADDED to them in fp32 (B.5), so that the child partitions sharing one gateway sum
+ * without bf16 rounding in between -- zero them before the first child.
+ * Runs on the tensor-core kernels only: bf16, d = 128, Hq / Hkv even (other
+ * arguments: TREE_ERR_SHAPE / TREE_ERR_DTYPE). workspace: device, at least
+ * tree_attn_gateway_workspace_size() bytes, 256-byte aligned. past_len = 0 is plain
+ * tree attention (the same results as tree_attn_fwd / tree_attn_bwd).
+ */
+size_t tree_attn_gateway_workspace_size(int64_t past_len, int64_t T, int Hq, int Hkv, int d, int dtype);
+int tree_attn_fwd_gateway(const void* q, const void* k, const void* v, void* o, float* lse,
+                          const float* attn_bias, const int32_t* subtree_end, int64_t past_len,
+                          int64_t T, int Hq, int Hkv, int d, int dtype, float softmax_scale,
+                          void* workspace, size_t workspace_bytes, tree_stream_t stream);
+int tree_attn_bwd_gateway(const void* q, const void* k, const void* v, const void* o,
+                          const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                          float* dk_past, float* dv_past, const float* attn_bias,
+                          const int32_t* subtree_end, int64_t past_len, int64_t T, int Hq,
+                          int Hkv, int d, int dtype, float softmax_scale, void* workspace,
+                          size_t workspace_bytes, tree_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* Tree-correct causal depthwise conv1d (short convolution of SSM layers)    */
 /* ------------------------------------------------------------------------ */
 /*

@@ -15,6 +15,9 @@ Functions (same names as the C ABI):
   tree_logprob_bwd(hidden, w_lm, lse, occ_row_ptr, occ_perm, occ_targets, grad_logp, ...)
                                                     -> (d_hidden, d_w)
   tree_policy_loss(logp, old_logp, advantage, ...)  -> (loss, grad_logp, loss_sum)
+  tree_attn_fwd_gateway(q, k, v, attn_bias, subtree_end) -> (o, lse)
+  tree_attn_bwd_gateway(q, k, v, o, dout, lse, attn_bias, subtree_end, dk_past, dv_past)
+                                                    -> (dq, dk, dv, dk_past, dv_past)
   tree_conv1d_fwd(x, w, parent_row, bias)           -> y
   tree_conv1d_bwd(x, w, dy, subtree_end, position_ids) -> (dx, dw, dbias)
 """
@@ -29,7 +32,8 @@ from ._lib import PackOut, PackSizes, TreeError, check, lib
 __all__ = [
     "tree_pack", "tree_validate_subtree_end", "tree_rope", "tree_attn_workspace_size",
     "tree_attn_fwd", "tree_attn_bwd", "tree_attn_bwd_rope", "tree_kernel_timing", "tree_kernel_last_ms", "tree_logprob_workspace_size", "tree_logprob_fwd", "tree_policy_loss",
-    "tree_conv1d_fwd", "tree_conv1d_bwd", "tree_conv1d_workspace_size",
+    "tree_conv1d_fwd", "tree_conv1d_bwd", "tree_conv1d_workspace_size", "tree_attn_fwd_gateway",
+    "tree_attn_bwd_gateway", "tree_attn_gateway_workspace_size",
     "tree_logprob_bwd", "tree_check_device_status", "tree_kernel_path", "tree_launch_count", "TreeError", "lib",
     "DTYPE_F32", "DTYPE_BF16",
 ]
@@ -254,6 +258,61 @@ def tree_policy_loss(logp, old_logp, advantage, weight=None, mask=None, eps_low:
                                  _dev(total, "loss_sum", f32), _stream(logp)),
           "tree_policy_loss")
     return loss, g, total
+
+
+def tree_attn_gateway_workspace_size(past_len, T, Hq, Hkv, d, dtype_code) -> int:
+    return int(lib().tree_attn_gateway_workspace_size(past_len, T, Hq, Hkv, d, dtype_code))
+
+
+def tree_attn_fwd_gateway(q, k, v, attn_bias, subtree_end, softmax_scale: float = 0.0, workspace=None, out=None,
+                          lse=None):
+    """Child-partition attention through a gateway: q [T,Hq,d]; k, v [past_len+T,Hkv,d]
+    (past rows first); attn_bias fp32 [past_len] (0 / -inf); subtree_end int32 [T] local
+    to the partition. Returns (o [T,Hq,d], lse [Hq,T])."""
+    torch = _torch()
+    T, Hq, d = q.shape
+    Tk, Hkv = k.shape[0], k.shape[1]
+    P = Tk - T
+    dt = _dtype_code(q)
+    o = torch.empty_like(q) if out is None else out
+    lse = torch.empty((Hq, T), dtype=torch.float32, device=q.device) if lse is None else lse
+    ws = _workspace(tree_attn_gateway_workspace_size(P, T, Hq, Hkv, d, dt), q.device, workspace)
+    check(lib().tree_attn_fwd_gateway(_dev(q, "q"), _dev(k, "k", q.dtype), _dev(v, "v", q.dtype), _dev(o, "o", q.dtype),
+                                      _dev(lse, "lse", torch.float32), _dev(attn_bias, "attn_bias", torch.float32),
+                                      _dev(subtree_end, "subtree_end", torch.int32), P, T, Hq, Hkv, d, dt,
+                                      float(softmax_scale), C.c_void_p(ws.data_ptr()), ws.numel() * ws.element_size(),
+                                      _stream(q)), "tree_attn_fwd_gateway")
+    return o, lse
+
+
+def tree_attn_bwd_gateway(q, k, v, o, dout, lse, attn_bias, subtree_end, dk_past=None, dv_past=None,
+                          softmax_scale: float = 0.0, workspace=None):
+    """Backward of tree_attn_fwd_gateway: returns (dq [T,Hq,d], dk [T,Hkv,d], dv [T,Hkv,d]) for
+    the partition's own rows and (dk_past, dv_past) fp32 [past_len,Hkv,d], to which the past
+    rows' gradients were added (new zeroed tensors when not given)."""
+    torch = _torch()
+    T, Hq, d = q.shape
+    Tk, Hkv = k.shape[0], k.shape[1]
+    P = Tk - T
+    dt = _dtype_code(q)
+    f32 = torch.float32
+    dq = torch.empty_like(q)
+    dk = torch.empty((T, Hkv, d), dtype=q.dtype, device=q.device)
+    dv = torch.empty((T, Hkv, d), dtype=q.dtype, device=q.device)
+    if dk_past is None:
+        dk_past = torch.zeros((P, Hkv, d), dtype=f32, device=q.device)
+    if dv_past is None:
+        dv_past = torch.zeros((P, Hkv, d), dtype=f32, device=q.device)
+    ws = _workspace(tree_attn_gateway_workspace_size(P, T, Hq, Hkv, d, dt), q.device, workspace)
+    check(lib().tree_attn_bwd_gateway(_dev(q, "q"), _dev(k, "k", q.dtype), _dev(v, "v", q.dtype), _dev(o, "o", q.dtype),
+                                      _dev(dout, "dout", q.dtype), _dev(lse, "lse", f32), _dev(dq, "dq", q.dtype),
+                                      _dev(dk, "dk", q.dtype), _dev(dv, "dv", q.dtype),
+                                      _dev(dk_past, "dk_past", f32) if P > 0 else None,
+                                      _dev(dv_past, "dv_past", f32) if P > 0 else None,
+                                      _dev(attn_bias, "attn_bias", f32), _dev(subtree_end, "subtree_end", torch.int32),
+                                      P, T, Hq, Hkv, d, dt, float(softmax_scale), C.c_void_p(ws.data_ptr()),
+                                      ws.numel() * ws.element_size(), _stream(q)), "tree_attn_bwd_gateway")
+    return dq, dk, dv, dk_past, dv_past
 
 
 def tree_conv1d_fwd(x, w, parent_row, bias=None, out=None):

@@ -57,6 +57,11 @@ SIGNATURES = {
     "tree_kernel_timing": (_int, [_int]),
     "tree_policy_loss": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _f, _f, _vp, _vp, _vp, _vp]),
     "tree_selftest_exp2": (_int, [_vp, _vp, _i64, _vp]),
+    "tree_attn_gateway_workspace_size": (_sz, [_i64, _i64, _int, _int, _int, _int]),
+    "tree_attn_fwd_gateway": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _int, _int, _int, _int, _f,
+                                     _vp, _sz, _vp]),
+    "tree_attn_bwd_gateway": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64,
+                                     _int, _int, _int, _int, _f, _vp, _sz, _vp]),
     "tree_conv1d_fwd": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _int, _int, _int, _vp]),
     "tree_conv1d_workspace_size": (_sz, [_i64, _int, _int]),
     "tree_conv1d_bwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _int, _int, _int, _vp, _sz,

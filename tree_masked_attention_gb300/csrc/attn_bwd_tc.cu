@@ -82,7 +82,8 @@ static_assert(offsetof(Smem, dout) == offsetof(Smem, q) + sizeof(Smem::q) &&
 static_assert(kSmemBytes + 64 <= 232448, "backward shared memory exceeds the 227 KB per-block limit");
 
 struct Params {
-  int T, T_pad, Hq, Hkv;
+  int T, T_pad, Hq, Hkv;  // T: key rows; T_pad: query rows rounded up to 64
+  int Tq, q_off;          // query rows, key rows before the first query
   float scale_log2, scale;
   const int32_t* kmax;
   const int32_t* endp;
@@ -116,12 +117,17 @@ __device__ __forceinline__ void red_add4(float* p, float a, float b, float c, fl
                : "memory");
 }
 
-// Query tiles of 64 rows seen by key tile kt: [qt_lo, qt_lo + nq).
+// Query tiles of 64 rows seen by key tile kt: [qt_lo, qt_lo + nq). The queries that can
+// see the tile are the key rows [max(first key, q_off), max subtree_end]; query tile t
+// holds key rows q_off + 64 t ...
+__device__ __forceinline__ int query_tiles_of(int kt, int kmax, int T, int q_off, int* qt_lo) {
+  const int first = max(kt * BN, q_off);
+  const int last_row = min(kmax, T - 1);
+  *qt_lo = (first - q_off) / BQ;
+  return last_row >= first ? (last_row - q_off) / BQ - *qt_lo + 1 : 0;
+}
 __device__ __forceinline__ int key_tile_queries(const Params& p, int kt, int* qt_lo) {
-  const int j0 = kt * BN;
-  const int last_row = min(p.kmax[kt], p.T - 1);
-  *qt_lo = j0 / BQ;
-  return last_row >= j0 ? last_row / BQ - *qt_lo + 1 : 0;
+  return query_tiles_of(kt, p.kmax[kt], p.T, p.q_off, qt_lo);
 }
 
 // Persistent: each CTA takes work units {key tile, KV head, steps [b, e)} from a counter.
@@ -235,7 +241,7 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
       bool ok = true;
       for (int l = 0; l < L; ++l) {
         const int g = g0 + l, st = g % NST, t = b + l;
-        const int i0 = (U.qt_lo + t / G) * BQ + wg * 32;  // first query of this half
+        const int i0 = p.q_off + (U.qt_lo + t / G) * BQ + wg * 32;  // first query of this half, among the keys
         if (!(ok = __all_sync(0xffffffffu, mbar_wait(&S.s_full[g & 1], (g >> 1) & 1, p.err) &&
                                                mbar_wait(&S.dp_full, g & 1, p.err) &&
                                                mbar_wait(&S.qdo_full[st], (g / NST) & 1, p.err))))
@@ -516,7 +522,7 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
           for (int t2 = 0; t2 < 32; ++t2) buf[t2 * D + r] = __uint_as_float(v[half][t2]) * p.scale;
           fence_proxy_async_smem();
           named_bar_sync(1, 128);
-          if (leader && i0 + half * (BQ / 2) < p.T) {
+          if (leader && i0 + half * (BQ / 2) < p.Tq) {
             tma_reduce_add_3d(&tmDQ, buf, 0, h, i0 + half * (BQ / 2));
             bulk_commit();
             last_stage = half;
@@ -551,8 +557,9 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
 }
 
 struct PrepParams {
-  const int32_t* end;  // subtree_end [T]
-  int T, T_pad, n_kt, Hq, Hkv, max_units;
+  const int32_t* end;  // subtree_end [T] (of the key rows)
+  int T, T_pad, n_kt, Hq, Hkv, max_units;  // T: key rows; T_pad: query rows rounded up to 64
+  int Tq, q_off, n_rows;                   // query rows, keys before them, rows the blocks cover
   int32_t* kmax;       // [n_kt] max subtree_end of each 128-key tile
   int32_t* kmin;       // [n_kt] min subtree_end of each 128-key tile
   int32_t* endp;       // [n_kt * 128] subtree_end, -1 past T
@@ -585,11 +592,18 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const PrepParams q) 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (blockIdx.x > 0) {
     const int64_t w = static_cast<int64_t>(blockIdx.x - 1) * 8 + warp;
-    if (w >= static_cast<int64_t>(q.T_pad) * q.Hq) return;
+    if (w >= static_cast<int64_t>(q.n_rows) * q.Hq) return;
     const int64_t i = w / q.Hq;
     const int h = static_cast<int>(w % q.Hq);
+    if (i < q.T && i >= q.Tq && h < q.Hkv) {  // key rows past the query rows: zero dK, dV only
+      const int64_t kv = (i * q.Hkv + h) * 128 + lane * 4;
+      const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+      *reinterpret_cast<float4*>(q.dk_acc + kv) = z;
+      *reinterpret_cast<float4*>(q.dv_acc + kv) = z;
+    }
+    if (i >= q.T_pad) return;
     float dl = 0.f, l2 = INFINITY;
-    if (i < q.T) {
+    if (i < q.Tq) {
       const int64_t off = w * 128 + lane * 4;
       const uint2 a = *reinterpret_cast<const uint2*>(q.o + off);
       const uint2 b = *reinterpret_cast<const uint2*>(q.dout + off);
@@ -600,7 +614,7 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const PrepParams q) 
       dl = a0.x * b0.x + a0.y * b0.y + a1.x * b1.x + a1.y * b1.y;
 #pragma unroll
       for (int s = 16; s > 0; s >>= 1) dl += __shfl_xor_sync(0xffffffffu, dl, s);
-      l2 = q.lse[static_cast<int64_t>(h) * q.T + i] * 1.4426950408889634f;
+      l2 = q.lse[static_cast<int64_t>(h) * q.Tq + i] * 1.4426950408889634f;
       const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
       *reinterpret_cast<float4*>(q.dq_acc + off) = z;
       if (h < q.Hkv) {
@@ -650,12 +664,7 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const PrepParams q) 
     }
   }
   __syncthreads();
-  auto tiles_of = [&](int kt, int* lo) -> int {
-    const int j0 = kt * BN;
-    const int last_row = min(q.kmax[kt], T - 1);
-    *lo = j0 / BQ;
-    return last_row >= j0 ? last_row / BQ - *lo + 1 : 0;
-  };
+  auto tiles_of = [&](int kt, int* lo) -> int { return query_tiles_of(kt, q.kmax[kt], T, q.q_off, lo); };
   long long local = 0;
   for (int kt = threadIdx.x; kt < q.n_kt; kt += blockDim.x) {
     int lo;
@@ -824,9 +833,26 @@ static int sm_count(int* n) {
   return TREE_OK;
 }
 
+// Gateway keys' gradients (the key rows before the queries): fp32 sums added into the
+// caller's accumulators, so that several child partitions sharing a gateway add up
+// without bf16 rounding between them.
+__global__ void gateway_past_grads_kernel(const float* __restrict__ dk_acc, const float* __restrict__ dv_acc,
+                                          int64_t n4, float* __restrict__ dk_past, float* __restrict__ dv_past) {
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= 2 * n4) return;
+  const bool is_v = t >= n4;
+  const int64_t u = is_v ? t - n4 : t;
+  const float4 g = reinterpret_cast<const float4*>(is_v ? dv_acc : dk_acc)[u];
+  float4* o = reinterpret_cast<float4*>(is_v ? dv_past : dk_past) + u;
+  float4 x = *o;
+  x.x += g.x; x.y += g.y; x.z += g.z; x.w += g.w;
+  *o = x;
+}
+
 int attn_bwd_tc(const AttnArgs& a, cudaStream_t st) {
   using namespace tcbwd;
-  const int64_t T_pad = (a.T + BQ - 1) / BQ * BQ;
+  const int64_t Tq = a.T - a.q_off;  // queries: the last Tq key rows
+  const int64_t T_pad = (Tq + BQ - 1) / BQ * BQ;
   const int n_kt = static_cast<int>((a.T + BN - 1) / BN);
   const int max_units = static_cast<int>(attn_bwd_max_units(a.T, a.Hkv));
   {
@@ -834,6 +860,9 @@ int attn_bwd_tc(const AttnArgs& a, cudaStream_t st) {
     q.end = a.end;
     q.T = static_cast<int>(a.T);
     q.T_pad = static_cast<int>(T_pad);
+    q.Tq = static_cast<int>(Tq);
+    q.q_off = static_cast<int>(a.q_off);
+    q.n_rows = static_cast<int>(std::max<int64_t>(T_pad, a.T));
     q.n_kt = n_kt;
     q.Hq = a.Hq;
     q.Hkv = a.Hkv;
@@ -854,18 +883,18 @@ int attn_bwd_tc(const AttnArgs& a, cudaStream_t st) {
     q.dk_acc = a.ws.dk_acc;
     q.dv_acc = a.ws.dv_acc;
     q.err = device_error_word();
-    const int64_t pre_blocks = (T_pad * a.Hq + 7) / 8;
+    const int64_t pre_blocks = (static_cast<int64_t>(q.n_rows) * a.Hq + 7) / 8;
     attn_bwd_prep_kernel<<<static_cast<unsigned>(1 + pre_blocks), 256, 0, st>>>(q);
     TREE_LAUNCH_CHECK("attn_bwd_prep_kernel");
   }
   int rc = TREE_OK;
   CUtensorMap mk, mv, mq, mdo, mdq;
   if ((rc = rows_map(&mk, a.k, a.T, a.Hkv, 128)) || (rc = rows_map(&mv, a.v, a.T, a.Hkv, 128)) ||
-      (rc = rows_map(&mq, a.q, a.T, a.Hq, BQ)) || (rc = rows_map(&mdo, a.dout, a.T, a.Hq, BQ)))
+      (rc = rows_map(&mq, a.q, Tq, a.Hq, BQ)) || (rc = rows_map(&mdo, a.dout, Tq, a.Hq, BQ)))
     return rc;
   {
-    // fp32 dQ accumulator [T, Hq, 128] as {d, head, row}, box {128, 1, 64}, no swizzle
-    const uint64_t dims[3] = {128, static_cast<uint64_t>(a.Hq), static_cast<uint64_t>(a.T)};
+    // fp32 dQ accumulator [Tq, Hq, 128] as {d, head, row}, box {128, 1, 64}, no swizzle
+    const uint64_t dims[3] = {128, static_cast<uint64_t>(a.Hq), static_cast<uint64_t>(Tq)};
     const uint64_t strides[2] = {128 * 4, static_cast<uint64_t>(a.Hq) * 128 * 4};
     const uint32_t box[3] = {128, 1, BQ / 2};
     if ((rc = make_tmap(&mdq, a.ws.dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, dims, strides, box, false))) return rc;
@@ -891,6 +920,8 @@ int attn_bwd_tc(const AttnArgs& a, cudaStream_t st) {
   Params p{};
   p.T = static_cast<int>(a.T);
   p.T_pad = static_cast<int>(T_pad);
+  p.Tq = static_cast<int>(Tq);
+  p.q_off = static_cast<int>(a.q_off);
   p.Hq = a.Hq;
   p.Hkv = a.Hkv;
   p.scale_log2 = a.scale * 1.4426950408889634f;
@@ -920,11 +951,20 @@ int attn_bwd_tc(const AttnArgs& a, cudaStream_t st) {
     TREE_LAUNCH_CHECK("attn_grads_rope_to_bf16_kernel");
     return TREE_OK;
   }
-  const int64_t nq4 = a.T * a.Hq * a.d / 4, nk4 = a.T * a.Hkv * a.d / 4;
+  // dQ of the queries; dK and dV of the key rows that are queries too (all of them but for
+  // gateway calls, whose leading q_off key rows go to the fp32 gateway sums instead)
+  const int64_t kv_off = a.q_off * a.Hkv * a.d;
+  const int64_t nq4 = Tq * a.Hq * a.d / 4, nk4 = Tq * a.Hkv * a.d / 4;
   attn_grads_to_bf16_kernel<<<static_cast<unsigned>((nq4 + 2 * nk4 + 255) / 256), 256, 0, st>>>(
-      a.ws.dq_acc, static_cast<__nv_bfloat16*>(a.dq), nq4, a.ws.dk_acc, static_cast<__nv_bfloat16*>(a.dk), nk4,
-      a.ws.dv_acc, static_cast<__nv_bfloat16*>(a.dv));
+      a.ws.dq_acc, static_cast<__nv_bfloat16*>(a.dq), nq4, a.ws.dk_acc + kv_off, static_cast<__nv_bfloat16*>(a.dk),
+      nk4, a.ws.dv_acc + kv_off, static_cast<__nv_bfloat16*>(a.dv));
   TREE_LAUNCH_CHECK("attn_grads_to_bf16_kernel");
+  if (a.q_off > 0) {
+    const int64_t n4 = kv_off / 4;
+    gateway_past_grads_kernel<<<static_cast<unsigned>((2 * n4 + 255) / 256), 256, 0, st>>>(
+        a.ws.dk_acc, a.ws.dv_acc, n4, a.dk_past, a.dv_past);
+    TREE_LAUNCH_CHECK("gateway_past_grads_kernel");
+  }
   return TREE_OK;
 }
 

@@ -37,10 +37,13 @@ struct AttnArgs {
   void* dk;
   void* dv;
   const int32_t* end;  // subtree_end [T]
-  int64_t T;
+  int64_t T;           // key rows; query rows are [q_off, T) of the same key space
+  int64_t q_off;       // rows of keys before the first query (0 but for gateway calls)
   int Hq, Hkv, d, dtype;
   float scale;
   int deterministic;
+  float* dk_past;      // gateway backward: fp32 [q_off, Hkv, d] sums the past keys' dK is added to
+  float* dv_past;      // gateway backward: the same for dV
   const int32_t* rope_pos;  // backward only: when set, dq/dk get the inverse depth rotation
   float rope_theta;
   AttnWs ws;

@@ -51,7 +51,8 @@ struct Smem {
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
 
 struct Params {
-  int T, Hq, Hkv, n_qt;
+  int T, Hq, Hkv, n_qt;  // T: key rows
+  int Tq, q_off, n_kt;   // query rows, key rows before the first query, key tiles
   float scale_log2;
   const int32_t* kmax;
   const int32_t* kmin;
@@ -126,7 +127,9 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int h0 = 2 * blockIdx.x;
   const int qt = p.n_qt - 1 - blockIdx.y;  // longest query tiles first
-  const int i0 = qt * BM;
+  const int i0 = qt * BM;                  // first query row of the tile (query buffers)
+  const int iq0 = p.q_off + i0;            // the same row among the keys
+  const int kt_hi = min((iq0 + BM - 1) / BN, p.n_kt - 1);  // last key tile before the tile's last query
   const int kvh = h0 / (p.Hq / p.Hkv);
 
   if (threadIdx.x == 0) {
@@ -157,8 +160,8 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       for (int hh = 0; hh < 2; ++hh)
         for (int sub = 0; sub < 2; ++sub) tma_load_3d(S.q[hh] + sub * kSub, &tmQ, &S.q_full, sub * 64, h0 + hh, i0);
       int n = 0;
-      for (int kt = 0; kt <= qt; ++kt) {
-        if (p.kmax[kt] < i0) continue;
+      for (int kt = 0; kt <= kt_hi; ++kt) {
+        if (p.kmax[kt] < iq0) continue;
         const int s = n & 1;
         if (n >= 2 && !mbar_wait(&S.kv_empty[s], ((n >> 1) - 1) & 1, p.err)) break;
         mbar_arrive_expect_tx(&S.k_full[s], kTile);
@@ -198,7 +201,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         mma_commit(&S.o_done[h]);
       };
       int N = 0;
-      for (int kt = 0; kt <= qt; ++kt) N += p.kmax[kt] >= i0;
+      for (int kt = 0; kt <= kt_hi; ++kt) N += p.kmax[kt] >= iq0;
       bool ok = N > 0 && mbar_wait(&S.q_full, 0, p.err) && mbar_wait(&S.k_full[0], 0, p.err);
       if (ok) {
         tc_fence_after();
@@ -229,7 +232,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
   } else if (warp < 8) {
     // ------------------------------------------------------------ softmax warps
     const int h = warp >> 2, q4 = warp & 3;
-    const int r = q4 * 32 + lane, i = i0 + r;
+    const int r = q4 * 32 + lane, ik = iq0 + r;  // the thread's query row, as a key row
     const uint32_t lanes = static_cast<uint32_t>(q4 * 32) << 16;
     const uint32_t tS = tmem + lanes + h * 128, tO = tmem + lanes + 256 + h * 128;
     const float sl2 = p.scale_log2;
@@ -237,15 +240,15 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     int n = 0;
     bool ok = true;
     const float rescale_raw = kRescaleLog2 / sl2;  // the 2^8 threshold in raw score units
-    for (int kt = 0; kt <= qt; ++kt) {
-      if (p.kmax[kt] < i0) continue;
+    for (int kt = 0; kt <= kt_hi; ++kt) {
+      if (p.kmax[kt] < iq0) continue;
       const int j0 = kt * BN;
-      const bool partial = !(j0 + BN - 1 <= i0 && p.kmin[kt] >= i0 + BM - 1);
+      const bool partial = !(j0 + BN - 1 <= iq0 && p.kmin[kt] >= iq0 + BM - 1);
       // visibility bits of this row's 128 keys, formed while the MMA of S runs
       uint32_t vis[4] = {~0u, ~0u, ~0u, ~0u};
       if (partial) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) vis[c] = visible32(p.endp, j0 + 32 * c, i);
+        for (int c = 0; c < 4; ++c) vis[c] = visible32(p.endp, j0 + 32 * c, ik);
       }
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(&S.s_full[h], n & 1, p.err)))) break;
       tc_fence_after();
@@ -336,7 +339,8 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
           *reinterpret_cast<uint4*>(row + chunk * 16) = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
         }
       }
-      if (i < p.T) p.lse[static_cast<int64_t>(h0 + h) * p.T + i] = (m_run * sl2 + log2f(l)) * 0.6931471805599453f;
+      const int i = i0 + r;
+      if (i < p.Tq) p.lse[static_cast<int64_t>(h0 + h) * p.Tq + i] = (m_run * sl2 + log2f(l)) * 0.6931471805599453f;
     }
     fence_proxy_async_smem();
     asm volatile("bar.sync %0, 128;" ::"r"(1 + h) : "memory");
@@ -407,9 +411,10 @@ int attn_fwd_tc(const AttnArgs& a, cudaStream_t st) {
   using namespace tcfwd;
   int rc = tile_meta128_launch(a, st);
   if (rc) return rc;
+  const int64_t Tq = a.T - a.q_off;  // queries: the last Tq key rows
   CUtensorMap mq, mk, mv, mo;
-  if ((rc = qkv_map(&mq, a.q, a.T, a.Hq)) || (rc = qkv_map(&mk, a.k, a.T, a.Hkv)) ||
-      (rc = qkv_map(&mv, a.v, a.T, a.Hkv)) || (rc = qkv_map(&mo, a.o, a.T, a.Hq)))
+  if ((rc = qkv_map(&mq, a.q, Tq, a.Hq)) || (rc = qkv_map(&mk, a.k, a.T, a.Hkv)) ||
+      (rc = qkv_map(&mv, a.v, a.T, a.Hkv)) || (rc = qkv_map(&mo, a.o, Tq, a.Hq)))
     return rc;
   static bool attr_set = false;
   if (!attr_set) {
@@ -421,7 +426,10 @@ int attn_fwd_tc(const AttnArgs& a, cudaStream_t st) {
   p.T = static_cast<int>(a.T);
   p.Hq = a.Hq;
   p.Hkv = a.Hkv;
-  p.n_qt = static_cast<int>((a.T + BM - 1) / BM);
+  p.Tq = static_cast<int>(Tq);
+  p.q_off = static_cast<int>(a.q_off);
+  p.n_qt = static_cast<int>((Tq + BM - 1) / BM);
+  p.n_kt = static_cast<int>((a.T + BN - 1) / BN);
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.kmax = a.ws.kmax128;
   p.kmin = a.ws.kmin128;
