@@ -57,6 +57,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-lm", action="store_true")
     ap.add_argument("--conv-steps", type=int, default=10)
     ap.add_argument("--no-conv", action="store_true")
+    ap.add_argument("--gateway-steps", type=int, default=5)
+    ap.add_argument("--no-gateway", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of graph replays")
@@ -411,6 +413,8 @@ def run_ours(args):
         out["lm_head"] = run_lm_head(args, dev, peaks, peak_src)
     if not args.no_conv and rank == 0:
         out["conv1d"] = run_conv1d(args, dev, peaks, peak_src, flush)
+    if not args.no_gateway and rank == 0:
+        out["gateway"] = run_gateway(args, dev, peaks, peak_src, flush)
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(args.workload, tree, (qh, kh, vh, doh), P, budget_s=25.0)
@@ -564,6 +568,85 @@ def run_conv1d(args, dev, peaks, peak_src, flush):
                      "traffic": profiled_traffic(("conv1d_bwd" if dom_b else "conv1d_fwd") + ":galton_watson_c8192_k4",
                                                  ["conv1d.cu"])},
         "data": "synthetic (seeded torch generator on device)",
+    }
+
+
+def run_gateway(args, dev, peaks, peak_src, flush):
+    """Partition-gateway attention: the long-prompt agentic tree cut below its shared
+    1024-token prompt. The prompt is the parent partition; every trajectory subtree is a
+    child partition whose gateway past is the prompt (all ancestors, bias 0). Each step
+    runs every child's tree_attn_fwd_gateway and tree_attn_bwd_gateway (the prompt rows'
+    dK / dV summed over the children in fp32). TFLOP/s on allowed pairs of the children."""
+    import torch
+    import tree_masked_attention_gb300 as tma
+    tree = synth.agentic_long()
+    pk = tma.tree_pack(tree.seqs)
+    c = synth.CONFIGS["agentic_long"]
+    Hq, Hkv, d = c["Hq"], c["Hkv"], c["d"]
+    end, par, pos = pk["subtree_end"], pk["parent_row"], pk["position_ids"]
+    prompt_end = int(pk["node_end"][0])          # the shared prompt: the root node
+    P = prompt_end + 1
+    kids = [int(r) for r in range(P, pk["T"]) if par[r] == prompt_end]
+    T = pk["T"]
+    q_all, k_all, v_all, do_all = synth.attention_config("agentic_long", T, seed=0)
+    bf = torch.bfloat16
+    past_k = torch.from_numpy(k_all[:P]).to(bf)
+    past_v = torch.from_numpy(v_all[:P]).to(bf)
+    bias = torch.zeros(P, dtype=torch.float32, device=dev)
+    parts, pairs = [], 0
+    for r in kids:
+        rows = slice(r, int(end[r]) + 1)
+        n = int(end[r]) + 1 - r
+        ce = (end[rows] - r).astype(np.int32)
+        parts.append(dict(
+            q=torch.from_numpy(q_all[rows]).to(bf).to(dev), do=torch.from_numpy(do_all[rows]).to(bf).to(dev),
+            k=torch.cat([past_k, torch.from_numpy(k_all[rows]).to(bf)]).to(dev),
+            v=torch.cat([past_v, torch.from_numpy(v_all[rows]).to(bf)]).to(dev),
+            end=torch.from_numpy(ce).to(dev), n=n))
+        pairs += int((pos[rows].astype(np.int64) + 1).sum())   # every past row is an ancestor
+    ws = torch.empty(max(tma.tree_attn_gateway_workspace_size(P, p["n"], Hq, Hkv, d, 1) for p in parts),
+                     dtype=torch.uint8, device=dev)
+    dkp = torch.zeros((P, Hkv, d), dtype=torch.float32, device=dev)
+    dvp = torch.zeros_like(dkp)
+    for p in parts:
+        p["o"] = torch.empty_like(p["q"])
+        p["lse"] = torch.empty((Hq, p["n"]), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        dkp.zero_()
+        dvp.zero_()
+        for p in parts:
+            tma.tree_attn_fwd_gateway(p["q"], p["k"], p["v"], bias, p["end"], workspace=ws, out=p["o"], lse=p["lse"])
+        for p in parts:
+            tma.tree_attn_bwd_gateway(p["q"], p["k"], p["v"], p["o"], p["do"], p["lse"], bias, p["end"],
+                                      dk_past=dkp, dv_past=dvp, workspace=ws)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    n = max(args.gateway_steps, 1)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+    for s in range(n):
+        flush.zero_()
+        evs[s][0].record(stream)
+        step()
+        evs[s][1].record(stream)
+    torch.cuda.synchronize()
+    tma.tree_check_device_status()
+    ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
+    fl = 14.0 * d * pairs * Hq
+    tf = fl / (ms / 1e3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    return {
+        "workload": f"gateway: long-prompt agentic tree ({T} rows) cut below its {P}-token prompt; "
+                    f"{len(parts)} child partitions of {min(p['n'] for p in parts)}-{max(p['n'] for p in parts)} rows, "
+                    f"each with the prompt as gateway past; bf16, {Hq}/{Hkv} heads, d = {d}",
+        "value": round(tf, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4), "steps": n,
+        "allowed_pairs": pairs, "flops_per_step": fl, "pct_bf16_peak": round(100 * tf / peak, 2),
+        "step": "tree_attn_fwd_gateway for every child, then tree_attn_bwd_gateway for every child "
+                "(prompt dK / dV summed in fp32); L2 flushed before each step",
+        "data": "synthetic (the long-prompt agentic configuration's seeded Q, K, V, dO)",
     }
 
 
