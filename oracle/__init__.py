@@ -39,6 +39,9 @@ The oracle follows the plain definitions on the pages:
                    mask), dense masked softmax forward and backward (Tree Training
                    §3.3 "Differentiable partition boundaries", Appendix B.1-B.5,
                    eq. 14-17).
+* ``gdn``       -- tree-routed Gated DeltaNet recurrence: each chunk starts from its
+                   parent chunk's end state; per-path token recurrence, forward and
+                   backward (Tree Training §3.2 "SSM Layers (GDN)", eq. 10, A.2).
 * ``metrics``   -- potential overlap ratio (Tree Training §4.1 eq. 12).
 
 Pins (tests/test_oracle_*.py) tie every function to values printed on the
@@ -55,6 +58,7 @@ from .metrics import por, token_ratio, allowed_pairs_from_paths
 
 from .policy import policy_loss_ref
 from .conv import conv1d_ref_fwd, conv1d_ref_bwd, conv1d_ref_rows
+from .gdn import gdn_ref_fwd, gdn_ref_bwd
 from .gateway import (gateway_mask_ref, gateway_attn_ref_fwd, gateway_attn_ref_bwd, gateway_for_child,
                       local_subtree_end, is_ancestor_or_self)
 
@@ -65,4 +69,5 @@ __all__ = [
     "logprob_ref_gz", "por", "token_ratio", "allowed_pairs_from_paths", "policy_loss_ref",
     "conv1d_ref_fwd", "conv1d_ref_bwd", "conv1d_ref_rows", "gateway_mask_ref", "gateway_attn_ref_fwd",
     "gateway_attn_ref_bwd", "gateway_for_child", "local_subtree_end", "is_ancestor_or_self",
+    "gdn_ref_fwd", "gdn_ref_bwd",
 ]
