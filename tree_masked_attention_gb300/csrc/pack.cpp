@@ -8,9 +8,10 @@
 // compress single-child chains into nodes, number them in preorder.
 //
 // The trie is stored as flat arrays with insertion-ordered child lists
-// (first_child / next_sibling) and a hash map from (parent, token) to child, so
-// building is O(total tokens) and the preorder walk needs no recursion (paths of
-// several thousand tokens are common).
+// (first_child / next_sibling); a child is looked up by scanning its parent's list, or,
+// for a node with many children, through a hash map from (parent, token), so building
+// is O(total tokens) and the preorder walk needs no recursion (paths of several
+// thousand tokens are common).
 #include <algorithm>
 #include <cstring>
 #include <new>
@@ -42,18 +43,33 @@ inline uint64_t edge_key(int32_t parent, int32_t token) {
          static_cast<uint32_t>(token);
 }
 
+// A child is found by scanning its parent's insertion-ordered child list (one compare
+// along a chain, a few at a fork); a node with more than kScan children also gets its
+// children into a hash map keyed by (parent, token), which serves its later lookups.
+constexpr int32_t kScan = 16;
+
 int build(tree_plan& p) {
   const int64_t n_tokens = p.offsets[p.n_seqs];
-  std::unordered_map<uint64_t, int32_t> child;
-  child.reserve(static_cast<size_t>(n_tokens) + 16);
+  std::unordered_map<uint64_t, int32_t> wide;  // children of nodes with > kScan children
   p.token_node.resize(static_cast<size_t>(n_tokens));
+  p.tok.reserve(static_cast<size_t>(n_tokens));
+  auto kids_of = [&](int32_t node) { return node < 0 ? p.first_root : p.first_child[node]; };
+  auto fanout = [&](int32_t node) -> int64_t { return node < 0 ? p.n_roots : p.n_child[node]; };
+  auto find_child = [&](int32_t node, int32_t tk) -> int32_t {
+    if (fanout(node) > kScan) {
+      auto it = wide.find(edge_key(node, tk));
+      return it == wide.end() ? -1 : it->second;
+    }
+    for (int32_t c = kids_of(node); c >= 0; c = p.next_sibling[c])
+      if (p.tok[c] == tk) return c;
+    return -1;
+  };
   for (int64_t k = 0; k < p.n_seqs; ++k) {
     int32_t node = -1;
     for (int64_t t = p.offsets[k]; t < p.offsets[k + 1]; ++t) {
       const int32_t tk = p.tokens[t];
-      auto it = child.find(edge_key(node, tk));
-      int32_t c;
-      if (it == child.end()) {
+      int32_t c = find_child(node, tk);
+      if (c < 0) {
         if (p.tok.size() >= static_cast<size_t>(INT32_MAX))
           return tree::fail(TREE_ERR_SHAPE, "tree_pack_plan: more than 2^31-1 packed rows");
         c = static_cast<int32_t>(p.tok.size());
@@ -75,9 +91,12 @@ int build(tree_plan& p) {
           p.last_child[node] = c;
           ++p.n_child[node];
         }
-        child.emplace(edge_key(node, tk), c);
-      } else {
-        c = it->second;
+        const int64_t f = fanout(node);
+        if (f == kScan + 1) {  // the node just became wide: index all its children
+          for (int32_t s = kids_of(node); s >= 0; s = p.next_sibling[s]) wide.emplace(edge_key(node, p.tok[s]), s);
+        } else if (f > kScan + 1) {
+          wide.emplace(edge_key(node, tk), c);
+        }
       }
       ++p.through[c];
       p.token_node[t] = c;
