@@ -327,6 +327,29 @@ int tree_attn_bwd_gateway(const void* q, const void* k, const void* v, const voi
                           size_t workspace_bytes, tree_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* Gated DeltaNet with tree state routing (forward)                          */
+/* ------------------------------------------------------------------------ */
+/*
+ * [TT] §3.2 "SSM Layers (GDN)", eq. 10, Appendix A.2: a GDN layer's recurrent state
+ * is routed along the tree -- each node (chunk) starts from its parent node's end
+ * state, a root node from zero -- so every row gets the state of an independent
+ * per-branch pass. Per head, with state S [Dv, Dk]:
+ *   S_t = exp(g_t) S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,   o_t = S_t q_t.
+ * q, k: device [T, H, Dk]; v, o: device [T, H, Dv] (dtype); g (log decay), beta:
+ * device fp32 [T, H]; q and k are used as given (normalising k or scaling q is the
+ * caller's). node_start / node_end (inclusive) / node_parent: device int32
+ * [n_nodes] from tree_pack_emit (nodes in preorder tiling [0, T), parents earlier; a
+ * violation sets the device error word and leaves o unwritten). Dk, Dv <= 128.
+ * fp32 arithmetic. workspace: device, >= tree_gdn_workspace_size() bytes, 256-byte
+ * aligned (sub-chunk table, flags, and every 64-row sub-chunk's end state).
+ */
+size_t tree_gdn_workspace_size(int64_t T, int64_t n_nodes, int H, int Dk, int Dv);
+int tree_gdn_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                 void* o, const int32_t* node_start, const int32_t* node_end,
+                 const int32_t* node_parent, int64_t T, int64_t n_nodes, int H, int Dk, int Dv,
+                 int dtype, void* workspace, size_t workspace_bytes, tree_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* Tree-correct causal depthwise conv1d (short convolution of SSM layers)    */
 /* ------------------------------------------------------------------------ */
 /*

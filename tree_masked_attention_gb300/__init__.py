@@ -18,6 +18,7 @@ Functions (same names as the C ABI):
   tree_attn_fwd_gateway(q, k, v, attn_bias, subtree_end) -> (o, lse)
   tree_attn_bwd_gateway(q, k, v, o, dout, lse, attn_bias, subtree_end, dk_past, dv_past)
                                                     -> (dq, dk, dv, dk_past, dv_past)
+  tree_gdn_fwd(q, k, v, g, beta, node_start, node_end, node_parent) -> o
   tree_conv1d_fwd(x, w, parent_row, bias)           -> y
   tree_conv1d_bwd(x, w, dy, subtree_end, position_ids) -> (dx, dw, dbias)
 """
@@ -33,7 +34,7 @@ __all__ = [
     "tree_pack", "tree_validate_subtree_end", "tree_rope", "tree_attn_workspace_size",
     "tree_attn_fwd", "tree_attn_bwd", "tree_attn_bwd_rope", "tree_kernel_timing", "tree_kernel_last_ms", "tree_logprob_workspace_size", "tree_logprob_fwd", "tree_policy_loss",
     "tree_conv1d_fwd", "tree_conv1d_bwd", "tree_conv1d_workspace_size", "tree_attn_fwd_gateway",
-    "tree_attn_bwd_gateway", "tree_attn_gateway_workspace_size",
+    "tree_attn_bwd_gateway", "tree_attn_gateway_workspace_size", "tree_gdn_fwd", "tree_gdn_workspace_size",
     "tree_logprob_bwd", "tree_check_device_status", "tree_kernel_path", "tree_launch_count", "TreeError", "lib",
     "DTYPE_F32", "DTYPE_BF16",
 ]
@@ -313,6 +314,28 @@ def tree_attn_bwd_gateway(q, k, v, o, dout, lse, attn_bias, subtree_end, dk_past
                                       P, T, Hq, Hkv, d, dt, float(softmax_scale), C.c_void_p(ws.data_ptr()),
                                       ws.numel() * ws.element_size(), _stream(q)), "tree_attn_bwd_gateway")
     return dq, dk, dv, dk_past, dv_past
+
+
+def tree_gdn_workspace_size(T, n_nodes, H, Dk, Dv) -> int:
+    return int(lib().tree_gdn_workspace_size(T, n_nodes, H, Dk, Dv))
+
+
+def tree_gdn_fwd(q, k, v, g, beta, node_start, node_end, node_parent, workspace=None, out=None):
+    """Gated DeltaNet forward with tree state routing: q, k [T,H,Dk]; v [T,H,Dv]; g, beta
+    fp32 [T,H]; node arrays int32 [n_nodes]. Returns o [T,H,Dv] in q's dtype."""
+    torch = _torch()
+    T, H, Dk = q.shape
+    Dv = v.shape[2]
+    n_nodes = node_start.shape[0]
+    o = torch.empty((T, H, Dv), dtype=q.dtype, device=q.device) if out is None else out
+    f32, i32 = torch.float32, torch.int32
+    ws = _workspace(tree_gdn_workspace_size(T, n_nodes, H, Dk, Dv), q.device, workspace)
+    check(lib().tree_gdn_fwd(_dev(q, "q"), _dev(k, "k", q.dtype), _dev(v, "v", q.dtype), _dev(g, "g", f32),
+                             _dev(beta, "beta", f32), _dev(o, "o", q.dtype), _dev(node_start, "node_start", i32),
+                             _dev(node_end, "node_end", i32), _dev(node_parent, "node_parent", i32), T, n_nodes,
+                             H, Dk, Dv, _dtype_code(q), C.c_void_p(ws.data_ptr()), ws.numel() * ws.element_size(),
+                             _stream(q)), "tree_gdn_fwd")
+    return o
 
 
 def tree_conv1d_fwd(x, w, parent_row, bias=None, out=None):

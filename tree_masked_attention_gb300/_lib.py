@@ -62,6 +62,9 @@ SIGNATURES = {
                                      _vp, _sz, _vp]),
     "tree_attn_bwd_gateway": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64,
                                      _int, _int, _int, _int, _f, _vp, _sz, _vp]),
+    "tree_gdn_workspace_size": (_sz, [_i64, _i64, _int, _int, _int]),
+    "tree_gdn_fwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _int, _int, _int, _int, _vp,
+                            _sz, _vp]),
     "tree_conv1d_fwd": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _int, _int, _int, _vp]),
     "tree_conv1d_workspace_size": (_sz, [_i64, _int, _int]),
     "tree_conv1d_bwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _int, _int, _int, _vp, _sz,
