@@ -59,6 +59,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-conv", action="store_true")
     ap.add_argument("--gateway-steps", type=int, default=5)
     ap.add_argument("--no-gateway", action="store_true")
+    ap.add_argument("--gdn-steps", type=int, default=5)
+    ap.add_argument("--no-gdn", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of graph replays")
@@ -415,6 +417,8 @@ def run_ours(args):
         out["conv1d"] = run_conv1d(args, dev, peaks, peak_src, flush)
     if not args.no_gateway and rank == 0:
         out["gateway"] = run_gateway(args, dev, peaks, peak_src, flush)
+    if not args.no_gdn and rank == 0:
+        out["gdn"] = run_gdn(args, dev, flush)
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(args.workload, tree, (qh, kh, vh, doh), P, budget_s=25.0)
@@ -647,6 +651,51 @@ def run_gateway(args, dev, peaks, peak_src, flush):
         "step": "tree_attn_fwd_gateway for every child, then tree_attn_bwd_gateway for every child "
                 "(prompt dK / dV summed in fp32); L2 flushed before each step",
         "data": "synthetic (the long-prompt agentic configuration's seeded Q, K, V, dO)",
+    }
+
+
+def run_gdn(args, dev, flush):
+    """Gated DeltaNet forward with tree state routing on the 16384-row Galton-Watson tree:
+    16 heads, Dk = Dv = 128, bf16 q / k / v, fp32 gates. Reported as packed tokens/s and
+    as the recurrence's own arithmetic (3 products of the [Dv, Dk] state per token and head:
+    S k, the rank-1 update, S q)."""
+    import torch
+    import tree_masked_attention_gb300 as tma
+    tree = synth.galton_watson()
+    pk = tma.tree_pack(tree.seqs)
+    T, H, D = pk["T"], 16, 128
+    g = torch.Generator(device=dev)
+    g.manual_seed(11)
+    q = (torch.randn((T, H, D), generator=g, device=dev) / D ** 0.5).to(torch.bfloat16)
+    k = torch.nn.functional.normalize(torch.randn((T, H, D), generator=g, device=dev), dim=-1).to(torch.bfloat16)
+    v = torch.randn((T, H, D), generator=g, device=dev).to(torch.bfloat16)
+    gate = -0.2 * torch.rand((T, H), generator=g, device=dev)
+    beta = torch.rand((T, H), generator=g, device=dev)
+    ns, ne, npar = (torch.from_numpy(pk[n]).to(dev) for n in ("node_start", "node_end", "node_parent"))
+    ws = torch.empty(tma.tree_gdn_workspace_size(T, len(pk["node_start"]), H, D, D), dtype=torch.uint8, device=dev)
+    o = torch.empty_like(v)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(2):
+        tma.tree_gdn_fwd(q, k, v, gate, beta, ns, ne, npar, workspace=ws, out=o)
+    torch.cuda.synchronize()
+    n = max(args.gdn_steps, 1)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+    for s in range(n):
+        flush.zero_()
+        evs[s][0].record(stream)
+        tma.tree_gdn_fwd(q, k, v, gate, beta, ns, ne, npar, workspace=ws, out=o)
+        evs[s][1].record(stream)
+    torch.cuda.synchronize()
+    tma.tree_check_device_status()
+    ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
+    fl = 6.0 * D * D * H * T
+    return {
+        "workload": f"gdn: Galton-Watson tree of {T} rows ({len(pk['node_start'])} nodes), {H} heads, Dk = Dv = {D}, "
+                    "bf16 q/k/v, fp32 gates; forward only",
+        "value": round(T / (ms / 1e3), 1), "unit": "packed tokens/s", "ms": round(ms, 4), "steps": n,
+        "recurrence_tflops": round(fl / (ms / 1e3) / 1e12, 3),
+        "kernel": "gdn_fwd_kernel (fp32 CUDA cores, one CTA per SM, 64-row sub-chunks)",
+        "data": "synthetic (seeded torch generator on device)",
     }
 
 
