@@ -15,10 +15,11 @@
 // which is the recurrence solved for the whole sub-chunk at once (the delta-rule
 // corrections u depend on each other only through the lower-triangular A).
 // The sub-chunk's h0 is the end state of its predecessor: the previous sub-chunk of the
-// same node, or the parent node's last sub-chunk (eq. 10). Items are handed out in
-// preorder from a counter; a predecessor always has a smaller index, so it was taken
-// earlier by a CTA that is running or done, and the bounded wait for its published end
-// state terminates. Sibling subtrees proceed in parallel.
+// same node, or the parent node's last sub-chunk (eq. 10). Items are handed out from a
+// counter in order of chain depth (a sub-chunk's depth is its predecessor's plus one), so
+// all sub-chunks of one depth -- siblings and other branches -- run together, and a
+// predecessor always comes earlier: it was taken by a CTA that is running or done, and
+// the bounded wait for its published end state terminates.
 //
 // One CTA (256 threads) per SM holds the sub-chunk's K, Q, V rows, the state, A and P in
 // ~197 KB of shared memory; arithmetic is fp32 on the CUDA cores (a first version: the
@@ -53,7 +54,8 @@ struct GdnParams {
   const float* beta;
   void* o;
   int T, H, Dk, Dv;
-  const int4* chunks;  // {first row, rows, predecessor sub-chunk or -1, node}
+  const int4* chunks;  // {first row, rows, predecessor sub-chunk or -1, chain depth}
+  const int* order;    // sub-chunks by increasing chain depth
   const int* n_chunks;
   int* counter;
   int* flags;          // [max_chunks * H] 1 once the end state is published
@@ -75,13 +77,16 @@ __device__ __forceinline__ void st_release(int* p, int v) {
 }
 
 // Sub-chunk table from the node arrays (one thread walks the nodes in preorder, checking
-// that they tile [0, T) with earlier parents); all threads clear the flags and counter.
+// that they tile [0, T) with earlier parents), then the schedule: sub-chunks by
+// increasing chain depth (a counting sort, stable in preorder); all threads clear the
+// flags and counter.
 __global__ void __launch_bounds__(1024) gdn_setup_kernel(const int32_t* __restrict__ node_start,
                                                          const int32_t* __restrict__ node_end,
                                                          const int32_t* __restrict__ node_parent, int n_nodes,
                                                          int T, int H, int max_chunks, int4* chunks,
-                                                         int* node_last, int* n_chunks, int* counter, int* flags,
-                                                         int* abort, int* err) {
+                                                         int* node_last, int* order, int* depth_count,
+                                                         int* n_chunks, int* counter, int* flags, int* abort,
+                                                         int* err) {
   for (int64_t i = threadIdx.x; i < static_cast<int64_t>(max_chunks) * H; i += blockDim.x) flags[i] = 0;
   if (threadIdx.x != 0) return;
   *counter = 0;
@@ -98,7 +103,8 @@ __global__ void __launch_bounds__(1024) gdn_setup_kernel(const int32_t* __restri
     int pred = par >= 0 ? node_last[par] : -1;
     for (int c0 = s; c0 < e; c0 += kChunk) {
       if (m >= max_chunks) { ok = false; break; }
-      chunks[m] = make_int4(c0, min(kChunk, e - c0), pred, n);
+      const int depth = pred >= 0 ? chunks[pred].w + 1 : 0;
+      chunks[m] = make_int4(c0, min(kChunk, e - c0), pred, depth);
       pred = m++;
     }
     node_last[n] = pred;
@@ -107,6 +113,11 @@ __global__ void __launch_bounds__(1024) gdn_setup_kernel(const int32_t* __restri
     raise_error(err, TREE_ERR_DEVICE_CHECK);
     m = 0;
   }
+  // counting sort by chain depth (depths are < m)
+  for (int d = 0; d <= m; ++d) depth_count[d] = 0;
+  for (int c = 0; c < m; ++c) ++depth_count[chunks[c].w + 1];
+  for (int d = 1; d <= m; ++d) depth_count[d] += depth_count[d - 1];
+  for (int c = 0; c < m; ++c) order[depth_count[chunks[c].w]++] = c;
   *n_chunks = m;
 }
 
@@ -138,7 +149,7 @@ __global__ void __launch_bounds__(kGdnThreads, 1) gdn_fwd_kernel(const GdnParams
     __syncthreads();
     const int item = s_item;
     if (item >= items) break;
-    const int c = item / H, h = item % H;
+    const int c = p.order[item / H], h = item % H;
     const int4 ck = p.chunks[c];
     const int r0 = ck.x, L = ck.y, pred = ck.z;
     // wait until the predecessor's end state is published (bounded)
@@ -282,6 +293,8 @@ int64_t gdn_max_chunks(int64_t T, int64_t n_nodes) { return n_nodes + T / kChunk
 struct GdnWs {
   int4* chunks;
   int* node_last;
+  int* order;
+  int* depth_count;
   int* n_chunks;
   int* counter;
   int* abort;
@@ -301,6 +314,8 @@ size_t gdn_ws_layout(int64_t T, int64_t n_nodes, int H, int Dk, int Dv, void* ba
   GdnWs x{};
   x.chunks = static_cast<int4*>(take(sizeof(int4) * mc));
   x.node_last = static_cast<int*>(take(sizeof(int) * std::max<int64_t>(n_nodes, 1)));
+  x.order = static_cast<int*>(take(sizeof(int) * mc));
+  x.depth_count = static_cast<int*>(take(sizeof(int) * (mc + 1)));
   x.n_chunks = static_cast<int*>(take(sizeof(int)));
   x.counter = static_cast<int*>(take(sizeof(int)));
   x.abort = static_cast<int*>(take(sizeof(int)));
@@ -368,12 +383,13 @@ extern "C" int tree_gdn_fwd(const void* q, const void* k, const void* v, const f
   const int64_t mc = gdn_max_chunks(T, n_nodes);
   gdn_setup_kernel<<<1, 1024, 0, st>>>(node_start, node_end, node_parent, static_cast<int>(n_nodes),
                                        static_cast<int>(T), H, static_cast<int>(mc), w.chunks, w.node_last,
-                                       w.n_chunks, w.counter, w.flags, w.abort, device_error_word());
+                                       w.order, w.depth_count, w.n_chunks, w.counter, w.flags, w.abort,
+                                       device_error_word());
   TREE_LAUNCH_CHECK("gdn_setup_kernel");
   GdnParams p{};
   p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.o = o;
   p.T = static_cast<int>(T); p.H = H; p.Dk = Dk; p.Dv = Dv;
-  p.chunks = w.chunks; p.n_chunks = w.n_chunks; p.counter = w.counter; p.flags = w.flags; p.abort = w.abort;
+  p.chunks = w.chunks; p.order = w.order; p.n_chunks = w.n_chunks; p.counter = w.counter; p.flags = w.flags; p.abort = w.abort;
   p.states = w.states; p.err = device_error_word();
   if (dtype == TREE_DTYPE_BF16) return launch_gdn<__nv_bfloat16>(p, st);
   return launch_gdn<float>(p, st);
