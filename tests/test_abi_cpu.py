@@ -129,3 +129,32 @@ def test_conv1d_rejects_bad_sizes(tma):
     # one fp32 partial of dw (K) and dbias (1) per row group: 38 groups of 432 rows here
     assert L.tree_conv1d_workspace_size(16384, 8192, 4) == 38 * 5 * 8192 * 4
     assert L.tree_conv1d_workspace_size(16, 16, 9) == 0
+
+
+def test_gateway_and_gdn_reject_bad_arguments(tma):
+    """Host-side checks of the gateway and GDN calls run before any device work."""
+    L = tma.lib()
+    # gateway: tensor-core kernels only (bf16, d = 128, even group), T >= 1, past_len >= 0
+    assert L.tree_attn_fwd_gateway(None, None, None, None, None, None, None, 10, 16, 4, 2, 64, 1, 0.0,
+                                   None, 0, None) == 2
+    assert L.tree_attn_fwd_gateway(None, None, None, None, None, None, None, 10, 16, 4, 2, 128, 0, 0.0,
+                                   None, 0, None) == 3
+    assert L.tree_attn_fwd_gateway(None, None, None, None, None, None, None, -1, 16, 4, 2, 128, 1, 0.0,
+                                   None, 0, None) == 2
+    assert L.tree_attn_fwd_gateway(None, None, None, None, None, None, None, 10, 16, 4, 2, 128, 1, 0.0,
+                                   None, 0, None) == 1
+    assert L.tree_attn_bwd_gateway(None, None, None, None, None, None, None, None, None, None, None, None,
+                                   None, 10, 0, 4, 2, 128, 1, 0.0, None, 0, None) == 2
+    assert L.tree_attn_gateway_workspace_size(100, 200, 4, 2, 128, 1) == L.tree_attn_workspace_size(300, 4, 2, 128, 1)
+    # GDN: Dk, Dv <= 128, nodes for the rows, dtype
+    assert L.tree_gdn_fwd(None, None, None, None, None, None, None, None, None, 64, 4, 2, 256, 64, 1,
+                          None, 0, None) == 2
+    assert L.tree_gdn_fwd(None, None, None, None, None, None, None, None, None, 64, 4, 2, 64, 64, 9,
+                          None, 0, None) == 3
+    assert L.tree_gdn_fwd(None, None, None, None, None, None, None, None, None, 64, 0, 2, 64, 64, 1,
+                          None, 0, None) == 2
+    assert L.tree_gdn_fwd(None, None, None, None, None, None, None, None, None, 64, 4, 2, 64, 64, 1,
+                          None, 0, None) == 1
+    # workspace: sub-chunk table, schedule and one 64-row sub-chunk end state per (sub-chunk, head)
+    ws = L.tree_gdn_workspace_size(16384, 55, 16, 128, 128)
+    assert ws >= (55 + 16384 // 64 + 1) * 16 * 128 * 128 * 4
