@@ -147,3 +147,107 @@ def test_backward_tree_equals_sum_over_branches():
             sbm = {"v": (q, k, xm, g, beta), "g": (q, k, v, xm, beta), "beta": (q, k, v, g, xm)}[name]
             fd = ((do * _chunked_tree(*sub, ref)).sum() - (do * _chunked_tree(*sbm, ref)).sum()) / (2 * eps)
             assert fd == pytest.approx(gx[idx], abs=1e-6, rel=1e-5), (name, idx)
+
+
+def _chunked_tree_bwd(q, k, v, g, beta, do, ref):
+    """Reverse-mode of the per-node chunked solution (_chunked_tree), node by node from
+    the leaves up: a node's end-state gradient is the sum of its children's start-state
+    gradients (siblings share their parent's end state), and within the node
+        u = M^{-1} r,  r = beta (V - E (K h0)),  O = E (Q h0) + P u,
+        h_end = E_{L-1} h0 + sum_s (E_{L-1}/E_s) k_s u_s^T,   E = exp(cumsum g),
+    are differentiated through the triangular solve (dr = M^{-T} du, dM = -dr u^T)."""
+    T, H, Dk = q.shape
+    Dv = v.shape[2]
+    n_nodes = len(ref["node_start"])
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    dg, dbeta = np.zeros_like(g), np.zeros_like(beta)
+    # forward pass once, keeping every node's start state
+    start = {}
+    end_state = {}
+    for n in range(n_nodes):
+        s0, s1 = int(ref["node_start"][n]), int(ref["node_end"][n]) + 1
+        par = int(ref["node_parent"][n])
+        for h in range(H):
+            h0 = end_state[(par, h)] if par >= 0 else np.zeros((Dk, Dv))
+            start[(n, h)] = h0
+            K, V = k[s0:s1, h], v[s0:s1, h]
+            lg = np.cumsum(g[s0:s1, h])
+            E, b = np.exp(lg), beta[s0:s1, h]
+            f = np.exp(lg[:, None] - lg[None, :])
+            M = np.eye(s1 - s0) + np.tril(b[:, None] * f * (K @ K.T), -1)
+            u = np.linalg.solve(M, b[:, None] * (V - E[:, None] * (K @ h0)))
+            end_state[(n, h)] = E[-1] * h0 + (K * np.exp(lg[-1] - lg)[:, None]).T @ u
+    dh_end = {(n, h): np.zeros((Dk, Dv)) for n in range(n_nodes) for h in range(H)}
+    for n in range(n_nodes - 1, -1, -1):          # children come after their parent in preorder
+        s0, s1 = int(ref["node_start"][n]), int(ref["node_end"][n]) + 1
+        par = int(ref["node_parent"][n])
+        L = s1 - s0
+        for h in range(H):
+            h0, dhe = start[(n, h)], dh_end[(n, h)]
+            K, Q, V, dO = k[s0:s1, h], q[s0:s1, h], v[s0:s1, h], do[s0:s1, h]
+            lg = np.cumsum(g[s0:s1, h])
+            E, b = np.exp(lg), beta[s0:s1, h]
+            f = np.exp(lg[:, None] - lg[None, :])
+            low, strict = np.tril(np.ones((L, L))), np.tril(np.ones((L, L)), -1)
+            KK, QK = K @ K.T, Q @ K.T
+            A = strict * b[:, None] * f * KK
+            P = low * f * QK
+            kh, qh = K @ h0, Q @ h0
+            r = b[:, None] * (V - E[:, None] * kh)
+            u = np.linalg.solve(np.eye(L) + A, r)
+            w = np.exp(lg[-1] - lg)
+            dK, dQ, dlg = np.zeros_like(K), np.zeros_like(Q), np.zeros(L)
+            dh0 = E[-1] * dhe
+            dlg[-1] += E[-1] * np.sum(dhe * h0)
+            # h_end = ... + sum_s w_s k_s u_s^T
+            du = w[:, None] * (K @ dhe)
+            dK += w[:, None] * (u @ dhe.T)
+            dw = np.sum((K @ dhe) * u, axis=1) * w
+            dlg[-1] += dw.sum()
+            dlg -= dw
+            # O = E qh + P u
+            dqh = E[:, None] * dO
+            dh0 += Q.T @ dqh
+            dQ += dqh @ h0.T
+            dlg += E * np.sum(dO * qh, axis=1)
+            du += P.T @ dO
+            dP = low * (dO @ u.T)
+            dQ += (dP * f) @ K
+            dK += (dP * f).T @ Q
+            dlg += np.sum(dP * P, axis=1) - np.sum(dP * P, axis=0)
+            # u = M^{-1} r
+            dr = np.linalg.solve((np.eye(L) + A).T, du)
+            dA = -strict * (dr @ u.T)
+            dbeta[s0:s1, h] += np.sum(dA * f * KK, axis=1)
+            dK += (dA * b[:, None] * f) @ K + (dA * b[:, None] * f).T @ K
+            dlg += np.sum(dA * A, axis=1) - np.sum(dA * A, axis=0)
+            # r = beta (V - E kh)
+            dbeta[s0:s1, h] += np.sum(dr * (V - E[:, None] * kh), axis=1)
+            dv[s0:s1, h] += b[:, None] * dr
+            dkh = -(b * E)[:, None] * dr
+            dh0 += K.T @ dkh
+            dK += dkh @ h0.T
+            dlg += -b * E * np.sum(dr * kh, axis=1)
+            dg[s0:s1, h] += np.cumsum(dlg[::-1])[::-1]
+            dq[s0:s1, h] += dQ
+            dk[s0:s1, h] += dK
+            if par >= 0:
+                dh_end[(par, h)] += dh0
+    return dq, dk, dv, dg, dbeta
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_backward_matches_chunked_reverse_mode(seed):
+    """The oracle's token-by-token reverse pass against the reverse mode of the per-node
+    chunked solution (a triangular solve per node, end-state gradients summed over the
+    children): two independent computations of the same gradients."""
+    r = np.random.default_rng(40 + seed)
+    seqs = synth.random_sequences(r, 9, 20, vocab=3, min_len=2)
+    ref = oracle.pack_ref(seqs)
+    T = ref["T"]
+    q, k, v, g, beta = _inputs(T, seed=40 + seed)
+    do = r.normal(size=(T, q.shape[1], v.shape[2]))
+    want = _chunked_tree_bwd(q, k, v, g, beta, do, ref)
+    got = oracle.gdn_ref_bwd(q, k, v, g, beta, do, ref["paths"])
+    for name, a, b in zip(("dq", "dk", "dv", "dg", "dbeta"), got, want):
+        assert np.allclose(a, b, atol=1e-9), (name, float(np.abs(a - b).max()))
