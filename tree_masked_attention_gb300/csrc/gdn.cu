@@ -370,6 +370,9 @@ extern "C" int tree_gdn_fwd(const void* q, const void* k, const void* v, const f
     return fail(TREE_ERR_SHAPE, "tree_gdn_fwd: H = %d, Dk = %d, Dv = %d (need Dk, Dv <= %d)", H, Dk, Dv, kMaxD);
   if (T == 0) return TREE_OK;
   if (n_nodes < 1) return fail(TREE_ERR_SHAPE, "tree_gdn_fwd: no nodes for %lld rows", (long long)T);
+  if (gdn_max_chunks(T, n_nodes) * H > INT32_MAX)  // work items are counted in 32 bits
+    return fail(TREE_ERR_SHAPE, "tree_gdn_fwd: %lld sub-chunks x %d heads exceed 2^31 work items",
+                (long long)gdn_max_chunks(T, n_nodes), H);
   if (!q || !k || !v || !g || !beta || !o || !node_start || !node_end || !node_parent)
     return fail(TREE_ERR_INVALID_ARG, "tree_gdn_fwd: null pointer");
   const size_t need = gdn_ws_layout(T, n_nodes, H, Dk, Dv, nullptr, nullptr);
