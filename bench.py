@@ -51,8 +51,11 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="agentic_short",
+    ap.add_argument("--workload", default="agentic_long",
                     choices=["agentic_short", "agentic_long", "galton_watson", "tiny_fp32"])
+    ap.add_argument("--secondary-steps", type=int, default=20,
+                    help="timed steps of each tree that is not the headline workload")
+    ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--lm-steps", type=int, default=3)
     ap.add_argument("--no-lm", action="store_true")
     ap.add_argument("--conv-steps", type=int, default=10)
@@ -222,124 +225,121 @@ def attn_flops(P, Hq, d):
 
 
 # ----------------------------------------------------------------------------- our arm
-def run_ours(args):
-    import torch
-    import tree_masked_attention_gb300 as tma
-    from tree_masked_attention_gb300 import build as _b
-    _b.build()
+class AttnStep:
+    """One packed tree's attention step on the device: RoPE, forward, backward with the
+    inverse rotation fused. Holds the tree, its host (pinned) and device tensors."""
 
-    rank, world, local = dist_env()
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
+    def __init__(self, tma, name: str, seed: int, dev):
+        import torch
+        self.tma, self.name, self.dev = tma, name, dev
+        self.tree, c = attention_workload(name, seed)
+        self.c = c
+        pk = tma.tree_pack(self.tree.seqs)
+        self.T, self.Hq, self.Hkv, self.d = pk["T"], c["Hq"], c["Hkv"], c["d"]
+        self.P = int((pk["position_ids"].astype(np.int64) + 1).sum())
+        self.n_tokens = sum(len(s) for s in self.tree.seqs)
+        self.f_fwd, self.f_bwd = attn_flops(self.P, self.Hq, self.d)
+        self.td = torch.bfloat16 if c["dtype"] == "bf16" else torch.float32
+        self.host = synth.attention_config(name, self.T, seed=seed)
+        pin = lambda a: torch.from_numpy(a).to(self.td).pin_memory()
+        self.hq, self.hk, self.hv, self.hdo = (pin(a) for a in self.host)
+        self.q, self.k, self.v, self.do = (x.to(dev) for x in (self.hq, self.hk, self.hv, self.hdo))
+        self.pos = torch.from_numpy(pk["position_ids"]).to(dev)
+        self.end = torch.from_numpy(pk["subtree_end"]).to(dev)
+        self.o = torch.empty_like(self.q)
+        self.lse = torch.empty((self.Hq, self.T), dtype=torch.float32, device=dev)
+        self.dq, self.dk, self.dv = (torch.empty_like(x) for x in (self.q, self.k, self.v))
+        self.dcode = 1 if self.td == torch.bfloat16 else 0
+        self.ws = torch.empty(tma.tree_attn_workspace_size(self.T, self.Hq, self.Hkv, self.d, self.dcode),
+                              dtype=torch.uint8, device=dev)
+        self.stream = torch.cuda.current_stream(dev)
 
-    tree, c = attention_workload(args.workload, rank_seed(rank))
-    pk = tma.tree_pack(tree.seqs)
-    T, Hq, Hkv, d = pk["T"], c["Hq"], c["Hkv"], c["d"]
-    P = int((pk["position_ids"].astype(np.int64) + 1).sum())
-    n_tokens = sum(len(s) for s in tree.seqs)
-    f_fwd, f_bwd = attn_flops(P, Hq, d)
-    td = torch.bfloat16 if c["dtype"] == "bf16" else torch.float32
-    qh, kh, vh, doh = synth.attention_config(args.workload, T, seed=rank_seed(rank))
-    pin = lambda a: torch.from_numpy(a).to(td).pin_memory()
-    hq, hk, hv, hdo = pin(qh), pin(kh), pin(vh), pin(doh)
-    q, k, v, do = (x.to(dev) for x in (hq, hk, hv, hdo))
-    pos = torch.from_numpy(pk["position_ids"]).to(dev)
-    end = torch.from_numpy(pk["subtree_end"]).to(dev)
-    o = torch.empty_like(q)
-    lse = torch.empty((Hq, T), dtype=torch.float32, device=dev)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ws = torch.empty(tma.tree_attn_workspace_size(T, Hq, Hkv, d, 1 if td == torch.bfloat16 else 0),
-                     dtype=torch.uint8, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
-
-    def step(ev=None):
-        if ev: ev[0].record(stream)
-        tma.tree_rope(q, k, pos)
-        if ev: ev[1].record(stream)
-        tma.tree_attn_fwd(q, k, v, end, workspace=ws, out=o, lse=lse)
-        if ev: ev[2].record(stream)
+    def step(self, ev=None):
+        tma, s = self.tma, self.stream
+        if ev: ev[0].record(s)
+        tma.tree_rope(self.q, self.k, self.pos)
+        if ev: ev[1].record(s)
+        tma.tree_attn_fwd(self.q, self.k, self.v, self.end, workspace=self.ws, out=self.o, lse=self.lse)
+        if ev: ev[2].record(s)
         # backward with the inverse rotation of dq, dk fused into the kernel that writes them
-        tma.tree_attn_bwd_rope(q, k, v, o, do, lse, end, pos, workspace=ws, grads=(dq, dk, dv))
-        if ev: ev[3].record(stream)
+        tma.tree_attn_bwd_rope(self.q, self.k, self.v, self.o, self.do, self.lse, self.end, self.pos,
+                               workspace=self.ws, grads=(self.dq, self.dk, self.dv))
+        if ev: ev[3].record(s)
 
-    clocks = ClockSampler(local).start()
-    for _ in range(max(args.warmup, 0)):
-        flush.zero_()
-        step()
-    torch.cuda.synchronize()
-    tma.tree_check_device_status()
+    def describe(self):
+        return describe(self.name, self.T, self.P, len(self.tree.seqs), self.n_tokens, self.c)
 
-    K = args.steps
-    # Per-call split: K eager steps with CUDA events between the calls, on the launching
-    # stream (these give the roofline's per-kernel-call durations).
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
-    barrier(world)
-    torch.cuda.synchronize()
-    n0 = tma.tree_launch_count()
-    # the library also brackets each call's main kernel with events (read after each step)
-    tma.tree_kernel_timing(True)
-    main_ms = []
-    for s in range(K):
-        flush.zero_()
-        step(evs[s])
-        main_ms.append((tma.tree_kernel_last_ms(0), tma.tree_kernel_last_ms(1)))
-    tma.tree_kernel_timing(False)
-    torch.cuda.synchronize()
-    launches_per_step = (tma.tree_launch_count() - n0) / K
-    op_ms = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(3)] for e in evs])  # [K, 3]
-    graph = None
-    if not args.no_graph:
-        # The step's launches captured once into a CUDA graph (static shapes and buffers),
-        # then replayed: the headline times K replays.
-        side = torch.cuda.Stream(dev)
-        side.wait_stream(stream)
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=side):
-            step()
-        stream.wait_stream(side)
-        for _ in range(2):
+    def measure(self, K: int, warmup: int, flush, use_graph: bool, world: int = 1, clocks=None):
+        """Warm-up, K eager steps with per-call events (the per-kernel split), then K timed
+        steps (CUDA-graph replays unless use_graph is false), L2 flushed before each."""
+        import torch
+        tma, stream = self.tma, self.stream
+        for _ in range(max(warmup, 0)):
             flush.zero_()
-            graph.replay()
+            self.step()
         torch.cuda.synchronize()
-    gev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
-    barrier(world)
-    torch.cuda.synchronize()
-    w0 = time.perf_counter()
-    for s in range(K):
-        flush.zero_()
-        gev[s][0].record(stream)
-        if graph is not None:
-            graph.replay()
-        else:
-            step()
-        gev[s][1].record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    w1 = time.perf_counter()
-    wall = w1 - w0
-    launches = int(round(launches_per_step * K))
-    clk = clocks.stop(w0, w1)
-    tma.tree_check_device_status()
-    step_ms = np.array([e[0].elapsed_time(e[1]) for e in gev])
-    total_s = reduce_max(float(step_ms.sum()) / 1e3, world)
-    flops_step = f_fwd + f_bwd
-    value = flops_step * K * world / total_s / 1e12
-    peaks, peak_src = load_peaks()
-    peak = float(peaks["bf16_tflops"])
+        tma.tree_check_device_status()
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+        barrier(world)
+        torch.cuda.synchronize()
+        n0 = tma.tree_launch_count()
+        # the library brackets each call's main kernel with events (read after each step)
+        tma.tree_kernel_timing(True)
+        main_ms = []
+        for s in range(K):
+            flush.zero_()
+            self.step(evs[s])
+            main_ms.append((tma.tree_kernel_last_ms(0), tma.tree_kernel_last_ms(1)))
+        tma.tree_kernel_timing(False)
+        torch.cuda.synchronize()
+        launches_per_step = (tma.tree_launch_count() - n0) / K
+        op_ms = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(3)] for e in evs])  # [K, 3]
+        graph = None
+        if use_graph:
+            # the step's launches captured once into a CUDA graph (static shapes and
+            # buffers), then replayed: the timed steps are K replays
+            side = torch.cuda.Stream(self.dev)
+            side.wait_stream(stream)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=side):
+                self.step()
+            stream.wait_stream(side)
+            for _ in range(2):
+                flush.zero_()
+                graph.replay()
+            torch.cuda.synchronize()
+        gev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+        barrier(world)
+        torch.cuda.synchronize()
+        w0 = time.perf_counter()
+        for s in range(K):
+            flush.zero_()
+            gev[s][0].record(stream)
+            if graph is not None:
+                graph.replay()
+            else:
+                self.step()
+            gev[s][1].record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        w1 = time.perf_counter()
+        clk = clocks.stop(w0, w1) if clocks is not None else None
+        tma.tree_check_device_status()
+        step_ms = np.array([e[0].elapsed_time(e[1]) for e in gev])
+        total_s = reduce_max(float(step_ms.sum()) / 1e3, world)
+        return {"total_s": total_s, "wall_s": w1 - w0, "op_ms": op_ms, "main_ms": np.array(main_ms),
+                "launches_per_step": launches_per_step, "graph": graph is not None, "clocks": clk}
 
-    # dominant kernel call: the op with the largest share of the step
-    names = ["tree_rope", "tree_attn_fwd", "tree_attn_bwd_rope"]
-    avg = op_ms.mean(axis=0)
-    dom = int(np.argmax(avg))
-    esize = 2 if td == torch.bfloat16 else 4
-    rope_bytes = 2.0 * (T * Hq * d + T * Hkv * d) * esize  # read and write q, k once
-    main = np.array(main_ms).mean(axis=0)  # [fwd, bwd] main-kernel ms (-1: not bracketed)
-    if dom in (1, 2):
-        fl = f_fwd if dom == 1 else f_bwd
+    def roofline(self, m, peak, peak_src):
+        """Roofline of the dominant kernel call (the backward on every bf16 tree), with the
+        main kernel's own duration from the library's event brackets."""
+        names = ["tree_rope", "tree_attn_fwd", "tree_attn_bwd_rope"]
+        avg = m["op_ms"].mean(axis=0)
+        main = m["main_ms"].mean(axis=0)  # [fwd, bwd] main-kernel ms (-1: not bracketed)
+        dom = int(np.argmax(avg))
+        if dom == 0:  # RoPE cannot dominate a bf16 tree; kept for completeness
+            dom = 2
+        fl = self.f_fwd if dom == 1 else self.f_bwd
         kms = float(main[dom - 1])
         timed_kernel = kms > 0
         dur = kms if timed_kernel else float(avg[dom])
@@ -347,53 +347,44 @@ def run_ours(args):
         kname = {1: "attn_fwd_tc_kernel", 2: "attn_bwd_tc_kernel"}[dom] if timed_kernel else names[dom]
         roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4), "of": peak_src, "kernel": kname,
-                "kernel_ms": round(dur, 4), "call": names[dom],
+                "kernel_ms": round(dur, 4), "kernel_flops": fl, "call": names[dom],
                 "call_achieved": round(fl / (avg[dom] / 1e3) / 1e12, 2)}
         key = {1: "attn_fwd", 2: "attn_bwd"}[dom]
-        roof["traffic"] = profiled_traffic(f"{key}:{args.workload}", kernel_sources(tma, key))
-    else:
-        achieved = rope_bytes / (avg[dom] / 1e3) / 1e9
-        hbm = float(peaks["hbm_gbs"])
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(achieved / hbm, 4), "of": peak_src, "kernel": names[dom], "traffic": None}
-    roof["per_call_ms"] = {n: round(float(x), 4) for n, x in zip(names, avg)}
-    roof["main_kernel_ms"] = {"attn_fwd_tc_kernel": round(float(main[0]), 4),
-                              "attn_bwd_tc_kernel": round(float(main[1]), 4)}
-    roof["kernel_family"] = {"attn_fwd": tma.tree_kernel_path(0, 1 if td == torch.bfloat16 else 0, d),
-                             "attn_bwd": tma.tree_kernel_path(1, 1 if td == torch.bfloat16 else 0, d)}
+        roof["traffic"] = profiled_traffic(f"{key}:{self.name}", kernel_sources(self.tma, key))
+        roof["per_call_ms"] = {n: round(float(x), 4) for n, x in zip(names, avg)}
+        roof["main_kernel_ms"] = {"attn_fwd_tc_kernel": round(float(main[0]), 4),
+                                  "attn_bwd_tc_kernel": round(float(main[1]), 4)}
+        if main[0] > 0:
+            fa = self.f_fwd / (main[0] / 1e3) / 1e12
+            roof["attn_fwd_tc_kernel"] = {"achieved": round(fa, 2), "frac": round(fa / peak, 4)}
+        if main[1] > 0:
+            ba = self.f_bwd / (main[1] / 1e3) / 1e12
+            roof["attn_bwd_tc_kernel"] = {"achieved": round(ba, 2), "frac": round(ba / peak, 4)}
+        roof["kernel_family"] = {"attn_fwd": self.tma.tree_kernel_path(0, self.dcode, self.d),
+                                 "attn_bwd": self.tma.tree_kernel_path(1, self.dcode, self.d)}
+        return roof
 
-    out = {
-        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
-        "warmup": args.warmup, "ms_per_step": round(total_s * 1e3 / K, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": c["dtype"], "data": "synthetic",
-        "config": describe(args.workload, T, P, len(tree.seqs), n_tokens, c),
-        "pct_bf16_peak": round(100.0 * value / (peak * world), 2),
-        "packed_tokens_per_s": round(T * K * world / total_s, 1),
-        "wall_s_timed_region": round(wall, 4),
-        "step_mode": "CUDA-graph replay of the device step" if graph is not None else "eager launches",
-        "gpu_launches": int(launches),
-        "gpu_launches_note": f"{launches_per_step:g} library kernels per step (counted on eager steps) x {K} steps",
-        "eager_ms_per_step": round(float(op_ms.sum(axis=1).mean()), 4),
-        "clocks": clk,
-        "roofline": roof,
-    }
-
-    # ---- e2e through the public API with host buffers (pack + H2D + step + D2H)
-    if not args.no_e2e:
-        hdq = torch.empty(dq.shape, dtype=td).pin_memory()
-        hdk = torch.empty(dk.shape, dtype=td).pin_memory()
-        hdv = torch.empty(dv.shape, dtype=td).pin_memory()
-        h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hdo)) + 2 * T * 4
+    def e2e(self, K: int, flush, world: int = 1):
+        """The same step through the public API with host buffers: tree_pack on the host,
+        pinned H2D of Q, K, V, dO, positions and subtree_end (non-blocking, one stream),
+        the step, D2H of dQ, dK, dV into pinned buffers."""
+        import torch
+        tma = self.tma
+        hdq, hdk, hdv = (torch.empty(x.shape, dtype=self.td).pin_memory() for x in (self.dq, self.dk, self.dv))
+        hpos = torch.empty(self.T, dtype=torch.int32).pin_memory()
+        hend = torch.empty(self.T, dtype=torch.int32).pin_memory()
+        h2d = sum(x.numel() * x.element_size() for x in (self.hq, self.hk, self.hv, self.hdo, hpos, hend))
         d2h = sum(x.numel() * x.element_size() for x in (hdq, hdk, hdv))
 
         def e2e_step():
-            p2 = tma.tree_pack(tree.seqs)
-            pos.copy_(torch.from_numpy(p2["position_ids"]), non_blocking=False)
-            end.copy_(torch.from_numpy(p2["subtree_end"]), non_blocking=False)
-            for dst, src in ((q, hq), (k, hk), (v, hv), (do, hdo)):
+            p2 = tma.tree_pack(self.tree.seqs)
+            hpos.numpy()[:] = p2["position_ids"]
+            hend.numpy()[:] = p2["subtree_end"]
+            for dst, src in ((self.pos, hpos), (self.end, hend), (self.q, self.hq), (self.k, self.hk),
+                             (self.v, self.hv), (self.do, self.hdo)):
                 dst.copy_(src, non_blocking=True)
-            step()
-            for dst, src in ((hdq, dq), (hdk, dk), (hdv, dv)):
+            self.step()
+            for dst, src in ((hdq, self.dq), (hdk, self.dk), (hdv, self.dv)):
                 dst.copy_(src, non_blocking=True)
             torch.cuda.synchronize()
 
@@ -406,10 +397,79 @@ def run_ours(args):
             e2e_step()
         torch.cuda.synchronize()
         e_s = reduce_max(time.perf_counter() - w0, world)
-        out["e2e"] = {"value": round(flops_step * K * world / e_s / 1e12, 3), "unit": "TFLOP/s",
-                      "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                      "includes": "tree_pack on host + pinned H2D of Q,K,V,dO,positions,subtree_end + "
-                                  "step + D2H of dQ,dK,dV; L2 flush write also inside"}
+        return {"value": round((self.f_fwd + self.f_bwd) * K * world / e_s / 1e12, 3), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "ms_per_step": round(e_s * 1e3 / K, 4),
+                "includes": "tree_pack on host + pinned non-blocking H2D of Q,K,V,dO,positions,subtree_end + "
+                            "step + D2H of dQ,dK,dV into pinned buffers; L2 flush write also inside"}
+
+
+def secondary_entry(leg: AttnStep, m, peak, peak_src):
+    """A smaller summary line for the trees that are not the headline workload."""
+    flops = leg.f_fwd + leg.f_bwd
+    K = len(m["op_ms"])
+    value = flops * K / m["total_s"] / 1e12
+    return {"config": leg.describe(), "value": round(value, 3), "unit": "TFLOP/s",
+            "ms_per_step": round(m["total_s"] * 1e3 / K, 4), "steps": K,
+            "pct_bf16_peak": round(100.0 * value / peak, 2),
+            "packed_tokens_per_s": round(leg.T * K / m["total_s"], 1),
+            "step_mode": "CUDA-graph replay of the device step" if m["graph"] else "eager launches",
+            "roofline": leg.roofline(m, peak, peak_src)}
+
+
+def run_ours(args):
+    import torch
+    import tree_masked_attention_gb300 as tma
+    from tree_masked_attention_gb300 import build as _b
+    _b.build()
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks, peak_src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    leg = AttnStep(tma, args.workload, rank_seed(rank), dev)
+    K = args.steps
+    clocks = ClockSampler(local).start()
+    m = leg.measure(K, args.warmup, flush, use_graph=not args.no_graph, world=world, clocks=clocks)
+    total_s = m["total_s"]
+    flops_step = leg.f_fwd + leg.f_bwd
+    value = flops_step * K * world / total_s / 1e12
+    launches = int(round(m["launches_per_step"] * K))
+    out = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(total_s * 1e3 / K, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": leg.c["dtype"], "data": "synthetic",
+        "config": leg.describe(),
+        "pct_bf16_peak": round(100.0 * value / (peak * world), 2),
+        "packed_tokens_per_s": round(leg.T * K * world / total_s, 1),
+        "wall_s_timed_region": round(m["wall_s"], 4),
+        "step_mode": "CUDA-graph replay of the device step" if m["graph"] else "eager launches",
+        "gpu_launches": int(launches),
+        "gpu_launches_note": f"{m['launches_per_step']:g} library kernels per step (counted on eager steps) x {K} steps",
+        "eager_ms_per_step": round(float(m["op_ms"].sum(axis=1).mean()), 4),
+        "clocks": m["clocks"],
+        "roofline": leg.roofline(m, peak, peak_src),
+    }
+    if not args.no_e2e:
+        out["e2e"] = leg.e2e(K, flush, world)
+
+    # the other bf16 trees, each with its own roofline (rank 0, one GPU's worth of work)
+    if rank == 0 and not args.no_secondary:
+        sec = {}
+        for name in ("galton_watson", "agentic_long", "agentic_short"):
+            if name == args.workload:
+                continue
+            other = AttnStep(tma, name, 0, dev)
+            m2 = other.measure(max(args.secondary_steps, 1), 3, flush, use_graph=not args.no_graph)
+            sec[name] = secondary_entry(other, m2, peak, peak_src)
+            del other
+        out["secondary"] = sec
 
     if not args.no_lm and rank == 0:
         out["lm_head"] = run_lm_head(args, dev, peaks, peak_src)
@@ -421,7 +481,7 @@ def run_ours(args):
         out["gdn"] = run_gdn(args, dev, flush)
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(args.workload, tree, (qh, kh, vh, doh), P, budget_s=25.0)
+        out["cpu_baseline"] = cpu_baseline(args.workload, leg.tree, leg.host, leg.P, budget_s=25.0)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
@@ -700,76 +760,95 @@ def run_gdn(args, dev, flush):
 
 
 # ----------------------------------------------------------------------------- oracle timing
-def _oracle_sample(tree, qkvdo, n_groups, Hq, Hkv):
+def _oracle_sample(ref, qkvdo, n_heads, n_paths, Hq, Hkv):
+    """The oracle's forward and backward over the first n_paths input sequences (their
+    union is a sub-tree: every prefix of a path is on it) for n_heads query heads. Returns
+    wall seconds, CPU seconds and the allowed pairs of that sub-tree."""
     import oracle
     q, k, v, do = qkvdo
-    g = Hq // Hkv
-    hs = slice(0, n_groups * g)
-    ks = slice(0, n_groups)
-    ref = oracle.pack_ref(tree.seqs)
+    G = Hq // Hkv
+    n_kv = max(1, n_heads // G) if n_heads >= G else 1
+    n_heads = n_kv * G if n_heads >= G else n_heads
+    hs, ks = slice(0, n_heads), slice(0, n_kv)
+    paths = ref["paths"][:n_paths]
+    rows = np.unique(np.concatenate([np.asarray(p, dtype=np.int64) for p in paths]))
+    pairs = int((ref["position_ids"][rows].astype(np.int64) + 1).sum())
     r0 = resource.getrusage(resource.RUSAGE_SELF)
     t0 = time.perf_counter()
-    oracle.attn_ref_fwd(q[:, hs], k[:, ks], v[:, ks], ref["paths"])
-    oracle.attn_ref_bwd(q[:, hs], k[:, ks], v[:, ks], do[:, hs], ref["paths"])
+    oracle.attn_ref_fwd(q[:, hs], k[:, ks], v[:, ks], paths)
+    oracle.attn_ref_bwd(q[:, hs], k[:, ks], v[:, ks], do[:, hs], paths)
     wall = time.perf_counter() - t0
     r1 = resource.getrusage(resource.RUSAGE_SELF)
     cpu = (r1.ru_utime - r0.ru_utime) + (r1.ru_stime - r0.ru_stime)
-    return wall, cpu
+    return wall, cpu, pairs, n_heads
+
+
+def _oracle_plan(ref, qkvdo, Hq, Hkv, budget_s):
+    """Sample size (query heads, leading input sequences) whose oracle pass takes about
+    budget_s: the oracle's cost grows with n_heads * sum of squared path lengths, so one
+    calibration pass over the first sixteenth of the paths on one head sets the scale."""
+    lens = np.array([len(p) for p in ref["paths"]], dtype=np.float64)
+    cost = np.cumsum(lens ** 2)
+    n_cal = max(1, len(lens) // 16)
+    wall, _, _, _ = _oracle_sample(ref, qkvdo, 1, n_cal, Hq, Hkv)
+    per_unit = max(wall, 1e-4) / cost[n_cal - 1]
+    if per_unit * cost[-1] <= budget_s:  # the whole tree fits: add heads
+        return int(max(1, min(Hq, budget_s // (per_unit * cost[-1])))), len(lens)
+    n_paths = int(np.searchsorted(cost, budget_s / per_unit, side="right"))
+    return 1, max(1, n_paths)
+
+
+def _sample_text(n_heads, n_paths, ref, Hq):
+    return (f"oracle fwd+bwd (float64 NumPy, per-path unpacked causal attention) over the sub-tree of the "
+            f"first {n_paths} of {len(ref['paths'])} input sequences, {n_heads} of {Hq} query heads; "
+            f"FLOPs counted on that sub-tree's allowed pairs")
 
 
 def cpu_baseline(name, tree, qkvdo, P, budget_s=25.0):
-    """The oracle (float64 NumPy, per-path unpacked attention) on the host cores, on
-    a bounded sample: all rows, the first n KV-head groups."""
+    """The oracle (float64 NumPy, per-path unpacked attention) on the host cores, on a
+    bounded sample of the same workload (a leading sub-tree, some query heads)."""
+    import oracle
     c = synth.CONFIGS[name]
     Hq, Hkv, d = c["Hq"], c["Hkv"], c["d"]
-    wall1, _ = _oracle_sample(tree, qkvdo, 1, Hq, Hkv)
-    n = int(max(1, min(Hkv, budget_s // max(wall1, 1e-3))))
-    wall, cpu = _oracle_sample(tree, qkvdo, n, Hq, Hkv) if n > 1 else (wall1, None)
-    if cpu is None:
-        wall, cpu = _oracle_sample(tree, qkvdo, 1, Hq, Hkv)
-    heads = n * (Hq // Hkv)
-    f = sum(attn_flops(P, heads, d))
+    ref = oracle.pack_ref(tree.seqs)
+    n_heads, n_paths = _oracle_plan(ref, qkvdo, Hq, Hkv, budget_s)
+    wall, cpu, pairs, n_heads = _oracle_sample(ref, qkvdo, n_heads, n_paths, Hq, Hkv)
+    f = sum(attn_flops(pairs, n_heads, d))
     return {"value": round(f / wall / 1e12, 6), "unit": "TFLOP/s", "cores": max(1, round(cpu / wall)),
-            "kind": "oracle",
-            "sample": f"oracle fwd+bwd (float64, per-path unpacked causal attention) over the whole tree, "
-                      f"{heads} of {Hq} query heads ({n} KV groups); {wall:.2f} s wall, {cpu:.1f} s CPU"}
+            "kind": "oracle", "sample": _sample_text(n_heads, n_paths, ref, Hq) + f"; {wall:.2f} s wall, {cpu:.1f} s CPU"}
 
 
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    import oracle  # noqa: F401  (reference arm: the oracle is the reference)
+    import oracle  # the reference arm: the oracle is the reference
     tree, c = attention_workload(args.workload, 0)
-    ref = __import__("oracle").pack_ref(tree.seqs)
+    ref = oracle.pack_ref(tree.seqs)
     T = ref["T"]
     P = int((ref["position_ids"].astype(np.int64) + 1).sum())
     qkvdo = synth.attention_config(args.workload, T, seed=0)
     Hq, Hkv, d = c["Hq"], c["Hkv"], c["d"]
     per_step = args.ref_budget_s / max(1, args.steps + args.warmup)
-    wall1, _ = _oracle_sample(tree, qkvdo, 1, Hq, Hkv)
-    n = int(max(1, min(Hkv, per_step // max(wall1, 1e-3))))
+    n_heads, n_paths = _oracle_plan(ref, qkvdo, Hq, Hkv, per_step)
     for _ in range(max(args.warmup - 1, 0)):
-        _oracle_sample(tree, qkvdo, n, Hq, Hkv)
+        _oracle_sample(ref, qkvdo, n_heads, n_paths, Hq, Hkv)
     walls, cpus = [], []
     for _ in range(args.steps):
-        w, cp = _oracle_sample(tree, qkvdo, n, Hq, Hkv)
+        w, cp, pairs, nh = _oracle_sample(ref, qkvdo, n_heads, n_paths, Hq, Hkv)
         walls.append(w)
         cpus.append(cp)
-    heads = n * (Hq // Hkv)
-    f = sum(attn_flops(P, heads, d))
+    f = sum(attn_flops(pairs, nh, d))
     tot = sum(walls)
     value = f * args.steps / tot / 1e12
     cores = max(1, round(sum(cpus) / tot))
-    sample = (f"oracle fwd+bwd (float64 NumPy, per-path unpacked causal attention) over the whole tree, "
-              f"{heads} of {Hq} query heads per step")
     out = {"metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot * 1e3 / args.steps, 2),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic", "impl": "reference",
            "config": describe(args.workload, T, P, len(tree.seqs), sum(len(s) for s in tree.seqs), c),
            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                            "sample": sample},
+                            "sample": _sample_text(nh, n_paths, ref, Hq) + " per step"},
            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
 

@@ -24,9 +24,11 @@
  *   - dtype is TREE_DTYPE_BF16 (bf16 storage, fp32 accumulation on tensor
  *     cores) or TREE_DTYPE_F32 (fp32 storage and arithmetic).
  *   - Pointers named "device" are CUDA device addresses owned by the caller;
- *     the library never allocates, frees or keeps device memory. Scratch space
- *     is the caller's `workspace` (device, at least the size returned by the
- *     matching *_workspace_size query, 256-byte aligned).
+ *     the library never allocates or frees device memory. Scratch space is the
+ *     caller's `workspace` (device, at least the size returned by the matching
+ *     *_workspace_size query, 256-byte aligned), with one exception:
+ *     tree_attn_fwd_noalloc keeps its scratch in a fixed device array that the
+ *     library holds (see that entry).
  *   - Every device call is asynchronous on `stream` (a cudaStream_t; NULL is
  *     the legacy default stream) and returns after enqueueing its kernels.
  *   - Every call returns a tree_status. Argument errors are found on the host

@@ -909,12 +909,7 @@ int attn_bwd_tc(const AttnArgs& a, cudaStream_t st) {
         (rc = make_tmap(&mdv, a.ws.dv_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, dims, strides, box, true)))
       return rc;
   }
-  static bool attr_set = false;
-  if (!attr_set) {
-    TREE_CUDA_TRY(cudaFuncSetAttribute(attn_bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kSmemBytes)));
-    attr_set = true;
-  }
+  if (int rc_ = smem_opt_in(reinterpret_cast<const void*>(attn_bwd_tc_kernel), static_cast<int>(kSmemBytes))) return rc_;
   int n_sm = 0;
   if ((rc = sm_count(&n_sm))) return rc;
   Params p{};

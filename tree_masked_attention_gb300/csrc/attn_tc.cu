@@ -416,12 +416,7 @@ int attn_fwd_tc(const AttnArgs& a, cudaStream_t st) {
   if ((rc = qkv_map(&mq, a.q, Tq, a.Hq)) || (rc = qkv_map(&mk, a.k, a.T, a.Hkv)) ||
       (rc = qkv_map(&mv, a.v, a.T, a.Hkv)) || (rc = qkv_map(&mo, a.o, Tq, a.Hq)))
     return rc;
-  static bool attr_set = false;
-  if (!attr_set) {
-    TREE_CUDA_TRY(cudaFuncSetAttribute(attn_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kSmemBytes)));
-    attr_set = true;
-  }
+  if (int rc_ = smem_opt_in(reinterpret_cast<const void*>(attn_fwd_tc_kernel), static_cast<int>(kSmemBytes))) return rc_;
   Params p{};
   p.T = static_cast<int>(a.T);
   p.Hq = a.Hq;

@@ -26,6 +26,10 @@ constexpr int kTimedKernels = 2;
 void timing_begin(int which, void* stream);
 void timing_end(int which, void* stream);
 
+// Opts `func` in to `bytes` of dynamic shared memory on the current device. The attribute
+// is per device, so the first call on each device sets it; later calls only look it up.
+int smem_opt_in(const void* func, int bytes);
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
 inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }

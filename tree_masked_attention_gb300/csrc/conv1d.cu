@@ -490,12 +490,7 @@ __global__ void __launch_bounds__(kRedC * kRedG) conv1d_reduce_kernel(const floa
 template <typename T, int K>
 int launch_fwd(const void* x, const void* w, const void* bias, void* y, const int32_t* parent, int64_t T_,
                int C, cudaStream_t st) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    TREE_CUDA_TRY(cudaFuncSetAttribute(conv1d_fwd_kernel<T, K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(fwd_smem<T>())));
-    attr_set = true;
-  }
+  if (int rc_ = smem_opt_in(reinterpret_cast<const void*>(conv1d_fwd_kernel<T, K>), static_cast<int>(fwd_smem<T>()))) return rc_;
   const ConvGrid g = conv_grid(T_, C, kFwdTargetCtas);
   dim3 grid(static_cast<unsigned>(g.groups), static_cast<unsigned>(g.ctiles));
   conv1d_fwd_kernel<T, K><<<grid, kConvThreads, fwd_smem<T>(), st>>>(
@@ -508,12 +503,7 @@ int launch_fwd(const void* x, const void* w, const void* bias, void* y, const in
 template <typename T, int K>
 int launch_bwd(const void* x, const void* w, const void* dy, void* dx, float* dw, float* dbias,
                const int32_t* end, const int32_t* pos, int64_t T_, int C, float* part, cudaStream_t st) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    TREE_CUDA_TRY(cudaFuncSetAttribute(conv1d_bwd_kernel<T, K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(bwd_smem<T>())));
-    attr_set = true;
-  }
+  if (int rc_ = smem_opt_in(reinterpret_cast<const void*>(conv1d_bwd_kernel<T, K>), static_cast<int>(bwd_smem<T>()))) return rc_;
   const ConvGrid g = conv_grid(T_, C, kBwdTargetCtas);
   dim3 grid(static_cast<unsigned>(g.groups), static_cast<unsigned>(g.ctiles));
   int* err = device_error_word();

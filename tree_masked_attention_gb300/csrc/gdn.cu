@@ -24,6 +24,7 @@
 // One CTA (256 threads) per SM holds the sub-chunk's K, Q, V rows, the state, A and P in
 // ~197 KB of shared memory; arithmetic is fp32 on the CUDA cores (a first version: the
 // chunk products are small GEMMs that a tensor-core version would take over).
+#include <algorithm>
 #include <cmath>
 
 #include "common.h"
@@ -34,6 +35,7 @@ namespace tree {
 namespace {
 
 constexpr int kGdnThreads = 256;
+constexpr int kMaxGdnCtas = 1024;  // upper bound of the persistent grid (one CTA per SM)
 constexpr int kChunk = 64;       // rows per sub-chunk
 constexpr int kMaxD = 128;       // largest Dk, Dv
 constexpr int kPad = kMaxD + 1;  // row stride of K, Q (bank-conflict-free column walks)
@@ -334,16 +336,11 @@ int sm_count_gdn(int* n) {
 
 template <typename Tin>
 int launch_gdn(const GdnParams& p, cudaStream_t st) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    TREE_CUDA_TRY(cudaFuncSetAttribute(gdn_fwd_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kGdnSmemBytes)));
-    attr_set = true;
-  }
+  if (int rc_ = smem_opt_in(reinterpret_cast<const void*>(gdn_fwd_kernel<Tin>), static_cast<int>(kGdnSmemBytes))) return rc_;
   int n_sm = 0;
   int rc = sm_count_gdn(&n_sm);
   if (rc) return rc;
-  gdn_fwd_kernel<Tin><<<n_sm, kGdnThreads, kGdnSmemBytes, st>>>(p);
+  gdn_fwd_kernel<Tin><<<std::min(n_sm, kMaxGdnCtas), kGdnThreads, kGdnSmemBytes, st>>>(p);
   TREE_LAUNCH_CHECK("gdn_fwd_kernel");
   return TREE_OK;
 }
@@ -370,8 +367,9 @@ extern "C" int tree_gdn_fwd(const void* q, const void* k, const void* v, const f
     return fail(TREE_ERR_SHAPE, "tree_gdn_fwd: H = %d, Dk = %d, Dv = %d (need Dk, Dv <= %d)", H, Dk, Dv, kMaxD);
   if (T == 0) return TREE_OK;
   if (n_nodes < 1) return fail(TREE_ERR_SHAPE, "tree_gdn_fwd: no nodes for %lld rows", (long long)T);
-  if (gdn_max_chunks(T, n_nodes) * H > INT32_MAX)  // work items are counted in 32 bits
-    return fail(TREE_ERR_SHAPE, "tree_gdn_fwd: %lld sub-chunks x %d heads exceed 2^31 work items",
+  // work items are counted in 32 bits, and every CTA draws once past the last item
+  if (gdn_max_chunks(T, n_nodes) * H + kMaxGdnCtas > INT32_MAX)
+    return fail(TREE_ERR_SHAPE, "tree_gdn_fwd: %lld sub-chunks x %d heads exceed the 32-bit work counter",
                 (long long)gdn_max_chunks(T, n_nodes), H);
   if (!q || !k || !v || !g || !beta || !o || !node_start || !node_end || !node_parent)
     return fail(TREE_ERR_INVALID_ARG, "tree_gdn_fwd: null pointer");

@@ -466,12 +466,7 @@ static int n_sms(int* n) {
 static int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const lmtc::Params& p, cudaStream_t st,
                        const char* name) {
   using namespace lmtc;
-  static bool attr_set = false;
-  if (!attr_set) {
-    TREE_CUDA_TRY(cudaFuncSetAttribute(lm_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kSmemBytes)));
-    attr_set = true;
-  }
+  if (int rc_ = smem_opt_in(reinterpret_cast<const void*>(lm_gemm_kernel), static_cast<int>(kSmemBytes))) return rc_;
   int sms = 0;
   int rc = n_sms(&sms);
   if (rc) return rc;

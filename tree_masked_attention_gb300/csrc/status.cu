@@ -3,6 +3,8 @@
 
 #include <atomic>
 #include <mutex>
+#include <tuple>
+#include <vector>
 
 #include "common.h"
 #include "sm100.cuh"
@@ -42,6 +44,21 @@ int* device_error_word() {
     g_err_ptr[dev] = static_cast<int*>(p);
   }
   return g_err_ptr[dev];
+}
+
+// (device, kernel) pairs whose dynamic shared-memory limit was raised, with the bytes set.
+static std::mutex g_attr_mu;
+static std::vector<std::tuple<int, const void*, int>> g_attr_done;
+
+int smem_opt_in(const void* func, int bytes) {
+  int dev = 0;
+  TREE_CUDA_TRY(cudaGetDevice(&dev));
+  std::lock_guard<std::mutex> lock(g_attr_mu);
+  for (const auto& e : g_attr_done)
+    if (std::get<0>(e) == dev && std::get<1>(e) == func && std::get<2>(e) >= bytes) return TREE_OK;
+  TREE_CUDA_TRY(cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes));
+  g_attr_done.emplace_back(dev, func, bytes);
+  return TREE_OK;
 }
 
 }  // namespace tree
