@@ -715,10 +715,11 @@ def run_gateway(args, dev, peaks, peak_src, flush):
 
 
 def run_gdn(args, dev, flush):
-    """Gated DeltaNet forward with tree state routing on the 16384-row Galton-Watson tree:
-    16 heads, Dk = Dv = 128, bf16 q / k / v, fp32 gates. Reported as packed tokens/s and
-    as the recurrence's own arithmetic (3 products of the [Dv, Dk] state per token and head:
-    S k, the rank-1 update, S q)."""
+    """Gated DeltaNet with tree state routing on the 16384-row Galton-Watson tree: 16
+    heads, Dk = Dv = 128, bf16 q / k / v / dO, fp32 gates. Forward and backward, each
+    timed with CUDA events after an L2 flush; packed tokens/s of the forward+backward
+    step, and the recurrence's own arithmetic (3 products of the [Dv, Dk] state per
+    token and head forward: S k, the rank-1 update, S q)."""
     import torch
     import tree_masked_attention_gb300 as tma
     tree = synth.galton_watson()
@@ -729,32 +730,46 @@ def run_gdn(args, dev, flush):
     q = (torch.randn((T, H, D), generator=g, device=dev) / D ** 0.5).to(torch.bfloat16)
     k = torch.nn.functional.normalize(torch.randn((T, H, D), generator=g, device=dev), dim=-1).to(torch.bfloat16)
     v = torch.randn((T, H, D), generator=g, device=dev).to(torch.bfloat16)
+    do = torch.randn((T, H, D), generator=g, device=dev).to(torch.bfloat16)
     gate = -0.2 * torch.rand((T, H), generator=g, device=dev)
     beta = torch.rand((T, H), generator=g, device=dev)
     ns, ne, npar = (torch.from_numpy(pk[n]).to(dev) for n in ("node_start", "node_end", "node_parent"))
-    ws = torch.empty(tma.tree_gdn_workspace_size(T, len(pk["node_start"]), H, D, D), dtype=torch.uint8, device=dev)
+    ws = torch.empty(tma.tree_gdn_bwd_workspace_size(T, len(pk["node_start"]), H, D, D), dtype=torch.uint8,
+                     device=dev)
     o = torch.empty_like(v)
+    grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(gate),
+             torch.empty_like(beta))
     stream = torch.cuda.current_stream(dev)
     for _ in range(2):
         tma.tree_gdn_fwd(q, k, v, gate, beta, ns, ne, npar, workspace=ws, out=o)
+        tma.tree_gdn_bwd(q, k, v, gate, beta, do, ns, ne, npar, workspace=ws, grads=grads)
     torch.cuda.synchronize()
     n = max(args.gdn_steps, 1)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
     for s in range(n):
         flush.zero_()
         evs[s][0].record(stream)
         tma.tree_gdn_fwd(q, k, v, gate, beta, ns, ne, npar, workspace=ws, out=o)
         evs[s][1].record(stream)
+        flush.zero_()
+        evs[s][2].record(stream)
+        tma.tree_gdn_bwd(q, k, v, gate, beta, do, ns, ne, npar, workspace=ws, grads=grads)
+        evs[s][3].record(stream)
     torch.cuda.synchronize()
     tma.tree_check_device_status()
-    ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
+    f_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
+    b_ms = float(np.mean([e[2].elapsed_time(e[3]) for e in evs]))
     fl = 6.0 * D * D * H * T
     return {
         "workload": f"gdn: Galton-Watson tree of {T} rows ({len(pk['node_start'])} nodes), {H} heads, Dk = Dv = {D}, "
-                    "bf16 q/k/v, fp32 gates; forward only",
-        "value": round(T / (ms / 1e3), 1), "unit": "packed tokens/s", "ms": round(ms, 4), "steps": n,
-        "recurrence_tflops": round(fl / (ms / 1e3) / 1e12, 3),
-        "kernel": "gdn_fwd_kernel (fp32 CUDA cores, one CTA per SM, 64-row sub-chunks)",
+                    "bf16 q/k/v/dO, fp32 gates",
+        "value": round(T / ((f_ms + b_ms) / 1e3), 1), "unit": "packed tokens/s (forward + backward)",
+        "ms_fwd": round(f_ms, 4), "ms_bwd": round(b_ms, 4), "steps": n,
+        "fwd_tokens_per_s": round(T / (f_ms / 1e3), 1),
+        "fwd_recurrence_tflops": round(fl / (f_ms / 1e3) / 1e12, 3),
+        "kernels": "fwd: gdn_setup, gdn_prep (chunk-parallel factors), gdn_chain (state chain over 32-column "
+                   "slices), gdn_out; bwd: setup, prep, chain, gdn_bchain (state-gradient chain), gdn_grads "
+                   "(fp32 CUDA cores)",
         "data": "synthetic (seeded torch generator on device)",
     }
 

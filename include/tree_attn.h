@@ -329,7 +329,7 @@ int tree_attn_bwd_gateway(const void* q, const void* k, const void* v, const voi
                           size_t workspace_bytes, tree_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
-/* Gated DeltaNet with tree state routing (forward)                          */
+/* Gated DeltaNet with tree state routing                                    */
 /* ------------------------------------------------------------------------ */
 /*
  * [TT] §3.2 "SSM Layers (GDN)", eq. 10, Appendix A.2: a GDN layer's recurrent state
@@ -341,15 +341,45 @@ int tree_attn_bwd_gateway(const void* q, const void* k, const void* v, const voi
  * device fp32 [T, H]; q and k are used as given (normalising k or scaling q is the
  * caller's). node_start / node_end (inclusive) / node_parent: device int32
  * [n_nodes] from tree_pack_emit (nodes in preorder tiling [0, T), parents earlier; a
- * violation sets the device error word and leaves o unwritten). Dk, Dv <= 128.
- * fp32 arithmetic. workspace: device, >= tree_gdn_workspace_size() bytes, 256-byte
- * aligned (sub-chunk table, flags, and every 64-row sub-chunk's end state).
+ * violation sets the device error word and leaves the outputs unwritten). Dk, Dv <=
+ * 128, H <= 65535. fp32 arithmetic. workspace: device, >= tree_gdn_workspace_size()
+ * bytes, 256-byte aligned (the sub-chunk table, the per-64-row-sub-chunk factors of
+ * the chunked solution, and every sub-chunk's end state). Waits between the CTAs
+ * that carry the state from a sub-chunk to the next are bounded (TREE_ERR_TIMEOUT in
+ * the device error word; outputs then unspecified).
  */
 size_t tree_gdn_workspace_size(int64_t T, int64_t n_nodes, int H, int Dk, int Dv);
 int tree_gdn_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
                  void* o, const int32_t* node_start, const int32_t* node_end,
                  const int32_t* node_parent, int64_t T, int64_t n_nodes, int H, int Dk, int Dv,
                  int dtype, void* workspace, size_t workspace_bytes, tree_stream_t stream);
+
+/*
+ * Backward of tree_gdn_fwd: the gradients of L = sum(dout * o) with respect to q, k,
+ * v (dq, dk: device [T, H, Dk]; dv: device [T, H, Dv]; dtype, written) and to g and
+ * beta (dg, dbeta: device fp32 [T, H], written). The state gradient flows back along
+ * the same routing: a node's end-state gradient is the sum of the start-state
+ * gradients of the nodes that continue from it (its next sub-chunk, or its children:
+ * siblings share their parent's end state), summed in a fixed order, so the results
+ * are reproducible run to run. dout: device [T, H, Dv] (dtype). The forward's states
+ * are recomputed (the call needs only the forward's inputs). Other arguments as
+ * tree_gdn_fwd; workspace: device, >= tree_gdn_bwd_workspace_size() bytes, 256-byte
+ * aligned.
+ */
+size_t tree_gdn_bwd_workspace_size(int64_t T, int64_t n_nodes, int H, int Dk, int Dv);
+int tree_gdn_bwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                 const void* dout, void* dq, void* dk, void* dv, float* dg, float* dbeta,
+                 const int32_t* node_start, const int32_t* node_end,
+                 const int32_t* node_parent, int64_t T, int64_t n_nodes, int H, int Dk, int Dv,
+                 int dtype, void* workspace, size_t workspace_bytes, tree_stream_t stream);
+
+/* Test hook for the bounded waits of the GDN calls: the next tree_gdn_fwd or
+ * tree_gdn_bwd call in this process withholds every publication of sub-chunk
+ * `sub_chunk` (its index in preorder, -1 for none) and gives up any wait after
+ * wait_seconds (0 < wait_seconds <= 2). Its successors' waits then run out: the call
+ * ends with TREE_ERR_TIMEOUT in the device error word and unspecified outputs, and
+ * the next call runs normally. TREE_ERR_INVALID_ARG for arguments out of range. */
+int tree_gdn_test_withhold(int64_t sub_chunk, double wait_seconds);
 
 /* ------------------------------------------------------------------------ */
 /* Tree-correct causal depthwise conv1d (short convolution of SSM layers)    */

@@ -155,6 +155,15 @@ def test_gateway_and_gdn_reject_bad_arguments(tma):
                           None, 0, None) == 2
     assert L.tree_gdn_fwd(None, None, None, None, None, None, None, None, None, 64, 4, 2, 64, 64, 1,
                           None, 0, None) == 1
+    # GDN backward: the same checks, and every gradient pointer
+    assert L.tree_gdn_bwd(*([None] * 14), 64, 4, 2, 256, 64, 1, None, 0, None) == 2
+    assert L.tree_gdn_bwd(*([None] * 14), 64, 4, 2, 64, 64, 9, None, 0, None) == 3
+    assert L.tree_gdn_bwd(*([None] * 14), 64, 4, 2, 64, 64, 1, None, 0, None) == 1
+    assert L.tree_gdn_bwd_workspace_size(16384, 55, 16, 128, 128) > L.tree_gdn_workspace_size(16384, 55, 16, 128, 128)
+    # the wait-limit test hook rejects limits outside (0, 2] s and sub-chunks below -1
+    assert L.tree_gdn_test_withhold(0, 0.0) == 1
+    assert L.tree_gdn_test_withhold(0, 3.0) == 1
+    assert L.tree_gdn_test_withhold(-2, 0.1) == 1
     # workspace: sub-chunk table, schedule and one 64-row sub-chunk end state per (sub-chunk, head)
     ws = L.tree_gdn_workspace_size(16384, 55, 16, 128, 128)
     assert ws >= (55 + 16384 // 64 + 1) * 16 * 128 * 128 * 4

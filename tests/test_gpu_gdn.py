@@ -83,3 +83,116 @@ def test_gdn_bad_nodes_set_device_flag():
         m.tree_check_device_status()
     assert ei.value.status == 7
     m.tree_check_device_status()
+
+
+# ------------------------------------------------------------------------------ backward
+def _check_bwd(m, seqs, H, Dk, Dv, seed, bf16):
+    """Every gradient of sum(dO * o) against the oracle's per-branch reverse pass."""
+    pk = m.tree_pack(seqs)
+    ref = oracle.pack_ref(seqs)
+    T = pk["T"]
+    q, k, v, g, beta = _inputs(T, H, Dk, Dv, seed, bf16)
+    r = np.random.default_rng(seed + 50)
+    do = r.normal(size=(T, H, Dv)).astype(np.float32)
+    if bf16:
+        do = synth.bf16_round(do)
+    td = torch.bfloat16 if bf16 else torch.float32
+    nodes = [dev(pk[n]) for n in ("node_start", "node_end", "node_parent")]
+    got = m.tree_gdn_bwd(dev(q, td), dev(k, td), dev(v, td), dev(g), dev(beta), dev(do, td), *nodes)
+    m.tree_check_device_status()
+    want = oracle.gdn_ref_bwd(q, k, v, g, beta, do, ref["paths"])
+    tol = BF16_TOL if bf16 else F32_TOL
+    for name, a, b in zip(("dq", "dk", "dv"), got[:3], want[:3]):
+        assert_close(name, a, b, tol)
+    # dg and dbeta are fp32 outputs of fp32 arithmetic on the same (rounded) inputs
+    for name, a, b in zip(("dg", "dbeta"), got[3:], want[3:]):
+        assert_close(name, a, b, F32_TOL)
+    return pk
+
+
+@pytest.mark.parametrize("seed,Dk,Dv,bf16", [(0, 64, 64, False), (1, 32, 96, False), (2, 128, 128, True)])
+def test_gdn_bwd_random_forests(seed, Dk, Dv, bf16):
+    """Many forks and several roots: sibling state gradients summed at the parent's end."""
+    need_cuda()
+    m = tma()
+    rng = np.random.default_rng(800 + seed)
+    seqs = synth.random_sequences(rng, 20, 90, vocab=2, min_len=1)
+    pk = _check_bwd(m, seqs, 2, Dk, Dv, seed, bf16)
+    assert pk["n_roots"] >= 2
+
+
+@pytest.mark.parametrize("bf16", [False, True])
+def test_gdn_bwd_galton_watson(bf16):
+    """Nodes of several 64-row sub-chunks and fanout up to 3 (a sub-chunk's end-state
+    gradient comes from the next sub-chunk of its node or from every child)."""
+    need_cuda()
+    m = tma()
+    t = synth.galton_watson(seed=4, budget=1500, seg=(20, 300), vocab=1000)
+    _check_bwd(m, t.seqs, 2, 128, 128, 4, bf16)
+
+
+def test_gdn_bwd_long_chain_and_wide_fork():
+    """A 700-row chain (eleven sub-chunks in one node) and a root with 30 children, whose
+    start-state gradients all add into the root's end state."""
+    need_cuda()
+    m = tma()
+    seqs = [list(range(700))] + [[0, 5000 + i, 6000 + i] for i in range(30)]
+    _check_bwd(m, seqs, 2, 64, 64, 6, False)
+
+
+def test_gdn_bwd_repeats_bitwise():
+    """Fixed summation orders: two backward calls give identical bits."""
+    need_cuda()
+    m = tma()
+    t = synth.galton_watson(seed=5, budget=1200, seg=(20, 200), vocab=1000)
+    pk = m.tree_pack(t.seqs)
+    T = pk["T"]
+    q, k, v, g, beta = _inputs(T, 2, 64, 64, 7, False)
+    do = np.random.default_rng(8).normal(size=(T, 2, 64)).astype(np.float32)
+    args = [dev(x) for x in (q, k, v, g, beta, do)] + [dev(pk[n]) for n in ("node_start", "node_end", "node_parent")]
+    a = m.tree_gdn_bwd(*args)
+    b = m.tree_gdn_bwd(*args)
+    m.tree_check_device_status()
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+# ------------------------------------------------------------------------------ bounded waits
+def _withheld_call(m, fn, args, sub_chunk):
+    rc = m.lib().tree_gdn_test_withhold(sub_chunk, 0.05)
+    assert rc == 0, m.lib().tree_last_error()
+    fn(*args)
+    with pytest.raises(m.TreeError) as ei:
+        m.tree_check_device_status()
+    return ei.value.status
+
+
+@pytest.mark.parametrize("which", ["fwd", "bwd"])
+def test_gdn_wait_runs_out_when_a_publication_is_withheld(which):
+    """The first sub-chunk never publishes its state (test hook), so the waits of the
+    sub-chunks that continue from it run out after 50 ms: the call ends with
+    TREE_ERR_TIMEOUT in the device error word, every CTA leaves, and the next call runs
+    normally and matches the oracle."""
+    need_cuda()
+    m = tma()
+    t = synth.galton_watson(seed=3, budget=600, seg=(20, 150), vocab=1000)
+    pk = m.tree_pack(t.seqs)
+    ref = oracle.pack_ref(t.seqs)
+    T = pk["T"]
+    q, k, v, g, beta = _inputs(T, 2, 64, 64, 9, False)
+    do = np.random.default_rng(10).normal(size=(T, 2, 64)).astype(np.float32)
+    nodes = [dev(pk[n]) for n in ("node_start", "node_end", "node_parent")]
+    ins = [dev(x) for x in (q, k, v, g, beta)]
+    if which == "fwd":
+        fn, args = m.tree_gdn_fwd, ins + nodes
+    else:
+        fn, args = m.tree_gdn_bwd, ins + [dev(do)] + nodes
+    assert _withheld_call(m, fn, args, 0) == 6          # TREE_ERR_TIMEOUT
+    m.tree_check_device_status()                          # cleared, context usable
+    if which == "fwd":
+        assert_close("o after a timeout", fn(*args), oracle.gdn_ref_fwd(q, k, v, g, beta, ref["paths"]), F32_TOL)
+    else:
+        want = oracle.gdn_ref_bwd(q, k, v, g, beta, do, ref["paths"])
+        for name, a, b in zip(("dq", "dk", "dv", "dg", "dbeta"), fn(*args), want):
+            assert_close(name + " after a timeout", a, b, F32_TOL)
+    m.tree_check_device_status()
