@@ -57,8 +57,9 @@ constexpr int kMaxD = 128;        // largest Dk, Dv
 constexpr int kSlice = 32;        // state columns per chain item
 constexpr int kMaxCtas = 1024;    // upper bound of a persistent grid
 constexpr int kRow = kMaxD + 4;   // row stride (floats) of [64][D] tiles: 16-byte rows, float4 reads conflict-free
-constexpr int kSq = kChunk + 1;   // row stride of [64][64] matrices
-constexpr int kSl = kSlice + 1;   // row stride of [*][32] slices
+constexpr int kSq = kChunk + 4;   // row stride of [64][64] matrices (16-byte rows)
+constexpr int kSl = kSlice + 4;   // row stride of [*][32] slices read along their rows (16-byte rows)
+constexpr int kSt = 17;           // row stride of [128][16] stagings read down their columns
 
 __device__ __forceinline__ float ldf(const float* p, int64_t i) { return p[i]; }
 __device__ __forceinline__ float ldf(const __nv_bfloat16* p, int64_t i) { return __bfloat162float(p[i]); }
@@ -72,6 +73,22 @@ __device__ __forceinline__ void st_release(int* p, int v) {
   asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// Asynchronous global -> shared copies (no registers, many in flight), waited for together.
+__device__ __forceinline__ void cp16(void* s, const void* g) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sm100::smem_u32(s)), "l"(g) : "memory");
+}
+__device__ __forceinline__ void cp4(void* s, const void* g) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(sm100::smem_u32(s)), "l"(g) : "memory");
+}
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// A row-major [rows][cols] fp32 block (cols a multiple of 4) into shared memory rows of
+// stride sstride floats (a multiple of 4), 16 bytes per copy.
+__device__ __forceinline__ void cp_block(float* s, int sstride, const float* g, int rows, int cols) {
+  const int per = cols / 4, n = rows * per;
+  for (int p = threadIdx.x; p < n; p += kThreads) cp16(s + (p / per) * sstride + (p % per) * 4, g + 4 * static_cast<int64_t>(p));
+}
+
 struct GdnWs {
   int4* chunks;     // [mc] {first row, rows, predecessor sub-chunk or -1, chain depth}
   int* node_last;   // [n_nodes] last sub-chunk of each node
@@ -83,25 +100,32 @@ struct GdnWs {
   int* flags_f;     // [mc, H, slices] end state published
   float* Pm;        // [mc, H, 64, 64]
   float* Xm;        // [mc, H, 64, 64]  (I + A)^-1
-  float* W;         // [T, H, Dk]
-  float* U0;        // [T, H, Dv]
-  float* u;         // [T, H, Dv]
-  float* states;    // [mc, H, Dk, Dv] end states
+  float* W;         // [mc, H, 64, DkP]  (DkP = Dk rounded up to 4; zero past Dk and past the rows)
+  float* U0;        // [mc, H, slices, 64, 32]
+  float* u;         // [mc, H, slices, 64, 32]
+  float* states;    // [mc, H, slices, Dk, 32] end states (columns past Dv zero)
   // backward only
   int* flags_b;     // [mc, H, slices] start-state gradient published
-  float* dstart;    // [mc, H, Dk, Dv] start-state gradients
-  float* dend;      // [mc, H, Dk, Dv] end-state gradients
-  float* dr;        // [T, H, Dv]
+  float* dstart;    // [mc, H, slices, Dk, 32] start-state gradients
+  float* dend;      // [mc, H, slices, Dk, 32] end-state gradients
+  float* dr;        // [mc, H, slices, 64, 32]
   float* part;      // [slices, 2, T, H] per-row partial sums (dw, dr . v)
   float* part_he;   // [slices, mc, H] partial sums of dh_end . h0
+  int* scratch;     // set-up working arrays when they do not fit in shared memory
 };
 
 int64_t gdn_max_chunks(int64_t T, int64_t n_nodes) { return n_nodes + T / kChunk + 1; }
 int gdn_slices(int Dv) { return (Dv + kSlice - 1) / kSlice; }
 
+// Block of one (sub-chunk, head, slice) in the [mc, H, slices, rows, 32] layouts.
+__device__ __forceinline__ float* slice_block(float* base, int c, int h, int sl, int H, int ns, int rows) {
+  return base + ((static_cast<int64_t>(c) * H + h) * ns + sl) * rows * kSlice;
+}
+
 size_t gdn_ws_layout(int64_t T, int64_t n_nodes, int H, int Dk, int Dv, bool bwd, void* base, GdnWs* w) {
   const int64_t mc = gdn_max_chunks(T, n_nodes);
   const int64_t ns = gdn_slices(Dv);
+  const int64_t DkP = (Dk + 3) / 4 * 4;
   size_t off = 0;
   auto take = [&](size_t bytes) {
     off = round_up(off, 256);
@@ -117,18 +141,19 @@ size_t gdn_ws_layout(int64_t T, int64_t n_nodes, int H, int Dk, int Dv, bool bwd
   x.succ_ptr = static_cast<int*>(take(sizeof(int) * (mc + 1)));
   x.succ = static_cast<int*>(take(sizeof(int) * mc));
   x.ctl = static_cast<int*>(take(sizeof(int) * 4));
+  x.scratch = static_cast<int*>(take(sizeof(int) * (4 * std::max<int64_t>(n_nodes, 1) + 4 * mc + 2)));
   x.flags_f = static_cast<int*>(take(sizeof(int) * mc * H * ns));
   x.Pm = static_cast<float*>(take(sizeof(float) * mc * H * kChunk * kChunk));
   x.Xm = static_cast<float*>(take(sizeof(float) * mc * H * kChunk * kChunk));
-  x.W = static_cast<float*>(take(sizeof(float) * T * H * Dk));
-  x.U0 = static_cast<float*>(take(sizeof(float) * T * H * Dv));
-  x.u = static_cast<float*>(take(sizeof(float) * T * H * Dv));
-  x.states = static_cast<float*>(take(sizeof(float) * mc * H * Dk * Dv));
+  x.W = static_cast<float*>(take(sizeof(float) * mc * H * kChunk * DkP));
+  x.U0 = static_cast<float*>(take(sizeof(float) * mc * H * ns * kChunk * kSlice));
+  x.u = static_cast<float*>(take(sizeof(float) * mc * H * ns * kChunk * kSlice));
+  x.states = static_cast<float*>(take(sizeof(float) * mc * H * ns * Dk * kSlice));
   if (bwd) {
     x.flags_b = static_cast<int*>(take(sizeof(int) * mc * H * ns));
-    x.dstart = static_cast<float*>(take(sizeof(float) * mc * H * Dk * Dv));
-    x.dend = static_cast<float*>(take(sizeof(float) * mc * H * Dk * Dv));
-    x.dr = static_cast<float*>(take(sizeof(float) * T * H * Dv));
+    x.dstart = static_cast<float*>(take(sizeof(float) * mc * H * ns * Dk * kSlice));
+    x.dend = static_cast<float*>(take(sizeof(float) * mc * H * ns * Dk * kSlice));
+    x.dr = static_cast<float*>(take(sizeof(float) * mc * H * ns * kChunk * kSlice));
     x.part = static_cast<float*>(take(sizeof(float) * ns * 2 * T * H));
     x.part_he = static_cast<float*>(take(sizeof(float) * ns * mc * H));
   }
@@ -140,15 +165,40 @@ size_t gdn_ws_layout(int64_t T, int64_t n_nodes, int H, int Dk, int Dv, bool bwd
 // Sub-chunk table from the node arrays (one thread walks the nodes in preorder, checking
 // that they tile [0, T) with earlier parents), the schedule (sub-chunks by increasing
 // chain depth: a counting sort, stable in preorder) and the successor lists; all threads
-// clear the flags. On a malformed table nothing is scheduled (n_chunks = 0).
-__global__ void __launch_bounds__(1024) gdn_setup_kernel(const int32_t* __restrict__ node_start,
-                                                         const int32_t* __restrict__ node_end,
-                                                         const int32_t* __restrict__ node_parent, int n_nodes,
-                                                         int T, int64_t n_flags, GdnWs w, int max_chunks, int* err) {
+// clear the flags. On a malformed table nothing is scheduled (n_chunks = 0). The walk's
+// working arrays (copies of the node arrays, each node's last sub-chunk, each sub-chunk's
+// depth and predecessor, the sort's counters) live in shared memory when they fit
+// (`fits`), else in the workspace.
+constexpr int kSetupThreads = 1024;
+
+__host__ __device__ constexpr int64_t setup_ints(int64_t n_nodes, int64_t max_chunks) {
+  return 4 * n_nodes + 4 * max_chunks + 2;  // node arrays, nlast; depth, pred, two counters of mc + 1
+}
+
+__global__ void __launch_bounds__(kSetupThreads) gdn_setup_kernel(const int32_t* __restrict__ node_start,
+                                                                  const int32_t* __restrict__ node_end,
+                                                                  const int32_t* __restrict__ node_parent,
+                                                                  int n_nodes, int T, int64_t n_flags, GdnWs w,
+                                                                  int max_chunks, int fits, int* err) {
+  extern __shared__ int ssm[];
   for (int64_t i = threadIdx.x; i < n_flags; i += blockDim.x) {
     w.flags_f[i] = 0;
     if (w.flags_b) w.flags_b[i] = 0;
   }
+  int* nst = fits ? ssm : w.scratch;
+  int* nen = nst + n_nodes;
+  int* npa = nen + n_nodes;
+  int* nlast = npa + n_nodes;
+  int* cdepth = nlast + n_nodes;
+  int* cpred = cdepth + max_chunks;
+  int* dc = cpred + max_chunks;   // [max_chunks + 1]
+  int* sp = dc + max_chunks + 1;  // [max_chunks + 1]
+  for (int i = threadIdx.x; i < n_nodes; i += blockDim.x) {
+    nst[i] = node_start[i];
+    nen[i] = node_end[i];
+    npa[i] = node_parent[i];
+  }
+  __syncthreads();
   if (threadIdx.x != 0) return;
   w.ctl[1] = 0;
   w.ctl[2] = 0;
@@ -156,74 +206,132 @@ __global__ void __launch_bounds__(1024) gdn_setup_kernel(const int32_t* __restri
   int m = 0, next = 0;
   bool ok = true;
   for (int n = 0; n < n_nodes && ok; ++n) {
-    const int s = node_start[n], e = node_end[n] + 1, par = node_parent[n];
+    const int s = nst[n], e = nen[n] + 1, par = npa[n];
     if (s != next || e <= s || e > T || par >= n || par < -1) {
       ok = false;
       break;
     }
     next = e;
-    int pred = par >= 0 ? w.node_last[par] : -1;
-    for (int c0 = s; c0 < e; c0 += kChunk) {
+    int pred = par >= 0 ? nlast[par] : -1;
+    int depth = pred >= 0 ? cdepth[pred] + 1 : 0;
+    for (int c0 = s; c0 < e; c0 += kChunk, ++depth) {
       if (m >= max_chunks) { ok = false; break; }
-      const int depth = pred >= 0 ? w.chunks[pred].w + 1 : 0;
+      cpred[m] = pred;
+      cdepth[m] = depth;
       w.chunks[m] = make_int4(c0, min(kChunk, e - c0), pred, depth);
       pred = m++;
     }
-    w.node_last[n] = pred;
+    nlast[n] = pred;
   }
   if (!ok || next != T) {
     raise_error(err, TREE_ERR_DEVICE_CHECK);
     m = 0;
   }
-  for (int d = 0; d <= m; ++d) w.depth_count[d] = 0;
-  for (int c = 0; c < m; ++c) ++w.depth_count[w.chunks[c].w + 1];
-  for (int d = 1; d <= m; ++d) w.depth_count[d] += w.depth_count[d - 1];
-  for (int c = 0; c < m; ++c) w.order[w.depth_count[w.chunks[c].w]++] = c;
+  for (int d = 0; d <= m; ++d) dc[d] = 0;
+  for (int c = 0; c < m; ++c) ++dc[cdepth[c] + 1];
+  for (int d = 1; d <= m; ++d) dc[d] += dc[d - 1];
+  for (int c = 0; c < m; ++c) w.order[dc[cdepth[c]]++] = c;
   // successor lists: the successors of c in increasing sub-chunk index
-  for (int c = 0; c <= m; ++c) w.succ_ptr[c] = 0;
+  for (int c = 0; c <= m; ++c) sp[c] = 0;
   for (int c = 0; c < m; ++c)
-    if (w.chunks[c].z >= 0) ++w.succ_ptr[w.chunks[c].z + 1];
-  for (int c = 1; c <= m; ++c) w.succ_ptr[c] += w.succ_ptr[c - 1];
-  for (int c = 0; c < m; ++c) w.depth_count[c] = w.succ_ptr[c];  // fill cursors
-  for (int c = 0; c < m; ++c) {
-    const int p = w.chunks[c].z;
-    if (p >= 0) w.succ[w.depth_count[p]++] = c;
+    if (cpred[c] >= 0) ++sp[cpred[c] + 1];
+  for (int c = 1; c <= m; ++c) sp[c] += sp[c - 1];
+  for (int c = 0; c <= m; ++c) {
+    w.succ_ptr[c] = sp[c];
+    dc[c] = sp[c];  // fill cursors
   }
+  for (int c = 0; c < m; ++c)
+    if (cpred[c] >= 0) w.succ[dc[cpred[c]]++] = c;
   w.ctl[0] = m;
 }
 
-// Running log-decay of a sub-chunk and the factors built from it (thread 0 sums in row
-// order; every thread then reads them). Ends with a block barrier.
+// Running log-decay of a sub-chunk and the factors built from it: the first two warps load
+// g and beta of one row each and form the running sum with a warp scan (the same order in
+// every kernel, so every kernel sees the same lg). Ends with a block barrier.
 __device__ __forceinline__ void decay_factors(const float* __restrict__ g, const float* __restrict__ beta, int r0,
                                               int L, int H, int h, float* lg, float* E, float* wv, float* bs) {
-  if (threadIdx.x == 0) {
-    float run = 0.f;
-    for (int t = 0; t < kChunk; ++t) {
-      const bool in = t < L;
-      const int64_t row = static_cast<int64_t>(r0 + t) * H + h;
-      run += in ? g[row] : 0.f;
-      lg[t] = run;
-      bs[t] = in ? beta[row] : 0.f;
+  __shared__ float s_carry;
+  const int t = threadIdx.x;
+  float x = 0.f;
+  if (t < kChunk) {
+    const bool in = t < L;
+    const int64_t row = static_cast<int64_t>(r0 + t) * H + h;
+    x = in ? g[row] : 0.f;
+    bs[t] = in ? beta[row] : 0.f;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, x, o);
+      if ((t & 31) >= o) x += y;
     }
+    if (t == 31) s_carry = x;
   }
   __syncthreads();
-  if (threadIdx.x < kChunk) {
-    const int t = threadIdx.x;
-    E[t] = t < L ? expf(lg[t]) : 0.f;
-    wv[t] = t < L ? expf(lg[L - 1] - lg[t]) : 0.f;
+  if (t < kChunk) {
+    if (t >= 32) x += s_carry;
+    lg[t] = x;
+    E[t] = t < L ? expf(x) : 0.f;
   }
+  __syncthreads();
+  if (t < kChunk) wv[t] = t < L ? expf(lg[L - 1] - lg[t]) : 0.f;
   __syncthreads();
 }
 
-// Rows [r0, r0 + 64) of a [T, H, D] tensor, head h, into a [64][kRow] tile (zero past L
-// rows and past D columns, up to the next multiple of 4).
+// 8 bf16 or 4 fp32 values of one 16-byte vector, widened to fp32.
+__device__ __forceinline__ void widen(const uint4& v, float* f, const __nv_bfloat16*) {
+  const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 x = __bfloat1622float2(b[i]);
+    f[2 * i] = x.x;
+    f[2 * i + 1] = x.y;
+  }
+}
+__device__ __forceinline__ void widen(const uint4& v, float* f, const float*) {
+  f[0] = __uint_as_float(v.x);
+  f[1] = __uint_as_float(v.y);
+  f[2] = __uint_as_float(v.z);
+  f[3] = __uint_as_float(v.w);
+}
+
+// Columns [col0, col0 + ncols) of rows [r0, r0 + 64) of a [T, H, D] tensor (head h) into
+// an fp32 shared tile (row stride `stride`), zero past L rows and past D columns (up to
+// ncols, a multiple of 4). Every thread issues all of its 16-byte loads before using any,
+// so their latencies overlap; rows whose width is not a whole number of vectors take a
+// scalar path. The input pointer is 16-byte aligned (checked on the host).
 template <typename Tin>
-__device__ __forceinline__ void load_rows(float* dst, const Tin* __restrict__ src, int r0, int L, int H, int h,
-                                          int D) {
-  const int D4 = (D + 3) & ~3;
-  for (int idx = threadIdx.x; idx < kChunk * D4; idx += blockDim.x) {
-    const int t = idx / D4, i = idx % D4;
-    dst[t * kRow + i] = (t < L && i < D) ? ldf(src, (static_cast<int64_t>(r0 + t) * H + h) * D + i) : 0.f;
+__device__ __forceinline__ void load_tile(float* dst, int stride, const Tin* __restrict__ src, int r0, int L, int H,
+                                          int h, int D, int col0, int ncols) {
+  constexpr int kVec = 16 / sizeof(Tin);                       // 8 bf16 or 4 fp32
+  constexpr int kPer = kChunk * kMaxD / kVec / kThreads;        // most vectors a thread loads
+  const int nv = ncols / kVec, total = kChunk * nv;
+  if (D % kVec == 0 && ncols % kVec == 0) {
+    uint4 buf[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int idx = threadIdx.x + u * kThreads;
+      const int t = idx / max(nv, 1), cv = col0 + (idx % max(nv, 1)) * kVec;
+      buf[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (idx < total && t < L && cv < D)
+        buf[u] = __ldg(reinterpret_cast<const uint4*>(src + (static_cast<int64_t>(r0 + t) * H + h) * D + cv));
+    }
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int idx = threadIdx.x + u * kThreads;
+      if (idx < total) {
+        const int t = idx / nv, cl = (idx % nv) * kVec;
+        float f[kVec];
+        widen(buf[u], f, src);
+#pragma unroll
+        for (int e = 0; e < kVec; e += 4)
+          *reinterpret_cast<float4*>(dst + t * stride + cl + e) = make_float4(f[e], f[e + 1], f[e + 2], f[e + 3]);
+      }
+    }
+  } else {
+#pragma unroll 8
+    for (int idx = threadIdx.x; idx < kChunk * ncols; idx += kThreads) {
+      const int t = idx / ncols, cl = idx % ncols, cv = col0 + cl;
+      dst[t * stride + cl] = (t < L && cv < D) ? ldf(src, (static_cast<int64_t>(r0 + t) * H + h) * D + cv) : 0.f;
+    }
   }
 }
 
@@ -253,7 +361,7 @@ struct GdnArgs {
   void* dv;
   float* dg;
   float* dbeta;
-  int T, H, Dk, Dv, ns;
+  int T, H, Dk, Dv, ns, DkP;
   int withhold;                 // test hook: this sub-chunk's publications are withheld (-1: none)
   unsigned long long wait_ns;   // limit of every wait on a publication
   GdnWs w;
@@ -262,12 +370,12 @@ struct GdnArgs {
 
 // ------------------------------------------------------------------------------ prep
 // Per (sub-chunk, head): P and X = (I + A)^-1 to the workspace, W = X (beta E o K) and
-// U0 = X (beta o V) per row.
+// U0 = X (beta o V), all 64 rows (zero past L) and every padding column written.
 constexpr size_t kPrepSmem = (2 * kChunk * kRow + 2 * kChunk * kSq + 4 * kChunk) * sizeof(float);
 
 template <typename Tin>
 __global__ void __launch_bounds__(kThreads) gdn_prep_kernel(const GdnArgs a) {
-  extern __shared__ float sm[];
+  extern __shared__ __align__(16) float sm[];
   float* Ks = sm;                        // [64][kRow]
   float* QV = Ks + kChunk * kRow;        // [64][kRow]: Q, then V
   float* Am = QV + kChunk * kRow;        // [64][kSq]
@@ -279,10 +387,10 @@ __global__ void __launch_bounds__(kThreads) gdn_prep_kernel(const GdnArgs a) {
   const int c = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
   if (c >= a.w.ctl[0]) return;
   const int4 ck = a.w.chunks[c];
-  const int r0 = ck.x, L = ck.y, H = a.H, Dk = a.Dk, Dv = a.Dv;
-  const int Dk4 = (Dk + 3) & ~3;
-  load_rows(Ks, static_cast<const Tin*>(a.k), r0, L, H, h, Dk);
-  load_rows(QV, static_cast<const Tin*>(a.q), r0, L, H, h, Dk);
+  const int r0 = ck.x, L = ck.y, H = a.H, Dk = a.Dk, Dv = a.Dv, DkP = a.DkP, ns = a.ns;
+  const int Dk4 = (Dk + 3) & ~3, Dv4 = (Dv + 3) & ~3;
+  load_tile(Ks, kRow, static_cast<const Tin*>(a.k), r0, L, H, h, Dk, 0, Dk4);
+  load_tile(QV, kRow, static_cast<const Tin*>(a.q), r0, L, H, h, Dk, 0, Dk4);
   decay_factors(a.g, a.beta, r0, L, H, h, lg, E, wv, bs);  // ends with a barrier
   float* Pg = a.w.Pm + (static_cast<int64_t>(c) * H + h) * kChunk * kChunk;
   float* Xg = a.w.Xm + (static_cast<int64_t>(c) * H + h) * kChunk * kChunk;
@@ -299,7 +407,7 @@ __global__ void __launch_bounds__(kThreads) gdn_prep_kernel(const GdnArgs a) {
   }
   __syncthreads();
   // V over Q (Q is done); X by forward substitution, one column per thread
-  load_rows(QV, static_cast<const Tin*>(a.v), r0, L, H, h, Dv);
+  load_tile(QV, kRow, static_cast<const Tin*>(a.v), r0, L, H, h, Dv, 0, Dv4);
   if (tid < kChunk) {
     const int cc = tid;
     for (int t = 0; t < kChunk; ++t) Xm[t * kSq + cc] = t == cc ? 1.f : 0.f;
@@ -313,16 +421,20 @@ __global__ void __launch_bounds__(kThreads) gdn_prep_kernel(const GdnArgs a) {
   for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) Xg[idx] = Xm[(idx / kChunk) * kSq + idx % kChunk];
   // W = X (beta E o K), U0 = X (beta o V): column `col` per thread, 32 rows each
   const int col = tid % kMaxD, half = tid / kMaxD;
-  for (int t = 32 * half; t < 32 * half + 32 && t < L; ++t) {
+  float* Wg = a.w.W + (static_cast<int64_t>(c) * H + h) * kChunk * DkP;
+  for (int m = 0; m < 32; ++m) {
+    const int t = 32 * half + m;
     float wa = 0.f, ua = 0.f;
-    for (int s = 0; s <= t; ++s) {
-      const float x = Xm[t * kSq + s] * bs[s];
-      wa = fmaf(x * E[s], Ks[s * kRow + col], wa);
-      ua = fmaf(x, QV[s * kRow + col], ua);
+    if (t < L) {
+      for (int s = 0; s <= t; ++s) {
+        const float x = Xm[t * kSq + s] * bs[s];
+        wa = fmaf(x * E[s], Ks[s * kRow + col], wa);
+        ua = fmaf(x, QV[s * kRow + col], ua);
+      }
     }
-    const int64_t row = static_cast<int64_t>(r0 + t) * H + h;
-    if (col < Dk) a.w.W[row * Dk + col] = wa;
-    if (col < Dv) a.w.U0[row * Dv + col] = ua;
+    if (col < DkP) Wg[t * DkP + col] = col < Dk ? wa : 0.f;
+    if (col < ns * kSlice)
+      slice_block(a.w.U0, c, h, col / kSlice, H, ns, kChunk)[t * kSlice + col % kSlice] = col < Dv ? ua : 0.f;
   }
 }
 
@@ -338,7 +450,7 @@ __device__ bool wait_flag(const int* f, const GdnArgs& a, int* abort) {
       atomicExch(abort, 1);
       return false;
     }
-    __nanosleep(128);
+    __nanosleep(64);
   }
   return true;
 }
@@ -354,11 +466,12 @@ __device__ __forceinline__ int next_item(int* counter, int* abort, int items, in
 // ------------------------------------------------------------------------------ chain
 // Per (sub-chunk, head, slice of 32 state columns), by increasing chain depth:
 //   u = U0 - W h0,   h_end = E_{L-1} h0 + sum_t w_t k_t u_t^T.
+// The item's loads are issued together right after its predecessor's flag is seen.
 constexpr size_t kChainSmem = (2 * kChunk * kRow + kMaxD * kSl + kChunk * kSl + 4 * kChunk) * sizeof(float);
 
 template <typename Tin>
 __global__ void __launch_bounds__(kThreads) gdn_chain_kernel(const GdnArgs a) {
-  extern __shared__ float sm[];
+  extern __shared__ __align__(16) float sm[];
   float* Ws = sm;                       // [64][kRow]
   float* Ks = Ws + kChunk * kRow;       // [64][kRow]
   float* Hs = Ks + kChunk * kRow;       // [128][kSl] h0 slice
@@ -370,7 +483,7 @@ __global__ void __launch_bounds__(kThreads) gdn_chain_kernel(const GdnArgs a) {
   __shared__ int s_item, s_ok;
   const GdnWs& w = a.w;
   const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
-  const int H = a.H, Dk = a.Dk, Dv = a.Dv, ns = a.ns;
+  const int H = a.H, Dk = a.Dk, ns = a.ns, DkP = a.DkP;
   const int Dk4 = (Dk + 3) & ~3;
   const int items = w.ctl[0] * H * ns;
   while (true) {
@@ -379,45 +492,43 @@ __global__ void __launch_bounds__(kThreads) gdn_chain_kernel(const GdnArgs a) {
     const int c = w.order[item / (H * ns)], rem = item % (H * ns), h = rem / ns, sl = rem % ns;
     const int4 ck = w.chunks[c];
     const int r0 = ck.x, L = ck.y, pred = ck.z;
-    const int j = sl * kSlice + lane;  // state column of this lane
+    // loads that do not depend on the predecessor first
+    cp_block(Ws, kRow, w.W + (static_cast<int64_t>(c) * H + h) * kChunk * DkP, kChunk, DkP);
+    cp_block(Us, kSl, slice_block(w.U0, c, h, sl, H, ns, kChunk), kChunk, kSlice);
+    load_tile(Ks, kRow, static_cast<const Tin*>(a.k), r0, L, H, h, Dk, 0, Dk4);
     if (tid == 0)
       s_ok = pred < 0 || wait_flag(w.flags_f + (static_cast<int64_t>(pred) * H + h) * ns + sl, a, &w.ctl[3]);
     __syncthreads();
-    if (!s_ok) break;
-    // h0 slice, W and K rows, U0 slice
-    const float* h0 = pred >= 0 ? w.states + (static_cast<int64_t>(pred) * H + h) * Dk * Dv : nullptr;
-    for (int idx = tid; idx < kMaxD * kSlice; idx += kThreads) {
-      const int i = idx / kSlice, jj = sl * kSlice + idx % kSlice;
-      Hs[i * kSl + idx % kSlice] = (h0 && i < Dk && jj < Dv) ? __ldcg(h0 + i * Dv + jj) : 0.f;
+    if (!s_ok) {
+      cp_wait();
+      break;
     }
-    for (int idx = tid; idx < kChunk * Dk4; idx += kThreads) {
-      const int t = idx / Dk4, i = idx % Dk4;
-      const int64_t row = static_cast<int64_t>(r0 + t) * H + h;
-      const bool in = t < L && i < Dk;
-      Ws[t * kRow + i] = in ? __ldcg(w.W + row * Dk + i) : 0.f;
-      Ks[t * kRow + i] = in ? ldf(static_cast<const Tin*>(a.k), row * Dk + i) : 0.f;
+    if (pred >= 0) {
+      cp_block(Hs, kSl, slice_block(w.states, pred, h, sl, H, ns, Dk), Dk, kSlice);
+    } else {
+      for (int idx = tid; idx < Dk * kSlice; idx += kThreads) Hs[(idx / kSlice) * kSl + idx % kSlice] = 0.f;
     }
-    for (int idx = tid; idx < kChunk * kSlice; idx += kThreads) {
-      const int t = idx / kSlice, jj = sl * kSlice + idx % kSlice;
-      Us[t * kSl + idx % kSlice] =
-          (t < L && jj < Dv) ? __ldcg(w.U0 + (static_cast<int64_t>(r0 + t) * H + h) * Dv + jj) : 0.f;
-    }
+    cp_wait();
     decay_factors(a.g, a.beta, r0, L, H, h, lg, E, wv, bs);  // ends with a barrier
-    // u = U0 - W h0: rows t = warp + 8 m of column `lane`
-    for (int t = warp; t < L; t += 8) {
-      float acc = Us[t * kSl + lane];
-      for (int i = 0; i < Dk; ++i) acc = fmaf(-Ws[t * kRow + i], Hs[i * kSl + lane], acc);
+    // u = U0 - W h0: rows t = warp + 8 m of column `lane` (zero past L)
+    float* ug = slice_block(w.u, c, h, sl, H, ns, kChunk);
+    for (int t = warp; t < kChunk; t += 8) {
+      float acc = 0.f;
+      if (t < L) {
+        acc = Us[t * kSl + lane];
+        for (int i = 0; i < Dk; ++i) acc = fmaf(-Ws[t * kRow + i], Hs[i * kSl + lane], acc);
+      }
       Us[t * kSl + lane] = acc;
-      if (j < Dv) w.u[(static_cast<int64_t>(r0 + t) * H + h) * Dv + j] = acc;
+      ug[t * kSlice + lane] = acc;
     }
     __syncthreads();
     // h_end = E_{L-1} h0 + sum_t w_t k_t u_t^T: rows i = warp + 8 m of column `lane`
-    float* hend = w.states + (static_cast<int64_t>(c) * H + h) * Dk * Dv;
+    float* hend = slice_block(w.states, c, h, sl, H, ns, Dk);
     const float gl = E[L - 1];
     for (int i = warp; i < Dk; i += 8) {
       float acc = gl * Hs[i * kSl + lane];
       for (int t = 0; t < L; ++t) acc = fmaf(wv[t] * Ks[t * kRow + i], Us[t * kSl + lane], acc);
-      if (j < Dv) __stcg(hend + i * Dv + j, acc);
+      __stcg(hend + i * kSlice + lane, acc);
     }
     __syncthreads();
     if (tid == 0 && c != a.withhold) {
@@ -429,14 +540,15 @@ __global__ void __launch_bounds__(kThreads) gdn_chain_kernel(const GdnArgs a) {
 
 // ------------------------------------------------------------------------------ out
 // Per (sub-chunk, head): O = E o (Q h0) + P u.
-constexpr size_t kOutSmem = (2 * kChunk * kRow + kChunk * kSq + 4 * kChunk) * sizeof(float);
+constexpr size_t kOutSmem = (2 * kChunk * kRow + kMaxD * kRow + kChunk * kSq + 4 * kChunk) * sizeof(float);
 
 template <typename Tin>
 __global__ void __launch_bounds__(kThreads) gdn_out_kernel(const GdnArgs a) {
-  extern __shared__ float sm[];
+  extern __shared__ __align__(16) float sm[];
   float* Qs = sm;                      // [64][kRow]
   float* Us = Qs + kChunk * kRow;      // [64][kRow] u
-  float* Ps = Us + kChunk * kRow;      // [64][kSq]
+  float* Hs = Us + kChunk * kRow;      // [128][kRow] h0
+  float* Ps = Hs + kMaxD * kRow;       // [64][kSq]
   float* lg = Ps + kChunk * kSq;
   float* E = lg + kChunk;
   float* wv = E + kChunk;
@@ -446,25 +558,25 @@ __global__ void __launch_bounds__(kThreads) gdn_out_kernel(const GdnArgs a) {
   if (c >= w.ctl[0]) return;
   if (*reinterpret_cast<volatile int*>(&w.ctl[3])) return;  // the chain gave up: outputs unspecified
   const int4 ck = w.chunks[c];
-  const int r0 = ck.x, L = ck.y, pred = ck.z, H = a.H, Dk = a.Dk, Dv = a.Dv;
-  load_rows(Qs, static_cast<const Tin*>(a.q), r0, L, H, h, Dk);
-  for (int idx = tid; idx < kChunk * Dv; idx += kThreads) {
-    const int t = idx / Dv, jj = idx % Dv;
-    Us[t * kRow + jj] = t < L ? __ldcg(w.u + (static_cast<int64_t>(r0 + t) * H + h) * Dv + jj) : 0.f;
+  const int r0 = ck.x, L = ck.y, pred = ck.z, H = a.H, Dk = a.Dk, Dv = a.Dv, ns = a.ns;
+  const int Dk4 = (Dk + 3) & ~3;
+  for (int sl = 0; sl < ns; ++sl) {
+    cp_block(Us + sl * kSlice, kRow, slice_block(w.u, c, h, sl, H, ns, kChunk), kChunk, kSlice);
+    if (pred >= 0) cp_block(Hs + sl * kSlice, kRow, slice_block(w.states, pred, h, sl, H, ns, Dk), Dk, kSlice);
   }
-  const float* Pg = w.Pm + (static_cast<int64_t>(c) * H + h) * kChunk * kChunk;
-  for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) Ps[(idx / kChunk) * kSq + idx % kChunk] = Pg[idx];
+  cp_block(Ps, kSq, w.Pm + (static_cast<int64_t>(c) * H + h) * kChunk * kChunk, kChunk, kChunk);
+  load_tile(Qs, kRow, static_cast<const Tin*>(a.q), r0, L, H, h, Dk, 0, Dk4);
+  cp_wait();
   decay_factors(a.g, a.beta, r0, L, H, h, lg, E, wv, bs);  // ends with a barrier
-  const float* h0 = pred >= 0 ? w.states + (static_cast<int64_t>(pred) * H + h) * Dk * Dv : nullptr;
   const int j = tid % kMaxD, half = tid / kMaxD;
   if (j >= Dv) return;
   Tin* o = static_cast<Tin*>(a.o);
   float acc[32];
 #pragma unroll
   for (int m = 0; m < 32; ++m) acc[m] = 0.f;
-  if (h0) {
+  if (pred >= 0) {
     for (int i = 0; i < Dk; ++i) {
-      const float hij = __ldcg(h0 + i * Dv + j);
+      const float hij = Hs[i * kRow + j];
 #pragma unroll
       for (int m = 0; m < 32; ++m) acc[m] = fmaf(Qs[(32 * half + m) * kRow + i], hij, acc[m]);
     }
@@ -488,7 +600,7 @@ constexpr size_t kBchainSmem =
 
 template <typename Tin>
 __global__ void __launch_bounds__(kThreads) gdn_bchain_kernel(const GdnArgs a) {
-  extern __shared__ float sm[];
+  extern __shared__ __align__(16) float sm[];
   float* Ks = sm;                        // [64][kRow]
   float* Qs = Ks + kChunk * kRow;        // [64][kRow]
   float* Ps = Qs + kChunk * kRow;        // [64][kSq]
@@ -508,11 +620,9 @@ __global__ void __launch_bounds__(kThreads) gdn_bchain_kernel(const GdnArgs a) {
   const GdnWs& w = a.w;
   const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
   const int H = a.H, Dk = a.Dk, Dv = a.Dv, ns = a.ns, T = a.T;
+  const int Dk4 = (Dk + 3) & ~3;
   const int n_chunks = w.ctl[0];
   const int items = n_chunks * H * ns;
-  const Tin* tk = static_cast<const Tin*>(a.k);
-  const Tin* tq = static_cast<const Tin*>(a.q);
-  const Tin* tv = static_cast<const Tin*>(a.v);
   const Tin* tdo = static_cast<const Tin*>(a.dout);
   Tin* tdv = static_cast<Tin*>(a.dv);
   while (true) {
@@ -523,6 +633,18 @@ __global__ void __launch_bounds__(kThreads) gdn_bchain_kernel(const GdnArgs a) {
     const int r0 = ck.x, L = ck.y, pred = ck.z;
     const int j = sl * kSlice + lane;
     const int sb = w.succ_ptr[c], se = w.succ_ptr[c + 1];
+    // loads that do not depend on the successors first
+    const int64_t mo = (static_cast<int64_t>(c) * H + h) * kChunk * kChunk;
+    cp_block(Ps, kSq, w.Pm + mo, kChunk, kChunk);
+    cp_block(Xs, kSq, w.Xm + mo, kChunk, kChunk);
+    cp_block(Us, kSl, slice_block(w.u, c, h, sl, H, ns, kChunk), kChunk, kSlice);
+    if (pred >= 0) cp_block(Hs, kSl, slice_block(w.states, pred, h, sl, H, ns, Dk), Dk, kSlice);
+    load_tile(Ks, kRow, static_cast<const Tin*>(a.k), r0, L, H, h, Dk, 0, Dk4);
+    load_tile(Qs, kRow, static_cast<const Tin*>(a.q), r0, L, H, h, Dk, 0, Dk4);
+    load_tile(Os, kSl, tdo, r0, L, H, h, Dv, sl * kSlice, kSlice);
+    load_tile(Vs, kSl, static_cast<const Tin*>(a.v), r0, L, H, h, Dv, sl * kSlice, kSlice);
+    if (pred < 0)
+      for (int idx = tid; idx < Dk * kSlice; idx += kThreads) Hs[(idx / kSlice) * kSl + idx % kSlice] = 0.f;
     if (tid == 0) {
       bool ok = true;
       for (int s = sb; ok && s < se; ++s)
@@ -530,38 +652,43 @@ __global__ void __launch_bounds__(kThreads) gdn_bchain_kernel(const GdnArgs a) {
       s_ok = ok;
     }
     __syncthreads();
-    if (!s_ok) break;
+    if (!s_ok) {
+      cp_wait();
+      break;
+    }
     // dh_end slice = the sum of the successors' dh0 (fixed order), kept for the grads kernel
-    float* dend = w.dend + (static_cast<int64_t>(c) * H + h) * Dk * Dv;
-    const float* h0 = pred >= 0 ? w.states + (static_cast<int64_t>(pred) * H + h) * Dk * Dv : nullptr;
-    float he = 0.f;  // partial sum of dh_end . h0
-    for (int idx = tid; idx < kMaxD * kSlice; idx += kThreads) {
-      const int i = idx / kSlice, jj = sl * kSlice + idx % kSlice;
-      float x = 0.f, hv = 0.f;
-      if (i < Dk && jj < Dv) {
-        for (int s = sb; s < se; ++s)
-          x += __ldcg(w.dstart + (static_cast<int64_t>(w.succ[s]) * H + h) * Dk * Dv + i * Dv + jj);
-        __stcg(dend + i * Dv + jj, x);
-        if (h0) hv = __ldcg(h0 + i * Dv + jj);
+    {
+      constexpr int kPer = kMaxD * kSlice / 4 / kThreads;  // float4 per thread
+      float4 acc[kPer];
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int s = sb; s < se; ++s) {
+        const float4* src = reinterpret_cast<const float4*>(slice_block(w.dstart, w.succ[s], h, sl, H, ns, Dk));
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+          const int p = tid + u * kThreads;
+          if (p < Dk * kSlice / 4) {
+            const float4 x = __ldcg(src + p);
+            acc[u].x += x.x; acc[u].y += x.y; acc[u].z += x.z; acc[u].w += x.w;
+          }
+        }
       }
-      Ds[i * kSl + idx % kSlice] = x;
-      Hs[i * kSl + idx % kSlice] = hv;
-      he = fmaf(x, hv, he);
+      float4* dend = reinterpret_cast<float4*>(slice_block(w.dend, c, h, sl, H, ns, Dk));
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        const int p = tid + u * kThreads;
+        if (p < Dk * kSlice / 4) {
+          __stcg(dend + p, acc[u]);
+          *reinterpret_cast<float4*>(Ds + (p / (kSlice / 4)) * kSl + (p % (kSlice / 4)) * 4) = acc[u];
+        }
+      }
     }
-    load_rows(Ks, tk, r0, L, H, h, Dk);
-    load_rows(Qs, tq, r0, L, H, h, Dk);
-    const int64_t mo = (static_cast<int64_t>(c) * H + h) * kChunk * kChunk;
-    for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) {
-      Ps[(idx / kChunk) * kSq + idx % kChunk] = __ldcg(w.Pm + mo + idx);
-      Xs[(idx / kChunk) * kSq + idx % kChunk] = __ldcg(w.Xm + mo + idx);
-    }
-    for (int idx = tid; idx < kChunk * kSlice; idx += kThreads) {
-      const int t = idx / kSlice, jj = sl * kSlice + idx % kSlice;
-      const int64_t off = (static_cast<int64_t>(r0 + t) * H + h) * Dv + jj;
-      const bool in = t < L && jj < Dv;
-      Os[t * kSl + idx % kSlice] = in ? ldf(tdo, off) : 0.f;
-      Us[t * kSl + idx % kSlice] = in ? __ldcg(w.u + off) : 0.f;
-      Vs[t * kSl + idx % kSlice] = in ? ldf(tv, off) : 0.f;
+    cp_wait();
+    __syncthreads();
+    float he = 0.f;  // partial sum of dh_end . h0
+    for (int idx = tid; idx < Dk * kSlice; idx += kThreads) {
+      const int i = idx / kSlice, jj = idx % kSlice;
+      he = fmaf(Ds[i * kSl + jj], Hs[i * kSl + jj], he);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) he += __shfl_xor_sync(0xffffffffu, he, o);
@@ -596,16 +723,14 @@ __global__ void __launch_bounds__(kThreads) gdn_bchain_kernel(const GdnArgs a) {
       drr[m] = x;
     }
     __syncthreads();
+    float* drg = slice_block(w.dr, c, h, sl, H, ns, kChunk);
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
       const int t = warp + 8 * m;
+      Rs[t * kSl + lane] = drr[m];
+      drg[t * kSlice + lane] = drr[m];
       if (t < L) {
-        Rs[t * kSl + lane] = drr[m];
-        const int64_t off = (static_cast<int64_t>(r0 + t) * H + h) * Dv + j;
-        if (j < Dv) {
-          w.dr[off] = drr[m];
-          tdv[off] = from_f32<Tin>(bs[t] * drr[m]);
-        }
+        if (j < Dv) tdv[(static_cast<int64_t>(r0 + t) * H + h) * Dv + j] = from_f32<Tin>(bs[t] * drr[m]);
         float rv = drr[m] * Vs[t * kSl + lane];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) rv += __shfl_xor_sync(0xffffffffu, rv, o);
@@ -614,14 +739,14 @@ __global__ void __launch_bounds__(kThreads) gdn_bchain_kernel(const GdnArgs a) {
     }
     __syncthreads();
     // dh0 = E_{L-1} dh_end + Q^T (E o dO) - K^T (beta E o dr)
-    float* dst = w.dstart + (static_cast<int64_t>(c) * H + h) * Dk * Dv;
+    float* dst = slice_block(w.dstart, c, h, sl, H, ns, Dk);
     const float gl = E[L - 1];
     for (int i = warp; i < Dk; i += 8) {
       float acc = gl * Ds[i * kSl + lane];
       for (int t = 0; t < L; ++t)
         acc = fmaf(E[t], fmaf(Qs[t * kRow + i], Os[t * kSl + lane], -bs[t] * Ks[t * kRow + i] * Rs[t * kSl + lane]),
                    acc);
-      if (j < Dv) __stcg(dst + i * Dv + j, acc);
+      __stcg(dst + i * kSlice + lane, acc);
     }
     __syncthreads();
     if (tid == 0 && c != a.withhold) {
@@ -638,11 +763,11 @@ static_assert(kGradsSmem <= 227 * 1024, "GDN grads shared memory exceeds the per
 static_assert(kBchainSmem <= 227 * 1024 && kPrepSmem <= 227 * 1024 && kChainSmem <= 227 * 1024 &&
                   kOutSmem <= 227 * 1024,
               "GDN shared memory exceeds the per-block limit");
-static_assert(2 * kMaxD * 16 <= kChunk * kSq, "h0 / dh_end staging must fit in the M1 buffer");
+static_assert(2 * kMaxD * kSt <= kChunk * kSq, "h0 / dh_end staging must fit in the M1 buffer");
 
 template <typename Tin>
 __global__ void __launch_bounds__(kThreads, 1) gdn_grads_kernel(const GdnArgs a) {
-  extern __shared__ float sm[];
+  extern __shared__ __align__(16) float sm[];
   float* Ks = sm;                       // [64][kRow]
   float* Qs = Ks + kChunk * kRow;       // [64][kRow]
   float* Us = Qs + kChunk * kRow;       // [64][kRow] u
@@ -657,6 +782,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_grads_kernel(const GdnArgs a)
   float* bs = wv + kChunk;
   float* dlg = bs + kChunk;             // d lg per row
   float* dbt = dlg + kChunk;            // dbeta per row
+  __shared__ float s_part[4];
   const int c = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
   const GdnWs& w = a.w;
   const int n_chunks = w.ctl[0];
@@ -665,16 +791,14 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_grads_kernel(const GdnArgs a)
   const int4 ck = w.chunks[c];
   const int r0 = ck.x, L = ck.y, pred = ck.z, H = a.H, Dk = a.Dk, Dv = a.Dv, T = a.T, ns = a.ns;
   const int Dk4 = (Dk + 3) & ~3, Dv4 = (Dv + 3) & ~3;
-  load_rows(Ks, static_cast<const Tin*>(a.k), r0, L, H, h, Dk);
-  load_rows(Qs, static_cast<const Tin*>(a.q), r0, L, H, h, Dk);
-  load_rows(Os, static_cast<const Tin*>(a.dout), r0, L, H, h, Dv);
-  for (int idx = tid; idx < kChunk * Dv4; idx += kThreads) {
-    const int t = idx / Dv4, jj = idx % Dv4;
-    const int64_t off = (static_cast<int64_t>(r0 + t) * H + h) * Dv + jj;
-    const bool in = t < L && jj < Dv;
-    Us[t * kRow + jj] = in ? __ldcg(w.u + off) : 0.f;
-    Rs[t * kRow + jj] = in ? __ldcg(w.dr + off) : 0.f;
+  for (int sl = 0; sl < ns; ++sl) {
+    cp_block(Us + sl * kSlice, kRow, slice_block(w.u, c, h, sl, H, ns, kChunk), kChunk, kSlice);
+    cp_block(Rs + sl * kSlice, kRow, slice_block(w.dr, c, h, sl, H, ns, kChunk), kChunk, kSlice);
   }
+  load_tile(Ks, kRow, static_cast<const Tin*>(a.k), r0, L, H, h, Dk, 0, Dk4);
+  load_tile(Qs, kRow, static_cast<const Tin*>(a.q), r0, L, H, h, Dk, 0, Dk4);
+  load_tile(Os, kRow, static_cast<const Tin*>(a.dout), r0, L, H, h, Dv, 0, Dv4);
+  cp_wait();
   decay_factors(a.g, a.beta, r0, L, H, h, lg, E, wv, bs);  // ends with a barrier
   // pairs (t, s), s <= t: four threads per row t, s = sub + 4 m
   {
@@ -718,10 +842,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_grads_kernel(const GdnArgs a)
   }
   // dQ, dK: column i per thread, 16 rows per pass, two passes per half
   const int i = tid % kMaxD, half = tid / kMaxD;
-  float* hst = M1;                      // [128][16] h0 columns staged
-  float* dst = M1 + kMaxD * 16;         // [128][16] dh_end columns staged
-  const float* h0 = pred >= 0 ? w.states + (static_cast<int64_t>(pred) * H + h) * Dk * Dv : nullptr;
-  const float* dhe = w.dend + (static_cast<int64_t>(c) * H + h) * Dk * Dv;
+  float* hst = M1;                      // [128][kSt] 16 columns of h0, staged
+  float* dst = M1 + kMaxD * kSt;        // [128][kSt] the same columns of dh_end
   Tin* dq = static_cast<Tin*>(a.dq);
   Tin* dk = static_cast<Tin*>(a.dk);
   for (int pass = 0; pass < 2; ++pass) {
@@ -739,24 +861,30 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_grads_kernel(const GdnArgs a)
         ka[m] = fmaf(Fa[t * kSq + s] + Fa[s * kSq + t], kv, ka[m]);     // (dA o b f) K + its transpose
       }
     }
-    for (int j0 = 0; j0 < Dv; j0 += 16) {
+    for (int j0 = 0; j0 < ns * kSlice; j0 += 16) {
+      const int sl = j0 / kSlice, off = j0 % kSlice;
       __syncthreads();
-      for (int idx = tid; idx < kMaxD * 16; idx += kThreads) {
-        const int ii = idx / 16, jj = j0 + idx % 16;
-        const bool in = ii < Dk && jj < Dv;
-        hst[idx] = (in && h0) ? __ldcg(h0 + ii * Dv + jj) : 0.f;
-        dst[idx] = in ? __ldcg(dhe + ii * Dv + jj) : 0.f;
+      const float* hg = pred >= 0 ? slice_block(w.states, pred, h, sl, H, ns, Dk) : nullptr;
+      const float* dg = slice_block(w.dend, c, h, sl, H, ns, Dk);
+      for (int idx = tid; idx < Dk * 16; idx += kThreads) {
+        const int ii = idx / 16, jj = idx % 16;
+        if (hg) cp4(hst + ii * kSt + jj, hg + ii * kSlice + off + jj);
+        else hst[ii * kSt + jj] = 0.f;
+        cp4(dst + ii * kSt + jj, dg + ii * kSlice + off + jj);
       }
+      cp_wait();
       __syncthreads();
       const int jn = min(16, Dv - j0);
-      for (int jj = 0; jj < jn; ++jj) {
-        const float hv = hst[i * 16 + jj], dv = dst[i * 16 + jj];
+      if (i < Dk) {
+        for (int jj = 0; jj < jn; ++jj) {
+          const float hv = hst[i * kSt + jj], dv = dst[i * kSt + jj];
 #pragma unroll
-        for (int m = 0; m < 16; ++m) {
-          const int t = t0 + m;
-          z1[m] = fmaf(Os[t * kRow + j0 + jj], hv, z1[m]);   // (dO h0^T)_ti
-          z2[m] = fmaf(Rs[t * kRow + j0 + jj], hv, z2[m]);   // (dr h0^T)_ti
-          z3[m] = fmaf(Us[t * kRow + j0 + jj], dv, z3[m]);   // (u dh_end^T)_ti
+          for (int m = 0; m < 16; ++m) {
+            const int t = t0 + m;
+            z1[m] = fmaf(Os[t * kRow + j0 + jj], hv, z1[m]);   // (dO h0^T)_ti
+            z2[m] = fmaf(Rs[t * kRow + j0 + jj], hv, z2[m]);   // (dr h0^T)_ti
+            z3[m] = fmaf(Us[t * kRow + j0 + jj], dv, z3[m]);   // (u dh_end^T)_ti
+          }
         }
       }
     }
@@ -796,28 +924,46 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_grads_kernel(const GdnArgs a)
   }
   __syncthreads();
   // the chain's per-row sums (over the slices, in order), then dg as the reverse running
-  // sum of d lg over the sub-chunk
-  if (tid == 0) {
-    float he = 0.f, dws = 0.f;
+  // sum of d lg over the sub-chunk: the first two warps own one row each
+  float dw = 0.f;
+  if (tid < kChunk && tid < L) {
+    float rv = 0.f;
+    for (int sl = 0; sl < ns; ++sl) {
+      dw += w.part[((static_cast<int64_t>(sl) * 2 + 0) * T + r0 + tid) * H + h];
+      rv += w.part[((static_cast<int64_t>(sl) * 2 + 1) * T + r0 + tid) * H + h];
+    }
+    dlg[tid] -= dw;
+    dbt[tid] += rv;
+  }
+  if (tid < kChunk) {
+    float x = dw;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    if (lane == 0) s_part[warp] = x;
+  }
+  if (tid == 64) {
+    float he = 0.f;
     for (int sl = 0; sl < ns; ++sl) he += w.part_he[(static_cast<int64_t>(sl) * n_chunks + c) * H + h];
-    for (int t = 0; t < L; ++t) {
-      float dw = 0.f, rv = 0.f;
-      for (int sl = 0; sl < ns; ++sl) {
-        dw += w.part[((static_cast<int64_t>(sl) * 2 + 0) * T + r0 + t) * H + h];
-        rv += w.part[((static_cast<int64_t>(sl) * 2 + 1) * T + r0 + t) * H + h];
-      }
-      dlg[t] -= dw;
-      dws += dw;
-      dbt[t] += rv;
+    s_part[2] = he;
+  }
+  __syncthreads();
+  if (tid == 0) dlg[L - 1] += (s_part[0] + s_part[1]) + E[L - 1] * s_part[2];
+  __syncthreads();
+  if (tid < kChunk) {
+    float x = tid < L ? dlg[L - 1 - tid] : 0.f;   // reversed rows, then an inclusive scan
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
     }
-    dlg[L - 1] += dws + E[L - 1] * he;
-    float run = 0.f;
-    for (int t = L - 1; t >= 0; --t) {
-      run += dlg[t];
-      const int64_t row = static_cast<int64_t>(r0 + t) * H + h;
-      a.dg[row] = run;
-      a.dbeta[row] = dbt[t];
-    }
+    if (tid == 31) s_part[3] = x;
+    M1[tid] = x;
+  }
+  __syncthreads();
+  if (tid < L) {
+    const float x = M1[tid] + (tid >= 32 ? s_part[3] : 0.f);
+    a.dg[static_cast<int64_t>(r0 + L - 1 - tid) * H + h] = x;
+    a.dbeta[static_cast<int64_t>(r0 + tid) * H + h] = dbt[tid];
   }
 }
 
@@ -872,21 +1018,30 @@ int gdn_begin(GdnArgs& a, const void* q, const void* k, const void* v, const flo
                 (long long)mc, H);
   if (!q || !k || !v || !g || !beta || !node_start || !node_end || !node_parent || !outs_ok)
     return fail(TREE_ERR_INVALID_ARG, "%s: null pointer", name);
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v))
+    return fail(TREE_ERR_ALIGNMENT, "%s: q, k or v not 16-byte aligned", name);
   const size_t need = gdn_ws_layout(T, n_nodes, H, Dk, Dv, bwd, nullptr, nullptr);
   if (workspace_bytes < need)
     return fail(TREE_ERR_WORKSPACE, "%s: workspace of %zu bytes, %zu needed", name, workspace_bytes, need);
   if (!workspace || !aligned256(workspace))
     return fail(TREE_ERR_ALIGNMENT, "%s: workspace null or not 256-byte aligned", name);
   a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta;
-  a.T = static_cast<int>(T); a.H = H; a.Dk = Dk; a.Dv = Dv; a.ns = gdn_slices(Dv);
+  a.T = static_cast<int>(T); a.H = H; a.Dk = Dk; a.Dv = Dv; a.ns = gdn_slices(Dv); a.DkP = (Dk + 3) / 4 * 4;
   a.withhold = static_cast<int>(g_withhold.exchange(-1));
   const unsigned long long wns = g_wait_ns.exchange(0);
   a.wait_ns = wns ? wns : sm100::kWaitNs;
   a.err = device_error_word();
   gdn_ws_layout(T, n_nodes, H, Dk, Dv, bwd, workspace, &a.w);
   const int64_t n_flags = mc * H * a.ns;
-  gdn_setup_kernel<<<1, 1024, 0, st>>>(node_start, node_end, node_parent, static_cast<int>(n_nodes),
-                                       static_cast<int>(T), n_flags, a.w, static_cast<int>(mc), a.err);
+  const size_t setup_bytes = sizeof(int) * setup_ints(n_nodes, mc);
+  const int fits = setup_bytes <= 200 * 1024;
+  if (fits) {
+    int rc = smem_opt_in(reinterpret_cast<const void*>(gdn_setup_kernel), static_cast<int>(setup_bytes));
+    if (rc) return rc;
+  }
+  gdn_setup_kernel<<<1, kSetupThreads, fits ? setup_bytes : 0, st>>>(
+      node_start, node_end, node_parent, static_cast<int>(n_nodes), static_cast<int>(T), n_flags, a.w,
+      static_cast<int>(mc), fits, a.err);
   TREE_LAUNCH_CHECK("gdn_setup_kernel");
   *mc_out = mc;
   return TREE_OK;
@@ -961,6 +1116,7 @@ extern "C" int tree_gdn_bwd(const void* q, const void* k, const void* v, const f
                      workspace, workspace_bytes, true, dout && dq && dk && dv && dg && dbeta, "tree_gdn_bwd", st,
                      &mc, &empty);
   if (rc || empty) return rc;
+  if (!aligned16(dout)) return fail(TREE_ERR_ALIGNMENT, "tree_gdn_bwd: dout not 16-byte aligned");
   a.dout = dout; a.dq = dq; a.dk = dk; a.dv = dv; a.dg = dg; a.dbeta = dbeta;
   return dtype == TREE_DTYPE_BF16 ? gdn_backward<__nv_bfloat16>(a, mc, st) : gdn_backward<float>(a, mc, st);
 }
