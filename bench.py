@@ -57,6 +57,8 @@ def parse_args(argv=None):
                     help="timed steps of each tree that is not the headline workload")
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--lm-steps", type=int, default=3)
+    ap.add_argument("--lm-rows", type=int, default=8192,
+                    help="packed rows of the LM-head tree (mean path count 2.2); smaller for profiling")
     ap.add_argument("--no-lm", action="store_true")
     ap.add_argument("--conv-steps", type=int, default=10)
     ap.add_argument("--no-conv", action="store_true")
@@ -500,7 +502,8 @@ def run_lm_head(args, dev, peaks, peak_src):
     """Shared-logit log-prob forward + backward on the 8192 x 4096 x 128256 workload."""
     import torch
     import tree_masked_attention_gb300 as tma
-    tree = synth.lm_head_tree()
+    rows = args.lm_rows
+    tree = synth.lm_head_tree(rows=rows, occ_range=(round(rows * 17500 / 8192), round(rows * 18500 / 8192)))
     pk = tma.tree_pack(tree.seqs)
     T, K, V = pk["T"], 4096, 128256
     n_occ = pk["n_occ"]

@@ -260,11 +260,15 @@ int tree_logprob_fwd(const void* hidden, const void* w_lm, const int32_t* occ_ro
                      int dtype, void* workspace, size_t workspace_bytes,
                      tree_stream_t stream);
 
+/* dw_fp32 = 1 writes d_w in fp32 ([K_h, V] floats: the fp32 accumulation itself, for a
+ * caller that keeps fp32 master weights; [TT] Appendix B.5 keeps gradients summed over
+ * shared rows in fp32), 0 writes it in dtype. With TREE_DTYPE_F32 d_w is fp32 either way.
+ * Any other value: TREE_ERR_INVALID_ARG. */
 int tree_logprob_bwd(const void* hidden, const void* w_lm, const float* lse,
                      const int32_t* occ_row_ptr, const int32_t* occ_perm,
                      const int32_t* occ_targets, const float* grad_logp, int64_t T,
                      int64_t K_h, int64_t V, int64_t n_occ, void* d_hidden, void* d_w,
-                     int dtype, void* workspace, size_t workspace_bytes,
+                     int dw_fp32, int dtype, void* workspace, size_t workspace_bytes,
                      tree_stream_t stream);
 
 /* ------------------------------------------------------------------------ */

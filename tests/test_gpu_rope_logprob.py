@@ -123,3 +123,58 @@ def test_logprob_full_size_sampled():
     assert_close("dH sampled", host(dh)[rows], gz @ w.astype(np.float64).T, BF16_TOL)
     colsum = dw.float().sum(dim=1).double().cpu().numpy()
     assert np.abs(colsum).max() < 0.5, np.abs(colsum).max()
+
+
+@pytest.mark.parametrize("T,K,V", [(200, 128, 1000), (333, 256, 4104)])
+def test_logprob_dw_fp32(T, K, V):
+    """dw_fp32: d_w written in fp32 straight from the accumulator. Its only rounding is
+    that of the G_z operand the tensor cores read in bf16 (relative 2^-9 at cells other
+    than the targets, whose exact values are added back), so per element
+    |dW - ref| <= 1e-4 + 2^-8 sum_r |H[r, m]| |G_z[r, v]|, with G_z from the oracle."""
+    need_cuda()
+    m = tma()
+    h, w, src, tg, wt, row_ptr, perm = _lm_case(T, K, V, T - 7, True, seed=T + 1)
+    tg[::5] = tg[0]
+    th, tw = dev(h, torch.bfloat16), dev(w, torch.bfloat16)
+    lse, _ = m.tree_logprob_fwd(th, tw, dev(row_ptr), dev(perm), dev(tg))
+    g = (-wt).astype(np.float32)
+    dh, dw = m.tree_logprob_bwd(th, tw, lse, dev(row_ptr), dev(perm), dev(tg), dev(g), dw_fp32=True)
+    m.tree_check_device_status()
+    assert dw.dtype == torch.float32
+    rdh, rdw = oracle.logprob_ref_bwd(h, w, src, tg, g)
+    rows = np.arange(T)
+    gz = oracle.logprob_ref_gz(h, w, src, tg, g, rows)
+    bound = 1e-4 + 2.0 ** -8 * (np.abs(h.astype(np.float64)).T @ np.abs(gz))
+    err = np.abs(dw.double().cpu().numpy() - rdw)
+    worst = np.unravel_index(np.argmax(err - bound), err.shape)
+    assert (err <= bound).all(), (float(err[worst]), float(bound[worst]), worst)
+    assert_close("dH", dh, rdh, BF16_TOL)
+
+
+def test_logprob_full_rows_and_vocab():
+    """Every row of the 8192-row tree (18,475 occurrences over 8,174 rows, targets over the
+    full 128,256-token vocabulary, some repeated) with hidden size 128: dH and dW, in bf16
+    and in fp32, checked element-wise against one oracle pass everywhere, so the
+    target-cell correction of dW runs at full occurrence density across every vocabulary
+    block."""
+    need_cuda()
+    m = tma()
+    t = synth.lm_head_tree()
+    pk = m.tree_pack(t.seqs)
+    T, K, V = pk["T"], 128, 128256
+    h, w, tg, wt = synth.lm_head_config(T, K, V, pk["n_occ"], bf16=True)
+    tg[::7] = tg[3]                     # a column that many occurrences share
+    src = pk["occ_source_rows"]
+    th, tw = dev(h, torch.bfloat16), dev(w, torch.bfloat16)
+    row_ptr, perm = dev(pk["occ_row_ptr"]), dev(pk["occ_perm"])
+    lse, logp = m.tree_logprob_fwd(th, tw, row_ptr, perm, dev(tg))
+    g = (-wt).astype(np.float32)
+    dh, dw = m.tree_logprob_bwd(th, tw, lse, row_ptr, perm, dev(tg), dev(g))
+    _, dw32 = m.tree_logprob_bwd(th, tw, lse, row_ptr, perm, dev(tg), dev(g), dw_fp32=True)
+    m.tree_check_device_status()
+    rdh, rdw = oracle.logprob_ref_bwd(h, w, src, tg, g, chunk=512)
+    assert_close("dH", dh, rdh, BF16_TOL)
+    assert_close("dW (bf16)", dw, rdw, BF16_TOL)
+    assert_close("dW (fp32)", dw32, rdw, BF16_TOL)
+    # the fp32 output is the accumulator the bf16 output rounds
+    assert torch.equal(dw32.to(torch.bfloat16), dw)

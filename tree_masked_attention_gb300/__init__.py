@@ -436,21 +436,26 @@ def tree_logprob_fwd(hidden, w_lm, occ_row_ptr, occ_perm, occ_targets, workspace
 
 
 def tree_logprob_bwd(hidden, w_lm, lse, occ_row_ptr, occ_perm, occ_targets, grad_logp, workspace=None,
-                     grads=None):
-    """Backward of the shared-logit log-probs; returns (d_hidden, d_w) in the input dtype."""
+                     grads=None, dw_fp32: bool = False):
+    """Backward of the shared-logit log-probs; returns (d_hidden, d_w): d_hidden in the
+    input dtype, d_w in the input dtype or, with dw_fp32, in fp32."""
     torch = _torch()
     T, K = hidden.shape
     V = w_lm.shape[1]
     n_occ = occ_targets.shape[0]
     dt = _dtype_code(hidden)
-    dh, dw = (torch.empty_like(hidden), torch.empty_like(w_lm)) if grads is None else grads
+    dw_dtype = torch.float32 if dw_fp32 else hidden.dtype
+    if grads is None:
+        dh, dw = torch.empty_like(hidden), torch.empty((K, V), dtype=dw_dtype, device=hidden.device)
+    else:
+        dh, dw = grads
     ws = _workspace(tree_logprob_workspace_size(T, K, V, n_occ, dt), hidden.device, workspace)
     i32 = torch.int32
     check(lib().tree_logprob_bwd(_dev(hidden, "hidden"), _dev(w_lm, "w_lm", hidden.dtype),
                                  _dev(lse, "lse", torch.float32), _dev(occ_row_ptr, "occ_row_ptr", i32),
                                  _dev(occ_perm, "occ_perm", i32), _dev(occ_targets, "occ_targets", i32),
                                  _dev(grad_logp, "grad_logp", torch.float32), T, K, V, n_occ,
-                                 _dev(dh, "d_hidden", hidden.dtype), _dev(dw, "d_w", hidden.dtype), dt,
+                                 _dev(dh, "d_hidden", hidden.dtype), _dev(dw, "d_w", dw_dtype), int(bool(dw_fp32)), dt,
                                  C.c_void_p(ws.data_ptr()), ws.numel() * ws.element_size(),
                                  _stream(hidden)), "tree_logprob_bwd")
     return dh, dw

@@ -80,7 +80,7 @@ SIGNATURES = {
     "tree_logprob_fwd": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp, _int,
                                 _vp, _sz, _vp]),
     "tree_logprob_bwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp,
-                                _vp, _int, _vp, _sz, _vp]),
+                                _vp, _int, _int, _vp, _sz, _vp]),
     "tree_check_device_status": (_int, [_vp]),
     "tree_last_error": (C.c_char_p, []),
     "tree_kernel_path": (_int, [_int, _int, _int]),

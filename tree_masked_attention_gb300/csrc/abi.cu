@@ -232,13 +232,14 @@ extern "C" int tree_logprob_fwd(const void* hidden, const void* w_lm, const int3
 extern "C" int tree_logprob_bwd(const void* hidden, const void* w_lm, const float* lse,
                                 const int32_t* occ_row_ptr, const int32_t* occ_perm,
                                 const int32_t* occ_targets, const float* grad_logp, int64_t T, int64_t K_h,
-                                int64_t V, int64_t n_occ, void* d_hidden, void* d_w, int dtype,
+                                int64_t V, int64_t n_occ, void* d_hidden, void* d_w, int dw_fp32, int dtype,
                                 void* workspace, size_t workspace_bytes, tree_stream_t stream) {
   clear_error();
   int rc = check_lm(hidden, w_lm, occ_row_ptr, occ_perm, occ_targets, T, K_h, V, n_occ, dtype);
   if (rc) return rc;
   if (!lse || !d_hidden || !d_w || (n_occ > 0 && !grad_logp))
     return fail(TREE_ERR_INVALID_ARG, "tree_logprob_bwd: null pointer");
+  if (dw_fp32 != 0 && dw_fp32 != 1) return fail(TREE_ERR_INVALID_ARG, "tree_logprob_bwd: dw_fp32 = %d", dw_fp32);
   if (!aligned16(d_hidden) || !aligned16(d_w))
     return fail(TREE_ERR_ALIGNMENT, "tree_logprob_bwd: d_hidden / d_w not 16-byte aligned");
   const size_t need = logprob_ws_layout(T, K_h, V, n_occ, dtype, nullptr, nullptr);
@@ -247,6 +248,7 @@ extern "C" int tree_logprob_bwd(const void* hidden, const void* w_lm, const floa
   a.h = hidden; a.w = w_lm; a.row_ptr = occ_row_ptr; a.perm = occ_perm; a.targets = occ_targets;
   a.grad = grad_logp; a.lse = const_cast<float*>(lse); a.dh = d_hidden; a.dw = d_w;
   a.T = T; a.K = K_h; a.V = V; a.n_occ = n_occ; a.dtype = dtype;
+  a.dw_fp32 = dtype == TREE_DTYPE_F32 ? 1 : dw_fp32;
   logprob_ws_layout(T, K_h, V, n_occ, dtype, workspace, &a.ws);
   if (logprob_tc_supported(dtype)) return logprob_bwd_tc(a, reinterpret_cast<cudaStream_t>(stream));
   return logprob_bwd_simt(a, reinterpret_cast<cudaStream_t>(stream));

@@ -92,6 +92,7 @@ struct LogprobArgs {
   void* dw;
   int64_t T, K, V, n_occ;
   int dtype;
+  int dw_fp32;         // backward: d_w in fp32 whatever dtype is
   LogprobWs ws;
 };
 

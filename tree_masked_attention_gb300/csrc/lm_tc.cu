@@ -79,6 +79,7 @@ struct Params {
   const float* crow;
   const float* grad;
   __nv_bfloat16* out;    // EPI_GZ: G_z [M, N]; EPI_STORE / EPI_DW: C [M, N]
+  float* out_f32;        // EPI_DW: when set, C [M, N] is written in fp32 here instead of `out`
   float* occ_delta;      // EPI_GZ writes, EPI_DW reads: exact - stored G_z at target cells
   const int32_t* blk_ptr;  // EPI_DW: occurrences grouped by 256-column target block
   const int32_t* blk_ent;  //         {source row, occurrence}
@@ -268,6 +269,21 @@ lm_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
             for (int u = 0; u < 32; ++u)
               if (u == idx) v[u] = __float_as_uint(__uint_as_float(v[u]) + x);
+          }
+          if (p.out_f32) {  // fp32 dW: the accumulator as it is
+            if (row_ok && c * 32 < ncols) {
+              float* dst = p.out_f32 + static_cast<int64_t>(m) * p.N + n0 + c * 32;
+              if (c * 32 + 32 <= ncols && (p.N % 4) == 0) {
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                  reinterpret_cast<float4*>(dst)[u] =
+                      make_float4(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
+                                  __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3]));
+              } else {
+                for (int u = 0; u < 32 && c * 32 + u < ncols; ++u) dst[u] = __uint_as_float(v[u]);
+              }
+            }
+            continue;
           }
 #pragma unroll
           for (int u = 0; u < 16; ++u) pk[u] = pack_bf16(__uint_as_float(v[2 * u]), __uint_as_float(v[2 * u + 1]));
@@ -580,7 +596,8 @@ int logprob_bwd_tc(const LogprobArgs& a, cudaStream_t st) {
     p.b_mn = 1;
     p.raster_group = LM_RASTER_GROUP_DW;
     p.epi = EPI_DW;
-    p.out = static_cast<__nv_bfloat16*>(a.dw);
+    if (a.dw_fp32) p.out_f32 = static_cast<float*>(a.dw);
+    else p.out = static_cast<__nv_bfloat16*>(a.dw);
     p.targets = a.targets;
     p.occ_delta = a.ws.occ_delta;
     p.blk_ptr = a.ws.blk_ptr;
