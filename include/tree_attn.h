@@ -176,8 +176,11 @@ int tree_rope(void* q, void* k, const int32_t* position_ids, int64_t T, int Hq, 
  * (end < i or end >= T) set TREE_ERR_DEVICE_CHECK in the device error word;
  * outputs are then unspecified (never out-of-bounds accesses). Nesting is not
  * checked on the device (see tree_validate_subtree_end).
- * deterministic: 0 lets dQ accumulate with fp32 atomics (order may vary run to
- * run); 1 computes dQ without atomics (bitwise reproducible, more FLOPs).
+ * deterministic: 0 lets dQ, dK and dV accumulate with fp32 reductions from work units
+ * that run in any order (results may differ in the last bits run to run); 1 makes
+ * every sum fixed-order and the results bitwise reproducible: dK and dV come from one
+ * work unit per key tile, and dQ from a second, query-stationary pass that walks each
+ * query tile's key tiles in order (S and dP recomputed: more FLOPs, slower).
  */
 size_t tree_attn_workspace_size(int64_t T, int Hq, int Hkv, int d, int dtype);
 

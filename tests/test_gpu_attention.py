@@ -69,6 +69,13 @@ def test_deterministic_matches_default():
     _full_check(t.seqs, 4, 2, 128, "bf16", seed=8, deterministic=True)
 
 
+def test_deterministic_short_prompt_agentic_full_size():
+    """The deterministic backward (one work unit per key tile for dK / dV, query-stationary
+    dQ in key-tile order) on the full short-prompt agentic tree, against the oracle."""
+    t = synth.agentic_short()
+    _full_check(t.seqs, 32, 8, 128, "bf16", seed=5, deterministic=True)
+
+
 def test_short_prompt_agentic_full_size():
     """The short-prompt agentic tree at full size (T = 2304, 32/8 heads, d = 128, bf16)."""
     t = synth.agentic_short()

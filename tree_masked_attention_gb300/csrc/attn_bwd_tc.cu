@@ -37,6 +37,7 @@
 #include <cmath>
 
 #include "attn_internal.h"
+#include "attn_mask.cuh"
 #include "common.h"
 #include "device_common.cuh"
 #include "sm100.cuh"
@@ -560,6 +561,7 @@ struct PrepParams {
   const int32_t* end;  // subtree_end [T] (of the key rows)
   int T, T_pad, n_kt, Hq, Hkv, max_units;  // T: key rows; T_pad: query rows rounded up to 64
   int Tq, q_off, n_rows;                   // query rows, keys before them, rows the blocks cover
+  int one_unit_per_tile;                   // deterministic mode: every key tile is one unit
   int32_t* kmax;       // [n_kt] max subtree_end of each 128-key tile
   int32_t* kmin;       // [n_kt] min subtree_end of each 128-key tile
   int32_t* endp;       // [n_kt * 128] subtree_end, -1 past T
@@ -675,7 +677,7 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const PrepParams q) 
   const long long steps_all = s_total * G * q.Hkv;
   // ~8 units per SM on large trees; on small ones the 16-step floor keeps units short
   const int chunk_steps = static_cast<int>(max(16LL, (steps_all + 1215) / 1216));
-  const int chunk_q = (chunk_steps + G - 1) / G;
+  const int chunk_q = q.one_unit_per_tile ? (INT32_MAX / 4) : (chunk_steps + G - 1) / G;
   for (int kt = threadIdx.x; kt < q.n_kt; kt += blockDim.x) {  // units per first query tile
     int lo;
     const int nq = tiles_of(kt, &lo);
@@ -715,6 +717,231 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const PrepParams q) 
 }
 
 }  // namespace tcbwd
+
+// ------------------------------------------------------------------------------------
+// Deterministic dQ (the backward's deterministic mode): query-stationary. One CTA owns 128
+// query rows of one query head and walks the key tiles its rows can see in increasing
+// order, with dQ accumulating in TMEM, so every dQ element is one fixed-order sum:
+//   S = Q K^T, dP = dO V^T                  (M = 128 queries, N = 128 keys, K = d; TMEM)
+//   P = exp2(S scale log2e - LSE log2e) on visible pairs, dS = P (dP - Delta)   (4 warps,
+//                                           one query row per thread, 64 keys at a time)
+//   dQ += dS K                               (A = dS bf16 from TMEM over S's columns,
+//                                           B = the K tile MN-major)
+// and scale * dQ is stored (not added) into the fp32 accumulator the conversion reads.
+// Warps 0-3 compute, warp 4 TMA, warp 5 MMA. TMEM: S [0, 128), dP [128, 256), dQ [256, 384).
+namespace tcdq {
+using tcbwd::ex2_approx;
+
+constexpr int BM = 128, BN = 128, D = 128;
+constexpr int kThreads = 192;
+constexpr int kWarpProducer = 4, kWarpMma = 5;
+constexpr uint32_t kSub = 128 * 128;   // 128 rows x 128 B: one swizzle-128 sub-tile
+constexpr uint32_t kTile = 2 * kSub;   // 128 rows x 128 bf16
+
+struct Smem {
+  uint8_t q[kTile];
+  uint8_t dout[kTile];
+  uint8_t k[2][kTile];
+  uint8_t v[2][kTile];
+  uint64_t qdo_full, k_full[2], v_full[2], kv_empty[2], sd_full, ds_full, mma_done;
+  uint32_t tmem_base;
+};
+constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
+static_assert(kSmemBytes <= 232448, "dQ kernel shared memory exceeds the per-block limit");
+
+struct Params {
+  int T, Tq, T_pad, Hq, Hkv, n_qt, n_kt;
+  float scale_log2, scale;
+  const int32_t* kmax;
+  const int32_t* kmin;
+  const int32_t* endp;
+  const float* lse2;    // [Hq, T_pad] LSE * log2(e)
+  const float* delta;   // [Hq, T_pad]
+  float* dq_acc;        // [Tq, Hq, d] fp32, written
+  int* err;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+attn_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
+                  const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  if (p.err && (*reinterpret_cast<volatile int*>(p.err) & (1 << TREE_ERR_TIMEOUT))) return;
+  Smem& S = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int h = blockIdx.y;
+  const int qt = p.n_qt - 1 - blockIdx.x;  // longest query tiles first
+  const int i0 = qt * BM;
+  const int kt_hi = min((i0 + BM - 1) / BN, p.n_kt - 1);
+  const int kvh = h / (p.Hq / p.Hkv);
+  if (threadIdx.x == 0) {
+    mbar_init(&S.qdo_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&S.k_full[s], 1);
+      mbar_init(&S.v_full[s], 1);
+      mbar_init(&S.kv_empty[s], 1);
+    }
+    mbar_init(&S.sd_full, 1);
+    mbar_init(&S.ds_full, 4);
+    mbar_init(&S.mma_done, 1);
+    fence_mbarrier_init();
+  }
+  if (warp == kWarpMma) tmem_alloc(&S.tmem_base, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = S.tmem_base;
+  constexpr uint32_t kColDP = 128, kColDQ = 256;
+
+  if (warp == kWarpProducer) {
+    if (lane == 0) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmDO);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      mbar_arrive_expect_tx(&S.qdo_full, 2 * kTile);
+      for (int sub = 0; sub < 2; ++sub) {
+        tma_load_3d(S.q + sub * kSub, &tmQ, &S.qdo_full, sub * 64, h, i0);
+        tma_load_3d(S.dout + sub * kSub, &tmDO, &S.qdo_full, sub * 64, h, i0);
+      }
+      int n = 0;
+      for (int kt = 0; kt <= kt_hi; ++kt) {
+        if (p.kmax[kt] < i0) continue;
+        const int s = n & 1;
+        if (n >= 2 && !mbar_wait(&S.kv_empty[s], ((n >> 1) - 1) & 1, p.err)) break;
+        mbar_arrive_expect_tx(&S.k_full[s], kTile);
+        tma_load_3d(S.k[s], &tmK, &S.k_full[s], 0, kvh, kt * BN);
+        tma_load_3d(S.k[s] + kSub, &tmK, &S.k_full[s], 64, kvh, kt * BN);
+        mbar_arrive_expect_tx(&S.v_full[s], kTile);
+        tma_load_3d(S.v[s], &tmV, &S.v_full[s], 0, kvh, kt * BN);
+        tma_load_3d(S.v[s] + kSub, &tmV, &S.v_full[s], 64, kvh, kt * BN);
+        ++n;
+      }
+      for (int m = (n >= 2 ? n - 2 : 0); m < n; ++m) {
+        mbar_wait(&S.k_full[m & 1], (m >> 1) & 1, p.err);
+        mbar_wait(&S.v_full[m & 1], (m >> 1) & 1, p.err);
+      }
+      mbar_wait(&S.qdo_full, 0, p.err);
+    }
+  } else if (warp == kWarpMma) {
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16(BM, BN, 0, 0);   // S, dP: both operands K-major
+      constexpr uint32_t idesc_q = idesc_bf16(BM, D, 0, 1);    // dQ: B = K tile MN-major
+      int N = 0;
+      for (int kt = 0; kt <= kt_hi; ++kt) N += p.kmax[kt] >= i0;
+      const uint32_t qa = smem_u32(S.q), oa = smem_u32(S.dout);
+      bool ok = mbar_wait(&S.qdo_full, 0, p.err);
+      for (int n = 0; ok && n < N; ++n) {
+        const int s = n & 1;
+        if (!(ok = mbar_wait(&S.k_full[s], (n >> 1) & 1, p.err) && mbar_wait(&S.v_full[s], (n >> 1) & 1, p.err)))
+          break;
+        tc_fence_after();
+        const uint32_t kb = smem_u32(S.k[s]), vb = smem_u32(S.v[s]);
+        // S over the columns dS(n-1) occupied: the MMAs run in issue order, so dQ(n-1),
+        // issued before, has read them
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kSub + (kk & 3) * 32;
+          mma_ss(tmem, desc_sw128(qa + off, 16, 1024), desc_sw128(kb + off, 16, 1024), idesc_s, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kSub + (kk & 3) * 32;
+          mma_ss(tmem + kColDP, desc_sw128(oa + off, 16, 1024), desc_sw128(vb + off, 16, 1024), idesc_s, kk > 0);
+        }
+        mma_commit(&S.sd_full);
+        if (!(ok = mbar_wait(&S.ds_full, n & 1, p.err))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)  // dQ += dS K: dS (bf16 pairs) at columns 0..63
+          mma_ts(tmem + kColDQ, tmem + kk * 8, desc_sw128(kb + kk * 2048, kSub, 1024), idesc_q,
+                 (n > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&S.kv_empty[s]);
+      }
+      mma_commit(&S.mma_done);
+      mbar_wait(&S.mma_done, 0, p.err);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ compute warps 0-3
+    const int r = warp * 32 + lane, i = i0 + r;
+    const uint32_t lanes = static_cast<uint32_t>(warp * 32) << 16;
+    const float sl2 = p.scale_log2;
+    const bool row_ok = i < p.Tq;
+    const float l2 = row_ok ? p.lse2[static_cast<int64_t>(h) * p.T_pad + i] : INFINITY;
+    const float dl = row_ok ? p.delta[static_cast<int64_t>(h) * p.T_pad + i] : 0.f;
+    int n = 0;
+    bool ok = true;
+    for (int kt = 0; kt <= kt_hi; ++kt) {
+      if (p.kmax[kt] < i0) continue;
+      const int j0 = kt * BN;
+      const bool partial = !(j0 + BN - 1 <= i0 && p.kmin[kt] >= i0 + BM - 1);
+      uint32_t vis[4] = {~0u, ~0u, ~0u, ~0u};
+      if (partial) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) vis[c] = visible32(p.endp, j0 + 32 * c, i);
+      }
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&S.sd_full, n & 1, p.err)))) break;
+      tc_fence_after();
+      // 64 keys at a time: S and dP of those keys, then dS (bf16 pairs) over S's first
+      // columns (half 0 -> columns 0..31, half 1 -> 32..63: both already read)
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        uint32_t sv[64], dp[64];
+        tmem_ld32(tmem + lanes + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+        tmem_ld32(tmem + lanes + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+        tmem_ld32(tmem + lanes + kColDP + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&dp[0]));
+        tmem_ld32(tmem + lanes + kColDP + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&dp[32]));
+        tmem_ld_wait();
+        uint32_t pk[32];
+#pragma unroll
+        for (int t = 0; t < 64; t += 2) {
+          const int key = half * 64 + t;
+          const bool v0 = (vis[key >> 5] >> (key & 31)) & 1u, v1 = (vis[(key + 1) >> 5] >> ((key + 1) & 31)) & 1u;
+          const float p0 = v0 ? ex2_approx(fmaf(__uint_as_float(sv[t]), sl2, -l2)) : 0.f;
+          const float p1 = v1 ? ex2_approx(fmaf(__uint_as_float(sv[t + 1]), sl2, -l2)) : 0.f;
+          pk[t / 2] = pack_bf16(p0 * (__uint_as_float(dp[t]) - dl), p1 * (__uint_as_float(dp[t + 1]) - dl));
+        }
+        tmem_st32(tmem + lanes + half * 32, pk);
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.ds_full);
+      ++n;
+    }
+    // epilogue: scale * dQ (fp32) into the accumulator rows of this head
+    ok = __all_sync(0xffffffffu, ok && mbar_wait(&S.mma_done, 0, p.err));
+    tc_fence_after();
+    if (ok) {
+      float4* dst = reinterpret_cast<float4*>(p.dq_acc + (static_cast<int64_t>(i) * p.Hq + h) * D);
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        if (n > 0) {
+          tmem_ld32(tmem + lanes + kColDQ + c * 32, o);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int t = 0; t < 32; ++t) o[t] = 0u;
+        }
+        if (row_ok) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            dst[8 * c + u] = make_float4(__uint_as_float(o[4 * u]) * p.scale, __uint_as_float(o[4 * u + 1]) * p.scale,
+                                         __uint_as_float(o[4 * u + 2]) * p.scale, __uint_as_float(o[4 * u + 3]) * p.scale);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace tcdq
 
 // dQ, dK and dV (bf16) from their fp32 accumulators in one launch, 4 elements per thread.
 __global__ void attn_grads_to_bf16_kernel(const float* __restrict__ aq, __nv_bfloat16* __restrict__ oq, int64_t nq4,
@@ -818,7 +1045,8 @@ static int rows_map(CUtensorMap* m, const void* base, int64_t T, int H, uint32_t
 }
 
 bool attn_bwd_tc_supported(int dtype, int d, int deterministic) {
-  return dtype == TREE_DTYPE_BF16 && d == 128 && deterministic == 0;
+  (void)deterministic;  // both modes run on the tensor-core kernels
+  return dtype == TREE_DTYPE_BF16 && d == 128;
 }
 
 int64_t attn_bwd_max_units(int64_t T, int Hkv) { return 4096 + static_cast<int64_t>(Hkv) * ((T + 127) / 128) + 64; }
@@ -883,6 +1111,7 @@ int attn_bwd_tc(const AttnArgs& a, cudaStream_t st) {
     q.dk_acc = a.ws.dk_acc;
     q.dv_acc = a.ws.dv_acc;
     q.err = device_error_word();
+    q.one_unit_per_tile = a.deterministic;
     const int64_t pre_blocks = (static_cast<int64_t>(q.n_rows) * a.Hq + 7) / 8;
     attn_bwd_prep_kernel<<<static_cast<unsigned>(1 + pre_blocks), 256, 0, st>>>(q);
     TREE_LAUNCH_CHECK("attn_bwd_prep_kernel");
@@ -937,6 +1166,36 @@ int attn_bwd_tc(const AttnArgs& a, cudaStream_t st) {
   attn_bwd_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(mk, mv, mq, mdo, mdq, mdk, mdv, p);
   TREE_LAUNCH_CHECK("attn_bwd_tc_kernel");
   timing_end(1, st);
+  if (a.deterministic) {
+    // dQ again, query-stationary in a fixed order, over the accumulator the kernel above
+    // added into in whatever order its units ran
+    using namespace tcdq;
+    CUtensorMap mq2, mdo2, mk2, mv2;
+    if ((rc = rows_map(&mq2, a.q, Tq, a.Hq, 128)) || (rc = rows_map(&mdo2, a.dout, Tq, a.Hq, 128)) ||
+        (rc = rows_map(&mk2, a.k, a.T, a.Hkv, 128)) || (rc = rows_map(&mv2, a.v, a.T, a.Hkv, 128)))
+      return rc;
+    if ((rc = smem_opt_in(reinterpret_cast<const void*>(attn_dq_tc_kernel), static_cast<int>(tcdq::kSmemBytes))))
+      return rc;
+    tcdq::Params d{};
+    d.T = static_cast<int>(a.T);
+    d.Tq = static_cast<int>(Tq);
+    d.T_pad = static_cast<int>(T_pad);
+    d.Hq = a.Hq;
+    d.Hkv = a.Hkv;
+    d.n_qt = static_cast<int>((Tq + 127) / 128);
+    d.n_kt = n_kt;
+    d.scale_log2 = a.scale * 1.4426950408889634f;
+    d.scale = a.scale;
+    d.kmax = a.ws.kmax128;
+    d.kmin = a.ws.kmin128;
+    d.endp = a.ws.end_pad;
+    d.lse2 = a.ws.lse2_pad;
+    d.delta = a.ws.delta_pad;
+    d.dq_acc = a.ws.dq_acc;
+    d.err = device_error_word();
+    attn_dq_tc_kernel<<<dim3(d.n_qt, a.Hq), tcdq::kThreads, tcdq::kSmemBytes, st>>>(mq2, mdo2, mk2, mv2, d);
+    TREE_LAUNCH_CHECK("attn_dq_tc_kernel");
+  }
   if (a.rope_pos) {
     const int64_t n = a.T * ((a.Hq + a.Hkv + 3) / 4) * 16 + a.T * a.Hkv * 32;
     const float e = static_cast<float>(-2.0 * std::log2(static_cast<double>(a.rope_theta)) / a.d);

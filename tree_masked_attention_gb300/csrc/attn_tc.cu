@@ -24,6 +24,7 @@
 #include <cmath>
 
 #include "attn_internal.h"
+#include "attn_mask.cuh"
 #include "common.h"
 #include "device_common.cuh"
 #include "sm100.cuh"
@@ -75,45 +76,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
-}
-
-// Bit t set iff key jb + t is visible to query i (jb <= i <= subtree_end[jb + t]).
-__device__ __forceinline__ uint32_t visible32(const int32_t* __restrict__ endp, int jb, int i) {
-  const int4* e4 = reinterpret_cast<const int4*>(endp + jb);
-  uint32_t bits = 0;
-#pragma unroll
-  for (int g = 0; g < 8; ++g) {
-    const int4 e = __ldg(e4 + g);
-    const int t = 4 * g;
-    bits |= (static_cast<uint32_t>((jb + t <= i) && (i <= e.x)) |
-             (static_cast<uint32_t>((jb + t + 1 <= i) && (i <= e.y)) << 1) |
-             (static_cast<uint32_t>((jb + t + 2 <= i) && (i <= e.z)) << 2) |
-             (static_cast<uint32_t>((jb + t + 3 <= i) && (i <= e.w)) << 3))
-            << t;
-  }
-  return bits;
-}
-
-// Masked, scaled scores of 32 keys (j0 .. j0+31) for query row i.
-__device__ __forceinline__ void scores32(const uint32_t (&raw)[32], float (&s)[32], float sl2, bool partial,
-                                         const int32_t* __restrict__ endp, int j0, int i) {
-  if (!partial) {
-#pragma unroll
-    for (int t = 0; t < 32; ++t) s[t] = __uint_as_float(raw[t]) * sl2;
-    return;
-  }
-  const int4* e4 = reinterpret_cast<const int4*>(endp + j0);
-#pragma unroll
-  for (int g = 0; g < 8; ++g) {
-    const int4 e = __ldg(e4 + g);
-    const int ev[4] = {e.x, e.y, e.z, e.w};
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int t = 4 * g + u;
-      const bool vis = (j0 + t <= i) && (i <= ev[u]);
-      s[t] = vis ? __uint_as_float(raw[t]) * sl2 : -INFINITY;
-    }
-  }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
