@@ -318,7 +318,7 @@ int tree_policy_loss(const float* logp, const float* old_logp, const float* adva
  * dk_past, dv_past: device fp32 [past_len, Hkv, d]: the past rows' gradients are
  * ADDED to them in fp32 (B.5), so that the child partitions sharing one gateway sum
  * without bf16 rounding in between -- zero them before the first child.
- * Runs on the tensor-core kernels only: bf16, d = 128, Hq / Hkv even (other
+ * Runs on the tensor-core kernels only: bf16, d = 128 (other
  * arguments: TREE_ERR_SHAPE / TREE_ERR_DTYPE). workspace: device, at least
  * tree_attn_gateway_workspace_size() bytes, 256-byte aligned. past_len = 0 is plain
  * tree attention (the same results as tree_attn_fwd / tree_attn_bwd).

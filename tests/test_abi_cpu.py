@@ -134,7 +134,7 @@ def test_conv1d_rejects_bad_sizes(tma):
 def test_gateway_and_gdn_reject_bad_arguments(tma):
     """Host-side checks of the gateway and GDN calls run before any device work."""
     L = tma.lib()
-    # gateway: tensor-core kernels only (bf16, d = 128, even group), T >= 1, past_len >= 0
+    # gateway: tensor-core kernels only (bf16, d = 128), T >= 1, past_len >= 0
     assert L.tree_attn_fwd_gateway(None, None, None, None, None, None, None, 10, 16, 4, 2, 64, 1, 0.0,
                                    None, 0, None) == 2
     assert L.tree_attn_fwd_gateway(None, None, None, None, None, None, None, 10, 16, 4, 2, 128, 0, 0.0,

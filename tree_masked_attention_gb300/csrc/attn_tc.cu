@@ -21,6 +21,8 @@
 //                     when the max grows by more than 2^8, P = exp2(s - m) to TMEM,
 //                     then the epilogue O / l -> bf16 -> swizzled smem -> TMA store.
 // TMEM: S_A [0,128) S_B [128,256) O_A [256,384) O_B [384,512) fp32 columns.
+// When the GQA group is odd, neighbouring query heads may read different KV heads: each
+// CTA then owns one query head (head B's columns, MMAs and softmax warps stay idle).
 #include <cmath>
 
 #include "attn_internal.h"
@@ -53,6 +55,7 @@ constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
 
 struct Params {
   int T, Hq, Hkv, n_qt;  // T: key rows
+  int nh;                // query heads per CTA: 2 (even GQA group), or 1 (odd group: head B idles)
   int Tq, q_off, n_kt;   // query rows, key rows before the first query, key tiles
   float scale_log2;
   const int32_t* kmax;
@@ -87,7 +90,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
   if (p.err && (*reinterpret_cast<volatile int*>(p.err) & (1 << TREE_ERR_TIMEOUT))) return;
   Smem& S = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int h0 = 2 * blockIdx.x;
+  const int h0 = p.nh * blockIdx.x;
   const int qt = p.n_qt - 1 - blockIdx.y;  // longest query tiles first
   const int i0 = qt * BM;                  // first query row of the tile (query buffers)
   const int iq0 = p.q_off + i0;            // the same row among the keys
@@ -118,8 +121,8 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
-      mbar_arrive_expect_tx(&S.q_full, 2 * kTile);
-      for (int hh = 0; hh < 2; ++hh)
+      mbar_arrive_expect_tx(&S.q_full, p.nh * kTile);
+      for (int hh = 0; hh < p.nh; ++hh)
         for (int sub = 0; sub < 2; ++sub) tma_load_3d(S.q[hh] + sub * kSub, &tmQ, &S.q_full, sub * 64, h0 + hh, i0);
       int n = 0;
       for (int kt = 0; kt <= kt_hi; ++kt) {
@@ -168,7 +171,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       if (ok) {
         tc_fence_after();
         issue_s(0, 0);
-        issue_s(1, 0);
+        if (p.nh == 2) issue_s(1, 0);
       }
       for (int n = 0; ok && n < N; ++n) {
         const int s = n & 1;
@@ -181,17 +184,19 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
           tc_fence_after();
           issue_s(0, s ^ 1);
         }
-        if (!(ok = mbar_wait(&S.p_full[1], n & 1, p.err))) break;
-        tc_fence_after();
-        issue_pv(1, s, n);
+        if (p.nh == 2) {
+          if (!(ok = mbar_wait(&S.p_full[1], n & 1, p.err))) break;
+          tc_fence_after();
+          issue_pv(1, s, n);
+        }
         mma_commit(&S.kv_empty[s]);
-        if (more) issue_s(1, s ^ 1);
+        if (more && p.nh == 2) issue_s(1, s ^ 1);
       }
       mma_commit(&S.mma_done);
       mbar_wait(&S.mma_done, 0, p.err);
     }
     __syncwarp();
-  } else if (warp < 8) {
+  } else if (warp < 4 * p.nh) {
     // ------------------------------------------------------------ softmax warps
     const int h = warp >> 2, q4 = warp & 3;
     const int r = q4 * 32 + lane, ik = iq0 + r;  // the thread's query row, as a key row
@@ -366,7 +371,9 @@ static int qkv_map(CUtensorMap* m, const void* base, int64_t T, int H) {
 }
 
 bool attn_fwd_tc_supported(int dtype, int d, int Hq, int Hkv) {
-  return dtype == TREE_DTYPE_BF16 && d == 128 && (Hq / Hkv) % 2 == 0;
+  (void)Hq;  // an odd GQA group runs one query head per CTA
+  (void)Hkv;
+  return dtype == TREE_DTYPE_BF16 && d == 128;
 }
 
 int attn_fwd_tc(const AttnArgs& a, cudaStream_t st) {
@@ -393,7 +400,8 @@ int attn_fwd_tc(const AttnArgs& a, cudaStream_t st) {
   p.endp = a.ws.end_pad;
   p.lse = a.lse;
   p.err = device_error_word();
-  dim3 grid(a.Hq / 2, p.n_qt);
+  p.nh = (a.Hq / a.Hkv) % 2 == 0 ? 2 : 1;
+  dim3 grid(a.Hq / p.nh, p.n_qt);
   timing_begin(0, st);
   attn_fwd_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(mq, mk, mv, mo, p);
   TREE_LAUNCH_CHECK("attn_fwd_tc_kernel");

@@ -61,7 +61,7 @@ int check_gateway(const char* who, int64_t P, int64_t T, int Hq, int Hkv, int d,
                       : attn_fwd_tc_supported(dtype, d, Hq, Hkv);
   if (!tc)
     return fail(dtype == TREE_DTYPE_BF16 ? TREE_ERR_SHAPE : TREE_ERR_DTYPE,
-                "%s: gateway attention runs on the tensor-core kernels: bf16, d = 128, Hq / Hkv even", who);
+                "%s: gateway attention runs on the tensor-core kernels: bf16, d = 128", who);
   return TREE_OK;
 }
 
