@@ -335,19 +335,6 @@ __device__ __forceinline__ void load_tile(float* dst, int stride, const Tin* __r
   }
 }
 
-__device__ __forceinline__ float dot4(const float* a, const float* b, int n4) {
-  float acc = 0.f;
-  for (int i = 0; i < n4; i += 4) {
-    const float4 x = *reinterpret_cast<const float4*>(a + i);
-    const float4 y = *reinterpret_cast<const float4*>(b + i);
-    acc = fmaf(x.x, y.x, acc);
-    acc = fmaf(x.y, y.y, acc);
-    acc = fmaf(x.z, y.z, acc);
-    acc = fmaf(x.w, y.w, acc);
-  }
-  return acc;
-}
-
 struct GdnArgs {
   const void* q;
   const void* k;
@@ -394,47 +381,108 @@ __global__ void __launch_bounds__(kThreads) gdn_prep_kernel(const GdnArgs a) {
   decay_factors(a.g, a.beta, r0, L, H, h, lg, E, wv, bs);  // ends with a barrier
   float* Pg = a.w.Pm + (static_cast<int64_t>(c) * H + h) * kChunk * kChunk;
   float* Xg = a.w.Xm + (static_cast<int64_t>(c) * H + h) * kChunk * kChunk;
-  for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) {
-    const int t = idx / kChunk, s = idx % kChunk;
-    float av = 0.f, pv = 0.f;
-    if (t < L && s <= t) {
-      const float f = expf(lg[t] - lg[s]);
-      pv = f * dot4(QV + t * kRow, Ks + s * kRow, Dk4);
-      if (s < t) av = bs[t] * f * dot4(Ks + t * kRow, Ks + s * kRow, Dk4);
+  const int lane = tid % 32, warp = tid / 32;
+  {
+    // A and P: each thread a 4 x 4 block of pairs, rows t0 + 16a, columns s0 + 16b (the
+    // eight lanes of a quarter-warp read eight consecutive K rows: no bank conflicts)
+    const int s0 = lane & 15, t0 = (lane >> 4) + 2 * warp;
+    float qk[4][4], kk[4][4];
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+      for (int y = 0; y < 4; ++y) qk[x][y] = kk[x][y] = 0.f;
+    for (int i = 0; i < Dk4; i += 4) {
+      float4 qv[4], kt[4], ks[4];
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        qv[x] = *reinterpret_cast<const float4*>(QV + (t0 + 16 * x) * kRow + i);
+        kt[x] = *reinterpret_cast<const float4*>(Ks + (t0 + 16 * x) * kRow + i);
+        ks[x] = *reinterpret_cast<const float4*>(Ks + (s0 + 16 * x) * kRow + i);
+      }
+#pragma unroll
+      for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) {
+          qk[x][y] = fmaf(qv[x].x, ks[y].x, fmaf(qv[x].y, ks[y].y, fmaf(qv[x].z, ks[y].z, fmaf(qv[x].w, ks[y].w, qk[x][y]))));
+          kk[x][y] = fmaf(kt[x].x, ks[y].x, fmaf(kt[x].y, ks[y].y, fmaf(kt[x].z, ks[y].z, fmaf(kt[x].w, ks[y].w, kk[x][y]))));
+        }
     }
-    Am[t * kSq + s] = av;
-    Pg[idx] = pv;
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+      for (int y = 0; y < 4; ++y) {
+        const int t = t0 + 16 * x, ss = s0 + 16 * y;
+        float av = 0.f, pv = 0.f;
+        if (t < L && ss <= t) {
+          const float f = expf(lg[t] - lg[ss]);
+          pv = f * qk[x][y];
+          if (ss < t) av = bs[t] * f * kk[x][y];
+        }
+        Am[t * kSq + ss] = av;
+        Pg[t * kChunk + ss] = pv;
+      }
   }
   __syncthreads();
   // V over Q (Q is done); X by forward substitution, one column per thread
   load_tile(QV, kRow, static_cast<const Tin*>(a.v), r0, L, H, h, Dv, 0, Dv4);
   if (tid < kChunk) {
+    // column cc of X: X[t][cc] = -sum_{cc <= q < t} A[t][q] X[q][cc]; four partial sums
+    // over aligned groups of q (X[q][cc] = 0 above the diagonal and A[t][q] = 0 for q >= t,
+    // so the groups may start below cc and end past t - 1)
     const int cc = tid;
     for (int t = 0; t < kChunk; ++t) Xm[t * kSq + cc] = t == cc ? 1.f : 0.f;
     for (int t = cc + 1; t < L; ++t) {
-      float acc = 0.f;
-      for (int s = cc; s < t; ++s) acc = fmaf(-Am[t * kSq + s], Xm[s * kSq + cc], acc);
-      Xm[t * kSq + cc] = acc;
+      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+      for (int q = cc & ~3; q < t; q += 4) {
+        const float4 a4 = *reinterpret_cast<const float4*>(Am + t * kSq + q);
+        s0 = fmaf(a4.x, Xm[q * kSq + cc], s0);
+        s1 = fmaf(a4.y, Xm[(q + 1) * kSq + cc], s1);
+        s2 = fmaf(a4.z, Xm[(q + 2) * kSq + cc], s2);
+        s3 = fmaf(a4.w, Xm[(q + 3) * kSq + cc], s3);
+      }
+      Xm[t * kSq + cc] = -((s0 + s1) + (s2 + s3));
     }
+  }
+  // beta E o K and beta o V in place (K is not needed otherwise any more)
+  for (int idx = tid; idx < kChunk * Dk4; idx += kThreads) {
+    const int t = idx / Dk4, i = idx % Dk4;
+    Ks[t * kRow + i] *= bs[t] * E[t];
+  }
+  for (int idx = tid; idx < kChunk * Dv4; idx += kThreads) {
+    const int t = idx / Dv4, j = idx % Dv4;
+    QV[t * kRow + j] *= bs[t];
   }
   __syncthreads();
   for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) Xg[idx] = Xm[(idx / kChunk) * kSq + idx % kChunk];
-  // W = X (beta E o K), U0 = X (beta o V): column `col` per thread, 32 rows each
-  const int col = tid % kMaxD, half = tid / kMaxD;
-  float* Wg = a.w.W + (static_cast<int64_t>(c) * H + h) * kChunk * DkP;
-  for (int m = 0; m < 32; ++m) {
-    const int t = 32 * half + m;
-    float wa = 0.f, ua = 0.f;
-    if (t < L) {
-      for (int s = 0; s <= t; ++s) {
-        const float x = Xm[t * kSq + s] * bs[s];
-        wa = fmaf(x * E[s], Ks[s * kRow + col], wa);
-        ua = fmaf(x, QV[s * kRow + col], ua);
+  // W = X (beta E o K), U0 = X (beta o V): four consecutive columns and rows warp + 8 m per
+  // thread; X is lower-triangular (identity rows past L)
+  {
+    const int c4 = lane * 4;
+    float4 wacc[8], uacc[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) wacc[m] = uacc[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int q = 0; q < L; ++q) {
+      const float4 k4 = *reinterpret_cast<const float4*>(Ks + q * kRow + c4);
+      const float4 v4 = *reinterpret_cast<const float4*>(QV + q * kRow + c4);
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const float x = Xm[(warp + 8 * m) * kSq + q];
+        wacc[m].x = fmaf(x, k4.x, wacc[m].x); wacc[m].y = fmaf(x, k4.y, wacc[m].y);
+        wacc[m].z = fmaf(x, k4.z, wacc[m].z); wacc[m].w = fmaf(x, k4.w, wacc[m].w);
+        uacc[m].x = fmaf(x, v4.x, uacc[m].x); uacc[m].y = fmaf(x, v4.y, uacc[m].y);
+        uacc[m].z = fmaf(x, v4.z, uacc[m].z); uacc[m].w = fmaf(x, v4.w, uacc[m].w);
       }
     }
-    if (col < DkP) Wg[t * DkP + col] = col < Dk ? wa : 0.f;
-    if (col < ns * kSlice)
-      slice_block(a.w.U0, c, h, col / kSlice, H, ns, kChunk)[t * kSlice + col % kSlice] = col < Dv ? ua : 0.f;
+    float* Wg = a.w.W + (static_cast<int64_t>(c) * H + h) * kChunk * DkP;
+    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const int t = warp + 8 * m;
+      if (c4 < DkP) *reinterpret_cast<float4*>(Wg + t * DkP + c4) = c4 < Dk4 ? wacc[m] : z4;
+      if (c4 < ns * kSlice)
+        *reinterpret_cast<float4*>(slice_block(a.w.U0, c, h, c4 / kSlice, H, ns, kChunk) + t * kSlice + c4 % kSlice) =
+            c4 < Dv4 ? uacc[m] : z4;
+    }
   }
 }
 
@@ -470,7 +518,7 @@ __device__ __forceinline__ int next_item(int* counter, int* abort, int items, in
 constexpr size_t kChainSmem = (2 * kChunk * kRow + kMaxD * kSl + kChunk * kSl + 4 * kChunk) * sizeof(float);
 
 template <typename Tin>
-__global__ void __launch_bounds__(kThreads) gdn_chain_kernel(const GdnArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) gdn_chain_kernel(const GdnArgs a) {
   extern __shared__ __align__(16) float sm[];
   float* Ws = sm;                       // [64][kRow]
   float* Ks = Ws + kChunk * kRow;       // [64][kRow]
@@ -505,30 +553,53 @@ __global__ void __launch_bounds__(kThreads) gdn_chain_kernel(const GdnArgs a) {
     }
     if (pred >= 0) {
       cp_block(Hs, kSl, slice_block(w.states, pred, h, sl, H, ns, Dk), Dk, kSlice);
+      for (int idx = Dk * kSlice + tid; idx < kMaxD * kSlice; idx += kThreads)  // rows past Dk
+        Hs[(idx / kSlice) * kSl + idx % kSlice] = 0.f;
     } else {
-      for (int idx = tid; idx < Dk * kSlice; idx += kThreads) Hs[(idx / kSlice) * kSl + idx % kSlice] = 0.f;
+      for (int idx = tid; idx < kMaxD * kSlice; idx += kThreads) Hs[(idx / kSlice) * kSl + idx % kSlice] = 0.f;
     }
     cp_wait();
     decay_factors(a.g, a.beta, r0, L, H, h, lg, E, wv, bs);  // ends with a barrier
-    // u = U0 - W h0: rows t = warp + 8 m of column `lane` (zero past L)
+    // u = U0 - W h0: rows t = warp + 8 m of column `lane`; W rows past L are zero
     float* ug = slice_block(w.u, c, h, sl, H, ns, kChunk);
-    for (int t = warp; t < kChunk; t += 8) {
-      float acc = 0.f;
-      if (t < L) {
-        acc = Us[t * kSl + lane];
-        for (int i = 0; i < Dk; ++i) acc = fmaf(-Ws[t * kRow + i], Hs[i * kSl + lane], acc);
+    {
+      float acc[8];
+#pragma unroll
+      for (int m = 0; m < 8; ++m) acc[m] = Us[(warp + 8 * m) * kSl + lane];
+      for (int i = 0; i < Dk4; i += 4) {
+        const float h0v = Hs[i * kSl + lane], h1v = Hs[(i + 1) * kSl + lane], h2v = Hs[(i + 2) * kSl + lane],
+                    h3v = Hs[(i + 3) * kSl + lane];
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+          const float4 w4 = *reinterpret_cast<const float4*>(Ws + (warp + 8 * m) * kRow + i);
+          acc[m] = fmaf(-w4.x, h0v, fmaf(-w4.y, h1v, fmaf(-w4.z, h2v, fmaf(-w4.w, h3v, acc[m]))));
+        }
       }
-      Us[t * kSl + lane] = acc;
-      ug[t * kSlice + lane] = acc;
+      __syncthreads();  // every thread has read U0
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const int t = warp + 8 * m;
+        Us[t * kSl + lane] = acc[m];
+        ug[t * kSlice + lane] = acc[m];
+      }
     }
     __syncthreads();
     // h_end = E_{L-1} h0 + sum_t w_t k_t u_t^T: rows i = warp + 8 m of column `lane`
-    float* hend = slice_block(w.states, c, h, sl, H, ns, Dk);
-    const float gl = E[L - 1];
-    for (int i = warp; i < Dk; i += 8) {
-      float acc = gl * Hs[i * kSl + lane];
-      for (int t = 0; t < L; ++t) acc = fmaf(wv[t] * Ks[t * kRow + i], Us[t * kSl + lane], acc);
-      __stcg(hend + i * kSlice + lane, acc);
+    {
+      float* hend = slice_block(w.states, c, h, sl, H, ns, Dk);
+      const float gl = E[L - 1];
+      float acc[16];
+#pragma unroll
+      for (int m = 0; m < 16; ++m) acc[m] = gl * Hs[(warp + 8 * m) * kSl + lane];
+      for (int t = 0; t < L; ++t) {
+        const float uw = Us[t * kSl + lane] * wv[t];
+        const float* kr = Ks + t * kRow + warp;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) acc[m] = fmaf(kr[8 * m], uw, acc[m]);
+      }
+#pragma unroll
+      for (int m = 0; m < 16; ++m)
+        if (warp + 8 * m < Dk) __stcg(hend + (warp + 8 * m) * kSlice + lane, acc[m]);
     }
     __syncthreads();
     if (tid == 0 && c != a.withhold) {
@@ -568,26 +639,47 @@ __global__ void __launch_bounds__(kThreads) gdn_out_kernel(const GdnArgs a) {
   load_tile(Qs, kRow, static_cast<const Tin*>(a.q), r0, L, H, h, Dk, 0, Dk4);
   cp_wait();
   decay_factors(a.g, a.beta, r0, L, H, h, lg, E, wv, bs);  // ends with a barrier
-  const int j = tid % kMaxD, half = tid / kMaxD;
-  if (j >= Dv) return;
+  // four consecutive columns and rows warp + 8 m per thread
+  const int lane = tid % 32, warp = tid / 32, c4 = lane * 4;
+  if (c4 >= Dv) return;
   Tin* o = static_cast<Tin*>(a.o);
-  float acc[32];
+  float4 acc[8];
 #pragma unroll
-  for (int m = 0; m < 32; ++m) acc[m] = 0.f;
+  for (int m = 0; m < 8; ++m) acc[m] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (pred >= 0) {
     for (int i = 0; i < Dk; ++i) {
-      const float hij = Hs[i * kRow + j];
+      const float4 h4 = *reinterpret_cast<const float4*>(Hs + i * kRow + c4);
 #pragma unroll
-      for (int m = 0; m < 32; ++m) acc[m] = fmaf(Qs[(32 * half + m) * kRow + i], hij, acc[m]);
+      for (int m = 0; m < 8; ++m) {
+        const float q = Qs[(warp + 8 * m) * kRow + i];
+        acc[m].x = fmaf(q, h4.x, acc[m].x); acc[m].y = fmaf(q, h4.y, acc[m].y);
+        acc[m].z = fmaf(q, h4.z, acc[m].z); acc[m].w = fmaf(q, h4.w, acc[m].w);
+      }
     }
   }
 #pragma unroll
-  for (int m = 0; m < 32; ++m) {
-    const int t = 32 * half + m;
+  for (int m = 0; m < 8; ++m) {
+    const float e = E[warp + 8 * m];
+    acc[m].x *= e; acc[m].y *= e; acc[m].z *= e; acc[m].w *= e;
+  }
+  for (int q = 0; q < L; ++q) {  // P is lower-triangular
+    const float4 u4 = *reinterpret_cast<const float4*>(Us + q * kRow + c4);
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const float pv = Ps[(warp + 8 * m) * kSq + q];
+      acc[m].x = fmaf(pv, u4.x, acc[m].x); acc[m].y = fmaf(pv, u4.y, acc[m].y);
+      acc[m].z = fmaf(pv, u4.z, acc[m].z); acc[m].w = fmaf(pv, u4.w, acc[m].w);
+    }
+  }
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    const int t = warp + 8 * m;
     if (t < L) {
-      float x = E[t] * acc[m];
-      for (int s = 0; s <= t; ++s) x = fmaf(Ps[t * kSq + s], Us[s * kRow + j], x);
-      o[(static_cast<int64_t>(r0 + t) * H + h) * Dv + j] = from_f32<Tin>(x);
+      const float v4[4] = {acc[m].x, acc[m].y, acc[m].z, acc[m].w};
+      Tin* dst = o + (static_cast<int64_t>(r0 + t) * H + h) * Dv + c4;
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (c4 + e < Dv) dst[e] = from_f32<Tin>(v4[e]);
     }
   }
 }
@@ -682,6 +774,8 @@ __global__ void __launch_bounds__(kThreads) gdn_bchain_kernel(const GdnArgs a) {
           *reinterpret_cast<float4*>(Ds + (p / (kSlice / 4)) * kSl + (p % (kSlice / 4)) * 4) = acc[u];
         }
       }
+      for (int idx = Dk * kSlice + tid; idx < kMaxD * kSlice; idx += kThreads)  // rows past Dk
+        Ds[(idx / kSlice) * kSl + idx % kSlice] = 0.f;
     }
     cp_wait();
     __syncthreads();
@@ -699,28 +793,52 @@ __global__ void __launch_bounds__(kThreads) gdn_bchain_kernel(const GdnArgs a) {
       for (int u = 0; u < kThreads / 32; ++u) x += s_red[u];
       w.part_he[(static_cast<int64_t>(sl) * n_chunks + c) * H + h] = x;
     }
-    // du = w o (K dh_end) + P^T dO; partial dw_t = w_t sum_j (K dh_end)_tj u_tj
-    for (int t = warp; t < L; t += 8) {
-      float kd = 0.f;
-      for (int i = 0; i < Dk; ++i) kd = fmaf(Ks[t * kRow + i], Ds[i * kSl + lane], kd);
-      float du = wv[t] * kd;
-      for (int t2 = t; t2 < L; ++t2) du = fmaf(Ps[t2 * kSq + t], Os[t2 * kSl + lane], du);
-      Rs[t * kSl + lane] = du;
-      float dw = wv[t] * kd * Us[t * kSl + lane];
+    // du = w o (K dh_end) + P^T dO for rows t = warp + 8 m of column `lane` (K, P, dO
+    // rows past L are zero, so every row is computed); partial dw_t = w_t sum_j (K dh_end)_tj u_tj
+    {
+      float kd[8];
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) dw += __shfl_xor_sync(0xffffffffu, dw, o);
-      if (lane == 0) w.part[((static_cast<int64_t>(sl) * 2 + 0) * T + r0 + t) * H + h] = dw;
+      for (int m = 0; m < 8; ++m) kd[m] = 0.f;
+      for (int i = 0; i < Dk4; i += 4) {
+        const float d0 = Ds[i * kSl + lane], d1 = Ds[(i + 1) * kSl + lane], d2 = Ds[(i + 2) * kSl + lane],
+                    d3 = Ds[(i + 3) * kSl + lane];
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+          const float4 k4 = *reinterpret_cast<const float4*>(Ks + (warp + 8 * m) * kRow + i);
+          kd[m] = fmaf(k4.x, d0, fmaf(k4.y, d1, fmaf(k4.z, d2, fmaf(k4.w, d3, kd[m]))));
+        }
+      }
+      float du[8];
+#pragma unroll
+      for (int m = 0; m < 8; ++m) du[m] = wv[warp + 8 * m] * kd[m];
+      for (int t2 = 0; t2 < L; ++t2) {  // P is lower-triangular: P[t2][t] = 0 for t > t2
+        const float o = Os[t2 * kSl + lane];
+        const float* pr = Ps + t2 * kSq + warp;
+#pragma unroll
+        for (int m = 0; m < 8; ++m) du[m] = fmaf(pr[8 * m], o, du[m]);
+      }
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const int t = warp + 8 * m;
+        Rs[t * kSl + lane] = du[m];
+        if (t < L) {
+          float dw = wv[t] * kd[m] * Us[t * kSl + lane];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) dw += __shfl_xor_sync(0xffffffffu, dw, o);
+          if (lane == 0) w.part[((static_cast<int64_t>(sl) * 2 + 0) * T + r0 + t) * H + h] = dw;
+        }
+      }
     }
     __syncthreads();
-    // dr = X^T du (in registers first: every row reads the whole column of du), dv = beta o dr
+    // dr = X^T du (X lower-triangular), dv = beta o dr
     float drr[8];
 #pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      const int t = warp + 8 * m;
-      float x = 0.f;
-      if (t < L)
-        for (int t2 = t; t2 < L; ++t2) x = fmaf(Xs[t2 * kSq + t], Rs[t2 * kSl + lane], x);
-      drr[m] = x;
+    for (int m = 0; m < 8; ++m) drr[m] = 0.f;
+    for (int t2 = 0; t2 < L; ++t2) {
+      const float rr = Rs[t2 * kSl + lane];
+      const float* xr = Xs + t2 * kSq + warp;
+#pragma unroll
+      for (int m = 0; m < 8; ++m) drr[m] = fmaf(xr[8 * m], rr, drr[m]);
     }
     __syncthreads();
     float* drg = slice_block(w.dr, c, h, sl, H, ns, kChunk);
@@ -738,15 +856,23 @@ __global__ void __launch_bounds__(kThreads) gdn_bchain_kernel(const GdnArgs a) {
       }
     }
     __syncthreads();
-    // dh0 = E_{L-1} dh_end + Q^T (E o dO) - K^T (beta E o dr)
-    float* dst = slice_block(w.dstart, c, h, sl, H, ns, Dk);
-    const float gl = E[L - 1];
-    for (int i = warp; i < Dk; i += 8) {
-      float acc = gl * Ds[i * kSl + lane];
-      for (int t = 0; t < L; ++t)
-        acc = fmaf(E[t], fmaf(Qs[t * kRow + i], Os[t * kSl + lane], -bs[t] * Ks[t * kRow + i] * Rs[t * kSl + lane]),
-                   acc);
-      __stcg(dst + i * kSlice + lane, acc);
+    // dh0 = E_{L-1} dh_end + Q^T (E o dO) - K^T (beta E o dr): rows i = warp + 8 m
+    {
+      float* dst = slice_block(w.dstart, c, h, sl, H, ns, Dk);
+      const float gl = E[L - 1];
+      float acc[16];
+#pragma unroll
+      for (int m = 0; m < 16; ++m) acc[m] = gl * Ds[(warp + 8 * m) * kSl + lane];
+      for (int t = 0; t < L; ++t) {
+        const float ao = E[t] * Os[t * kSl + lane], br = bs[t] * E[t] * Rs[t * kSl + lane];
+        const float* qr = Qs + t * kRow + warp;
+        const float* kr = Ks + t * kRow + warp;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) acc[m] = fmaf(qr[8 * m], ao, fmaf(-kr[8 * m], br, acc[m]));
+      }
+#pragma unroll
+      for (int m = 0; m < 16; ++m)
+        if (warp + 8 * m < Dk) __stcg(dst + (warp + 8 * m) * kSlice + lane, acc[m]);
     }
     __syncthreads();
     if (tid == 0 && c != a.withhold) {
@@ -800,38 +926,80 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_grads_kernel(const GdnArgs a)
   load_tile(Os, kRow, static_cast<const Tin*>(a.dout), r0, L, H, h, Dv, 0, Dv4);
   cp_wait();
   decay_factors(a.g, a.beta, r0, L, H, h, lg, E, wv, bs);  // ends with a barrier
-  // pairs (t, s), s <= t: four threads per row t, s = sub + 4 m
+  // pairs (t, s): each thread a 4 x 4 block, rows t0 + 16 x, columns s0 + 16 y (the eight
+  // lanes of a quarter-warp read eight consecutive rows of the column operand)
   {
-    const int t = tid / 4, sub = tid % 4;
-    float rowsum = 0.f, rowb = 0.f;
-    for (int s = sub; s < kChunk; s += 4) {
-      float fp = 0.f, fa = 0.f, m1 = 0.f;
-      if (t < L && s <= t) {
-        const float f = expf(lg[t] - lg[s]);
-        const float qk = dot4(Qs + t * kRow, Ks + s * kRow, Dk4);
-        const float dp = dot4(Os + t * kRow, Us + s * kRow, Dv4);
-        fp = dp * f;
-        m1 = fp * qk;  // dP o P
-        if (s < t) {
-          const float kk = dot4(Ks + t * kRow, Ks + s * kRow, Dk4);
-          const float da = -dot4(Rs + t * kRow, Us + s * kRow, Dv4);
-          fa = da * bs[t] * f;
-          m1 = fmaf(fa, kk, m1);           // dA o A
-          rowb = fmaf(da * f, kk, rowb);   // dA o f o KK (dbeta)
-        }
+    const int s0 = lane & 15, t0 = (lane >> 4) + 2 * warp;
+    float qk[4][4], kk[4][4], dp[4][4], da[4][4];
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+      for (int y = 0; y < 4; ++y) qk[x][y] = kk[x][y] = dp[x][y] = da[x][y] = 0.f;
+    for (int i = 0; i < Dk4; i += 4) {
+      float4 qv[4], kt[4], ks[4];
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        qv[x] = *reinterpret_cast<const float4*>(Qs + (t0 + 16 * x) * kRow + i);
+        kt[x] = *reinterpret_cast<const float4*>(Ks + (t0 + 16 * x) * kRow + i);
+        ks[x] = *reinterpret_cast<const float4*>(Ks + (s0 + 16 * x) * kRow + i);
       }
-      Fp[t * kSq + s] = fp;
-      Fa[t * kSq + s] = fa;
-      M1[t * kSq + s] = m1;
-      rowsum += m1;
+#pragma unroll
+      for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) {
+          qk[x][y] = fmaf(qv[x].x, ks[y].x, fmaf(qv[x].y, ks[y].y, fmaf(qv[x].z, ks[y].z, fmaf(qv[x].w, ks[y].w, qk[x][y]))));
+          kk[x][y] = fmaf(kt[x].x, ks[y].x, fmaf(kt[x].y, ks[y].y, fmaf(kt[x].z, ks[y].z, fmaf(kt[x].w, ks[y].w, kk[x][y]))));
+        }
     }
-    rowsum += __shfl_xor_sync(0xffffffffu, rowsum, 1);
-    rowsum += __shfl_xor_sync(0xffffffffu, rowsum, 2);
-    rowb += __shfl_xor_sync(0xffffffffu, rowb, 1);
-    rowb += __shfl_xor_sync(0xffffffffu, rowb, 2);
-    if (sub == 0) {
-      dlg[t] = rowsum;
-      dbt[t] = rowb;
+    for (int j = 0; j < Dv4; j += 4) {
+      float4 ov[4], rv[4], us[4];
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        ov[x] = *reinterpret_cast<const float4*>(Os + (t0 + 16 * x) * kRow + j);
+        rv[x] = *reinterpret_cast<const float4*>(Rs + (t0 + 16 * x) * kRow + j);
+        us[x] = *reinterpret_cast<const float4*>(Us + (s0 + 16 * x) * kRow + j);
+      }
+#pragma unroll
+      for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) {
+          dp[x][y] = fmaf(ov[x].x, us[y].x, fmaf(ov[x].y, us[y].y, fmaf(ov[x].z, us[y].z, fmaf(ov[x].w, us[y].w, dp[x][y]))));
+          da[x][y] = fmaf(rv[x].x, us[y].x, fmaf(rv[x].y, us[y].y, fmaf(rv[x].z, us[y].z, fmaf(rv[x].w, us[y].w, da[x][y]))));
+        }
+    }
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      const int t = t0 + 16 * x;
+      float rowsum = 0.f, rowb = 0.f;
+#pragma unroll
+      for (int y = 0; y < 4; ++y) {
+        const int ss = s0 + 16 * y;
+        float fp = 0.f, fa = 0.f, m1 = 0.f;
+        if (t < L && ss <= t) {
+          const float f = expf(lg[t] - lg[ss]);
+          fp = dp[x][y] * f;
+          m1 = fp * qk[x][y];                      // dP o P
+          if (ss < t) {
+            const float dav = -da[x][y];
+            fa = dav * bs[t] * f;
+            m1 = fmaf(fa, kk[x][y], m1);           // dA o A
+            rowb = fmaf(dav * f, kk[x][y], rowb);  // dA o f o KK (dbeta)
+          }
+        }
+        Fp[t * kSq + ss] = fp;
+        Fa[t * kSq + ss] = fa;
+        M1[t * kSq + ss] = m1;
+        rowsum += m1;
+      }
+#pragma unroll
+      for (int o = 1; o < 16; o <<= 1) {  // over the 16 lanes that share row t
+        rowsum += __shfl_xor_sync(0xffffffffu, rowsum, o);
+        rowb += __shfl_xor_sync(0xffffffffu, rowb, o);
+      }
+      if (s0 == 0) {
+        dlg[t] = rowsum;
+        dbt[t] = rowb;
+      }
     }
   }
   __syncthreads();
@@ -840,25 +1008,33 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_grads_kernel(const GdnArgs a)
     for (int t = 0; t < kChunk; ++t) x += M1[t * kSq + tid];
     dlg[tid] -= x;
   }
-  // dQ, dK: column i per thread, 16 rows per pass, two passes per half
-  const int i = tid % kMaxD, half = tid / kMaxD;
-  float* hst = M1;                      // [128][kSt] 16 columns of h0, staged
-  float* dst = M1 + kMaxD * kSt;        // [128][kSt] the same columns of dh_end
+  // dQ, dK: four consecutive columns c4 and rows warp + 8 m per thread, in two passes of
+  // four rows; h0 and dh_end are staged 16 state columns at a time, transposed ([j][i])
+  const int c4 = lane * 4;
+  constexpr int kHt = kMaxD + 4;        // row stride of the transposed staging
+  static_assert(2 * 16 * kHt <= kChunk * kSq, "h0 / dh_end staging must fit in the M1 buffer");
+  float* hst = M1;                      // [16][kHt] h0 columns j0..j0+15, transposed
+  float* dst = M1 + 16 * kHt;           // [16][kHt] the same columns of dh_end
   Tin* dq = static_cast<Tin*>(a.dq);
   Tin* dk = static_cast<Tin*>(a.dk);
   for (int pass = 0; pass < 2; ++pass) {
-    const int t0 = 32 * half + 16 * pass;
-    float qa[16], ka[16], z1[16], z2[16], z3[16];
+    float4 qa[4], ka[4], z1[4], z2[4], z3[4];
 #pragma unroll
-    for (int m = 0; m < 16; ++m) qa[m] = ka[m] = z1[m] = z2[m] = z3[m] = 0.f;
-    for (int s = 0; s < kChunk; ++s) {
-      const float kv = Ks[s * kRow + i], qv = Qs[s * kRow + i];
+    for (int m = 0; m < 4; ++m) qa[m] = ka[m] = z1[m] = z2[m] = z3[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int tb = warp + 32 * pass;    // rows tb + 8 m, m < 4
+    for (int q = 0; q < kChunk; ++q) {
+      const float4 k4 = *reinterpret_cast<const float4*>(Ks + q * kRow + c4);
+      const float4 q4 = *reinterpret_cast<const float4*>(Qs + q * kRow + c4);
 #pragma unroll
-      for (int m = 0; m < 16; ++m) {
-        const int t = t0 + m;
-        qa[m] = fmaf(Fp[t * kSq + s], kv, qa[m]);                       // (dP o f) K
-        ka[m] = fmaf(Fp[s * kSq + t], qv, ka[m]);                       // (dP o f)^T Q
-        ka[m] = fmaf(Fa[t * kSq + s] + Fa[s * kSq + t], kv, ka[m]);     // (dA o b f) K + its transpose
+      for (int m = 0; m < 4; ++m) {
+        const int t = tb + 8 * m;
+        const float a1 = Fp[t * kSq + q], a2 = Fp[q * kSq + t], a3 = Fa[t * kSq + q] + Fa[q * kSq + t];
+        qa[m].x = fmaf(a1, k4.x, qa[m].x); qa[m].y = fmaf(a1, k4.y, qa[m].y);         // (dP o f) K
+        qa[m].z = fmaf(a1, k4.z, qa[m].z); qa[m].w = fmaf(a1, k4.w, qa[m].w);
+        ka[m].x = fmaf(a2, q4.x, fmaf(a3, k4.x, ka[m].x));                              // (dP o f)^T Q
+        ka[m].y = fmaf(a2, q4.y, fmaf(a3, k4.y, ka[m].y));                              // + (dA o b f) K
+        ka[m].z = fmaf(a2, q4.z, fmaf(a3, k4.z, ka[m].z));                              //   and transpose
+        ka[m].w = fmaf(a2, q4.w, fmaf(a3, k4.w, ka[m].w));
       }
     }
     for (int j0 = 0; j0 < ns * kSlice; j0 += 16) {
@@ -866,60 +1042,71 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_grads_kernel(const GdnArgs a)
       __syncthreads();
       const float* hg = pred >= 0 ? slice_block(w.states, pred, h, sl, H, ns, Dk) : nullptr;
       const float* dg = slice_block(w.dend, c, h, sl, H, ns, Dk);
-      for (int idx = tid; idx < Dk * 16; idx += kThreads) {
+      for (int idx = tid; idx < kMaxD * 16; idx += kThreads) {
         const int ii = idx / 16, jj = idx % 16;
-        if (hg) cp4(hst + ii * kSt + jj, hg + ii * kSlice + off + jj);
-        else hst[ii * kSt + jj] = 0.f;
-        cp4(dst + ii * kSt + jj, dg + ii * kSlice + off + jj);
+        if (ii < Dk) {
+          if (hg) cp4(hst + jj * kHt + ii, hg + ii * kSlice + off + jj);
+          else hst[jj * kHt + ii] = 0.f;
+          cp4(dst + jj * kHt + ii, dg + ii * kSlice + off + jj);
+        } else {
+          hst[jj * kHt + ii] = 0.f;
+          dst[jj * kHt + ii] = 0.f;
+        }
       }
       cp_wait();
       __syncthreads();
       const int jn = min(16, Dv - j0);
-      if (i < Dk) {
-        for (int jj = 0; jj < jn; ++jj) {
-          const float hv = hst[i * kSt + jj], dv = dst[i * kSt + jj];
+      for (int jj = 0; jj < jn; ++jj) {
+        const float4 h4 = *reinterpret_cast<const float4*>(hst + jj * kHt + c4);
+        const float4 d4 = *reinterpret_cast<const float4*>(dst + jj * kHt + c4);
 #pragma unroll
-          for (int m = 0; m < 16; ++m) {
-            const int t = t0 + m;
-            z1[m] = fmaf(Os[t * kRow + j0 + jj], hv, z1[m]);   // (dO h0^T)_ti
-            z2[m] = fmaf(Rs[t * kRow + j0 + jj], hv, z2[m]);   // (dr h0^T)_ti
-            z3[m] = fmaf(Us[t * kRow + j0 + jj], dv, z3[m]);   // (u dh_end^T)_ti
-          }
+        for (int m = 0; m < 4; ++m) {
+          const int t = tb + 8 * m;
+          const float o = Os[t * kRow + j0 + jj], rr = Rs[t * kRow + j0 + jj], u = Us[t * kRow + j0 + jj];
+          z1[m].x = fmaf(o, h4.x, z1[m].x); z1[m].y = fmaf(o, h4.y, z1[m].y);       // (dO h0^T)_ti
+          z1[m].z = fmaf(o, h4.z, z1[m].z); z1[m].w = fmaf(o, h4.w, z1[m].w);
+          z2[m].x = fmaf(rr, h4.x, z2[m].x); z2[m].y = fmaf(rr, h4.y, z2[m].y);     // (dr h0^T)_ti
+          z2[m].z = fmaf(rr, h4.z, z2[m].z); z2[m].w = fmaf(rr, h4.w, z2[m].w);
+          z3[m].x = fmaf(u, d4.x, z3[m].x); z3[m].y = fmaf(u, d4.y, z3[m].y);       // (u dh_end^T)_ti
+          z3[m].z = fmaf(u, d4.z, z3[m].z); z3[m].w = fmaf(u, d4.w, z3[m].w);
         }
       }
     }
-    __syncthreads();
-    // the d lg terms E_t q_t . (dO h0^T)_t and -beta_t E_t k_t . (dr h0^T)_t and the dbeta
-    // term -E_t k_t . (dr h0^T)_t: dot products over i, reduced over the 128 threads of a half
-    float* red = M1;  // [2 halves][16 rows][8]
+    // rows tb + 8 m: dq, dk, and the d lg / dbeta terms E_t q_t . (dO h0^T)_t,
+    // -beta_t E_t k_t . (dr h0^T)_t and -E_t k_t . (dr h0^T)_t (a row lives in one warp)
 #pragma unroll
-    for (int m = 0; m < 16; ++m) {
-      const int t = t0 + m;
-      float cq = i < Dk ? Qs[t * kRow + i] * z1[m] : 0.f;   // columns past Dk hold no data
-      float ck2 = i < Dk ? Ks[t * kRow + i] * z2[m] : 0.f;
+    for (int m = 0; m < 4; ++m) {
+      const int t = tb + 8 * m;
+      const float4 qv = *reinterpret_cast<const float4*>(Qs + t * kRow + c4);
+      const float4 kv = *reinterpret_cast<const float4*>(Ks + t * kRow + c4);
+      float cq = 0.f, ck2 = 0.f;
+      if (c4 < Dk4) {  // columns past Dk hold zeros in Q and K; columns past Dk4 hold no data
+        cq = qv.x * z1[m].x + qv.y * z1[m].y + qv.z * z1[m].z + qv.w * z1[m].w;
+        ck2 = kv.x * z2[m].x + kv.y * z2[m].y + kv.z * z2[m].z + kv.w * z2[m].w;
+      }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         cq += __shfl_xor_sync(0xffffffffu, cq, o);
         ck2 += __shfl_xor_sync(0xffffffffu, ck2, o);
       }
       if (lane == 0) {
-        red[(half * 16 + m) * 8 + (warp % 4)] = cq;
-        red[(half * 16 + m) * 8 + 4 + (warp % 4)] = ck2;
+        dlg[t] += E[t] * cq - bs[t] * E[t] * ck2;
+        dbt[t] -= E[t] * ck2;
       }
-      if (t < L && i < Dk) {
-        const int64_t off = (static_cast<int64_t>(r0 + t) * H + h) * Dk + i;
-        dq[off] = from_f32<Tin>(qa[m] + E[t] * z1[m]);
-        dk[off] = from_f32<Tin>(ka[m] + wv[t] * z3[m] - bs[t] * E[t] * z2[m]);
+      if (t < L) {
+        const float e = E[t], wt = wv[t], be = bs[t] * E[t];
+        const float qo[4] = {qa[m].x + e * z1[m].x, qa[m].y + e * z1[m].y, qa[m].z + e * z1[m].z,
+                             qa[m].w + e * z1[m].w};
+        const float ko[4] = {ka[m].x + wt * z3[m].x - be * z2[m].x, ka[m].y + wt * z3[m].y - be * z2[m].y,
+                             ka[m].z + wt * z3[m].z - be * z2[m].z, ka[m].w + wt * z3[m].w - be * z2[m].w};
+        const int64_t base = (static_cast<int64_t>(r0 + t) * H + h) * Dk + c4;
+#pragma unroll
+        for (int e2 = 0; e2 < 4; ++e2)
+          if (c4 + e2 < Dk) {
+            dq[base + e2] = from_f32<Tin>(qo[e2]);
+            dk[base + e2] = from_f32<Tin>(ko[e2]);
+          }
       }
-    }
-    __syncthreads();
-    if (tid < 32) {  // lane (half, m) finishes row 32 half + 16 pass + m
-      const int hh = tid / 16, m = tid % 16, t = 32 * hh + 16 * pass + m;
-      const float* rr = red + (hh * 16 + m) * 8;
-      const float cq = (rr[0] + rr[1]) + (rr[2] + rr[3]);
-      const float ck2 = (rr[4] + rr[5]) + (rr[6] + rr[7]);
-      dlg[t] += E[t] * cq - bs[t] * E[t] * ck2;
-      dbt[t] -= E[t] * ck2;
     }
   }
   __syncthreads();
