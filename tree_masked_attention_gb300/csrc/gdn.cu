@@ -425,23 +425,44 @@ __global__ void __launch_bounds__(kThreads) gdn_prep_kernel(const GdnArgs a) {
   __syncthreads();
   // V over Q (Q is done); X by forward substitution, one column per thread
   load_tile(QV, kRow, static_cast<const Tin*>(a.v), r0, L, H, h, Dv, 0, Dv4);
+  // X = (I + A)^-1 in 16 x 16 blocks (A strictly lower-triangular, so X is unit lower-
+  // triangular): first the four diagonal blocks, each column by forward substitution
+  // (64 threads), then the blocks below the diagonal by their distance d = k - l:
+  //   X_kl = -X_kk sum_{l <= m < k} A_km X_ml,
+  // all blocks of one distance at once, every thread a few elements of the sums.
+  for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) Xm[(idx / kChunk) * kSq + idx % kChunk] = 0.f;
+  __syncthreads();
   if (tid < kChunk) {
-    // column cc of X: X[t][cc] = -sum_{cc <= q < t} A[t][q] X[q][cc]; four partial sums
-    // over aligned groups of q (X[q][cc] = 0 above the diagonal and A[t][q] = 0 for q >= t,
-    // so the groups may start below cc and end past t - 1)
-    const int cc = tid;
-    for (int t = 0; t < kChunk; ++t) Xm[t * kSq + cc] = t == cc ? 1.f : 0.f;
-    for (int t = cc + 1; t < L; ++t) {
-      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-      for (int q = cc & ~3; q < t; q += 4) {
-        const float4 a4 = *reinterpret_cast<const float4*>(Am + t * kSq + q);
-        s0 = fmaf(a4.x, Xm[q * kSq + cc], s0);
-        s1 = fmaf(a4.y, Xm[(q + 1) * kSq + cc], s1);
-        s2 = fmaf(a4.z, Xm[(q + 2) * kSq + cc], s2);
-        s3 = fmaf(a4.w, Xm[(q + 3) * kSq + cc], s3);
-      }
-      Xm[t * kSq + cc] = -((s0 + s1) + (s2 + s3));
+    const int cc = tid, b0 = cc & ~15;  // column cc of the diagonal block starting at b0
+    Xm[cc * kSq + cc] = 1.f;
+    for (int t = cc + 1; t < b0 + 16; ++t) {
+      float acc = 0.f;
+      for (int q = cc; q < t; ++q) acc = fmaf(Am[t * kSq + q], Xm[q * kSq + cc], acc);
+      Xm[t * kSq + cc] = -acc;
     }
+  }
+  __syncthreads();
+  float* Ym = Am;  // A's blocks on and above the diagonal are not read: Y blocks go there
+  for (int d = 1; d < 4; ++d) {
+    const int nb = 4 - d;  // blocks (k, l) = (l + d, l), l < nb
+    // Y_kl = sum_{l <= m < k} A_km X_ml  -> stored in A's upper block (l, k)
+    for (int e = tid; e < nb * 256; e += kThreads) {
+      const int l = e / 256, k = l + d, r = (e % 256) / 16, cl = e % 16;
+      float acc = 0.f;
+      for (int m = l; m < k; ++m)
+        for (int q = 0; q < 16; ++q) acc = fmaf(Am[(16 * k + r) * kSq + 16 * m + q], Xm[(16 * m + q) * kSq + 16 * l + cl], acc);
+      Ym[(16 * l + r) * kSq + 16 * k + cl] = acc;
+    }
+    __syncthreads();
+    // X_kl = -X_kk Y_kl
+    for (int e = tid; e < nb * 256; e += kThreads) {
+      const int l = e / 256, k = l + d, r = (e % 256) / 16, cl = e % 16;
+      float acc = 0.f;
+      for (int q = 0; q <= r; ++q)
+        acc = fmaf(Xm[(16 * k + r) * kSq + 16 * k + q], Ym[(16 * l + q) * kSq + 16 * k + cl], acc);
+      Xm[(16 * k + r) * kSq + 16 * l + cl] = -acc;
+    }
+    __syncthreads();
   }
   // beta E o K and beta o V in place (K is not needed otherwise any more)
   for (int idx = tid; idx < kChunk * Dk4; idx += kThreads) {
@@ -584,22 +605,29 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_chain_kernel(const GdnArgs a)
       }
     }
     __syncthreads();
-    // h_end = E_{L-1} h0 + sum_t w_t k_t u_t^T: rows i = warp + 8 m of column `lane`
+    // h_end = E_{L-1} h0 + sum_t w_t k_t u_t^T: rows i = 16 warp + m of column `lane`
     {
       float* hend = slice_block(w.states, c, h, sl, H, ns, Dk);
       const float gl = E[L - 1];
+      const int i0 = 16 * warp;
       float acc[16];
 #pragma unroll
-      for (int m = 0; m < 16; ++m) acc[m] = gl * Hs[(warp + 8 * m) * kSl + lane];
+      for (int m = 0; m < 16; ++m) acc[m] = gl * Hs[(i0 + m) * kSl + lane];
       for (int t = 0; t < L; ++t) {
         const float uw = Us[t * kSl + lane] * wv[t];
-        const float* kr = Ks + t * kRow + warp;
+        const float4* kr = reinterpret_cast<const float4*>(Ks + t * kRow + i0);
 #pragma unroll
-        for (int m = 0; m < 16; ++m) acc[m] = fmaf(kr[8 * m], uw, acc[m]);
+        for (int q = 0; q < 4; ++q) {
+          const float4 k4 = kr[q];
+          acc[4 * q] = fmaf(k4.x, uw, acc[4 * q]);
+          acc[4 * q + 1] = fmaf(k4.y, uw, acc[4 * q + 1]);
+          acc[4 * q + 2] = fmaf(k4.z, uw, acc[4 * q + 2]);
+          acc[4 * q + 3] = fmaf(k4.w, uw, acc[4 * q + 3]);
+        }
       }
 #pragma unroll
       for (int m = 0; m < 16; ++m)
-        if (warp + 8 * m < Dk) __stcg(hend + (warp + 8 * m) * kSlice + lane, acc[m]);
+        if (i0 + m < Dk) __stcg(hend + (i0 + m) * kSlice + lane, acc[m]);
     }
     __syncthreads();
     if (tid == 0 && c != a.withhold) {
@@ -804,22 +832,24 @@ __global__ void __launch_bounds__(kThreads) gdn_bchain_kernel(const GdnArgs a) {
                     d3 = Ds[(i + 3) * kSl + lane];
 #pragma unroll
         for (int m = 0; m < 8; ++m) {
-          const float4 k4 = *reinterpret_cast<const float4*>(Ks + (warp + 8 * m) * kRow + i);
+          const float4 k4 = *reinterpret_cast<const float4*>(Ks + (8 * warp + m) * kRow + i);
           kd[m] = fmaf(k4.x, d0, fmaf(k4.y, d1, fmaf(k4.z, d2, fmaf(k4.w, d3, kd[m]))));
         }
       }
       float du[8];
 #pragma unroll
-      for (int m = 0; m < 8; ++m) du[m] = wv[warp + 8 * m] * kd[m];
+      for (int m = 0; m < 8; ++m) du[m] = wv[8 * warp + m] * kd[m];
       for (int t2 = 0; t2 < L; ++t2) {  // P is lower-triangular: P[t2][t] = 0 for t > t2
         const float o = Os[t2 * kSl + lane];
-        const float* pr = Ps + t2 * kSq + warp;
-#pragma unroll
-        for (int m = 0; m < 8; ++m) du[m] = fmaf(pr[8 * m], o, du[m]);
+        const float4 p0 = *reinterpret_cast<const float4*>(Ps + t2 * kSq + 8 * warp);
+        const float4 p1 = *reinterpret_cast<const float4*>(Ps + t2 * kSq + 8 * warp + 4);
+        du[0] = fmaf(p0.x, o, du[0]); du[1] = fmaf(p0.y, o, du[1]); du[2] = fmaf(p0.z, o, du[2]);
+        du[3] = fmaf(p0.w, o, du[3]); du[4] = fmaf(p1.x, o, du[4]); du[5] = fmaf(p1.y, o, du[5]);
+        du[6] = fmaf(p1.z, o, du[6]); du[7] = fmaf(p1.w, o, du[7]);
       }
 #pragma unroll
       for (int m = 0; m < 8; ++m) {
-        const int t = warp + 8 * m;
+        const int t = 8 * warp + m;
         Rs[t * kSl + lane] = du[m];
         if (t < L) {
           float dw = wv[t] * kd[m] * Us[t * kSl + lane];
@@ -836,15 +866,17 @@ __global__ void __launch_bounds__(kThreads) gdn_bchain_kernel(const GdnArgs a) {
     for (int m = 0; m < 8; ++m) drr[m] = 0.f;
     for (int t2 = 0; t2 < L; ++t2) {
       const float rr = Rs[t2 * kSl + lane];
-      const float* xr = Xs + t2 * kSq + warp;
-#pragma unroll
-      for (int m = 0; m < 8; ++m) drr[m] = fmaf(xr[8 * m], rr, drr[m]);
+      const float4 x0 = *reinterpret_cast<const float4*>(Xs + t2 * kSq + 8 * warp);
+      const float4 x1 = *reinterpret_cast<const float4*>(Xs + t2 * kSq + 8 * warp + 4);
+      drr[0] = fmaf(x0.x, rr, drr[0]); drr[1] = fmaf(x0.y, rr, drr[1]); drr[2] = fmaf(x0.z, rr, drr[2]);
+      drr[3] = fmaf(x0.w, rr, drr[3]); drr[4] = fmaf(x1.x, rr, drr[4]); drr[5] = fmaf(x1.y, rr, drr[5]);
+      drr[6] = fmaf(x1.z, rr, drr[6]); drr[7] = fmaf(x1.w, rr, drr[7]);
     }
     __syncthreads();
     float* drg = slice_block(w.dr, c, h, sl, H, ns, kChunk);
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
-      const int t = warp + 8 * m;
+      const int t = 8 * warp + m;
       Rs[t * kSl + lane] = drr[m];
       drg[t * kSlice + lane] = drr[m];
       if (t < L) {
@@ -856,23 +888,30 @@ __global__ void __launch_bounds__(kThreads) gdn_bchain_kernel(const GdnArgs a) {
       }
     }
     __syncthreads();
-    // dh0 = E_{L-1} dh_end + Q^T (E o dO) - K^T (beta E o dr): rows i = warp + 8 m
+    // dh0 = E_{L-1} dh_end + Q^T (E o dO) - K^T (beta E o dr): rows i = 16 warp + m
     {
       float* dst = slice_block(w.dstart, c, h, sl, H, ns, Dk);
       const float gl = E[L - 1];
+      const int i0 = 16 * warp;
       float acc[16];
 #pragma unroll
-      for (int m = 0; m < 16; ++m) acc[m] = gl * Ds[(warp + 8 * m) * kSl + lane];
+      for (int m = 0; m < 16; ++m) acc[m] = gl * Ds[(i0 + m) * kSl + lane];
       for (int t = 0; t < L; ++t) {
-        const float ao = E[t] * Os[t * kSl + lane], br = bs[t] * E[t] * Rs[t * kSl + lane];
-        const float* qr = Qs + t * kRow + warp;
-        const float* kr = Ks + t * kRow + warp;
+        const float ao = E[t] * Os[t * kSl + lane], br = -bs[t] * E[t] * Rs[t * kSl + lane];
+        const float4* qr = reinterpret_cast<const float4*>(Qs + t * kRow + i0);
+        const float4* kr = reinterpret_cast<const float4*>(Ks + t * kRow + i0);
 #pragma unroll
-        for (int m = 0; m < 16; ++m) acc[m] = fmaf(qr[8 * m], ao, fmaf(-kr[8 * m], br, acc[m]));
+        for (int q = 0; q < 4; ++q) {
+          const float4 q4 = qr[q], k4 = kr[q];
+          acc[4 * q] = fmaf(q4.x, ao, fmaf(k4.x, br, acc[4 * q]));
+          acc[4 * q + 1] = fmaf(q4.y, ao, fmaf(k4.y, br, acc[4 * q + 1]));
+          acc[4 * q + 2] = fmaf(q4.z, ao, fmaf(k4.z, br, acc[4 * q + 2]));
+          acc[4 * q + 3] = fmaf(q4.w, ao, fmaf(k4.w, br, acc[4 * q + 3]));
+        }
       }
 #pragma unroll
       for (int m = 0; m < 16; ++m)
-        if (warp + 8 * m < Dk) __stcg(dst + (warp + 8 * m) * kSlice + lane, acc[m]);
+        if (i0 + m < Dk) __stcg(dst + (i0 + m) * kSlice + lane, acc[m]);
     }
     __syncthreads();
     if (tid == 0 && c != a.withhold) {
