@@ -87,6 +87,10 @@ struct Params {
   int* err;
 };
 
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ uint32_t tmem_ld1(uint32_t taddr) {
   uint32_t v;
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(v) : "r"(taddr));
@@ -251,25 +255,28 @@ lm_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const bool row_ok = m < p.M;
       const int ncols = min(BN, p.N - n0);
       if (p.epi == EPI_STORE || p.epi == EPI_DW) {
-        const int lb = p.epi == EPI_DW ? p.blk_ptr[nb] : 0, le = p.epi == EPI_DW ? p.blk_ptr[nb + 1] : 0;
+        if (p.epi == EPI_DW) {
+          // dW only: add back, in fp32, what storing G_z in bf16 dropped at target cells:
+          // dW[m, y] += H[r, m] * (exact - stored) for every occurrence cell (r, y) of this
+          // vocabulary block, straight into the accumulator column, in the block's entry order
+          const int lb = p.blk_ptr[nb], le = p.blk_ptr[nb + 1];
+          for (int q = lb; q < le; ++q) {  // warp-uniform
+            const int oo = p.blk_ent[2 * q + 1];
+            const int col = p.targets[oo] - n0;
+            const float dlt = p.occ_delta[oo];
+            if (dlt == 0.f || col < 0 || col >= BN) continue;
+            const float x =
+                row_ok ? dlt * __bfloat162float(p.h[static_cast<int64_t>(p.blk_ent[2 * q]) * p.M + m]) : 0.f;
+            const uint32_t cur = tmem_ld1(acc + col);
+            tmem_st1(acc + col, __float_as_uint(__uint_as_float(cur) + x));
+            tmem_st_wait();  // a later entry may hit the same column
+          }
+        }
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t v[32], pk[16];
           tmem_ld32(acc + c * 32, v);
           tmem_ld_wait();
-          // dW only: add back, in fp32, what storing G_z in bf16 dropped at target cells:
-          // dW[m, y] += H[r, m] * (exact - stored) for every occurrence cell (r, y).
-          for (int q = lb; q < le; ++q) {
-            const int oo = p.blk_ent[2 * q + 1];
-            const int idx = p.targets[oo] - n0 - c * 32;
-            if (idx < 0 || idx >= 32) continue;
-            const float dlt = p.occ_delta[oo];
-            if (dlt == 0.f || !row_ok) continue;
-            const float x = dlt * __bfloat162float(p.h[static_cast<int64_t>(p.blk_ent[2 * q]) * p.M + m]);
-#pragma unroll
-            for (int u = 0; u < 32; ++u)
-              if (u == idx) v[u] = __float_as_uint(__uint_as_float(v[u]) + x);
-          }
           if (p.out_f32) {  // fp32 dW: the accumulator as it is
             if (row_ok && c * 32 < ncols) {
               float* dst = p.out_f32 + static_cast<int64_t>(m) * p.N + n0 + c * 32;
@@ -411,49 +418,99 @@ lm_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   }
 }
 
-// Occurrences grouped by 256-column target block, in CSR order within a block (so the
-// grouping, and every sum taken over it, is the same on every run). One warp per block:
-// pass 0 counts into blk_ptr[b + 1], pass 1 writes {source row, occurrence} entries.
-__global__ void lm_block_lists_kernel(const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ perm,
-                                      const int32_t* __restrict__ targets, int T, int n_occ, int V, int n_blk,
-                                      int32_t* __restrict__ blk_ptr, int32_t* __restrict__ blk_ent, int pass) {
-  const int w = (blockIdx.x * blockDim.x + threadIdx.x) / 32, lane = threadIdx.x % 32;
-  if (w >= n_blk) return;
-  int cursor = pass ? blk_ptr[w] : 0;
-  for (int k0 = 0; k0 < n_occ; k0 += 32) {
-    const int k = k0 + lane;
-    int o = -1;
-    bool match = false;
-    if (k < n_occ) {
-      o = perm[k];
-      if (o >= 0 && o < n_occ) {
-        const int y = targets[o];
-        match = y >= 0 && y < V && y / BN == w;
-      }
-    }
-    const unsigned bal = __ballot_sync(0xffffffffu, match);
-    if (pass && match) {
-      int lo = 0, hi = T - 1;  // last row r with row_ptr[r] <= k
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) / 2;
-        if (row_ptr[mid] <= k) lo = mid; else hi = mid - 1;
-      }
-      const int pos = cursor + __popc(bal & ((1u << lane) - 1u));
-      blk_ent[2 * pos] = lo;
-      blk_ent[2 * pos + 1] = o;
-    }
-    cursor += __popc(bal);
-  }
-  if (!pass && lane == 0) blk_ptr[w + 1] = cursor;
-}
+// Occurrences grouped by the 256-column vocabulary block of their target, for the dW
+// epilogue's correction: a stable counting sort in one CTA. Block b's entries are
+// blk_ent[2 e .. 2 e + 1] = {source row, occurrence} for e in [blk_ptr[b], blk_ptr[b + 1]),
+// in increasing CSR position k (the order the dW epilogue adds them in, so the sums are
+// reproducible). Counts with shared atomics, an exclusive scan, then, chunk by chunk, one
+// warp hands out positions in k order (lanes with the same block take consecutive slots).
+// Occurrences with an out-of-range id or target are left out (the GEMM epilogues flag them).
+// Also zeroes occ_delta.
+constexpr int kGroupThreads = 1024;
 
-// Prefix sum of the block counts (one block) and zeroed residuals.
-__global__ void lm_block_scan_kernel(int32_t* __restrict__ blk_ptr, int n_blk, float* __restrict__ occ_delta,
-                                     int n_occ) {
-  for (int i = threadIdx.x; i < n_occ; i += blockDim.x) occ_delta[i] = 0.f;
-  if (threadIdx.x == 0) {
-    blk_ptr[0] = 0;
-    for (int b = 1; b <= n_blk; ++b) blk_ptr[b] += blk_ptr[b - 1];
+__global__ void __launch_bounds__(kGroupThreads) lm_group_occ_kernel(
+    const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ perm, const int32_t* __restrict__ targets, int T,
+    int n_occ, int V, int n_blk, int chunk, int32_t* __restrict__ blk_ptr, int32_t* __restrict__ blk_ent,
+    float* __restrict__ occ_delta) {
+  extern __shared__ int gsm[];
+  int* cur = gsm;            // [n_blk] counts, then the next free slot of each block
+  int* sb = cur + n_blk;     // [chunk] block of each occurrence of the chunk (-1: none)
+  int* so = sb + chunk;      // [chunk] occurrence id
+  int* sr = so + chunk;      // [chunk] source row
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  auto block_of = [&](int k, int* o_out) {
+    const int o = perm[k];
+    int b = -1;
+    if (o >= 0 && o < n_occ) {
+      const int y = targets[o];
+      if (y >= 0 && y < V) b = y / BN;
+    }
+    *o_out = o;
+    return b;
+  };
+  for (int i = tid; i < n_occ; i += kGroupThreads) occ_delta[i] = 0.f;
+  for (int b = tid; b < n_blk; b += kGroupThreads) cur[b] = 0;
+  __syncthreads();
+  for (int k = tid; k < n_occ; k += kGroupThreads) {
+    int o;
+    const int b = block_of(k, &o);
+    if (b >= 0) atomicAdd(&cur[b], 1);
+  }
+  __syncthreads();
+  if (warp == 0) {  // exclusive scan of the counts
+    int run = 0;
+    for (int b0 = 0; b0 < n_blk; b0 += 32) {
+      const int b = b0 + lane;
+      const int x = b < n_blk ? cur[b] : 0;
+      int incl = x;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += y;
+      }
+      if (b < n_blk) {
+        cur[b] = run + incl - x;
+        blk_ptr[b] = run + incl - x;
+      }
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) blk_ptr[n_blk] = run;
+  }
+  __syncthreads();
+  for (int c0 = 0; c0 < n_occ; c0 += chunk) {
+    const int len = min(chunk, n_occ - c0);
+    for (int i = tid; i < len; i += kGroupThreads) {
+      int o;
+      sb[i] = block_of(c0 + i, &o);
+      so[i] = o;
+      sr[i] = 0;
+    }
+    __syncthreads();
+    for (int r = tid; r < T; r += kGroupThreads) {  // the row holding each position of the chunk
+      const int lo = max(row_ptr[r], c0), hi = min(row_ptr[r + 1], c0 + len);
+      for (int k = lo; k < hi; ++k) sr[k - c0] = r;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      for (int i0 = 0; i0 < len; i0 += 32) {
+        const int i = i0 + lane;
+        const int b = i < len ? sb[i] : -1;
+        const unsigned mask = __match_any_sync(0xffffffffu, b >= 0 ? b : -1 - lane);
+        const int leader = __ffs(mask) - 1;
+        int base = 0;
+        if (b >= 0 && lane == leader) {
+          base = cur[b];
+          cur[b] = base + __popc(mask);
+        }
+        base = __shfl_sync(0xffffffffu, base, leader);
+        if (b >= 0) {
+          const int pos = base + __popc(mask & ((1u << lane) - 1u));
+          blk_ent[2 * pos] = sr[i];
+          blk_ent[2 * pos + 1] = so[i];
+        }
+      }
+    }
+    __syncthreads();
   }
 }
 
@@ -531,17 +588,17 @@ int logprob_bwd_tc(const LogprobArgs& a, cudaStream_t st) {
   if (rc) return rc;
   const int n_blk = static_cast<int>((a.V + BN - 1) / BN);
   {
-    const unsigned grid = static_cast<unsigned>((n_blk * 32 + 255) / 256);
-    lm_block_lists_kernel<<<grid, 256, 0, st>>>(a.row_ptr, a.perm, a.targets, static_cast<int>(a.T),
-                                                static_cast<int>(a.n_occ), static_cast<int>(a.V), n_blk, a.ws.blk_ptr,
-                                                a.ws.blk_ent, 0);
-    TREE_LAUNCH_CHECK("lm_block_lists_kernel<count>");
-    lm_block_scan_kernel<<<1, 1024, 0, st>>>(a.ws.blk_ptr, n_blk, a.ws.occ_delta, static_cast<int>(a.n_occ));
-    TREE_LAUNCH_CHECK("lm_block_scan_kernel");
-    lm_block_lists_kernel<<<grid, 256, 0, st>>>(a.row_ptr, a.perm, a.targets, static_cast<int>(a.T),
-                                                static_cast<int>(a.n_occ), static_cast<int>(a.V), n_blk, a.ws.blk_ptr,
-                                                a.ws.blk_ent, 1);
-    TREE_LAUNCH_CHECK("lm_block_lists_kernel<fill>");
+    // the counting sort's shared memory: block counters, then three arrays per chunk
+    const int budget = 200 * 1024 / 4;
+    if (n_blk > budget / 2)
+      return fail(TREE_ERR_SHAPE, "tree_logprob_bwd: V = %lld has too many 256-column blocks", (long long)a.V);
+    const int chunk = std::min(8192, (budget - n_blk) / 3);
+    const size_t smem = sizeof(int) * (static_cast<size_t>(n_blk) + 3 * static_cast<size_t>(chunk));
+    if ((rc = smem_opt_in(reinterpret_cast<const void*>(lm_group_occ_kernel), static_cast<int>(smem)))) return rc;
+    lm_group_occ_kernel<<<1, kGroupThreads, smem, st>>>(a.row_ptr, a.perm, a.targets, static_cast<int>(a.T),
+                                                        static_cast<int>(a.n_occ), static_cast<int>(a.V), n_blk, chunk,
+                                                        a.ws.blk_ptr, a.ws.blk_ent, a.ws.occ_delta);
+    TREE_LAUNCH_CHECK("lm_group_occ_kernel");
   }
   __nv_bfloat16* gz = static_cast<__nv_bfloat16*>(a.ws.gz);
   // 1) G_z = recomputed softmax terms and target terms, bf16 [T, V]
