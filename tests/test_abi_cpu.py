@@ -103,6 +103,23 @@ def test_host_argument_errors(tma):
     assert L.tree_logprob_workspace_size(64, 64, 512, 100, 0) > 0
 
 
+def test_every_workload_runs_on_tensor_cores(tma):
+    """Kernel family per call (0 CUDA cores, 1 tcgen05 kind::f16, 2 tcgen05 kind::tf32 with
+    the two-term split): the tiny fp32 tree (head size 64, fp32 LM head) takes the tf32
+    kernels, the bf16 trees at head size 128 and the bf16 LM head the kind::f16 kernels; bf16
+    at head size 64 runs on the tf32 kernels; only fp32 at head size 128 is left on CUDA
+    cores."""
+    F32, BF16 = 0, 1
+    for op in (0, 1, 2, 3):
+        assert tma.tree_kernel_path(op, F32, 64) == 2
+    for op in (0, 1):
+        assert tma.tree_kernel_path(op, BF16, 128) == 1
+        assert tma.tree_kernel_path(op, BF16, 64) == 2
+        assert tma.tree_kernel_path(op, F32, 128) == 0
+    for op in (2, 3):
+        assert tma.tree_kernel_path(op, BF16, 128) == 1
+
+
 def test_kernel_timing_without_brackets(tma):
     """Without a recorded bracket (or a device) the timing query answers -1."""
     tma.tree_kernel_timing(False)

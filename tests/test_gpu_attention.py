@@ -96,16 +96,28 @@ def test_degenerate_trees(case):
     _full_check(seqs, 2, 1, 128, "bf16")
 
 
-def test_deterministic_flag_repeats_bitwise():
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("f32", 64), ("bf16", 64)])
+def test_deterministic_flag_repeats_bitwise(dtype, d):
+    """bf16 at d = 128 on the kind::f16 kernels; fp32 and bf16 at d = 64 on the tf32-split
+    kernels (whose backward has one fixed summation order whatever the flag)."""
     need_cuda()
     t = synth.galton_watson(seed=4, budget=600, seg=(5, 90), vocab=1000)
     m = tma()
     pk = m.tree_pack(t.seqs)
-    q, k, v, do = synth.attention_config("agentic_short", pk["T"], seed=3)
-    r1 = _run(m, pk, q, k, v, do, "bf16", deterministic=True)
-    r2 = _run(m, pk, q, k, v, do, "bf16", deterministic=True)
+    if d == 128:
+        q, k, v, do = synth.attention_config("agentic_short", pk["T"], seed=3)
+    else:
+        T, bf = pk["T"], dtype == "bf16"
+        q, k, v, do = (synth.normal(30 + s, shape, bf16=bf) for s, shape in
+                       enumerate(((T, 8, d), (T, 2, d), (T, 2, d), (T, 8, d))))
+    r1 = _run(m, pk, q, k, v, do, dtype, deterministic=True)
+    r2 = _run(m, pk, q, k, v, do, dtype, deterministic=True)
     for a, b in zip(r1, r2):
         assert torch.equal(a, b)
+    if d == 64:
+        r3 = _run(m, pk, q, k, v, do, dtype, deterministic=False)
+        for a, b in zip(r1, r3):
+            assert torch.equal(a, b)
 
 
 @pytest.mark.parametrize("name", ["agentic_long", "galton_watson"])

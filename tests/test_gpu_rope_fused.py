@@ -54,8 +54,9 @@ def test_fused_rope_random_trees_bf16(seed):
     _case(t.seqs, 8, 2, 128, "bf16", seed)
 
 
-def test_fused_rope_fp32_fallback():
-    """fp32 and d = 64 take the SIMT backward, then the rotation as its own pass."""
+def test_fused_rope_fp32_head_64():
+    """fp32 and d = 64 take the tf32-split tensor-core backward, then the rotation as its
+    own pass."""
     t = synth.galton_watson(seed=2, budget=300, seg=(5, 60), vocab=1000)
     _case(t.seqs, 4, 2, 64, "f32", 2)
 

@@ -70,7 +70,8 @@ def test_logprob_tiny_fp32():
     assert_close("dW", dw, rdw, F32_TOL)
 
 
-@pytest.mark.parametrize("T,K,V,bf16", [(200, 128, 1000, True), (333, 256, 4104, True), (130, 64, 520, False)])
+@pytest.mark.parametrize("T,K,V,bf16", [(200, 128, 1000, True), (333, 256, 4104, True), (130, 64, 520, False),
+                                        (333, 128, 1000, False)])
 def test_logprob_random(T, K, V, bf16):
     """Ragged row/vocabulary tails, rows without occurrences, repeated targets."""
     need_cuda()

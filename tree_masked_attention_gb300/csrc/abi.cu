@@ -129,6 +129,7 @@ extern "C" int tree_attn_fwd(const void* q, const void* k, const void* v, void* 
   a.scale = softmax_scale > 0.f ? softmax_scale : static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
   attn_ws_layout(T, Hq, Hkv, d, dtype, workspace, &a.ws);
   if (attn_fwd_tc_supported(dtype, d, Hq, Hkv)) return attn_fwd_tc(a, reinterpret_cast<cudaStream_t>(stream));
+  if (attn_tc32_supported(dtype, d)) return attn_fwd_tc32(a, reinterpret_cast<cudaStream_t>(stream));
   return attn_fwd_simt(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -161,7 +162,7 @@ static int attn_bwd_common(const char* name, const void* q, const void* k, const
     a.rope_theta = rope_theta;
     return attn_bwd_tc(a, st);
   }
-  if ((rc = attn_bwd_simt(a, st)) || !rope_pos) return rc;
+  if ((rc = attn_tc32_supported(dtype, d) ? attn_bwd_tc32(a, st) : attn_bwd_simt(a, st)) || !rope_pos) return rc;
   return tree_rope(dq, dk, rope_pos, T, Hq, Hkv, d, rope_theta, dtype, 1, stream);
 }
 
@@ -226,7 +227,7 @@ extern "C" int tree_logprob_fwd(const void* hidden, const void* w_lm, const int3
   a.lse = lse; a.logp = logp; a.T = T; a.K = K_h; a.V = V; a.n_occ = n_occ; a.dtype = dtype;
   logprob_ws_layout(T, K_h, V, n_occ, dtype, workspace, &a.ws);
   if (logprob_tc_supported(dtype)) return logprob_fwd_tc(a, reinterpret_cast<cudaStream_t>(stream));
-  return logprob_fwd_simt(a, reinterpret_cast<cudaStream_t>(stream));
+  return logprob_fwd_tc32(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" int tree_logprob_bwd(const void* hidden, const void* w_lm, const float* lse,
@@ -251,12 +252,14 @@ extern "C" int tree_logprob_bwd(const void* hidden, const void* w_lm, const floa
   a.dw_fp32 = dtype == TREE_DTYPE_F32 ? 1 : dw_fp32;
   logprob_ws_layout(T, K_h, V, n_occ, dtype, workspace, &a.ws);
   if (logprob_tc_supported(dtype)) return logprob_bwd_tc(a, reinterpret_cast<cudaStream_t>(stream));
-  return logprob_bwd_simt(a, reinterpret_cast<cudaStream_t>(stream));
+  return logprob_bwd_tc32(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" int tree_kernel_path(int op, int dtype, int d) {
-  if (op == 0) return attn_fwd_tc_supported(dtype, d, 2, 1) ? 1 : 0;
-  if (op == 1) return attn_bwd_tc_supported(dtype, d, 0) ? 1 : 0;
-  if (op == 2 || op == 3) return logprob_tc_supported(dtype) ? 1 : 0;
+  if (op == 0 || op == 1) {
+    if (op == 0 ? attn_fwd_tc_supported(dtype, d, 2, 1) : attn_bwd_tc_supported(dtype, d, 0)) return 1;
+    return attn_tc32_supported(dtype, d) ? 2 : 0;
+  }
+  if (op == 2 || op == 3) return logprob_tc_supported(dtype) ? 1 : 2;
   return 0;
 }

@@ -104,5 +104,6 @@ extern "C" int tree_attn_fwd_noalloc(const void* q, const void* k, const void* v
   a.ws.end_pad = reinterpret_cast<int32_t*>(b + kOffPad);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (attn_fwd_tc_supported(dtype, d, Hq, Hkv)) return attn_fwd_tc(a, st);
+  if (attn_tc32_supported(dtype, d)) return attn_fwd_tc32(a, st);
   return attn_fwd_simt(a, st);
 }

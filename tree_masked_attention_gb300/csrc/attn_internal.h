@@ -54,8 +54,14 @@ size_t attn_ws_layout(int64_t T, int Hq, int Hkv, int d, int dtype, void* base, 
 
 int tile_meta_launch(const int32_t* end, int64_t n, int tile, int32_t* kmax, int32_t* kmin,
                      cudaStream_t st);
+// CUDA-core kernels: fp32 storage with head size 128, the one shape no tensor-core kernel serves
 int attn_fwd_simt(const AttnArgs& a, cudaStream_t st);
 int attn_bwd_simt(const AttnArgs& a, cudaStream_t st);
+
+// tcgen05 kind::tf32 kernels with a two-term split (head size 64, fp32 or bf16 storage)
+bool attn_tc32_supported(int dtype, int d);
+int attn_fwd_tc32(const AttnArgs& a, cudaStream_t st);
+int attn_bwd_tc32(const AttnArgs& a, cudaStream_t st);
 
 // tcgen05 / TMA kernels (bf16, d = 128, even GQA group)
 bool attn_fwd_tc_supported(int dtype, int d, int Hq, int Hkv);
@@ -73,7 +79,7 @@ struct LogprobWs {
   float* part_max;   // [n_vtiles, T] per vocabulary tile: row max of the logits
   float* part_sum;   // [n_vtiles, T] per vocabulary tile: sum exp(z - max)
   float* crow;       // [T]           sum of grad_logp over the row's occurrences
-  void* gz;          // [T, V]        G_z (fp32 on the SIMT path, bf16 on the tensor-core path)
+  void* gz;          // [T, V]        G_z (fp32 on the fp32 path, bf16 on the bf16 path)
   float* occ_delta;  // [n_occ]       exact minus bf16-stored G_z at each occurrence's target cell
   int32_t* blk_ptr;  // [ceil(V/256)+1] occurrences grouped by 256-column target block
   int32_t* blk_ent;  // [2 * n_occ]   {source row, occurrence} per group entry
@@ -97,8 +103,14 @@ struct LogprobArgs {
 };
 
 size_t logprob_ws_layout(int64_t T, int64_t K, int64_t V, int64_t n_occ, int dtype, void* base, LogprobWs* ws);
-int logprob_fwd_simt(const LogprobArgs& a, cudaStream_t st);
-int logprob_bwd_simt(const LogprobArgs& a, cudaStream_t st);
+// fp32: tcgen05 kind::tf32 GEMMs with a two-term split
+int logprob_fwd_tc32(const LogprobArgs& a, cudaStream_t st);
+int logprob_bwd_tc32(const LogprobArgs& a, cudaStream_t st);
+int lse_combine_launch(const float* part_max, const float* part_sum, int n_tiles, int64_t T, const int32_t* row_ptr,
+                       const int32_t* perm, int64_t n_occ, float* lse, float* logp, cudaStream_t st);
+int row_grad_sum_launch(const int32_t* row_ptr, const int32_t* perm, const float* grad, int64_t T, int64_t n_occ,
+                        float* crow, cudaStream_t st);
+// bf16: the kind::f16 GEMM with fused epilogues
 bool logprob_tc_supported(int dtype);
 int logprob_fwd_tc(const LogprobArgs& a, cudaStream_t st);
 int logprob_bwd_tc(const LogprobArgs& a, cudaStream_t st);

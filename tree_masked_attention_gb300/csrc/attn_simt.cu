@@ -1,5 +1,8 @@
-// Tree attention, SIMT fp32 kernels: the fp32 path, and the reference-grade path
-// for any head size. Forward, backward preprocess (Delta), dQ and dK/dV.
+// Tree attention on the CUDA cores, for the one shape the tensor-core kernels leave out:
+// fp32 storage with head size 128. (The tf32-split kernels hold each fp32 operand as two
+// tf32 tiles; at head size 128 the dQ pass would need Q and dO resident as 4 x 64 KB, more
+// than a CTA's shared memory.) Forward, backward preprocess (Delta), dQ and dK/dV. The
+// per-tile metadata kernel here also serves the tf32-split kernels.
 //
 // Visibility (Tree Training, arXiv 2511.00413, §3.2 "Attention Mask"; Trie
 // packing "Step 2 - Allow only ancestors and self"): key j is visible to query i
@@ -332,15 +335,15 @@ static int bwd_simt(const AttnArgs& a, cudaStream_t st) {
 }
 
 int attn_fwd_simt(const AttnArgs& a, cudaStream_t st) {
-  if (a.dtype == TREE_DTYPE_BF16)
-    return a.d == 64 ? fwd_simt<__nv_bfloat16, 64>(a, st) : fwd_simt<__nv_bfloat16, 128>(a, st);
-  return a.d == 64 ? fwd_simt<float, 64>(a, st) : fwd_simt<float, 128>(a, st);
+  if (a.dtype != TREE_DTYPE_F32 || a.d != 128)
+    return fail(TREE_ERR_SHAPE, "CUDA-core attention serves fp32 with head size 128 only");
+  return fwd_simt<float, 128>(a, st);
 }
 
 int attn_bwd_simt(const AttnArgs& a, cudaStream_t st) {
-  if (a.dtype == TREE_DTYPE_BF16)
-    return a.d == 64 ? bwd_simt<__nv_bfloat16, 64>(a, st) : bwd_simt<__nv_bfloat16, 128>(a, st);
-  return a.d == 64 ? bwd_simt<float, 64>(a, st) : bwd_simt<float, 128>(a, st);
+  if (a.dtype != TREE_DTYPE_F32 || a.d != 128)
+    return fail(TREE_ERR_SHAPE, "CUDA-core attention serves fp32 with head size 128 only");
+  return bwd_simt<float, 128>(a, st);
 }
 
 }  // namespace tree

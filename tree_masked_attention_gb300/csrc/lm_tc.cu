@@ -550,12 +550,6 @@ static int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const lmtc:
   return TREE_OK;
 }
 
-// Defined in logprob_simt.cu.
-int lse_combine_launch(const float* part_max, const float* part_sum, int n_tiles, int64_t T, const int32_t* row_ptr,
-                       const int32_t* perm, int64_t n_occ, float* lse, float* logp, cudaStream_t st);
-int row_grad_sum_launch(const int32_t* row_ptr, const int32_t* perm, const float* grad, int64_t T, int64_t n_occ,
-                        float* crow, cudaStream_t st);
-
 int logprob_fwd_tc(const LogprobArgs& a, cudaStream_t st) {
   using namespace lmtc;
   CUtensorMap ta, tb;
