@@ -180,7 +180,18 @@ int tree_rope(void* q, void* k, const int32_t* position_ids, int64_t T, int Hq, 
  * that run in any order (results may differ in the last bits run to run); 1 makes
  * every sum fixed-order and the results bitwise reproducible: dK and dV come from one
  * work unit per key tile, and dQ from a second, query-stationary pass that walks each
- * query tile's key tiles in order (S and dP recomputed: more FLOPs, slower).
+ * query tile's key tiles in order (S and dP recomputed: more FLOPs, slower). The
+ * kernels at head size 64 (below) always sum in one fixed order, so there both values
+ * give bitwise reproducible results.
+ *
+ * Kernels by (dtype, d) -- tree_kernel_path tells which a call takes:
+ *   bf16, d = 128   tcgen05 kind::f16 (bf16 operands, fp32 TMEM accumulators), TMA-fed.
+ *   fp32 or bf16, d = 64   tcgen05 kind::tf32 with every fp32 operand split into
+ *                   hi = tf32(x) and lo = tf32(x - hi), products taken as hi.hi + hi.lo
+ *                   + lo.hi (about 2^-21 relative error each; terms with an exactly
+ *                   representable operand are skipped).
+ *   fp32, d = 128   CUDA cores (fp32 FMA): the hi/lo tiles of a 128-row, 128-wide fp32
+ *                   operand pair do not fit a CTA's shared memory next to each other.
  */
 size_t tree_attn_workspace_size(int64_t T, int Hq, int Hkv, int d, int dtype);
 
@@ -254,6 +265,10 @@ int tree_attn_bwd_rope(const void* q, const void* k, const void* v, const void* 
  * 16-byte aligned; K_h % 64 == 0 and V % 8 == 0. lse: device fp32 [T];
  * logp, grad_logp: device fp32 [n_occ]; index arrays device int32.
  * Out-of-range targets or CSR entries set TREE_ERR_DEVICE_CHECK and are skipped.
+ *
+ * Kernels: bf16 runs the tcgen05 kind::f16 GEMM with the LSE / G_z / dW-correction
+ * epilogues; fp32 runs tcgen05 kind::tf32 GEMMs with the two-term operand split
+ * (hi.hi + hi.lo + lo.hi) and the same epilogue arithmetic, G_z kept in fp32.
  */
 size_t tree_logprob_workspace_size(int64_t T, int64_t K_h, int64_t V, int64_t n_occ, int dtype);
 
@@ -274,9 +289,6 @@ int tree_logprob_bwd(const void* hidden, const void* w_lm, const float* lse,
                      int dw_fp32, int dtype, void* workspace, size_t workspace_bytes,
                      tree_stream_t stream);
 
-/* ------------------------------------------------------------------------ */
-/* Status                                                                    */
-/* ------------------------------------------------------------------------ */
 /* ------------------------------------------------------------------------ */
 /* Per-occurrence clipped policy objective                                   */
 /* ------------------------------------------------------------------------ */
@@ -434,6 +446,9 @@ int tree_conv1d_bwd(const void* x, const void* w, const void* dy, void* dx, floa
                     int64_t T, int C, int K, int dtype, void* workspace,
                     size_t workspace_bytes, tree_stream_t stream);
 
+/* ------------------------------------------------------------------------ */
+/* Status                                                                    */
+/* ------------------------------------------------------------------------ */
 /* Synchronises `stream`, reads and clears the device error word of the current
  * device: TREE_OK, TREE_ERR_DEVICE_CHECK or TREE_ERR_TIMEOUT (a bounded
  * pipeline wait gave up; the kernel then returned early and its outputs are
@@ -444,8 +459,9 @@ int tree_check_device_status(tree_stream_t stream);
  * next call into the library from the same thread. */
 const char* tree_last_error(void);
 
-/* Which kernel family a call with these arguments runs: 0 = SIMT fp32 kernels,
- * 1 = tcgen05/TMA tensor-core kernels. op: 0 attention forward, 1 attention
+/* Which kernel family a call with these arguments runs: 0 = CUDA-core fp32 kernels,
+ * 1 = tcgen05 kind::f16 tensor-core kernels (bf16 operands), 2 = tcgen05 kind::tf32
+ * tensor-core kernels with the two-term split. op: 0 attention forward, 1 attention
  * backward, 2 log-prob forward, 3 log-prob backward. */
 int tree_kernel_path(int op, int dtype, int d);
 
