@@ -63,6 +63,24 @@ def test_pack_bit_exact_workloads(tma, gen):
     _same(tma.tree_pack(t.seqs), oracle.pack_ref(t.seqs))
 
 
+@pytest.mark.parametrize("fields", [("position_ids", "subtree_end"), ("paths", "node_parent"),
+                                    ("occ_row_ptr", "occ_perm", "occ_targets"), ()])
+def test_pack_field_subsets(tma, fields):
+    """tree_pack(fields=...) returns exactly the named arrays, bit-equal to the oracle's."""
+    t = synth.galton_watson(seed=2, budget=900, seg=(5, 60), vocab=50)
+    got = tma.tree_pack(t.seqs, fields=fields)
+    ref = oracle.pack_ref(t.seqs)
+    arrays = {k for k, v in got.items() if not isinstance(v, int)}
+    assert arrays == set(fields) | ({"token_rows"} if "paths" in fields else set())
+    for f in fields:
+        if f == "paths":
+            assert all(np.array_equal(a, b) for a, b in zip(got["paths"], ref["paths"]))
+        else:
+            assert np.array_equal(got[f], ref[f]), f
+    with pytest.raises(ValueError):
+        tma.tree_pack(t.seqs, fields=("no_such_field",))
+
+
 def test_pack_pages_examples(tma):
     from conftest import golden
     g = golden("trie_packing_example.json")

@@ -151,6 +151,33 @@ def test_full_size_sampled(name):
     assert_close("sum dK", host(dk).sum(0), np.zeros_like(sum_do), 0.5)
 
 
+@pytest.mark.parametrize("name,g", [("agentic_long", 5), ("galton_watson", 2)])
+def test_full_size_one_kv_group_every_row(name, g):
+    """The 16k-row trees at full size (32 / 8 heads): every row of O, LSE and dQ of the four
+    query heads of KV group g, and every row of that group's dK and dV -- the prompt and
+    root keys, whose subtrees hold every query, included -- against the per-path oracle
+    run on that group alone (KV groups are independent, so the group's slice of the inputs
+    is a complete problem of its own)."""
+    need_cuda()
+    m = tma()
+    t = synth.CONFIGS[name]["tree"]()
+    pk = m.tree_pack(t.seqs)
+    T = pk["T"]
+    q, k, v, do = synth.attention_config(name, T)
+    o, lse, dq, dk, dv = _run(m, pk, q, k, v, do, "bf16")
+    G = q.shape[1] // k.shape[1]
+    hs = slice(G * g, G * (g + 1))
+    paths = oracle.pack_ref(t.seqs)["paths"]
+    sq, sk, sv, sdo = q[:, hs], k[:, g:g + 1], v[:, g:g + 1], do[:, hs]
+    ro, rlse = oracle.attn_ref_fwd(sq, sk, sv, paths)
+    rdq, rdk, rdv = oracle.attn_ref_bwd(sq, sk, sv, sdo, paths)
+    assert_close("O", host(o)[:, hs], ro, BF16_TOL)
+    assert_close("LSE", host(lse)[hs], rlse, F32_TOL)
+    assert_close("dQ", host(dq)[:, hs], rdq, BF16_TOL)
+    assert_close("dK", host(dk)[:, g:g + 1], rdk, BF16_TOL)
+    assert_close("dV", host(dv)[:, g:g + 1], rdv, BF16_TOL)
+
+
 def test_bad_subtree_end_sets_device_flag():
     """An out-of-range subtree_end is reported through the device error word;
     the kernels never index memory with it, so nothing faults."""

@@ -54,11 +54,13 @@ def _ptr(a: np.ndarray, ctype):
     return a.ctypes.data_as(C.POINTER(ctype))
 
 
-def tree_pack(seqs, seq_weights=None) -> dict:
+def tree_pack(seqs, seq_weights=None, fields=None) -> dict:
     """Pack host token sequences (iterables of ints) into a preorder trie.
 
     Returns numpy arrays named as in tree_pack_out (include/tree_attn.h), plus
     T, n_nodes, n_occ, n_roots and ``paths`` (packed rows of every sequence).
+    ``fields`` (an iterable of those names, "paths" included) limits the arrays
+    computed and returned to the ones named; the library skips the work of the rest.
     """
     L = lib()
     seqs = [np.asarray(s, dtype=np.int32).reshape(-1) for s in seqs]
@@ -77,9 +79,18 @@ def tree_pack(seqs, seq_weights=None) -> dict:
         res["occ_weights"] = np.empty(no, np.float32)
         res["occ_row_ptr"] = np.empty(T + 1, np.int32)
         res["token_rows"] = np.empty(sizes.n_tokens, np.int32)
+        if fields is not None:
+            want = set(fields)
+            unknown = want - set(res) - {"paths"}
+            if unknown:
+                raise ValueError(f"tree_pack: unknown fields {sorted(unknown)}")
+            if "paths" in want:
+                want.add("token_rows")
+            res = {n: a for n, a in res.items() if n in want}
         out = PackOut()
         for name, _ in PackOut._fields_:
-            setattr(out, name, _ptr(res[name], C.c_float if name == "occ_weights" else C.c_int32))
+            if name in res:
+                setattr(out, name, _ptr(res[name], C.c_float if name == "occ_weights" else C.c_int32))
         w = None
         if seq_weights is not None:
             w = np.ascontiguousarray(seq_weights, dtype=np.float32)
@@ -90,7 +101,8 @@ def tree_pack(seqs, seq_weights=None) -> dict:
     finally:
         L.tree_plan_free(plan)
     res.update(T=T, n_nodes=nn, n_occ=no, n_roots=sizes.n_roots)
-    res["paths"] = [res["token_rows"][offs[k]:offs[k + 1]] for k in range(len(seqs))]
+    if "token_rows" in res:
+        res["paths"] = [res["token_rows"][offs[k]:offs[k + 1]] for k in range(len(seqs))]
     return res
 
 

@@ -182,8 +182,8 @@ extern "C" int tree_pack_emit(const tree_plan* plan, const float* seq_weights, c
     }
     for (int32_t i = T - 1; i >= 0; --i)
       if (prow[i] >= 0) size[prow[i]] += size[i];
-    std::vector<int32_t> node_of(T);
-    for (int32_t c = 0; c < n_nodes; ++c) {
+    std::vector<int32_t> node_of(out->node_of_token || out->node_parent ? T : 0);
+    for (int32_t c = 0; c < n_nodes && !node_of.empty(); ++c) {
       const int32_t s = p.node_start[c], e = c + 1 < n_nodes ? p.node_start[c + 1] : T;
       for (int32_t i = s; i < e; ++i) node_of[i] = c;
     }
@@ -206,6 +206,9 @@ extern "C" int tree_pack_emit(const tree_plan* plan, const float* seq_weights, c
     if (out->token_rows)
       for (int64_t t = 0; t < n_tokens; ++t) out->token_rows[t] = p.row_of[p.token_node[t]];
     // occurrences, sequence-major; CSR by source row through a stable counting sort
+    if (!out->occ_source_rows && !out->occ_targets && !out->occ_seq && !out->occ_weights && !out->occ_row_ptr &&
+        !out->occ_perm)
+      return TREE_OK;
     std::vector<int32_t> count(static_cast<size_t>(T) + 1, 0);
     int32_t o = 0;
     for (int64_t k = 0; k < p.n_seqs; ++k) {
