@@ -256,16 +256,18 @@ class AttnStep:
                               dtype=torch.uint8, device=dev)
         self.stream = torch.cuda.current_stream(dev)
 
-    def step(self, ev=None):
+    def step(self, ev=None, b=None):
+        """One step on the leg's device tensors, or on those of buffer set `b`."""
         tma, s = self.tma, self.stream
+        b = self if b is None else b
         if ev: ev[0].record(s)
-        tma.tree_rope(self.q, self.k, self.pos)
+        tma.tree_rope(b.q, b.k, b.pos)
         if ev: ev[1].record(s)
-        tma.tree_attn_fwd(self.q, self.k, self.v, self.end, workspace=self.ws, out=self.o, lse=self.lse)
+        tma.tree_attn_fwd(b.q, b.k, b.v, b.end, workspace=b.ws, out=b.o, lse=b.lse)
         if ev: ev[2].record(s)
         # backward with the inverse rotation of dq, dk fused into the kernel that writes them
-        tma.tree_attn_bwd_rope(self.q, self.k, self.v, self.o, self.do, self.lse, self.end, self.pos,
-                               workspace=self.ws, grads=(self.dq, self.dk, self.dv))
+        tma.tree_attn_bwd_rope(b.q, b.k, b.v, b.o, b.do, b.lse, b.end, b.pos,
+                               workspace=b.ws, grads=(b.dq, b.dk, b.dv))
         if ev: ev[3].record(s)
 
     def describe(self):
@@ -370,16 +372,28 @@ class AttnStep:
         """The same step through the public API with host buffers, as a training loop runs
         it: every step packs its tree on the host (tree_pack, position_ids and subtree_end
         only), copies Q, K, V, dO, positions and subtree_end from pinned memory to the
-        device (non-blocking, one stream), runs the step and reads dQ, dK, dV back into
-        pinned buffers. The host packs step s + 1's tree while the GPU works on step s (two
-        pinned position / subtree_end buffers), so the loop is bound by the slower side."""
+        device, runs the step and copies dQ, dK, dV back into pinned memory. Two device
+        buffer sets and three streams let step s + 1's inputs travel while step s computes
+        and step s - 1's gradients come back; the host packs step s + 1's tree meanwhile."""
+        import types
         import torch
-        tma = self.tma
-        hdq, hdk, hdv = (torch.empty(x.shape, dtype=self.td).pin_memory() for x in (self.dq, self.dk, self.dv))
+        tma, dev, comp = self.tma, self.dev, self.stream
+        h2d_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        sets = [self]
+        extra = types.SimpleNamespace()
+        extra.q, extra.k, extra.v, extra.do = (torch.empty_like(x) for x in (self.q, self.k, self.v, self.do))
+        extra.pos, extra.end = torch.empty_like(self.pos), torch.empty_like(self.end)
+        extra.o, extra.lse = torch.empty_like(self.o), torch.empty_like(self.lse)
+        extra.dq, extra.dk, extra.dv = (torch.empty_like(x) for x in (self.dq, self.dk, self.dv))
+        extra.ws = torch.empty_like(self.ws)
+        sets.append(extra)
+        hgrad = [tuple(torch.empty(x.shape, dtype=self.td).pin_memory() for x in (self.dq, self.dk, self.dv))
+                 for _ in range(2)]
         hpos = [torch.empty(self.T, dtype=torch.int32).pin_memory() for _ in range(2)]
         hend = [torch.empty(self.T, dtype=torch.int32).pin_memory() for _ in range(2)]
         h2d = sum(x.numel() * x.element_size() for x in (self.hq, self.hk, self.hv, self.hdo, hpos[0], hend[0]))
-        d2h = sum(x.numel() * x.element_size() for x in (hdq, hdk, hdv))
+        d2h = sum(x.numel() * x.element_size() for x in hgrad[0])
+        ev = {n: [torch.cuda.Event() for _ in range(2)] for n in ("h2d", "comp", "d2h")}
 
         def pack_into(b):
             p2 = tma.tree_pack(self.tree.seqs, fields=("position_ids", "subtree_end"))
@@ -387,32 +401,48 @@ class AttnStep:
             hend[b].numpy()[:] = p2["subtree_end"]
 
         def run(n):
+            torch.cuda.synchronize()
+            used = [False, False]
             pack_into(0)
             for s_ in range(n):
-                b = s_ & 1
+                b, S = s_ & 1, sets[s_ & 1]
+                if used[b]:
+                    h2d_s.wait_event(ev["comp"][b])  # step s - 2 is done with this set's inputs
+                with torch.cuda.stream(h2d_s):
+                    for dst, src in ((S.pos, hpos[b]), (S.end, hend[b]), (S.q, self.hq), (S.k, self.hk),
+                                     (S.v, self.hv), (S.do, self.hdo)):
+                        dst.copy_(src, non_blocking=True)
+                    ev["h2d"][b].record(h2d_s)
+                comp.wait_event(ev["h2d"][b])
+                if used[b]:
+                    comp.wait_event(ev["d2h"][b])  # step s - 2's gradients have left this set
                 flush.zero_()
-                for dst, src in ((self.pos, hpos[b]), (self.end, hend[b]), (self.q, self.hq), (self.k, self.hk),
-                                 (self.v, self.hv), (self.do, self.hdo)):
-                    dst.copy_(src, non_blocking=True)
-                self.step()
-                for dst, src in ((hdq, self.dq), (hdk, self.dk), (hdv, self.dv)):
-                    dst.copy_(src, non_blocking=True)
+                self.step(b=S)
+                ev["comp"][b].record(comp)
+                d2h_s.wait_event(ev["comp"][b])
+                with torch.cuda.stream(d2h_s):
+                    for dst, src in zip(hgrad[b], (S.dq, S.dk, S.dv)):
+                        dst.copy_(src, non_blocking=True)
+                    ev["d2h"][b].record(d2h_s)
+                used[b] = True
                 if s_ + 1 < n:
-                    pack_into(b ^ 1)  # overlaps the GPU's work on this step
-                torch.cuda.synchronize()
+                    if s_ >= 1:
+                        ev["h2d"][b ^ 1].synchronize()  # step s - 1's index copies have left hpos/hend
+                    pack_into(b ^ 1)
+            torch.cuda.synchronize()
 
-        run(2)
+        run(3)
         barrier(world)
         w0 = time.perf_counter()
         run(K)
-        torch.cuda.synchronize()
         e_s = reduce_max(time.perf_counter() - w0, world)
         return {"value": round((self.f_fwd + self.f_bwd) * K * world / e_s / 1e12, 3), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "ms_per_step": round(e_s * 1e3 / K, 4),
-                "includes": "per step: tree_pack on the host (overlapping the previous step's GPU work), "
-                            "pinned non-blocking H2D of Q,K,V,dO,positions,subtree_end, the step, D2H of "
-                            "dQ,dK,dV into pinned buffers; L2 flush write also inside"}
+                "includes": "per step: tree_pack on the host, pinned H2D of Q,K,V,dO,positions,subtree_end, "
+                            "the step, D2H of dQ,dK,dV into pinned buffers, L2 flush write; two device buffer "
+                            "sets and separate copy streams overlap step s+1's H2D and step s-1's D2H with "
+                            "step s, and the host packs the next tree meanwhile; wall clock around all K steps"}
 
 
 def secondary_entry(leg: AttnStep, m, peak, peak_src):
@@ -612,6 +642,11 @@ def run_conv1d(args, dev, peaks, peak_src, flush):
         tma.tree_conv1d_bwd(x, w, dy, end, pos, workspace=ws, grads=(dx, dw, db))
     torch.cuda.synchronize()
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
+    kern = []
+    # the library brackets each call's kernels with events right at the launches, so the
+    # kernel times carry none of the host's call overhead; the call times (events recorded
+    # from Python around each call) are reported beside them
+    tma.tree_kernel_timing(True)
     for s in range(n):
         flush.zero_()
         evs[s][0].record(stream)
@@ -621,10 +656,15 @@ def run_conv1d(args, dev, peaks, peak_src, flush):
         evs[s][2].record(stream)
         tma.tree_conv1d_bwd(x, w, dy, end, pos, workspace=ws, grads=(dx, dw, db))
         evs[s][3].record(stream)
+        kern.append((tma.tree_kernel_last_ms(2), tma.tree_kernel_last_ms(3)))
+    tma.tree_kernel_timing(False)
     torch.cuda.synchronize()
     tma.tree_check_device_status()
-    f_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
-    b_ms = float(np.mean([e[2].elapsed_time(e[3]) for e in evs]))
+    call_f = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
+    call_b = float(np.mean([e[2].elapsed_time(e[3]) for e in evs]))
+    kern = np.array(kern)
+    f_ms = float(kern[:, 0].mean()) if (kern[:, 0] > 0).all() else call_f
+    b_ms = float(kern[:, 1].mean()) if (kern[:, 1] > 0).all() else call_b
     el = 2
     # algorithmic bytes: forward reads x and writes y once, reads parent_row and the taps;
     # backward reads x and dy and writes dx once, reads subtree_end, positions and the
@@ -638,6 +678,7 @@ def run_conv1d(args, dev, peaks, peak_src, flush):
         "workload": f"conv1d: Galton-Watson tree of {T} rows, {C} channels, kernel size {K}, bf16, with bias",
         "value": round((f_bytes + b_bytes) / ((f_ms + b_ms) / 1e3) / 1e9, 1), "unit": "GB/s",
         "ms_fwd": round(f_ms, 4), "ms_bwd": round(b_ms, 4), "steps": n,
+        "call_ms": {"fwd": round(call_f, 4), "bwd": round(call_b, 4)},
         "gbs_fwd": round(fg, 1), "gbs_bwd": round(bg, 1),
         "step": "tree_conv1d_fwd -> tree_conv1d_bwd (dx, dw, dbias), L2 flushed before each call",
         "roofline": {"bound": "hbm", "achieved": round(bg if dom_b else fg, 1), "peak": hbm, "unit": "GB/s",
@@ -780,6 +821,7 @@ def run_gdn(args, dev, flush):
                     "bf16 q/k/v/dO, fp32 gates",
         "value": round(T / ((f_ms + b_ms) / 1e3), 1), "unit": "packed tokens/s (forward + backward)",
         "ms_fwd": round(f_ms, 4), "ms_bwd": round(b_ms, 4), "steps": n,
+        "call_ms": {"fwd": round(call_f, 4), "bwd": round(call_b, 4)},
         "fwd_tokens_per_s": round(T / (f_ms / 1e3), 1),
         "fwd_recurrence_tflops": round(fl / (f_ms / 1e3) / 1e12, 3),
         "kernels": "fwd: gdn_setup, gdn_prep (chunk-parallel factors), gdn_chain (state chain over 32-column "

@@ -471,7 +471,8 @@ uint64_t tree_launch_count(void);
 
 /* Kernel timing for benchmarks. With tree_kernel_timing(1), each attention call
  * brackets its main kernel with CUDA events on its stream (which = 0: the
- * forward's, 1: the backward's); tree_kernel_last_ms(which) waits for the latest
+ * forward's, 1: the backward's), and each conv1d call its kernels (2: forward,
+ * 3: backward with its dw / dbias reduction); tree_kernel_last_ms(which) waits for the latest
  * bracket on the current device and returns its duration in ms, or -1 if there
  * is none. Off by default; leave it off while a stream is being captured. */
 int tree_kernel_timing(int enable);

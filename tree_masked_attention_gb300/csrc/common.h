@@ -21,8 +21,9 @@ int* device_error_word();
 void count_launch();
 
 // CUDA-event brackets around a call's main kernel, when tree_kernel_timing(1) is on:
-// 0 = attention forward, 1 = attention backward (tree_kernel_last_ms reads them).
-constexpr int kTimedKernels = 2;
+// 0 = attention forward, 1 = attention backward, 2 = conv1d forward, 3 = conv1d backward
+// (its kernel and the dw / dbias reduction); tree_kernel_last_ms reads them.
+constexpr int kTimedKernels = 4;
 void timing_begin(int which, void* stream);
 void timing_end(int which, void* stream);
 

@@ -493,10 +493,12 @@ int launch_fwd(const void* x, const void* w, const void* bias, void* y, const in
   if (int rc_ = smem_opt_in(reinterpret_cast<const void*>(conv1d_fwd_kernel<T, K>), static_cast<int>(fwd_smem<T>()))) return rc_;
   const ConvGrid g = conv_grid(T_, C, kFwdTargetCtas);
   dim3 grid(static_cast<unsigned>(g.groups), static_cast<unsigned>(g.ctiles));
+  timing_begin(2, st);
   conv1d_fwd_kernel<T, K><<<grid, kConvThreads, fwd_smem<T>(), st>>>(
       static_cast<const T*>(x), static_cast<const T*>(w), static_cast<const T*>(bias), static_cast<T*>(y), parent,
       T_, C, g.rows_per_group, device_error_word());
   TREE_LAUNCH_CHECK("conv1d_fwd_kernel");
+  timing_end(2, st);
   return TREE_OK;
 }
 
@@ -507,6 +509,7 @@ int launch_bwd(const void* x, const void* w, const void* dy, void* dx, float* dw
   const ConvGrid g = conv_grid(T_, C, kBwdTargetCtas);
   dim3 grid(static_cast<unsigned>(g.groups), static_cast<unsigned>(g.ctiles));
   int* err = device_error_word();
+  timing_begin(3, st);
   conv1d_bwd_kernel<T, K><<<grid, kConvThreads, bwd_smem<T>(), st>>>(
       static_cast<const T*>(x), static_cast<const T*>(w), static_cast<const T*>(dy), static_cast<T*>(dx), end, pos,
       T_, C, g.rows_per_group, part, err);
@@ -516,6 +519,7 @@ int launch_bwd(const void* x, const void* w, const void* dy, void* dx, float* dw
     conv1d_reduce_kernel<<<rgrid, dim3(kRedC, kRedG), 0, st>>>(part, g.groups, C, K, dw, dbias);
     TREE_LAUNCH_CHECK("conv1d_reduce_kernel");
   }
+  timing_end(3, st);
   return TREE_OK;
 }
 
