@@ -821,9 +821,16 @@ def run_gdn(args, dev, flush):
                     "bf16 q/k/v/dO, fp32 gates",
         "value": round(T / ((f_ms + b_ms) / 1e3), 1), "unit": "packed tokens/s (forward + backward)",
         "ms_fwd": round(f_ms, 4), "ms_bwd": round(b_ms, 4), "steps": n,
-        "call_ms": {"fwd": round(call_f, 4), "bwd": round(call_b, 4)},
         "fwd_tokens_per_s": round(T / (f_ms / 1e3), 1),
         "fwd_recurrence_tflops": round(fl / (f_ms / 1e3) / 1e12, 3),
+        # fp32 on the CUDA cores: the ALU roofline is 152 SMs x 128 fp32 lanes x 2 FLOP per FMA
+        # at the 2070 MHz maximum SM clock = 80.5 TFLOP/s; the algorithmic work counted is the
+        # recurrence's, 6 Dk Dv per row and head forward and twice that backward (the chunked
+        # form's extra products -- the triangular factors -- are not counted)
+        "roofline": {"bound": "alu", "achieved": round(2 * fl / (b_ms / 1e3) / 1e12, 3), "peak": 80.5,
+                     "unit": "TFLOP/s", "frac": round(2 * fl / (b_ms / 1e3) / 1e12 / 80.5, 4),
+                     "of": "152 SMs x 128 fp32 FMA lanes x 2 x 2.07 GHz", "kernel": "tree_gdn_bwd",
+                     "traffic": None},
         "kernels": "fwd: gdn_setup, gdn_prep (chunk-parallel factors), gdn_chain (state chain over 32-column "
                    "slices), gdn_out; bwd: setup, prep, chain, gdn_bchain (state-gradient chain), gdn_grads "
                    "(fp32 CUDA cores)",
