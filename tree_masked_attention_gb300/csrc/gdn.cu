@@ -84,9 +84,10 @@ __device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_all;" ::
 
 // A row-major [rows][cols] fp32 block (cols a multiple of 4) into shared memory rows of
 // stride sstride floats (a multiple of 4), 16 bytes per copy.
+template <int NT = kThreads>
 __device__ __forceinline__ void cp_block(float* s, int sstride, const float* g, int rows, int cols) {
   const int per = cols / 4, n = rows * per;
-  for (int p = threadIdx.x; p < n; p += kThreads) cp16(s + (p / per) * sstride + (p % per) * 4, g + 4 * static_cast<int64_t>(p));
+  for (int p = threadIdx.x; p < n; p += NT) cp16(s + (p / per) * sstride + (p % per) * 4, g + 4 * static_cast<int64_t>(p));
 }
 
 struct GdnWs {
@@ -298,17 +299,17 @@ __device__ __forceinline__ void widen(const uint4& v, float* f, const float*) {
 // ncols, a multiple of 4). Every thread issues all of its 16-byte loads before using any,
 // so their latencies overlap; rows whose width is not a whole number of vectors take a
 // scalar path. The input pointer is 16-byte aligned (checked on the host).
-template <typename Tin>
+template <typename Tin, int NT = kThreads>
 __device__ __forceinline__ void load_tile(float* dst, int stride, const Tin* __restrict__ src, int r0, int L, int H,
                                           int h, int D, int col0, int ncols) {
   constexpr int kVec = 16 / sizeof(Tin);                       // 8 bf16 or 4 fp32
-  constexpr int kPer = kChunk * kMaxD / kVec / kThreads;        // most vectors a thread loads
+  constexpr int kPer = (kChunk * kMaxD / kVec + NT - 1) / NT;   // most vectors a thread loads
   const int nv = ncols / kVec, total = kChunk * nv;
   if (D % kVec == 0 && ncols % kVec == 0) {
     uint4 buf[kPer];
 #pragma unroll
     for (int u = 0; u < kPer; ++u) {
-      const int idx = threadIdx.x + u * kThreads;
+      const int idx = threadIdx.x + u * NT;
       const int t = idx / max(nv, 1), cv = col0 + (idx % max(nv, 1)) * kVec;
       buf[u] = make_uint4(0u, 0u, 0u, 0u);
       if (idx < total && t < L && cv < D)
@@ -316,7 +317,7 @@ __device__ __forceinline__ void load_tile(float* dst, int stride, const Tin* __r
     }
 #pragma unroll
     for (int u = 0; u < kPer; ++u) {
-      const int idx = threadIdx.x + u * kThreads;
+      const int idx = threadIdx.x + u * NT;
       if (idx < total) {
         const int t = idx / nv, cl = (idx % nv) * kVec;
         float f[kVec];
@@ -328,7 +329,7 @@ __device__ __forceinline__ void load_tile(float* dst, int stride, const Tin* __r
     }
   } else {
 #pragma unroll 8
-    for (int idx = threadIdx.x; idx < kChunk * ncols; idx += kThreads) {
+    for (int idx = threadIdx.x; idx < kChunk * ncols; idx += NT) {
       const int t = idx / ncols, cl = idx % ncols, cv = col0 + cl;
       dst[t * stride + cl] = (t < L && cv < D) ? ldf(src, (static_cast<int64_t>(r0 + t) * H + h) * D + cv) : 0.f;
     }
@@ -715,11 +716,14 @@ __global__ void __launch_bounds__(kThreads) gdn_out_kernel(const GdnArgs a) {
 // ------------------------------------------------------------------------------ bchain
 // Per (sub-chunk, head, slice), by decreasing chain depth: dh_end (the sum of the
 // successors' start-state gradients), du, dr, dv, dh0; per-row partial sums for dg, dbeta.
+constexpr int kBThreads = 512;                  // 16 warps: latency of one chain item is the critical path
+constexpr int kBRows = kChunk / (kBThreads / 32);  // rows of du / dr per warp (4); dh0 rows per warp 2 kBRows
+static_assert(kBRows == 4 && 2 * kBRows * (kBThreads / 32) == kMaxD, "bchain row mapping");
 constexpr size_t kBchainSmem =
     (2 * kChunk * kRow + 2 * kChunk * kSq + 2 * kMaxD * kSl + 4 * kChunk * kSl + 4 * kChunk) * sizeof(float);
 
 template <typename Tin>
-__global__ void __launch_bounds__(kThreads) gdn_bchain_kernel(const GdnArgs a) {
+__global__ void __launch_bounds__(kBThreads, 1) gdn_bchain_kernel(const GdnArgs a) {
   extern __shared__ __align__(16) float sm[];
   float* Ks = sm;                        // [64][kRow]
   float* Qs = Ks + kChunk * kRow;        // [64][kRow]
@@ -736,7 +740,7 @@ __global__ void __launch_bounds__(kThreads) gdn_bchain_kernel(const GdnArgs a) {
   float* wv = E + kChunk;
   float* bs = wv + kChunk;
   __shared__ int s_item, s_ok;
-  __shared__ float s_red[kThreads / 32];
+  __shared__ float s_red[kBThreads / 32];
   const GdnWs& w = a.w;
   const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
   const int H = a.H, Dk = a.Dk, Dv = a.Dv, ns = a.ns, T = a.T;
@@ -755,16 +759,16 @@ __global__ void __launch_bounds__(kThreads) gdn_bchain_kernel(const GdnArgs a) {
     const int sb = w.succ_ptr[c], se = w.succ_ptr[c + 1];
     // loads that do not depend on the successors first
     const int64_t mo = (static_cast<int64_t>(c) * H + h) * kChunk * kChunk;
-    cp_block(Ps, kSq, w.Pm + mo, kChunk, kChunk);
-    cp_block(Xs, kSq, w.Xm + mo, kChunk, kChunk);
-    cp_block(Us, kSl, slice_block(w.u, c, h, sl, H, ns, kChunk), kChunk, kSlice);
-    if (pred >= 0) cp_block(Hs, kSl, slice_block(w.states, pred, h, sl, H, ns, Dk), Dk, kSlice);
-    load_tile(Ks, kRow, static_cast<const Tin*>(a.k), r0, L, H, h, Dk, 0, Dk4);
-    load_tile(Qs, kRow, static_cast<const Tin*>(a.q), r0, L, H, h, Dk, 0, Dk4);
-    load_tile(Os, kSl, tdo, r0, L, H, h, Dv, sl * kSlice, kSlice);
-    load_tile(Vs, kSl, static_cast<const Tin*>(a.v), r0, L, H, h, Dv, sl * kSlice, kSlice);
+    cp_block<kBThreads>(Ps, kSq, w.Pm + mo, kChunk, kChunk);
+    cp_block<kBThreads>(Xs, kSq, w.Xm + mo, kChunk, kChunk);
+    cp_block<kBThreads>(Us, kSl, slice_block(w.u, c, h, sl, H, ns, kChunk), kChunk, kSlice);
+    if (pred >= 0) cp_block<kBThreads>(Hs, kSl, slice_block(w.states, pred, h, sl, H, ns, Dk), Dk, kSlice);
+    load_tile<Tin, kBThreads>(Ks, kRow, static_cast<const Tin*>(a.k), r0, L, H, h, Dk, 0, Dk4);
+    load_tile<Tin, kBThreads>(Qs, kRow, static_cast<const Tin*>(a.q), r0, L, H, h, Dk, 0, Dk4);
+    load_tile<Tin, kBThreads>(Os, kSl, tdo, r0, L, H, h, Dv, sl * kSlice, kSlice);
+    load_tile<Tin, kBThreads>(Vs, kSl, static_cast<const Tin*>(a.v), r0, L, H, h, Dv, sl * kSlice, kSlice);
     if (pred < 0)
-      for (int idx = tid; idx < Dk * kSlice; idx += kThreads) Hs[(idx / kSlice) * kSl + idx % kSlice] = 0.f;
+      for (int idx = tid; idx < Dk * kSlice; idx += kBThreads) Hs[(idx / kSlice) * kSl + idx % kSlice] = 0.f;
     if (tid == 0) {
       bool ok = true;
       for (int s = sb; ok && s < se; ++s)
@@ -778,7 +782,7 @@ __global__ void __launch_bounds__(kThreads) gdn_bchain_kernel(const GdnArgs a) {
     }
     // dh_end slice = the sum of the successors' dh0 (fixed order), kept for the grads kernel
     {
-      constexpr int kPer = kMaxD * kSlice / 4 / kThreads;  // float4 per thread
+      constexpr int kPer = kMaxD * kSlice / 4 / kBThreads;  // float4 per thread
       float4 acc[kPer];
 #pragma unroll
       for (int u = 0; u < kPer; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -786,7 +790,7 @@ __global__ void __launch_bounds__(kThreads) gdn_bchain_kernel(const GdnArgs a) {
         const float4* src = reinterpret_cast<const float4*>(slice_block(w.dstart, w.succ[s], h, sl, H, ns, Dk));
 #pragma unroll
         for (int u = 0; u < kPer; ++u) {
-          const int p = tid + u * kThreads;
+          const int p = tid + u * kBThreads;
           if (p < Dk * kSlice / 4) {
             const float4 x = __ldcg(src + p);
             acc[u].x += x.x; acc[u].y += x.y; acc[u].z += x.z; acc[u].w += x.w;
@@ -796,19 +800,19 @@ __global__ void __launch_bounds__(kThreads) gdn_bchain_kernel(const GdnArgs a) {
       float4* dend = reinterpret_cast<float4*>(slice_block(w.dend, c, h, sl, H, ns, Dk));
 #pragma unroll
       for (int u = 0; u < kPer; ++u) {
-        const int p = tid + u * kThreads;
+        const int p = tid + u * kBThreads;
         if (p < Dk * kSlice / 4) {
           __stcg(dend + p, acc[u]);
           *reinterpret_cast<float4*>(Ds + (p / (kSlice / 4)) * kSl + (p % (kSlice / 4)) * 4) = acc[u];
         }
       }
-      for (int idx = Dk * kSlice + tid; idx < kMaxD * kSlice; idx += kThreads)  // rows past Dk
+      for (int idx = Dk * kSlice + tid; idx < kMaxD * kSlice; idx += kBThreads)  // rows past Dk
         Ds[(idx / kSlice) * kSl + idx % kSlice] = 0.f;
     }
     cp_wait();
     __syncthreads();
     float he = 0.f;  // partial sum of dh_end . h0
-    for (int idx = tid; idx < Dk * kSlice; idx += kThreads) {
+    for (int idx = tid; idx < Dk * kSlice; idx += kBThreads) {
       const int i = idx / kSlice, jj = idx % kSlice;
       he = fmaf(Ds[i * kSl + jj], Hs[i * kSl + jj], he);
     }
@@ -818,38 +822,36 @@ __global__ void __launch_bounds__(kThreads) gdn_bchain_kernel(const GdnArgs a) {
     decay_factors(a.g, a.beta, r0, L, H, h, lg, E, wv, bs);  // ends with a barrier
     if (tid == 0) {
       float x = 0.f;
-      for (int u = 0; u < kThreads / 32; ++u) x += s_red[u];
+      for (int u = 0; u < kBThreads / 32; ++u) x += s_red[u];
       w.part_he[(static_cast<int64_t>(sl) * n_chunks + c) * H + h] = x;
     }
-    // du = w o (K dh_end) + P^T dO for rows t = warp + 8 m of column `lane` (K, P, dO
+    // du = w o (K dh_end) + P^T dO for rows t = 4 warp + m of column `lane` (K, P, dO
     // rows past L are zero, so every row is computed); partial dw_t = w_t sum_j (K dh_end)_tj u_tj
     {
-      float kd[8];
+      float kd[kBRows];
 #pragma unroll
-      for (int m = 0; m < 8; ++m) kd[m] = 0.f;
+      for (int m = 0; m < kBRows; ++m) kd[m] = 0.f;
       for (int i = 0; i < Dk4; i += 4) {
         const float d0 = Ds[i * kSl + lane], d1 = Ds[(i + 1) * kSl + lane], d2 = Ds[(i + 2) * kSl + lane],
                     d3 = Ds[(i + 3) * kSl + lane];
 #pragma unroll
-        for (int m = 0; m < 8; ++m) {
-          const float4 k4 = *reinterpret_cast<const float4*>(Ks + (8 * warp + m) * kRow + i);
+        for (int m = 0; m < kBRows; ++m) {
+          const float4 k4 = *reinterpret_cast<const float4*>(Ks + (kBRows * warp + m) * kRow + i);
           kd[m] = fmaf(k4.x, d0, fmaf(k4.y, d1, fmaf(k4.z, d2, fmaf(k4.w, d3, kd[m]))));
         }
       }
-      float du[8];
+      float du[kBRows];
 #pragma unroll
-      for (int m = 0; m < 8; ++m) du[m] = wv[8 * warp + m] * kd[m];
+      for (int m = 0; m < kBRows; ++m) du[m] = wv[kBRows * warp + m] * kd[m];
       for (int t2 = 0; t2 < L; ++t2) {  // P is lower-triangular: P[t2][t] = 0 for t > t2
         const float o = Os[t2 * kSl + lane];
-        const float4 p0 = *reinterpret_cast<const float4*>(Ps + t2 * kSq + 8 * warp);
-        const float4 p1 = *reinterpret_cast<const float4*>(Ps + t2 * kSq + 8 * warp + 4);
+        const float4 p0 = *reinterpret_cast<const float4*>(Ps + t2 * kSq + kBRows * warp);
         du[0] = fmaf(p0.x, o, du[0]); du[1] = fmaf(p0.y, o, du[1]); du[2] = fmaf(p0.z, o, du[2]);
-        du[3] = fmaf(p0.w, o, du[3]); du[4] = fmaf(p1.x, o, du[4]); du[5] = fmaf(p1.y, o, du[5]);
-        du[6] = fmaf(p1.z, o, du[6]); du[7] = fmaf(p1.w, o, du[7]);
+        du[3] = fmaf(p0.w, o, du[3]);
       }
 #pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        const int t = 8 * warp + m;
+      for (int m = 0; m < kBRows; ++m) {
+        const int t = kBRows * warp + m;
         Rs[t * kSl + lane] = du[m];
         if (t < L) {
           float dw = wv[t] * kd[m] * Us[t * kSl + lane];
@@ -861,22 +863,20 @@ __global__ void __launch_bounds__(kThreads) gdn_bchain_kernel(const GdnArgs a) {
     }
     __syncthreads();
     // dr = X^T du (X lower-triangular), dv = beta o dr
-    float drr[8];
+    float drr[kBRows];
 #pragma unroll
-    for (int m = 0; m < 8; ++m) drr[m] = 0.f;
+    for (int m = 0; m < kBRows; ++m) drr[m] = 0.f;
     for (int t2 = 0; t2 < L; ++t2) {
       const float rr = Rs[t2 * kSl + lane];
-      const float4 x0 = *reinterpret_cast<const float4*>(Xs + t2 * kSq + 8 * warp);
-      const float4 x1 = *reinterpret_cast<const float4*>(Xs + t2 * kSq + 8 * warp + 4);
+      const float4 x0 = *reinterpret_cast<const float4*>(Xs + t2 * kSq + kBRows * warp);
       drr[0] = fmaf(x0.x, rr, drr[0]); drr[1] = fmaf(x0.y, rr, drr[1]); drr[2] = fmaf(x0.z, rr, drr[2]);
-      drr[3] = fmaf(x0.w, rr, drr[3]); drr[4] = fmaf(x1.x, rr, drr[4]); drr[5] = fmaf(x1.y, rr, drr[5]);
-      drr[6] = fmaf(x1.z, rr, drr[6]); drr[7] = fmaf(x1.w, rr, drr[7]);
+      drr[3] = fmaf(x0.w, rr, drr[3]);
     }
     __syncthreads();
     float* drg = slice_block(w.dr, c, h, sl, H, ns, kChunk);
 #pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      const int t = 8 * warp + m;
+    for (int m = 0; m < kBRows; ++m) {
+      const int t = kBRows * warp + m;
       Rs[t * kSl + lane] = drr[m];
       drg[t * kSlice + lane] = drr[m];
       if (t < L) {
@@ -888,20 +888,20 @@ __global__ void __launch_bounds__(kThreads) gdn_bchain_kernel(const GdnArgs a) {
       }
     }
     __syncthreads();
-    // dh0 = E_{L-1} dh_end + Q^T (E o dO) - K^T (beta E o dr): rows i = 16 warp + m
+    // dh0 = E_{L-1} dh_end + Q^T (E o dO) - K^T (beta E o dr): rows i = 8 warp + m
     {
       float* dst = slice_block(w.dstart, c, h, sl, H, ns, Dk);
       const float gl = E[L - 1];
-      const int i0 = 16 * warp;
-      float acc[16];
+      const int i0 = 2 * kBRows * warp;
+      float acc[2 * kBRows];
 #pragma unroll
-      for (int m = 0; m < 16; ++m) acc[m] = gl * Ds[(i0 + m) * kSl + lane];
+      for (int m = 0; m < 2 * kBRows; ++m) acc[m] = gl * Ds[(i0 + m) * kSl + lane];
       for (int t = 0; t < L; ++t) {
         const float ao = E[t] * Os[t * kSl + lane], br = -bs[t] * E[t] * Rs[t * kSl + lane];
         const float4* qr = reinterpret_cast<const float4*>(Qs + t * kRow + i0);
         const float4* kr = reinterpret_cast<const float4*>(Ks + t * kRow + i0);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < 2 * kBRows / 4; ++q) {
           const float4 q4 = qr[q], k4 = kr[q];
           acc[4 * q] = fmaf(q4.x, ao, fmaf(k4.x, br, acc[4 * q]));
           acc[4 * q + 1] = fmaf(q4.y, ao, fmaf(k4.y, br, acc[4 * q + 1]));
@@ -910,7 +910,7 @@ __global__ void __launch_bounds__(kThreads) gdn_bchain_kernel(const GdnArgs a) {
         }
       }
 #pragma unroll
-      for (int m = 0; m < 16; ++m)
+      for (int m = 0; m < 2 * kBRows; ++m)
         if (i0 + m < Dk) __stcg(dst + (i0 + m) * kSlice + lane, acc[m]);
     }
     __syncthreads();
@@ -1290,7 +1290,7 @@ int gdn_backward(GdnArgs& a, int64_t mc, cudaStream_t st) {
   if ((rc = smem_opt_in(reinterpret_cast<const void*>(gdn_bchain_kernel<Tin>), static_cast<int>(kBchainSmem))) ||
       (rc = smem_opt_in(reinterpret_cast<const void*>(gdn_grads_kernel<Tin>), static_cast<int>(kGradsSmem))))
     return rc;
-  gdn_bchain_kernel<Tin><<<std::min(n_sm, kMaxCtas), kThreads, kBchainSmem, st>>>(a);
+  gdn_bchain_kernel<Tin><<<std::min(n_sm, kMaxCtas), kBThreads, kBchainSmem, st>>>(a);
   TREE_LAUNCH_CHECK("gdn_bchain_kernel");
   gdn_grads_kernel<Tin><<<dim3(static_cast<unsigned>(mc), static_cast<unsigned>(a.H)), kThreads, kGradsSmem, st>>>(a);
   TREE_LAUNCH_CHECK("gdn_grads_kernel");
