@@ -56,6 +56,9 @@ def parse_args(argv=None):
     ap.add_argument("--secondary-steps", type=int, default=20,
                     help="timed steps of each tree that is not the headline workload")
     ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--attn-heads", default="",
+                    help="HQ,HKV: the attention trees with fewer heads (a smaller case for ncu captures; "
+                         "not a bench configuration)")
     ap.add_argument("--lm-steps", type=int, default=3)
     ap.add_argument("--lm-rows", type=int, default=8192,
                     help="packed rows of the LM-head tree (mean path count 2.2); smaller for profiling")
@@ -231,10 +234,12 @@ class AttnStep:
     """One packed tree's attention step on the device: RoPE, forward, backward with the
     inverse rotation fused. Holds the tree, its host (pinned) and device tensors."""
 
-    def __init__(self, tma, name: str, seed: int, dev):
+    def __init__(self, tma, name: str, seed: int, dev, heads=None):
         import torch
         self.tma, self.name, self.dev = tma, name, dev
         self.tree, c = attention_workload(name, seed)
+        if heads is not None:  # fewer heads of the same tree: a smaller case for profiling
+            c = dict(c, Hq=heads[0], Hkv=heads[1])
         self.c = c
         pk = tma.tree_pack(self.tree.seqs)
         self.T, self.Hq, self.Hkv, self.d = pk["T"], c["Hq"], c["Hkv"], c["d"]
@@ -243,6 +248,10 @@ class AttnStep:
         self.f_fwd, self.f_bwd = attn_flops(self.P, self.Hq, self.d)
         self.td = torch.bfloat16 if c["dtype"] == "bf16" else torch.float32
         self.host = synth.attention_config(name, self.T, seed=seed)
+        if heads is not None:
+            q_, k_, v_, do_ = self.host
+            self.host = tuple(np.ascontiguousarray(x) for x in
+                              (q_[:, :self.Hq], k_[:, :self.Hkv], v_[:, :self.Hkv], do_[:, :self.Hq]))
         pin = lambda a: torch.from_numpy(a).to(self.td).pin_memory()
         self.hq, self.hk, self.hv, self.hdo = (pin(a) for a in self.host)
         self.q, self.k, self.v, self.do = (x.to(dev) for x in (self.hq, self.hk, self.hv, self.hdo))
@@ -474,7 +483,8 @@ def run_ours(args):
     peak = float(peaks["bf16_tflops"])
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
-    leg = AttnStep(tma, args.workload, rank_seed(rank), dev)
+    heads = tuple(int(x) for x in args.attn_heads.split(",")) if args.attn_heads else None
+    leg = AttnStep(tma, args.workload, rank_seed(rank), dev, heads)
     K = args.steps
     clocks = ClockSampler(local).start()
     m = leg.measure(K, args.warmup, flush, use_graph=not args.no_graph, world=world, clocks=clocks)
@@ -506,7 +516,7 @@ def run_ours(args):
         for name in ("galton_watson", "agentic_long", "agentic_short"):
             if name == args.workload:
                 continue
-            other = AttnStep(tma, name, 0, dev)
+            other = AttnStep(tma, name, 0, dev, heads)
             m2 = other.measure(max(args.secondary_steps, 1), 3, flush, use_graph=not args.no_graph)
             sec[name] = secondary_entry(other, m2, peak, peak_src)
             del other
