@@ -582,53 +582,62 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_chain_kernel(const GdnArgs a)
     }
     cp_wait();
     decay_factors(a.g, a.beta, r0, L, H, h, lg, E, wv, bs);  // ends with a barrier
-    // u = U0 - W h0: rows t = warp + 8 m of column `lane`; W rows past L are zero
+    // u = U0 - W h0: each thread rows t and t + 32 (t = lane / 8 + 4 warp) by four
+    // consecutive columns j0 = 4 (lane % 8): two float4 of W and four of h0 per four steps
+    // of i feed 32 FMAs. W rows past L are zero.
     float* ug = slice_block(w.u, c, h, sl, H, ns, kChunk);
+    const int cg = (lane & 7) * 4;
     {
-      float acc[8];
-#pragma unroll
-      for (int m = 0; m < 8; ++m) acc[m] = Us[(warp + 8 * m) * kSl + lane];
+      const int t = (lane >> 3) + 4 * warp;
+      float4 acc0 = *reinterpret_cast<const float4*>(Us + t * kSl + cg);
+      float4 acc1 = *reinterpret_cast<const float4*>(Us + (t + 32) * kSl + cg);
       for (int i = 0; i < Dk4; i += 4) {
-        const float h0v = Hs[i * kSl + lane], h1v = Hs[(i + 1) * kSl + lane], h2v = Hs[(i + 2) * kSl + lane],
-                    h3v = Hs[(i + 3) * kSl + lane];
+        const float4 w0 = *reinterpret_cast<const float4*>(Ws + t * kRow + i);
+        const float4 w1 = *reinterpret_cast<const float4*>(Ws + (t + 32) * kRow + i);
+        const float wa[4] = {w0.x, w0.y, w0.z, w0.w}, wb[4] = {w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-        for (int m = 0; m < 8; ++m) {
-          const float4 w4 = *reinterpret_cast<const float4*>(Ws + (warp + 8 * m) * kRow + i);
-          acc[m] = fmaf(-w4.x, h0v, fmaf(-w4.y, h1v, fmaf(-w4.z, h2v, fmaf(-w4.w, h3v, acc[m]))));
+        for (int e = 0; e < 4; ++e) {
+          const float4 h4 = *reinterpret_cast<const float4*>(Hs + (i + e) * kSl + cg);
+          acc0.x = fmaf(-wa[e], h4.x, acc0.x); acc0.y = fmaf(-wa[e], h4.y, acc0.y);
+          acc0.z = fmaf(-wa[e], h4.z, acc0.z); acc0.w = fmaf(-wa[e], h4.w, acc0.w);
+          acc1.x = fmaf(-wb[e], h4.x, acc1.x); acc1.y = fmaf(-wb[e], h4.y, acc1.y);
+          acc1.z = fmaf(-wb[e], h4.z, acc1.z); acc1.w = fmaf(-wb[e], h4.w, acc1.w);
         }
       }
       __syncthreads();  // every thread has read U0
-#pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        const int t = warp + 8 * m;
-        Us[t * kSl + lane] = acc[m];
-        ug[t * kSlice + lane] = acc[m];
-      }
+      *reinterpret_cast<float4*>(Us + t * kSl + cg) = acc0;
+      *reinterpret_cast<float4*>(Us + (t + 32) * kSl + cg) = acc1;
+      *reinterpret_cast<float4*>(ug + t * kSlice + cg) = acc0;
+      *reinterpret_cast<float4*>(ug + (t + 32) * kSlice + cg) = acc1;
     }
     __syncthreads();
-    // h_end = E_{L-1} h0 + sum_t w_t k_t u_t^T: rows i = 16 warp + m of column `lane`
+    // h_end = E_{L-1} h0 + sum_t w_t k_t u_t^T: each thread rows 4 rq .. 4 rq + 3
+    // (rq = lane / 8 + 4 warp) by columns j0 .. j0 + 3: one float4 of K and one of u per t
+    // feed 16 FMAs
     {
       float* hend = slice_block(w.states, c, h, sl, H, ns, Dk);
       const float gl = E[L - 1];
-      const int i0 = 16 * warp;
-      float acc[16];
+      const int i0 = 4 * ((lane >> 3) + 4 * warp);
+      float4 acc[4];
 #pragma unroll
-      for (int m = 0; m < 16; ++m) acc[m] = gl * Hs[(i0 + m) * kSl + lane];
+      for (int m = 0; m < 4; ++m) {
+        const float4 h4 = *reinterpret_cast<const float4*>(Hs + (i0 + m) * kSl + cg);
+        acc[m] = make_float4(gl * h4.x, gl * h4.y, gl * h4.z, gl * h4.w);
+      }
       for (int t = 0; t < L; ++t) {
-        const float uw = Us[t * kSl + lane] * wv[t];
-        const float4* kr = reinterpret_cast<const float4*>(Ks + t * kRow + i0);
+        const float wt = wv[t];
+        const float4 u4 = *reinterpret_cast<const float4*>(Us + t * kSl + cg);
+        const float4 k4 = *reinterpret_cast<const float4*>(Ks + t * kRow + i0);
+        const float ka[4] = {k4.x * wt, k4.y * wt, k4.z * wt, k4.w * wt};
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float4 k4 = kr[q];
-          acc[4 * q] = fmaf(k4.x, uw, acc[4 * q]);
-          acc[4 * q + 1] = fmaf(k4.y, uw, acc[4 * q + 1]);
-          acc[4 * q + 2] = fmaf(k4.z, uw, acc[4 * q + 2]);
-          acc[4 * q + 3] = fmaf(k4.w, uw, acc[4 * q + 3]);
+        for (int m = 0; m < 4; ++m) {
+          acc[m].x = fmaf(ka[m], u4.x, acc[m].x); acc[m].y = fmaf(ka[m], u4.y, acc[m].y);
+          acc[m].z = fmaf(ka[m], u4.z, acc[m].z); acc[m].w = fmaf(ka[m], u4.w, acc[m].w);
         }
       }
 #pragma unroll
-      for (int m = 0; m < 16; ++m)
-        if (i0 + m < Dk) __stcg(hend + (i0 + m) * kSlice + lane, acc[m]);
+      for (int m = 0; m < 4; ++m)
+        if (i0 + m < Dk) __stcg(reinterpret_cast<float4*>(hend + (i0 + m) * kSlice + cg), acc[m]);
     }
     __syncthreads();
     if (tid == 0 && c != a.withhold) {
