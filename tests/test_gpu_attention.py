@@ -82,8 +82,9 @@ def test_short_prompt_agentic_full_size():
     _full_check(t.seqs, 32, 8, 128, "bf16")
 
 
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("f32", 64)])
 @pytest.mark.parametrize("case", ["chain", "forest_of_singletons", "single_token", "two_roots"])
-def test_degenerate_trees(case):
+def test_degenerate_trees(case, dtype, d):
     rng = np.random.default_rng(5)
     if case == "chain":
         seqs = [rng.integers(0, 100, size=1000)]
@@ -93,7 +94,7 @@ def test_degenerate_trees(case):
         seqs = [[42]]
     else:
         seqs = [rng.integers(0, 100, size=200), [1000] + list(rng.integers(0, 100, size=150))]
-    _full_check(seqs, 2, 1, 128, "bf16")
+    _full_check(seqs, 2, 1, d, dtype)
 
 
 @pytest.mark.parametrize("dtype,d", [("bf16", 128), ("f32", 64), ("bf16", 64)])

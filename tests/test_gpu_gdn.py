@@ -140,6 +140,18 @@ def test_gdn_bwd_long_chain_and_wide_fork():
     _check_bwd(m, seqs, 2, 64, 64, 6, False)
 
 
+@pytest.mark.parametrize("case", ["single_token", "forest_of_singletons", "exactly_64_rows", "65_rows"])
+def test_gdn_degenerate_trees(case):
+    """One row; 200 one-row roots (every node starts from zero); a node of exactly one
+    64-row sub-chunk; one row past it (a one-row second sub-chunk). Forward and backward."""
+    need_cuda()
+    m = tma()
+    seqs = {"single_token": [[7]], "forest_of_singletons": [[i] for i in range(200)],
+            "exactly_64_rows": [list(range(64))], "65_rows": [list(range(65))]}[case]
+    _check(m, seqs, 2, 64, 64, 8, False)
+    _check_bwd(m, seqs, 2, 64, 64, 8, False)
+
+
 def test_gdn_bwd_repeats_bitwise():
     """Fixed summation orders: two backward calls give identical bits."""
     need_cuda()

@@ -53,6 +53,32 @@ def _run_lm(m, h, w, tg, wt, row_ptr, perm, bf16):
     return lse, logp, dh, dw, g
 
 
+@pytest.mark.parametrize("bf16", [True, False])
+def test_logprob_without_occurrences(bf16):
+    """Single-token sequences predict nothing: n_occ = 0. The forward still writes every
+    row's LSE; the backward gives zero dH and dW."""
+    need_cuda()
+    m = tma()
+    seqs = [[i] for i in range(150)]
+    pk = m.tree_pack(seqs)
+    assert pk["n_occ"] == 0
+    T, K, V = pk["T"], 64, 520
+    h, w, _, _ = synth.lm_head_config(T, K, V, 0, bf16=bf16)
+    td = torch.bfloat16 if bf16 else torch.float32
+    th, tw = dev(h, td), dev(w, td)
+    empty = torch.zeros(0, dtype=torch.int32, device="cuda")
+    lse, logp = m.tree_logprob_fwd(th, tw, dev(pk["occ_row_ptr"]), empty, empty)
+    dh, dw = m.tree_logprob_bwd(th, tw, lse, dev(pk["occ_row_ptr"]), empty, empty,
+                                torch.zeros(0, dtype=torch.float32, device="cuda"))
+    m.tree_check_device_status()
+    assert logp.numel() == 0
+    z = h.astype(np.float64) @ w.astype(np.float64)
+    zmax = z.max(axis=1, keepdims=True)
+    want = (zmax + np.log(np.exp(z - zmax).sum(axis=1, keepdims=True)))[:, 0]
+    assert_close("lse", lse, want, F32_TOL)
+    assert float(dh.abs().max()) == 0.0 and float(dw.abs().max()) == 0.0
+
+
 def test_logprob_tiny_fp32():
     need_cuda()
     m = tma()
@@ -71,9 +97,10 @@ def test_logprob_tiny_fp32():
 
 
 @pytest.mark.parametrize("T,K,V,bf16", [(200, 128, 1000, True), (333, 256, 4104, True), (130, 64, 520, False),
-                                        (333, 128, 1000, False)])
+                                        (333, 128, 1000, False), (1500, 128, 4096, False)])
 def test_logprob_random(T, K, V, bf16):
-    """Ragged row/vocabulary tails, rows without occurrences, repeated targets."""
+    """Ragged row/vocabulary tails, rows without occurrences, repeated targets; the last
+    fp32 case has long contractions (dH over 4096 vocabulary columns, dW over 1500 rows)."""
     need_cuda()
     m = tma()
     h, w, src, tg, wt, row_ptr, perm = _lm_case(T, K, V, T - 7, bf16, seed=T)

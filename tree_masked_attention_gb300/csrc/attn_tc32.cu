@@ -97,6 +97,27 @@ __device__ __forceinline__ void ld_row32(uint32_t taddr, float (&x)[32]) {
   for (int c = 0; c < 32; ++c) x[c] = __uint_as_float(r[c]);
 }
 
+// The tensor cores' fp32 accumulation does not round to nearest, and its error grows with
+// the number of MMAs that add into one accumulator (a thousand-row chain put dV 2e-5
+// relative off). So each step's products go to a fresh TMEM block (a dozen MMAs), and the
+// running sum is kept in a second block, added to with IEEE fp32 adds: `run` (+)= `step`
+// over D columns of this warp's lanes; `first` copies instead of adding.
+__device__ __forceinline__ void tmem_accumulate(uint32_t run, uint32_t step, bool first) {
+#pragma unroll
+  for (int c0 = 0; c0 < D; c0 += 32) {
+    uint32_t x[32], y[32];
+    tmem_ld32(step + c0, x);
+    if (!first) tmem_ld32(run + c0, y);
+    tmem_ld_wait();
+    if (!first) {
+#pragma unroll
+      for (int c = 0; c < 32; ++c) x[c] = __float_as_uint(__uint_as_float(x[c]) + __uint_as_float(y[c]));
+    }
+    tmem_st32(run + c0, x);
+  }
+  tmem_st_wait();
+}
+
 // Waits for the next MMA commit on `bar`; every thread of the CTA takes part and gets the
 // same answer.
 __device__ __forceinline__ bool wait_mma(uint64_t* bar, uint32_t& phase, int* err) {
@@ -285,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_dkdv_tc32_kernel(Params p) {
     mbar_init(bar, 1);
     fence_mbarrier_init();
   }
-  if (warp == 0) tmem_alloc(tmem_slot, 256);
+  if (warp == 0) tmem_alloc(tmem_slot, 512);
   __syncthreads();
   atomicMax(&qmax_s, ej);
   stage_rows<BM>(static_cast<const T*>(p.k), k0, p.T, p.Hkv, kvh, Kh, Kl, nullptr, nullptr);
@@ -293,7 +314,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_dkdv_tc32_kernel(Params p) {
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot, tST = tmem, tdPT = tmem + 32, tdV = tmem + 64, tdK = tmem + 64 + D;
+  // S^T, dP^T, this step's dV and dK, their running sums
+  const uint32_t tmem = *tmem_slot, tST = tmem, tdPT = tmem + 32, tdV = tmem + 64, tdK = tmem + 64 + D,
+                 tV = tmem + 64 + 2 * D, tK = tmem + 64 + 3 * D;
   const uint32_t lanes = static_cast<uint32_t>(warp * 32) << 16;
   const int64_t q_last = min(static_cast<int64_t>(qmax_s), p.T - 1);
 
@@ -336,8 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_dkdv_tc32_kernel(Params p) {
       __syncthreads();
       if (t == 0) {
         tc_fence_after();
-        mma3<BM, D, BQ>(tdV, smem_u32(Xh), smem_u32(Xl), smem_u32(OTh), smem_u32(OTl), first ? 0 : 1, false,
-                        kExact<T>);
+        mma3<BM, D, BQ>(tdV, smem_u32(Xh), smem_u32(Xl), smem_u32(OTh), smem_u32(OTl), 0, false, kExact<T>);
         mma_commit(bar);
       }
       if (!(ok = wait_mma(bar, phase, p.err))) break;
@@ -349,11 +371,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_dkdv_tc32_kernel(Params p) {
       __syncthreads();
       if (t == 0) {
         tc_fence_after();
-        mma3<BM, D, BQ>(tdK, smem_u32(Xh), smem_u32(Xl), smem_u32(QTh), smem_u32(QTl), first ? 0 : 1, false,
-                        kExact<T>);
+        mma3<BM, D, BQ>(tdK, smem_u32(Xh), smem_u32(Xl), smem_u32(QTh), smem_u32(QTl), 0, false, kExact<T>);
         mma_commit(bar);
       }
       if (!(ok = wait_mma(bar, phase, p.err))) break;
+      tmem_accumulate(tV + lanes, tdV + lanes, first);
+      tmem_accumulate(tK + lanes, tdK + lanes, first);
+      tc_fence_before();  // the next step's MMAs overwrite the step blocks
       first = false;
     }
   }
@@ -367,8 +391,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_dkdv_tc32_kernel(Params p) {
 #pragma unroll
         for (int c = 0; c < 32; ++c) a[c] = b[c] = 0.f;
       } else {
-        ld_row32(tdK + lanes + c0, a);
-        ld_row32(tdV + lanes + c0, b);
+        ld_row32(tK + lanes + c0, a);
+        ld_row32(tV + lanes + c0, b);
       }
       if (!jvalid) continue;
 #pragma unroll
@@ -382,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_dkdv_tc32_kernel(Params p) {
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, 512);
   }
 }
 
@@ -411,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_dq_tc32_kernel(Params p) {
     mbar_init(bar, 1);
     fence_mbarrier_init();
   }
-  if (warp == 0) tmem_alloc(tmem_slot, 128);
+  if (warp == 0) tmem_alloc(tmem_slot, 256);
   stage_rows<BM>(static_cast<const T*>(p.q), q0, p.T, p.Hq, h, Qh, Ql, nullptr, nullptr);
   stage_rows<BM>(static_cast<const T*>(p.dout), q0, p.T, p.Hq, h, Oh, Ol, nullptr, nullptr);
   const float lse2 = valid ? p.lse[static_cast<int64_t>(h) * p.T + i] * kLog2e : 0.f;
@@ -419,7 +443,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_dq_tc32_kernel(Params p) {
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot, tS = tmem, tdP = tmem + 32, tdQ = tmem + 64;
+  // S, dP, this key tile's dQ, the running sum
+  const uint32_t tmem = *tmem_slot, tS = tmem, tdP = tmem + 32, tdQ = tmem + 64, tQ = tmem + 64 + D;
   const uint32_t lanes = static_cast<uint32_t>(warp * 32) << 16;
 
   uint32_t phase = 0;
@@ -457,11 +482,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_dq_tc32_kernel(Params p) {
     __syncthreads();
     if (t == 0) {
       tc_fence_after();
-      mma3<BM, D, BNQ>(tdQ, smem_u32(Xh), smem_u32(Xl), smem_u32(KTh), smem_u32(KTl), first ? 0 : 1, false,
-                       kExact<T>);
+      mma3<BM, D, BNQ>(tdQ, smem_u32(Xh), smem_u32(Xl), smem_u32(KTh), smem_u32(KTl), 0, false, kExact<T>);
       mma_commit(bar);
     }
     if (!(ok = wait_mma(bar, phase, p.err))) break;
+    tmem_accumulate(tQ + lanes, tdQ + lanes, first);
+    tc_fence_before();
     first = false;
   }
   if (ok) {  // warp-collective TMEM loads by every lane, stores by valid rows
@@ -473,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_dq_tc32_kernel(Params p) {
 #pragma unroll
         for (int c = 0; c < 32; ++c) a[c] = 0.f;
       } else {
-        ld_row32(tdQ + lanes + c0, a);
+        ld_row32(tQ + lanes + c0, a);
       }
       if (!valid) continue;
 #pragma unroll
@@ -485,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_dq_tc32_kernel(Params p) {
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, 128);
+    tmem_dealloc(tmem, 256);
   }
 }
 

@@ -85,6 +85,28 @@ __device__ __forceinline__ void stage_op(const TX* X, int64_t s_r, int64_t s_k, 
   }
 }
 
+// The tensor cores' fp32 accumulation does not round to nearest and its error grows with
+// the number of MMAs adding into one accumulator; over a long K (dW sums over every row)
+// that would leave fp32 results short of fp32 accuracy. So the MMAs of kGroup K steps go
+// to a fresh TMEM block, which is then added into a running sum with IEEE fp32 adds.
+constexpr int kGroup = 4;
+
+__device__ __forceinline__ void tmem_accumulate128(uint32_t run, uint32_t step, bool first) {
+#pragma unroll 1
+  for (int c0 = 0; c0 < TN; c0 += 32) {
+    uint32_t x[32], y[32];
+    tmem_ld32(step + c0, x);
+    if (!first) tmem_ld32(run + c0, y);
+    tmem_ld_wait();
+    if (!first) {
+#pragma unroll
+      for (int c = 0; c < 32; ++c) x[c] = __float_as_uint(__uint_as_float(x[c]) + __uint_as_float(y[c]));
+    }
+    tmem_st32(run + c0, x);
+  }
+  tmem_st_wait();
+}
+
 // C[m, n] = sum_k A(m, k) B(k, n); A(m, k) = A[m*sam + k*sak], B(k, n) = B[k*sbk + n*sbn].
 template <typename TA, typename TB, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -101,11 +123,12 @@ lm_gemm_tc32_kernel(const TA* __restrict__ A, int64_t sam, int64_t sak, const TB
     mbar_init(&bar[1], 1);
     fence_mbarrier_init();
   }
-  if (warp == 0) tmem_alloc(tmem_slot, TN);
+  if (warp == 0) tmem_alloc(tmem_slot, 2 * TN);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
+  const uint32_t tstep = *tmem_slot, tmem = tstep + TN;  // a group's products; the running sum
+  const uint32_t lanes = static_cast<uint32_t>(warp * 32) << 16;
   constexpr bool a_exact = !std::is_same<TA, float>::value, b_exact = !std::is_same<TB, float>::value;
 
   const int64_t n_k = (K + TK - 1) / TK;
@@ -124,11 +147,18 @@ lm_gemm_tc32_kernel(const TA* __restrict__ A, int64_t sam, int64_t sak, const TB
     __syncthreads();
     if (t == 0) {
       tc_fence_after();
-      mma3<TM, TN, TK>(tmem, smem_u32(st), smem_u32(st + kOpB), smem_u32(st + 2 * kOpB), smem_u32(st + 3 * kOpB),
-                       kb > 0 ? 1u : 0u, a_exact, b_exact);
+      mma3<TM, TN, TK>(tstep, smem_u32(st), smem_u32(st + kOpB), smem_u32(st + 2 * kOpB),
+                       smem_u32(st + 3 * kOpB), kb % kGroup ? 1u : 0u, a_exact, b_exact);
       mma_commit(&bar[s]);
     }
     ++used[s];
+    if (kb % kGroup == kGroup - 1 || kb == n_k - 1) {  // the group's MMAs done: add it to the sum
+      ok = mbar_wait(&bar[s], (used[s] - 1) & 1, ep.err);
+      if (!(ok = __syncthreads_and(ok) != 0)) break;
+      tc_fence_after();
+      tmem_accumulate128(tmem + lanes, tstep + lanes, kb < kGroup);
+      tc_fence_before();  // the next group's MMAs overwrite the step block
+    }
   }
   // the last commit covers every MMA issued before it
   if (ok && n_k > 0) {
@@ -141,7 +171,6 @@ lm_gemm_tc32_kernel(const TA* __restrict__ A, int64_t sam, int64_t sak, const TB
   if (ok) {
     const int64_t m = m0 + t;
     const bool row_ok = m < M;
-    const uint32_t lanes = static_cast<uint32_t>(warp * 32) << 16;
     int64_t o_begin = 0, o_end = 0;
     if constexpr (EPI != EPI_STORE) {
       if (row_ok) {
@@ -239,7 +268,7 @@ lm_gemm_tc32_kernel(const TA* __restrict__ A, int64_t sam, int64_t sak, const TB
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, TN);
+    tmem_dealloc(tstep, 2 * TN);
   }
 }
 
