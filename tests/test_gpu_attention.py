@@ -56,6 +56,14 @@ def test_random_trees(d, dtype, seed):
     _full_check(t.seqs, 4, 2, d, dtype, seed=seed)
 
 
+def test_fp32_head64_deeper_tree():
+    """fp32 at head size 64 (the tf32-split kernels) on a Galton-Watson tree of about 3000
+    rows: paths up to ~1500 rows, so dQ sums over dozens of key tiles and dK/dV over many
+    query tiles, every partial added in fp32 outside the tensor cores."""
+    t = synth.galton_watson(seed=21, budget=3000, seg=(40, 300), vocab=1000)
+    _full_check(t.seqs, 4, 2, 64, "f32", seed=21)
+
+
 @pytest.mark.parametrize("Hq,Hkv", [(3, 1), (8, 8), (8, 2), (6, 3)])
 def test_group_sizes(Hq, Hkv):
     """Odd and even GQA groups, MHA: the tensor-core kernels and their fallbacks."""

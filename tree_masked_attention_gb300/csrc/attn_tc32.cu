@@ -13,8 +13,10 @@
 //   forward   one CTA per (128 query rows, query head); 64-key tiles; online softmax in
 //             registers (base 2), O accumulated in registers from a fresh P V per tile.
 //   dK / dV   one CTA per (128 keys, KV head); every query head of the group and every 32-row
-//             query tile the key tile serves, in a fixed order; dV and dK accumulate in TMEM.
-//   dQ        one CTA per (128 query rows, query head); 32-key tiles in key order.
+//             query tile the key tile serves, in a fixed order; each step's dV and dK come
+//             out of the MMAs into a fresh TMEM block and are added into running sums in fp32.
+//   dQ        one CTA per (128 query rows, query head); 32-key tiles in key order, each
+//             tile's dQ added into a running sum likewise.
 // The backward takes no atomics: both gradients come out in one fixed order, so repeated
 // calls are bitwise equal whatever `deterministic` asks.
 #include <cmath>

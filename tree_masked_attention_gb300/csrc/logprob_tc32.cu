@@ -16,8 +16,9 @@
 //
 // GEMM kernel: 128 threads, one 128 x 128 output tile per CTA, K in steps of 32 (one 128-byte
 // swizzle row of fp32), operand tiles double-buffered in shared memory: while the MMAs of
-// step k run, the threads load, split and store step k + 1. Thread t then owns accumulator
-// row t (TMEM lane t) for the epilogue.
+// step k run, the threads load, split and store step k + 1; every kGroup steps the products
+// are added into a running fp32 sum in TMEM. Thread t then owns accumulator row t (TMEM
+// lane t) for the epilogue.
 #include <cmath>
 #include <type_traits>
 
