@@ -208,3 +208,34 @@ def test_gdn_wait_runs_out_when_a_publication_is_withheld(which):
         for name, a, b in zip(("dq", "dk", "dv", "dg", "dbeta"), fn(*args), want):
             assert_close(name + " after a timeout", a, b, F32_TOL)
     m.tree_check_device_status()
+
+
+def test_gdn_full_size_two_heads():
+    """The bench's GDN configuration at full size (the 16,384-row Galton-Watson tree,
+    16 heads, Dk = Dv = 128, bf16 q / k / v / dO, fp32 gates): forward and backward of all
+    16 heads on the GPU, heads 3 and 12 against the per-branch oracle element by element
+    (heads are independent, so two heads of the same call stand for all of them)."""
+    need_cuda()
+    m = tma()
+    t = synth.galton_watson()
+    pk = m.tree_pack(t.seqs)
+    ref = oracle.pack_ref(t.seqs)
+    T, H, D = pk["T"], 16, 128
+    q, k, v, g, beta = _inputs(T, H, D, D, 31, True)
+    r = np.random.default_rng(32)
+    do = synth.bf16_round(r.normal(size=(T, H, D)).astype(np.float32))
+    td = torch.bfloat16
+    nodes = [dev(pk[n]) for n in ("node_start", "node_end", "node_parent")]
+    args = (dev(q, td), dev(k, td), dev(v, td), dev(g), dev(beta))
+    o = m.tree_gdn_fwd(*args, *nodes)
+    got = m.tree_gdn_bwd(*args, dev(do, td), *nodes)
+    m.tree_check_device_status()
+    hs = [3, 12]
+    sub = lambda x: np.ascontiguousarray(x[:, hs])
+    ro = oracle.gdn_ref_fwd(sub(q), sub(k), sub(v), sub(g), sub(beta), ref["paths"])
+    assert_close("o", host(o)[:, hs], ro, BF16_TOL)
+    want = oracle.gdn_ref_bwd(sub(q), sub(k), sub(v), sub(g), sub(beta), sub(do), ref["paths"])
+    for name, a, b in zip(("dq", "dk", "dv"), got[:3], want[:3]):
+        assert_close(name, host(a)[:, hs], b, BF16_TOL)
+    for name, a, b in zip(("dg", "dbeta"), got[3:], want[3:]):
+        assert_close(name, host(a)[:, hs], b, F32_TOL)
