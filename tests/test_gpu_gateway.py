@@ -152,3 +152,49 @@ def test_gateway_bad_bias_sets_device_flag():
         m.tree_check_device_status()
     assert ei.value.status == 7
     m.tree_check_device_status()
+
+
+def test_gateway_full_size_one_kv_group():
+    """The bench's gateway configuration at full size: the long-prompt agentic tree
+    (16,640 rows, 32 / 8 heads) cut below its 1024-token prompt, three of its six child
+    partitions (2048 rows each) run with all heads, the prompt's dK / dV summed over them
+    in fp32; every row of KV group 2 (its four query heads) against the oracle run on that
+    group alone."""
+    need_cuda()
+    m = tma()
+    tree = synth.agentic_long()
+    pk = m.tree_pack(tree.seqs)
+    end, par = pk["subtree_end"], pk["parent_row"]
+    P = int(pk["node_end"][0]) + 1
+    kids = [int(r) for r in range(P, pk["T"]) if par[r] == P - 1][:3]
+    q, k, v, do = synth.attention_config("agentic_long", pk["T"])
+    g, G = 2, 4
+    hs = slice(G * g, G * (g + 1))
+    bf = torch.bfloat16
+    pv = np.ones(P, dtype=bool)
+    bias = dev(np.zeros(P, dtype=np.float32))
+    dkp = torch.zeros((P, 8, 128), dtype=torch.float32, device="cuda")
+    dvp = torch.zeros_like(dkp)
+    sum_dk = np.zeros((P, 1, 128))
+    sum_dv = np.zeros((P, 1, 128))
+    for r in kids:
+        rows = slice(r, int(end[r]) + 1)
+        ce = (end[rows] - r).astype(np.int32)
+        kk, vv = np.concatenate([k[:P], k[rows]]), np.concatenate([v[:P], v[rows]])
+        tq, tk, tv, tdo = dev(q[rows], bf), dev(kk, bf), dev(vv, bf), dev(do[rows], bf)
+        o, lse = m.tree_attn_fwd_gateway(tq, tk, tv, bias, dev(ce))
+        dq, dk, dv, dkp, dvp = m.tree_attn_bwd_gateway(tq, tk, tv, o, tdo, lse, bias, dev(ce),
+                                                       dk_past=dkp, dv_past=dvp)
+        m.tree_check_device_status()
+        gq, gk, gv, gdo = q[rows, hs], kk[:, g:g + 1], vv[:, g:g + 1], do[rows, hs]
+        ro, rl = oracle.gateway_attn_ref_fwd(gq, gk, gv, P, pv, ce)
+        rdq, rdk, rdv = oracle.gateway_attn_ref_bwd(gq, gk, gv, gdo, P, pv, ce)
+        assert_close("O", host(o)[:, hs], ro, BF16_TOL)
+        assert_close("LSE", host(lse)[hs], rl, F32_TOL)
+        assert_close("dQ", host(dq)[:, hs], rdq, BF16_TOL)
+        assert_close("dK own", host(dk)[:, g:g + 1], rdk[P:], BF16_TOL)
+        assert_close("dV own", host(dv)[:, g:g + 1], rdv[P:], BF16_TOL)
+        sum_dk += rdk[:P]
+        sum_dv += rdv[:P]
+    assert_close("dK past (sum over children)", host(dkp)[:, g:g + 1], sum_dk, BF16_TOL)
+    assert_close("dV past (sum over children)", host(dvp)[:, g:g + 1], sum_dv, BF16_TOL)
