@@ -60,6 +60,8 @@ struct Params {
   float scale_log2;
   const int32_t* kmax;
   const int32_t* kmin;
+  const int32_t* kmax32;  // per 32-key chunk: max and min subtree_end (ceil(T / 32) entries)
+  const int32_t* kmin32;
   const int32_t* endp;  // subtree_end padded with -1 to a multiple of 128
   float* lse;
   int* err;
@@ -211,11 +213,24 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       if (p.kmax[kt] < iq0) continue;
       const int j0 = kt * BN;
       const bool partial = !(j0 + BN - 1 <= iq0 && p.kmin[kt] >= iq0 + BM - 1);
-      // visibility bits of this row's 128 keys, formed while the MMA of S runs
+      // visibility bits of this row's 128 keys, formed while the MMA of S runs. A 32-key
+      // chunk lying wholly at or before the row, whose smallest subtree_end reaches the row,
+      // is visible whole; one after the row, or whose largest subtree_end stops short of
+      // it, is hidden whole; only the rest is tested key by key.
       uint32_t vis[4] = {~0u, ~0u, ~0u, ~0u};
       if (partial) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) vis[c] = visible32(p.endp, j0 + 32 * c, ik);
+        for (int c = 0; c < 4; ++c) {
+          const int jb = j0 + 32 * c;
+          if (jb >= p.T || ik < jb) {
+            vis[c] = 0u;
+          } else {
+            const int kx = __ldg(p.kmax32 + (jb >> 5)), kn = __ldg(p.kmin32 + (jb >> 5));
+            if (ik > kx) vis[c] = 0u;
+            else if (jb + 31 <= ik && ik <= kn) vis[c] = ~0u;
+            else vis[c] = visible32(p.endp, jb, ik);
+          }
+        }
       }
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(&S.s_full[h], n & 1, p.err)))) break;
       tc_fence_after();
@@ -224,7 +239,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
       tmem_ld_wait();
-      if (partial) {
+      if (partial && (vis[0] & vis[1] & vis[2] & vis[3]) != ~0u) {
 #pragma unroll
         for (int t = 0; t < 128; ++t)
           if (!((vis[t >> 5] >> (t & 31)) & 1u)) sr[t] = 0xff800000u;  // -inf: p = 0
@@ -330,7 +345,8 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
 
 // Per 128-key tile: max / min subtree_end, plus subtree_end padded with -1.
 __global__ void tile_meta128_kernel(const int32_t* __restrict__ end, int64_t n, int32_t* __restrict__ kmax,
-                                    int32_t* __restrict__ kmin, int32_t* __restrict__ endp, int* err) {
+                                    int32_t* __restrict__ kmin, int32_t* __restrict__ kmax32,
+                                    int32_t* __restrict__ kmin32, int32_t* __restrict__ endp, int* err) {
   __shared__ int smax[4], smin[4];
   const int64_t j = static_cast<int64_t>(blockIdx.x) * 128 + threadIdx.x;
   const bool in = j < n;
@@ -346,6 +362,10 @@ __global__ void tile_meta128_kernel(const int32_t* __restrict__ end, int64_t n, 
   if (threadIdx.x % 32 == 0) {
     smax[threadIdx.x / 32] = mx;
     smin[threadIdx.x / 32] = mn;
+    if (in) {  // this warp's 32-key chunk starts inside the tree
+      kmax32[j / 32] = mx;
+      kmin32[j / 32] = mn;
+    }
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -356,8 +376,8 @@ __global__ void tile_meta128_kernel(const int32_t* __restrict__ end, int64_t n, 
 
 int tile_meta128_launch(const AttnArgs& a, cudaStream_t st) {
   const int64_t n_tiles = (a.T + 127) / 128;
-  tile_meta128_kernel<<<static_cast<unsigned>(n_tiles), 128, 0, st>>>(a.end, a.T, a.ws.kmax128, a.ws.kmin128,
-                                                                      a.ws.end_pad, device_error_word());
+  tile_meta128_kernel<<<static_cast<unsigned>(n_tiles), 128, 0, st>>>(
+      a.end, a.T, a.ws.kmax128, a.ws.kmin128, a.ws.kmax32, a.ws.kmin32, a.ws.end_pad, device_error_word());
   TREE_LAUNCH_CHECK("tile_meta128_kernel");
   return TREE_OK;
 }
@@ -397,6 +417,8 @@ int attn_fwd_tc(const AttnArgs& a, cudaStream_t st) {
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.kmax = a.ws.kmax128;
   p.kmin = a.ws.kmin128;
+  p.kmax32 = a.ws.kmax32;
+  p.kmin32 = a.ws.kmin32;
   p.endp = a.ws.end_pad;
   p.lse = a.lse;
   p.err = device_error_word();
