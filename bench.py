@@ -70,6 +70,9 @@ def parse_args(argv=None):
     ap.add_argument("--gdn-steps", type=int, default=5)
     ap.add_argument("--no-gdn", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--leg-rest-s", type=float, default=2.0,
+                    help="idle seconds before each leg after the headline, so that one leg's power "
+                         "state (the LM GEMMs run at the power cap) does not carry into the next")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of graph replays")
     ap.add_argument("--ref-budget-s", type=float, default=150.0,
@@ -510,12 +513,17 @@ def run_ours(args):
     if not args.no_e2e:
         out["e2e"] = leg.e2e(K, flush, world)
 
+    def rest():
+        torch.cuda.synchronize()
+        time.sleep(max(args.leg_rest_s, 0.0))
+
     # the other bf16 trees, each with its own roofline (rank 0, one GPU's worth of work)
     if rank == 0 and not args.no_secondary:
         sec = {}
         for name in ("galton_watson", "agentic_long", "agentic_short"):
             if name == args.workload:
                 continue
+            rest()
             other = AttnStep(tma, name, 0, dev, heads)
             m2 = other.measure(max(args.secondary_steps, 1), 3, flush, use_graph=not args.no_graph)
             sec[name] = secondary_entry(other, m2, peak, peak_src)
@@ -523,12 +531,16 @@ def run_ours(args):
         out["secondary"] = sec
 
     if not args.no_lm and rank == 0:
+        rest()
         out["lm_head"] = run_lm_head(args, dev, peaks, peak_src)
     if not args.no_conv and rank == 0:
+        rest()
         out["conv1d"] = run_conv1d(args, dev, peaks, peak_src, flush)
     if not args.no_gateway and rank == 0:
+        rest()
         out["gateway"] = run_gateway(args, dev, peaks, peak_src, flush)
     if not args.no_gdn and rank == 0:
+        rest()
         out["gdn"] = run_gdn(args, dev, flush)
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
