@@ -818,12 +818,16 @@ def run_gdn(args, dev, flush):
     grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(gate),
              torch.empty_like(beta))
     stream = torch.cuda.current_stream(dev)
+    # the step: the forward on the backward-sized workspace, then the backward that takes
+    # the forward's states from it (tree_gdn_bwd_saved); the backward that recomputes them
+    # from the inputs alone (tree_gdn_bwd) is timed beside it
     for _ in range(2):
         tma.tree_gdn_fwd(q, k, v, gate, beta, ns, ne, npar, workspace=ws, out=o)
+        tma.tree_gdn_bwd(q, k, v, gate, beta, do, ns, ne, npar, workspace=ws, grads=grads, saved=True)
         tma.tree_gdn_bwd(q, k, v, gate, beta, do, ns, ne, npar, workspace=ws, grads=grads)
     torch.cuda.synchronize()
     n = max(args.gdn_steps, 1)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(n)]
     for s in range(n):
         flush.zero_()
         evs[s][0].record(stream)
@@ -831,18 +835,23 @@ def run_gdn(args, dev, flush):
         evs[s][1].record(stream)
         flush.zero_()
         evs[s][2].record(stream)
-        tma.tree_gdn_bwd(q, k, v, gate, beta, do, ns, ne, npar, workspace=ws, grads=grads)
+        tma.tree_gdn_bwd(q, k, v, gate, beta, do, ns, ne, npar, workspace=ws, grads=grads, saved=True)
         evs[s][3].record(stream)
+        flush.zero_()
+        evs[s][4].record(stream)
+        tma.tree_gdn_bwd(q, k, v, gate, beta, do, ns, ne, npar, workspace=ws, grads=grads)
+        evs[s][5].record(stream)
     torch.cuda.synchronize()
     tma.tree_check_device_status()
     f_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
     b_ms = float(np.mean([e[2].elapsed_time(e[3]) for e in evs]))
+    r_ms = float(np.mean([e[4].elapsed_time(e[5]) for e in evs]))
     fl = 6.0 * D * D * H * T
     return {
         "workload": f"gdn: Galton-Watson tree of {T} rows ({len(pk['node_start'])} nodes), {H} heads, Dk = Dv = {D}, "
                     "bf16 q/k/v/dO, fp32 gates",
         "value": round(T / ((f_ms + b_ms) / 1e3), 1), "unit": "packed tokens/s (forward + backward)",
-        "ms_fwd": round(f_ms, 4), "ms_bwd": round(b_ms, 4), "steps": n,
+        "ms_fwd": round(f_ms, 4), "ms_bwd": round(b_ms, 4), "ms_bwd_recompute": round(r_ms, 4), "steps": n,
         "fwd_tokens_per_s": round(T / (f_ms / 1e3), 1),
         "fwd_recurrence_tflops": round(fl / (f_ms / 1e3) / 1e12, 3),
         # fp32 on the CUDA cores: the ALU roofline is 152 SMs x 128 fp32 lanes x 2 FLOP per FMA
@@ -851,11 +860,11 @@ def run_gdn(args, dev, flush):
         # form's extra products -- the triangular factors -- are not counted)
         "roofline": {"bound": "alu", "achieved": round(2 * fl / (b_ms / 1e3) / 1e12, 3), "peak": 80.5,
                      "unit": "TFLOP/s", "frac": round(2 * fl / (b_ms / 1e3) / 1e12 / 80.5, 4),
-                     "of": "152 SMs x 128 fp32 FMA lanes x 2 x 2.07 GHz", "kernel": "tree_gdn_bwd",
+                     "of": "152 SMs x 128 fp32 FMA lanes x 2 x 2.07 GHz", "kernel": "tree_gdn_bwd_saved",
                      "traffic": None},
         "kernels": "fwd: gdn_setup, gdn_prep (chunk-parallel factors), gdn_chain (state chain over 32-column "
-                   "slices), gdn_out; bwd: setup, prep, chain, gdn_bchain (state-gradient chain), gdn_grads "
-                   "(fp32 CUDA cores)",
+                   "slices), gdn_out; bwd (saved): setup, gdn_bchain (state-gradient chain), gdn_grads; bwd "
+                   "(recompute): setup, prep, chain, bchain, grads (fp32 CUDA cores)",
         "data": "synthetic (seeded torch generator on device)",
     }
 

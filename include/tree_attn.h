@@ -392,6 +392,25 @@ int tree_gdn_bwd(const void* q, const void* k, const void* v, const float* g, co
                  const int32_t* node_parent, int64_t T, int64_t n_nodes, int H, int Dk, int Dv,
                  int dtype, void* workspace, size_t workspace_bytes, tree_stream_t stream);
 
+/*
+ * tree_gdn_bwd without recomputing the forward: the sub-chunk factors, the delta-rule
+ * corrections and the end states are taken from `workspace`, which must be the buffer
+ * (>= tree_gdn_bwd_workspace_size() bytes) that the most recent tree_gdn_fwd on these
+ * inputs ran with, on the same stream or synchronised since. Arguments and results as
+ * tree_gdn_bwd, which it matches bit for bit. The forward marks the workspace with a
+ * stamp of its shapes, dtype and input addresses; this call checks it on the device
+ * and consumes it (a second call needs a new forward). On a mismatch -- another
+ * workspace, other inputs or shapes, or no forward since the last use -- it schedules
+ * nothing, sets TREE_ERR_DEVICE_CHECK in the device error word and leaves the outputs
+ * unwritten. The stamp cannot see inputs changed in place between the two calls: they
+ * must hold the forward's values.
+ */
+int tree_gdn_bwd_saved(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                       const void* dout, void* dq, void* dk, void* dv, float* dg, float* dbeta,
+                       const int32_t* node_start, const int32_t* node_end,
+                       const int32_t* node_parent, int64_t T, int64_t n_nodes, int H, int Dk, int Dv,
+                       int dtype, void* workspace, size_t workspace_bytes, tree_stream_t stream);
+
 /* Test hook for the bounded waits of the GDN calls: the next tree_gdn_fwd or
  * tree_gdn_bwd call in this process withholds every publication of sub-chunk
  * `sub_chunk` (its index in preorder, -1 for none) and gives up any wait after

@@ -169,6 +169,83 @@ def test_gdn_bwd_repeats_bitwise():
         assert torch.equal(x, y)
 
 
+# ------------------------------------------------------------------------------ saved forward
+def _gdn_case(m, seed, H, D, bf16):
+    t = synth.galton_watson(seed=seed, budget=1500, seg=(20, 300), vocab=1000)
+    pk = m.tree_pack(t.seqs)
+    T = pk["T"]
+    q, k, v, g, beta = _inputs(T, H, D, D, seed + 20, bf16)
+    do = np.random.default_rng(seed + 21).normal(size=(T, H, D)).astype(np.float32)
+    if bf16:
+        do = synth.bf16_round(do)
+    return t, pk, (q, k, v, g, beta, do)
+
+
+def test_gdn_bwd_saved_matches_recompute_and_oracle():
+    """tree_gdn_bwd_saved after tree_gdn_fwd on the backward-sized workspace takes the
+    forward's factors, corrections and end states from it: the same bits as tree_gdn_bwd,
+    which recomputes them from the inputs, and the oracle's gradients."""
+    need_cuda()
+    m = tma()
+    H, D = 2, 128
+    t, pk, (q, k, v, g, beta, do) = _gdn_case(m, 6, H, D, True)
+    ref = oracle.pack_ref(t.seqs)
+    T, td = pk["T"], torch.bfloat16
+    nodes = [dev(pk[n]) for n in ("node_start", "node_end", "node_parent")]
+    ins = [dev(q, td), dev(k, td), dev(v, td), dev(g), dev(beta)]
+    d_o = dev(do, td)
+    ws = torch.empty(m.tree_gdn_bwd_workspace_size(T, len(pk["node_start"]), H, D, D), dtype=torch.uint8,
+                     device="cuda")
+    m.tree_gdn_fwd(*ins, *nodes, workspace=ws)
+    saved = m.tree_gdn_bwd_saved(*ins, d_o, *nodes, workspace=ws)
+    recomputed = m.tree_gdn_bwd(*ins, d_o, *nodes)
+    m.tree_check_device_status()
+    for name, a, b in zip(("dq", "dk", "dv", "dg", "dbeta"), saved, recomputed):
+        assert torch.equal(a, b), name
+    want = oracle.gdn_ref_bwd(q, k, v, g, beta, do, ref["paths"])
+    for name, a, b in zip(("dq", "dk", "dv"), saved[:3], want[:3]):
+        assert_close(name, a, b, BF16_TOL)
+    for name, a, b in zip(("dg", "dbeta"), saved[3:], want[3:]):
+        assert_close(name, a, b, F32_TOL)
+
+
+def test_gdn_bwd_saved_needs_the_forward_of_its_inputs():
+    """The workspace stamp: a second saved backward without a new forward, one after a
+    forward of other inputs, and one on a workspace no forward ran with each set
+    TREE_ERR_DEVICE_CHECK and schedule nothing; a matched pair afterwards runs normally."""
+    need_cuda()
+    m = tma()
+    H, D = 2, 64
+    t, pk, (q, k, v, g, beta, do) = _gdn_case(m, 7, H, D, False)
+    T = pk["T"]
+    nodes = [dev(pk[n]) for n in ("node_start", "node_end", "node_parent")]
+    ins = [dev(x) for x in (q, k, v, g, beta)]
+    d_o = dev(do)
+    size = m.tree_gdn_bwd_workspace_size(T, len(pk["node_start"]), H, D, D)
+    ws = torch.empty(size, dtype=torch.uint8, device="cuda")
+
+    def rejected(workspace, inputs=ins):
+        m.tree_gdn_bwd_saved(*inputs, d_o, *nodes, workspace=workspace)
+        with pytest.raises(m.TreeError) as ei:
+            m.tree_check_device_status()
+        assert ei.value.status == 7   # TREE_ERR_DEVICE_CHECK
+        m.tree_check_device_status()  # cleared
+
+    m.tree_gdn_fwd(*ins, *nodes, workspace=ws)
+    first = m.tree_gdn_bwd_saved(*ins, d_o, *nodes, workspace=ws)
+    m.tree_check_device_status()
+    rejected(ws)                                          # the stamp was consumed
+    other = [dev(x) for x in (q, k, v, g, beta)]          # same values, other buffers
+    m.tree_gdn_fwd(*other, *nodes, workspace=ws)
+    rejected(ws)                                          # the forward was of other inputs
+    rejected(torch.zeros(size, dtype=torch.uint8, device="cuda"))  # no forward on this workspace
+    m.tree_gdn_fwd(*ins, *nodes, workspace=ws)
+    again = m.tree_gdn_bwd_saved(*ins, d_o, *nodes, workspace=ws)
+    m.tree_check_device_status()
+    for a, b in zip(first, again):
+        assert torch.equal(a, b)
+
+
 # ------------------------------------------------------------------------------ bounded waits
 def _withheld_call(m, fn, args, sub_chunk):
     rc = m.lib().tree_gdn_test_withhold(sub_chunk, 0.05)

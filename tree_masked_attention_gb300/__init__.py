@@ -19,7 +19,7 @@ Functions (same names as the C ABI):
   tree_attn_bwd_gateway(q, k, v, o, dout, lse, attn_bias, subtree_end, dk_past, dv_past)
                                                     -> (dq, dk, dv, dk_past, dv_past)
   tree_gdn_fwd(q, k, v, g, beta, node_start, node_end, node_parent) -> o
-  tree_gdn_bwd(q, k, v, g, beta, dout, node_start, node_end, node_parent)
+  tree_gdn_bwd(q, k, v, g, beta, dout, node_start, node_end, node_parent, saved=False)
                                                     -> (dq, dk, dv, dg, dbeta)
   tree_conv1d_fwd(x, w, parent_row, bias)           -> y
   tree_conv1d_bwd(x, w, dy, subtree_end, position_ids) -> (dx, dw, dbias)
@@ -37,7 +37,7 @@ __all__ = [
     "tree_attn_fwd", "tree_attn_bwd", "tree_attn_bwd_rope", "tree_kernel_timing", "tree_kernel_last_ms", "tree_logprob_workspace_size", "tree_logprob_fwd", "tree_policy_loss",
     "tree_conv1d_fwd", "tree_conv1d_bwd", "tree_conv1d_workspace_size", "tree_attn_fwd_gateway",
     "tree_attn_bwd_gateway", "tree_attn_gateway_workspace_size", "tree_gdn_fwd", "tree_gdn_workspace_size",
-    "tree_gdn_bwd", "tree_gdn_bwd_workspace_size",
+    "tree_gdn_bwd", "tree_gdn_bwd_saved", "tree_gdn_bwd_workspace_size",
     "tree_logprob_bwd", "tree_check_device_status", "tree_kernel_path", "tree_launch_count", "TreeError", "lib",
     "DTYPE_F32", "DTYPE_BF16",
 ]
@@ -357,10 +357,15 @@ def tree_gdn_bwd_workspace_size(T, n_nodes, H, Dk, Dv) -> int:
     return int(lib().tree_gdn_bwd_workspace_size(T, n_nodes, H, Dk, Dv))
 
 
-def tree_gdn_bwd(q, k, v, g, beta, dout, node_start, node_end, node_parent, workspace=None, grads=None):
+def tree_gdn_bwd(q, k, v, g, beta, dout, node_start, node_end, node_parent, workspace=None, grads=None,
+                 saved=False):
     """Gradients of sum(dout * o) for tree_gdn_fwd: returns (dq, dk, dv, dg, dbeta), dq, dk
     [T,H,Dk] and dv [T,H,Dv] in q's dtype, dg, dbeta fp32 [T,H]. grads: optional
-    preallocated tuple of the five outputs."""
+    preallocated tuple of the five outputs. saved=True (tree_gdn_bwd_saved) takes the
+    forward's states from `workspace`, which must be the tree_gdn_bwd_workspace_size()
+    buffer the last tree_gdn_fwd on these inputs ran with, instead of recomputing them."""
+    if saved and workspace is None:
+        raise ValueError("tree_gdn_bwd(saved=True) needs the workspace the forward ran with")
     torch = _torch()
     T, H, Dk = q.shape
     Dv = v.shape[2]
@@ -372,14 +377,22 @@ def tree_gdn_bwd(q, k, v, g, beta, dout, node_start, node_end, node_parent, work
     dq, dk, dv, dg, db = grads
     f32, i32 = torch.float32, torch.int32
     ws = _workspace(tree_gdn_bwd_workspace_size(T, n_nodes, H, Dk, Dv), q.device, workspace)
-    check(lib().tree_gdn_bwd(_dev(q, "q"), _dev(k, "k", q.dtype), _dev(v, "v", q.dtype), _dev(g, "g", f32),
-                             _dev(beta, "beta", f32), _dev(dout, "dout", q.dtype), _dev(dq, "dq", q.dtype),
-                             _dev(dk, "dk", q.dtype), _dev(dv, "dv", q.dtype), _dev(dg, "dg", f32),
-                             _dev(db, "dbeta", f32), _dev(node_start, "node_start", i32),
-                             _dev(node_end, "node_end", i32), _dev(node_parent, "node_parent", i32), T, n_nodes,
-                             H, Dk, Dv, _dtype_code(q), C.c_void_p(ws.data_ptr()), ws.numel() * ws.element_size(),
-                             _stream(q)), "tree_gdn_bwd")
+    name = "tree_gdn_bwd_saved" if saved else "tree_gdn_bwd"
+    check(getattr(lib(), name)(_dev(q, "q"), _dev(k, "k", q.dtype), _dev(v, "v", q.dtype), _dev(g, "g", f32),
+                               _dev(beta, "beta", f32), _dev(dout, "dout", q.dtype), _dev(dq, "dq", q.dtype),
+                               _dev(dk, "dk", q.dtype), _dev(dv, "dv", q.dtype), _dev(dg, "dg", f32),
+                               _dev(db, "dbeta", f32), _dev(node_start, "node_start", i32),
+                               _dev(node_end, "node_end", i32), _dev(node_parent, "node_parent", i32), T,
+                               n_nodes, H, Dk, Dv, _dtype_code(q), C.c_void_p(ws.data_ptr()),
+                               ws.numel() * ws.element_size(), _stream(q)), name)
     return dq, dk, dv, dg, db
+
+
+def tree_gdn_bwd_saved(q, k, v, g, beta, dout, node_start, node_end, node_parent, workspace, grads=None):
+    """tree_gdn_bwd taking the forward's states from `workspace` (the
+    tree_gdn_bwd_workspace_size() buffer the last tree_gdn_fwd on these inputs ran with)."""
+    return tree_gdn_bwd(q, k, v, g, beta, dout, node_start, node_end, node_parent, workspace=workspace,
+                        grads=grads, saved=True)
 
 
 def tree_conv1d_fwd(x, w, parent_row, bias=None, out=None):

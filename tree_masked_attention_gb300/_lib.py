@@ -68,6 +68,8 @@ SIGNATURES = {
     "tree_gdn_bwd_workspace_size": (_sz, [_i64, _i64, _int, _int, _int]),
     "tree_gdn_bwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64,
                             _int, _int, _int, _int, _vp, _sz, _vp]),
+    "tree_gdn_bwd_saved": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64,
+                                  _i64, _int, _int, _int, _int, _vp, _sz, _vp]),
     "tree_gdn_test_withhold": (_int, [_i64, C.c_double]),
     "tree_conv1d_fwd": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _int, _int, _int, _vp]),
     "tree_conv1d_workspace_size": (_sz, [_i64, _int, _int]),

@@ -97,7 +97,7 @@ struct GdnWs {
   int* depth_count; // [mc + 1]
   int* succ_ptr;    // [mc + 1] successors (sub-chunks whose predecessor is c), CSR
   int* succ;        // [mc]
-  int* ctl;         // [4] n_chunks, forward counter, backward counter, abort
+  int* ctl;         // [8] n_chunks, forward counter, backward counter, abort, stamp (below)
   int* flags_f;     // [mc, H, slices] end state published
   float* Pm;        // [mc, H, 64, 64]
   float* Xm;        // [mc, H, 64, 64]  (I + A)^-1
@@ -141,7 +141,7 @@ size_t gdn_ws_layout(int64_t T, int64_t n_nodes, int H, int Dk, int Dv, bool bwd
   x.depth_count = static_cast<int*>(take(sizeof(int) * (mc + 1)));
   x.succ_ptr = static_cast<int*>(take(sizeof(int) * (mc + 1)));
   x.succ = static_cast<int*>(take(sizeof(int) * mc));
-  x.ctl = static_cast<int*>(take(sizeof(int) * 4));
+  x.ctl = static_cast<int*>(take(sizeof(int) * 8));
   x.scratch = static_cast<int*>(take(sizeof(int) * (4 * std::max<int64_t>(n_nodes, 1) + 4 * mc + 2)));
   x.flags_f = static_cast<int*>(take(sizeof(int) * mc * H * ns));
   x.Pm = static_cast<float*>(take(sizeof(float) * mc * H * kChunk * kChunk));
@@ -166,11 +166,16 @@ size_t gdn_ws_layout(int64_t T, int64_t n_nodes, int H, int Dk, int Dv, bool bwd
 // Sub-chunk table from the node arrays (one thread walks the nodes in preorder, checking
 // that they tile [0, T) with earlier parents), the schedule (sub-chunks by increasing
 // chain depth: a counting sort, stable in preorder) and the successor lists; all threads
-// clear the flags. On a malformed table nothing is scheduled (n_chunks = 0). The walk's
+// clear the flags. On a malformed table nothing is scheduled (n_chunks = 0). ctl[4] holds
+// the stamp of the inputs whose forward results (factors, corrections, end states) the
+// workspace holds: written by the calls that compute them (kStampWrite), checked and then
+// cleared by a backward that takes them from the workspace (kStampUse), which schedules
+// nothing on a mismatch. The walk's
 // working arrays (copies of the node arrays, each node's last sub-chunk, each sub-chunk's
 // depth and predecessor, the sort's counters) live in shared memory when they fit
 // (`fits`), else in the workspace.
 constexpr int kSetupThreads = 1024;
+constexpr int kStampWrite = 0, kStampUse = 1;
 
 __host__ __device__ constexpr int64_t setup_ints(int64_t n_nodes, int64_t max_chunks) {
   return 4 * n_nodes + 4 * max_chunks + 2;  // node arrays, nlast; depth, pred, two counters of mc + 1
@@ -180,7 +185,8 @@ __global__ void __launch_bounds__(kSetupThreads) gdn_setup_kernel(const int32_t*
                                                                   const int32_t* __restrict__ node_end,
                                                                   const int32_t* __restrict__ node_parent,
                                                                   int n_nodes, int T, int64_t n_flags, GdnWs w,
-                                                                  int max_chunks, int fits, int* err) {
+                                                                  int max_chunks, int fits, int stamp,
+                                                                  int stamp_mode, int* err) {
   extern __shared__ int ssm[];
   for (int64_t i = threadIdx.x; i < n_flags; i += blockDim.x) {
     w.flags_f[i] = 0;
@@ -206,7 +212,13 @@ __global__ void __launch_bounds__(kSetupThreads) gdn_setup_kernel(const int32_t*
   w.ctl[3] = 0;
   int m = 0, next = 0;
   bool ok = true;
-  for (int n = 0; n < n_nodes && ok; ++n) {
+  if (stamp_mode == kStampUse) {
+    ok = w.ctl[4] == stamp;  // the forward of exactly these inputs ran on this workspace
+    w.ctl[4] = 0;            // and its results serve one backward
+  } else {
+    w.ctl[4] = stamp;
+  }
+  for (int n = 0; ok && n < n_nodes; ++n) {
     const int s = nst[n], e = nen[n] + 1, par = npa[n];
     if (s != next || e <= s || e > T || par >= n || par < -1) {
       ok = false;
@@ -1233,7 +1245,7 @@ int run_forward_chain(GdnArgs& a, int64_t mc, int n_sm, cudaStream_t st) {
 int gdn_begin(GdnArgs& a, const void* q, const void* k, const void* v, const float* g, const float* beta,
               const int32_t* node_start, const int32_t* node_end, const int32_t* node_parent, int64_t T,
               int64_t n_nodes, int H, int Dk, int Dv, int dtype, void* workspace, size_t workspace_bytes,
-              bool bwd, bool outs_ok, const char* name, cudaStream_t st, int64_t* mc_out, bool* empty) {
+              bool bwd, bool saved, bool outs_ok, const char* name, cudaStream_t st, int64_t* mc_out, bool* empty) {
   *empty = false;
   if (dtype != TREE_DTYPE_F32 && dtype != TREE_DTYPE_BF16) return fail(TREE_ERR_DTYPE, "%s: bad dtype %d", name, dtype);
   if (T < 0 || n_nodes < 0 || T > (1 << 30) || n_nodes > T)
@@ -1274,9 +1286,22 @@ int gdn_begin(GdnArgs& a, const void* q, const void* k, const void* v, const flo
     int rc = smem_opt_in(reinterpret_cast<const void*>(gdn_setup_kernel), static_cast<int>(setup_bytes));
     if (rc) return rc;
   }
+  // stamp of the inputs: FNV-1a over the shapes, the dtype and the input addresses (never 0)
+  uint32_t stamp = 2166136261u;
+  auto mix = [&](uint64_t x) {
+    for (int b = 0; b < 8; ++b) stamp = (stamp ^ static_cast<uint32_t>((x >> (8 * b)) & 0xffu)) * 16777619u;
+  };
+  for (const void* ptr : {q, k, v, static_cast<const void*>(g), static_cast<const void*>(beta),
+                          static_cast<const void*>(node_start), static_cast<const void*>(node_end),
+                          static_cast<const void*>(node_parent)})
+    mix(reinterpret_cast<uintptr_t>(ptr));
+  for (int64_t x : {T, n_nodes, static_cast<int64_t>(H), static_cast<int64_t>(Dk), static_cast<int64_t>(Dv),
+                    static_cast<int64_t>(dtype)})
+    mix(static_cast<uint64_t>(x));
+  stamp |= 1u;
   gdn_setup_kernel<<<1, kSetupThreads, fits ? setup_bytes : 0, st>>>(
       node_start, node_end, node_parent, static_cast<int>(n_nodes), static_cast<int>(T), n_flags, a.w,
-      static_cast<int>(mc), fits, a.err);
+      static_cast<int>(mc), fits, static_cast<int>(stamp), saved ? kStampUse : kStampWrite, a.err);
   TREE_LAUNCH_CHECK("gdn_setup_kernel");
   *mc_out = mc;
   return TREE_OK;
@@ -1292,10 +1317,13 @@ int gdn_forward(GdnArgs& a, int64_t mc, cudaStream_t st) {
   return TREE_OK;
 }
 
+// saved: the forward's factors, corrections and end states are in the workspace already
+// (checked by the set-up kernel's stamp); otherwise they are recomputed first.
 template <typename Tin>
-int gdn_backward(GdnArgs& a, int64_t mc, cudaStream_t st) {
+int gdn_backward(GdnArgs& a, int64_t mc, bool saved, cudaStream_t st) {
   int n_sm = 0, rc;
-  if ((rc = sm_count(&n_sm)) || (rc = run_forward_chain<Tin>(a, mc, n_sm, st))) return rc;
+  if ((rc = sm_count(&n_sm))) return rc;
+  if (!saved && (rc = run_forward_chain<Tin>(a, mc, n_sm, st))) return rc;
   if ((rc = smem_opt_in(reinterpret_cast<const void*>(gdn_bchain_kernel<Tin>), static_cast<int>(kBchainSmem))) ||
       (rc = smem_opt_in(reinterpret_cast<const void*>(gdn_grads_kernel<Tin>), static_cast<int>(kGradsSmem))))
     return rc;
@@ -1331,10 +1359,32 @@ extern "C" int tree_gdn_fwd(const void* q, const void* k, const void* v, const f
   int64_t mc = 0;
   bool empty = false;
   int rc = gdn_begin(a, q, k, v, g, beta, node_start, node_end, node_parent, T, n_nodes, H, Dk, Dv, dtype,
-                     workspace, workspace_bytes, false, o != nullptr, "tree_gdn_fwd", st, &mc, &empty);
+                     workspace, workspace_bytes, false, false, o != nullptr, "tree_gdn_fwd", st, &mc, &empty);
   if (rc || empty) return rc;
   a.o = o;
   return dtype == TREE_DTYPE_BF16 ? gdn_forward<__nv_bfloat16>(a, mc, st) : gdn_forward<float>(a, mc, st);
+}
+
+static int gdn_bwd_call(const char* name, bool saved, const void* q, const void* k, const void* v, const float* g,
+                        const float* beta, const void* dout, void* dq, void* dk, void* dv, float* dg, float* dbeta,
+                        const int32_t* node_start, const int32_t* node_end, const int32_t* node_parent, int64_t T,
+                        int64_t n_nodes, int H, int Dk, int Dv, int dtype, void* workspace, size_t workspace_bytes,
+                        tree_stream_t stream) {
+  clear_error();
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  GdnArgs a{};
+  int64_t mc = 0;
+  bool empty = false;
+  // the alignment of dout is checked before anything is enqueued (a saved call's set-up
+  // consumes the stamp)
+  if (dout && !aligned16(dout)) return fail(TREE_ERR_ALIGNMENT, "%s: dout not 16-byte aligned", name);
+  int rc = gdn_begin(a, q, k, v, g, beta, node_start, node_end, node_parent, T, n_nodes, H, Dk, Dv, dtype,
+                     workspace, workspace_bytes, true, saved, dout && dq && dk && dv && dg && dbeta, name, st,
+                     &mc, &empty);
+  if (rc || empty) return rc;
+  a.dout = dout; a.dq = dq; a.dk = dk; a.dv = dv; a.dg = dg; a.dbeta = dbeta;
+  return dtype == TREE_DTYPE_BF16 ? gdn_backward<__nv_bfloat16>(a, mc, saved, st)
+                                  : gdn_backward<float>(a, mc, saved, st);
 }
 
 extern "C" int tree_gdn_bwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
@@ -1342,18 +1392,17 @@ extern "C" int tree_gdn_bwd(const void* q, const void* k, const void* v, const f
                             const int32_t* node_start, const int32_t* node_end, const int32_t* node_parent,
                             int64_t T, int64_t n_nodes, int H, int Dk, int Dv, int dtype, void* workspace,
                             size_t workspace_bytes, tree_stream_t stream) {
-  clear_error();
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  GdnArgs a{};
-  int64_t mc = 0;
-  bool empty = false;
-  int rc = gdn_begin(a, q, k, v, g, beta, node_start, node_end, node_parent, T, n_nodes, H, Dk, Dv, dtype,
-                     workspace, workspace_bytes, true, dout && dq && dk && dv && dg && dbeta, "tree_gdn_bwd", st,
-                     &mc, &empty);
-  if (rc || empty) return rc;
-  if (!aligned16(dout)) return fail(TREE_ERR_ALIGNMENT, "tree_gdn_bwd: dout not 16-byte aligned");
-  a.dout = dout; a.dq = dq; a.dk = dk; a.dv = dv; a.dg = dg; a.dbeta = dbeta;
-  return dtype == TREE_DTYPE_BF16 ? gdn_backward<__nv_bfloat16>(a, mc, st) : gdn_backward<float>(a, mc, st);
+  return gdn_bwd_call("tree_gdn_bwd", false, q, k, v, g, beta, dout, dq, dk, dv, dg, dbeta, node_start, node_end,
+                      node_parent, T, n_nodes, H, Dk, Dv, dtype, workspace, workspace_bytes, stream);
+}
+
+extern "C" int tree_gdn_bwd_saved(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                                  const void* dout, void* dq, void* dk, void* dv, float* dg, float* dbeta,
+                                  const int32_t* node_start, const int32_t* node_end, const int32_t* node_parent,
+                                  int64_t T, int64_t n_nodes, int H, int Dk, int Dv, int dtype, void* workspace,
+                                  size_t workspace_bytes, tree_stream_t stream) {
+  return gdn_bwd_call("tree_gdn_bwd_saved", true, q, k, v, g, beta, dout, dq, dk, dv, dg, dbeta, node_start,
+                      node_end, node_parent, T, n_nodes, H, Dk, Dv, dtype, workspace, workspace_bytes, stream);
 }
 
 extern "C" int tree_gdn_test_withhold(int64_t sub_chunk, double wait_seconds) {
