@@ -863,8 +863,9 @@ def run_gdn(args, dev, flush):
                      "of": "152 SMs x 128 fp32 FMA lanes x 2 x 2.07 GHz", "kernel": "tree_gdn_bwd_saved",
                      "traffic": None},
         "kernels": "fwd: gdn_setup, gdn_prep (chunk-parallel factors), gdn_chain (state chain over 32-column "
-                   "slices), gdn_out; bwd (saved): setup, gdn_bchain (state-gradient chain), gdn_grads; bwd "
-                   "(recompute): setup, prep, chain, bchain, grads (fp32 CUDA cores)",
+                   "slices), gdn_out; bwd (saved): setup, gdn_bprep (chain-independent products), gdn_bchain "
+                   "(state-gradient chain), gdn_grads; bwd (recompute): setup, prep, chain, bprep, bchain, "
+                   "grads (fp32 CUDA cores)",
         "data": "synthetic (seeded torch generator on device)",
     }
 

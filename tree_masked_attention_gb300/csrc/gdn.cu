@@ -26,11 +26,13 @@
 //          the slices are independent chains;
 //   out    per (sub-chunk, head), in parallel: O = E o (Q h0) + P u.
 // Backward (gradients of sum(dO . O)): setup, prep and chain again (they give every h0
-// and u), then
+// and u; the saved form takes them from the forward's workspace), then
+//   bprep  per (sub-chunk, head), in parallel: the chain-independent products
+//          du0 = P^T dO and c0 = Q^T (E o dO);
 //   bchain per (sub-chunk, head, slice) by decreasing chain depth: the end-state gradient
 //          dh_end is the sum, in a fixed order, of the successors' start-state gradients;
-//          du = w o (K dh_end) + P^T dO, dr = X^T du, dv = beta o dr,
-//          dh0 = E_{L-1} dh_end + Q^T (E o dO) - K^T (beta E o dr), published;
+//          du = w o (K dh_end) + du0, dr = X^T du, dv = beta o dr,
+//          dh0 = E_{L-1} dh_end + c0 - K^T (beta E o dr), published;
 //   grads  per (sub-chunk, head), in parallel: dP = lower(dO u^T), dA = -strict(dr u^T),
 //          dQ = (dP o f) K + (E o dO) h0^T,
 //          dK = (dP o f)^T Q + (dA o beta f) K + (dA o beta f)^T K + w o (u dh_end^T)
@@ -112,6 +114,8 @@ struct GdnWs {
   float* dr;        // [mc, H, slices, 64, 32]
   float* part;      // [slices, 2, T, H] per-row partial sums (dw, dr . v)
   float* part_he;   // [slices, mc, H] partial sums of dh_end . h0
+  float* du0;       // [mc, H, slices, 64, 32] P^T dO
+  float* c0;        // [mc, H, slices, Dk, 32] Q^T (E o dO)
   int* scratch;     // set-up working arrays when they do not fit in shared memory
 };
 
@@ -157,6 +161,8 @@ size_t gdn_ws_layout(int64_t T, int64_t n_nodes, int H, int Dk, int Dv, bool bwd
     x.dr = static_cast<float*>(take(sizeof(float) * mc * H * ns * kChunk * kSlice));
     x.part = static_cast<float*>(take(sizeof(float) * ns * 2 * T * H));
     x.part_he = static_cast<float*>(take(sizeof(float) * ns * mc * H));
+    x.du0 = static_cast<float*>(take(sizeof(float) * mc * H * ns * kChunk * kSlice));
+    x.c0 = static_cast<float*>(take(sizeof(float) * mc * H * ns * Dk * kSlice));
   }
   if (w) *w = x;
   return round_up(off, 256);
@@ -734,9 +740,93 @@ __global__ void __launch_bounds__(kThreads) gdn_out_kernel(const GdnArgs a) {
   }
 }
 
+// ------------------------------------------------------------------------------ bprep
+// Per (sub-chunk, head), in parallel: the two products of the state-gradient chain that do
+// not depend on it, du0 = P^T dO ([64, Dv]) and c0 = Q^T (E o dO) ([Dk, Dv]), into the
+// [mc, H, slices, rows, 32] layout the chain reads. Each thread owns four consecutive
+// columns c4 of rows warp + 8 m.
+constexpr size_t kBprepSmem = (kChunk * kSq + 2 * kChunk * kRow + 4 * kChunk) * sizeof(float);
+
+template <typename Tin>
+__global__ void __launch_bounds__(kThreads, 2) gdn_bprep_kernel(const GdnArgs a) {
+  extern __shared__ __align__(16) float sm[];
+  float* Ps = sm;                 // [64][kSq]
+  float* Qs = Ps + kChunk * kSq;  // [64][kRow]
+  float* Os = Qs + kChunk * kRow; // [64][kRow] dO, then E o dO
+  float* lg = Os + kChunk * kRow;
+  float* E = lg + kChunk;
+  float* wv = E + kChunk;
+  float* bs = wv + kChunk;
+  const int c = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
+  const GdnWs& w = a.w;
+  if (c >= w.ctl[0]) return;
+  if (*reinterpret_cast<volatile int*>(&w.ctl[3])) return;  // a chain gave up: outputs unspecified
+  const int4 ck = w.chunks[c];
+  const int r0 = ck.x, L = ck.y, H = a.H, Dk = a.Dk, Dv = a.Dv, ns = a.ns;
+  const int Dk4 = (Dk + 3) & ~3, nc = ns * kSlice;  // dO columns past Dv up to the slices' end are zero
+  cp_block(Ps, kSq, w.Pm + (static_cast<int64_t>(c) * H + h) * kChunk * kChunk, kChunk, kChunk);
+  load_tile(Qs, kRow, static_cast<const Tin*>(a.q), r0, L, H, h, Dk, 0, Dk4);
+  load_tile(Os, kRow, static_cast<const Tin*>(a.dout), r0, L, H, h, Dv, 0, nc);
+  cp_wait();
+  decay_factors(a.g, a.beta, r0, L, H, h, lg, E, wv, bs);  // ends with a barrier
+  const int c4 = lane * 4;
+  const bool col_ok = c4 < nc;
+  {  // du0 = P^T dO (P lower-triangular, zero past L): rows warp + 8 m, m < 8
+    float4 acc[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) acc[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int t2 = 0; t2 < L; ++t2) {
+      const float4 o4 = *reinterpret_cast<const float4*>(Os + t2 * kRow + c4);
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const float pv = Ps[t2 * kSq + warp + 8 * m];
+        acc[m].x = fmaf(pv, o4.x, acc[m].x); acc[m].y = fmaf(pv, o4.y, acc[m].y);
+        acc[m].z = fmaf(pv, o4.z, acc[m].z); acc[m].w = fmaf(pv, o4.w, acc[m].w);
+      }
+    }
+    if (col_ok) {
+      float* dst = slice_block(w.du0, c, h, c4 / kSlice, H, ns, kChunk) + c4 % kSlice;
+#pragma unroll
+      for (int m = 0; m < 8; ++m) *reinterpret_cast<float4*>(dst + (warp + 8 * m) * kSlice) = acc[m];
+    }
+  }
+  __syncthreads();
+  for (int idx = tid; idx < L * (nc / 4); idx += kThreads) {  // E o dO
+    const int t = idx / (nc / 4), j = (idx % (nc / 4)) * 4;
+    float4* o = reinterpret_cast<float4*>(Os + t * kRow + j);
+    const float e = E[t];
+    float4 x = *o;
+    x.x *= e; x.y *= e; x.z *= e; x.w *= e;
+    *o = x;
+  }
+  __syncthreads();
+  {  // c0 = Q^T (E o dO): rows i = warp + 8 m, m < 16
+    float4 acc[16];
+#pragma unroll
+    for (int m = 0; m < 16; ++m) acc[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int t = 0; t < L; ++t) {
+      const float4 o4 = *reinterpret_cast<const float4*>(Os + t * kRow + c4);
+#pragma unroll
+      for (int m = 0; m < 16; ++m) {
+        const float qv = Qs[t * kRow + warp + 8 * m];
+        acc[m].x = fmaf(qv, o4.x, acc[m].x); acc[m].y = fmaf(qv, o4.y, acc[m].y);
+        acc[m].z = fmaf(qv, o4.z, acc[m].z); acc[m].w = fmaf(qv, o4.w, acc[m].w);
+      }
+    }
+    if (col_ok) {
+      float* dst = slice_block(w.c0, c, h, c4 / kSlice, H, ns, Dk) + c4 % kSlice;
+#pragma unroll
+      for (int m = 0; m < 16; ++m)
+        if (warp + 8 * m < Dk) *reinterpret_cast<float4*>(dst + (warp + 8 * m) * kSlice) = acc[m];
+    }
+  }
+}
+
 // ------------------------------------------------------------------------------ bchain
 // Per (sub-chunk, head, slice), by decreasing chain depth: dh_end (the sum of the
 // successors' start-state gradients), du, dr, dv, dh0; per-row partial sums for dg, dbeta.
+// The chain-independent du0 and c0 come from gdn_bprep_kernel, staged in the Os and Qs
+// buffers.
 constexpr int kBThreads = 512;                  // 16 warps: latency of one chain item is the critical path
 constexpr int kBRows = kChunk / (kBThreads / 32);  // rows of du / dr per warp (4); dh0 rows per warp 2 kBRows
 static_assert(kBRows == 4 && 2 * kBRows * (kBThreads / 32) == kMaxD, "bchain row mapping");
@@ -747,12 +837,12 @@ template <typename Tin>
 __global__ void __launch_bounds__(kBThreads, 1) gdn_bchain_kernel(const GdnArgs a) {
   extern __shared__ __align__(16) float sm[];
   float* Ks = sm;                        // [64][kRow]
-  float* Qs = Ks + kChunk * kRow;        // [64][kRow]
-  float* Ps = Qs + kChunk * kRow;        // [64][kSq]
+  float* Qs = Ks + kChunk * kRow;        // [128][kSl] c0 slice (the region of a [64][kRow] tile)
+  float* Ps = Qs + kChunk * kRow;        // [64][kSq] (unused)
   float* Xs = Ps + kChunk * kSq;         // [64][kSq]
   float* Ds = Xs + kChunk * kSq;         // [128][kSl] dh_end slice
   float* Hs = Ds + kMaxD * kSl;          // [128][kSl] h0 slice
-  float* Os = Hs + kMaxD * kSl;          // [64][kSl] dO slice
+  float* Os = Hs + kMaxD * kSl;          // [64][kSl] du0 slice
   float* Us = Os + kChunk * kSl;         // [64][kSl] u slice
   float* Vs = Us + kChunk * kSl;         // [64][kSl] v slice
   float* Rs = Vs + kChunk * kSl;         // [64][kSl] du, then dr
@@ -768,7 +858,6 @@ __global__ void __launch_bounds__(kBThreads, 1) gdn_bchain_kernel(const GdnArgs 
   const int Dk4 = (Dk + 3) & ~3;
   const int n_chunks = w.ctl[0];
   const int items = n_chunks * H * ns;
-  const Tin* tdo = static_cast<const Tin*>(a.dout);
   Tin* tdv = static_cast<Tin*>(a.dv);
   while (true) {
     const int item = next_item(&w.ctl[2], &w.ctl[3], items, &s_item);
@@ -780,13 +869,12 @@ __global__ void __launch_bounds__(kBThreads, 1) gdn_bchain_kernel(const GdnArgs 
     const int sb = w.succ_ptr[c], se = w.succ_ptr[c + 1];
     // loads that do not depend on the successors first
     const int64_t mo = (static_cast<int64_t>(c) * H + h) * kChunk * kChunk;
-    cp_block<kBThreads>(Ps, kSq, w.Pm + mo, kChunk, kChunk);
     cp_block<kBThreads>(Xs, kSq, w.Xm + mo, kChunk, kChunk);
+    cp_block<kBThreads>(Os, kSl, slice_block(w.du0, c, h, sl, H, ns, kChunk), kChunk, kSlice);
+    cp_block<kBThreads>(Qs, kSl, slice_block(w.c0, c, h, sl, H, ns, Dk), Dk, kSlice);
     cp_block<kBThreads>(Us, kSl, slice_block(w.u, c, h, sl, H, ns, kChunk), kChunk, kSlice);
     if (pred >= 0) cp_block<kBThreads>(Hs, kSl, slice_block(w.states, pred, h, sl, H, ns, Dk), Dk, kSlice);
     load_tile<Tin, kBThreads>(Ks, kRow, static_cast<const Tin*>(a.k), r0, L, H, h, Dk, 0, Dk4);
-    load_tile<Tin, kBThreads>(Qs, kRow, static_cast<const Tin*>(a.q), r0, L, H, h, Dk, 0, Dk4);
-    load_tile<Tin, kBThreads>(Os, kSl, tdo, r0, L, H, h, Dv, sl * kSlice, kSlice);
     load_tile<Tin, kBThreads>(Vs, kSl, static_cast<const Tin*>(a.v), r0, L, H, h, Dv, sl * kSlice, kSlice);
     if (pred < 0)
       for (int idx = tid; idx < Dk * kSlice; idx += kBThreads) Hs[(idx / kSlice) * kSl + idx % kSlice] = 0.f;
@@ -846,8 +934,8 @@ __global__ void __launch_bounds__(kBThreads, 1) gdn_bchain_kernel(const GdnArgs 
       for (int u = 0; u < kBThreads / 32; ++u) x += s_red[u];
       w.part_he[(static_cast<int64_t>(sl) * n_chunks + c) * H + h] = x;
     }
-    // du = w o (K dh_end) + P^T dO for rows t = 4 warp + m of column `lane` (K, P, dO
-    // rows past L are zero, so every row is computed); partial dw_t = w_t sum_j (K dh_end)_tj u_tj
+    // du = w o (K dh_end) + du0 for rows t = 4 warp + m of column `lane` (K and du0 rows
+    // past L are zero, so every row is computed); partial dw_t = w_t sum_j (K dh_end)_tj u_tj
     {
       float kd[kBRows];
 #pragma unroll
@@ -863,13 +951,8 @@ __global__ void __launch_bounds__(kBThreads, 1) gdn_bchain_kernel(const GdnArgs 
       }
       float du[kBRows];
 #pragma unroll
-      for (int m = 0; m < kBRows; ++m) du[m] = wv[kBRows * warp + m] * kd[m];
-      for (int t2 = 0; t2 < L; ++t2) {  // P is lower-triangular: P[t2][t] = 0 for t > t2
-        const float o = Os[t2 * kSl + lane];
-        const float4 p0 = *reinterpret_cast<const float4*>(Ps + t2 * kSq + kBRows * warp);
-        du[0] = fmaf(p0.x, o, du[0]); du[1] = fmaf(p0.y, o, du[1]); du[2] = fmaf(p0.z, o, du[2]);
-        du[3] = fmaf(p0.w, o, du[3]);
-      }
+      for (int m = 0; m < kBRows; ++m)
+        du[m] = fmaf(wv[kBRows * warp + m], kd[m], Os[(kBRows * warp + m) * kSl + lane]);
 #pragma unroll
       for (int m = 0; m < kBRows; ++m) {
         const int t = kBRows * warp + m;
@@ -909,25 +992,26 @@ __global__ void __launch_bounds__(kBThreads, 1) gdn_bchain_kernel(const GdnArgs 
       }
     }
     __syncthreads();
-    // dh0 = E_{L-1} dh_end + Q^T (E o dO) - K^T (beta E o dr): rows i = 8 warp + m
+    // dh0 = E_{L-1} dh_end + c0 - K^T (beta E o dr): rows i = 8 warp + m (c0 rows past Dk
+    // are never read: those rows are not stored)
     {
       float* dst = slice_block(w.dstart, c, h, sl, H, ns, Dk);
       const float gl = E[L - 1];
       const int i0 = 2 * kBRows * warp;
       float acc[2 * kBRows];
 #pragma unroll
-      for (int m = 0; m < 2 * kBRows; ++m) acc[m] = gl * Ds[(i0 + m) * kSl + lane];
+      for (int m = 0; m < 2 * kBRows; ++m)
+        acc[m] = i0 + m < Dk ? fmaf(gl, Ds[(i0 + m) * kSl + lane], Qs[(i0 + m) * kSl + lane]) : 0.f;
       for (int t = 0; t < L; ++t) {
-        const float ao = E[t] * Os[t * kSl + lane], br = -bs[t] * E[t] * Rs[t * kSl + lane];
-        const float4* qr = reinterpret_cast<const float4*>(Qs + t * kRow + i0);
+        const float br = -bs[t] * E[t] * Rs[t * kSl + lane];
         const float4* kr = reinterpret_cast<const float4*>(Ks + t * kRow + i0);
 #pragma unroll
         for (int q = 0; q < 2 * kBRows / 4; ++q) {
-          const float4 q4 = qr[q], k4 = kr[q];
-          acc[4 * q] = fmaf(q4.x, ao, fmaf(k4.x, br, acc[4 * q]));
-          acc[4 * q + 1] = fmaf(q4.y, ao, fmaf(k4.y, br, acc[4 * q + 1]));
-          acc[4 * q + 2] = fmaf(q4.z, ao, fmaf(k4.z, br, acc[4 * q + 2]));
-          acc[4 * q + 3] = fmaf(q4.w, ao, fmaf(k4.w, br, acc[4 * q + 3]));
+          const float4 k4 = kr[q];
+          acc[4 * q] = fmaf(k4.x, br, acc[4 * q]);
+          acc[4 * q + 1] = fmaf(k4.y, br, acc[4 * q + 1]);
+          acc[4 * q + 2] = fmaf(k4.z, br, acc[4 * q + 2]);
+          acc[4 * q + 3] = fmaf(k4.w, br, acc[4 * q + 3]);
         }
       }
 #pragma unroll
@@ -947,6 +1031,7 @@ __global__ void __launch_bounds__(kBThreads, 1) gdn_bchain_kernel(const GdnArgs 
 constexpr size_t kGradsSmem = (5 * kChunk * kRow + 3 * kChunk * kSq + 6 * kChunk) * sizeof(float);
 static_assert(kGradsSmem <= 227 * 1024, "GDN grads shared memory exceeds the per-block limit");
 static_assert(kBchainSmem <= 227 * 1024 && kPrepSmem <= 227 * 1024 && kChainSmem <= 227 * 1024 &&
+                  2 * kBprepSmem <= 227 * 1024 && kMaxD * kSl <= kChunk * kRow &&
                   kOutSmem <= 227 * 1024,
               "GDN shared memory exceeds the per-block limit");
 static_assert(2 * kMaxD * kSt <= kChunk * kSq, "h0 / dh_end staging must fit in the M1 buffer");
@@ -1324,6 +1409,10 @@ int gdn_backward(GdnArgs& a, int64_t mc, bool saved, cudaStream_t st) {
   int n_sm = 0, rc;
   if ((rc = sm_count(&n_sm))) return rc;
   if (!saved && (rc = run_forward_chain<Tin>(a, mc, n_sm, st))) return rc;
+  if ((rc = smem_opt_in(reinterpret_cast<const void*>(gdn_bprep_kernel<Tin>), static_cast<int>(kBprepSmem))))
+    return rc;
+  gdn_bprep_kernel<Tin><<<dim3(static_cast<unsigned>(mc), static_cast<unsigned>(a.H)), kThreads, kBprepSmem, st>>>(a);
+  TREE_LAUNCH_CHECK("gdn_bprep_kernel");
   if ((rc = smem_opt_in(reinterpret_cast<const void*>(gdn_bchain_kernel<Tin>), static_cast<int>(kBchainSmem))) ||
       (rc = smem_opt_in(reinterpret_cast<const void*>(gdn_grads_kernel<Tin>), static_cast<int>(kGradsSmem))))
     return rc;
